@@ -1,0 +1,479 @@
+"""Benchmark: packed (block-diagonal causal) attention forward + backward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one pass of the whole path over one batch: segment-range tile table,
+forward, tile table again, delta, dQ, dK/dV -- the same kernels, in the same
+order, as pa_fwd followed by pa_bwd. The default workload is the 8k row
+(B=1, N=8192, Hq=32, Hkv=8, D=128, bf16) in one segment; the same row split
+into packed segments is measured too and reported under "packed".
+
+Timing: W warm-up steps, then K timed steps; every step is bracketed by CUDA
+events on the launching stream, with the L2 flushed (a 256 MiB write) between
+steps outside the events. Useful FLOPs count only visible pairs (j <= i, same
+segment, padding segments excluded): 4*D per pair forward, 10*D backward.
+Under torchrun each rank runs its own replica of the workload (weak scaling,
+no collective on the data path); the reported time is the max over ranks.
+
+--impl reference times the fp64 CPU oracle on this machine's host cores on a
+bounded sample of the same workload (one query head with its kv head per
+step), in the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "packed causal attn fwd+bwd useful TFLOPS at N=8192; % of GB300 bf16 tensor peak"
+UNIT = "TFLOPS"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+KERNEL_SOURCES = {"fwd": "fwd.cu", "dq": "bwd_dq.cu", "dkv": "bwd_dkv.cu", "delta": "prologue.cu"}
+# algorithmic flops per visible pair, per kernel (executed by the split design)
+FLOPS_PER_PAIR = {"fwd": 4, "dq": 6, "dkv": 8}
+
+
+# ------------------------------------------------------------------ accounting
+def segment_lengths(w: synth.Workload):
+    for b in range(w.B):
+        lens = list(w.lengths[b])
+        pad = w.pad[b] if w.pad else 0
+        yield lens, pad
+
+
+def visible_pairs_per_head(w: synth.Workload, exclude_padding: bool = True) -> int:
+    """Pairs (i, j) with j <= i in the same segment, summed over rows; the
+    padding segment (last of a row, when the row has padding) is excluded."""
+    total = 0
+    for lens, pad in segment_lengths(w):
+        use = lens[:-1] if (exclude_padding and pad) else lens
+        total += sum(L * (L + 1) // 2 for L in use)
+    return total
+
+
+def useful_flops(w: synth.Workload) -> float:
+    return 14.0 * w.D * visible_pairs_per_head(w) * w.Hq
+
+
+def executed_tile_pairs(w: synth.Workload) -> int:
+    """(query tile, key tile) pairs the kernels visit per head (range-overlap walk)."""
+    T = w.N // 128
+    n = 0
+    for b in range(w.B):
+        s = w.seg[b].reshape(T, 128)
+        lo, hi = s.min(1), s.max(1)
+        for tq in range(T):
+            n += int(np.sum((lo[: tq + 1] <= hi[tq]) & (lo[tq] <= hi[: tq + 1])))
+    return n
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"bf16_tflops": float(d["bf16_tflops"]), "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", 0)),
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of that kernel and on this workload (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d or d.get("workload") != workload:
+        return None
+    src = os.path.join(ROOT, "segment_masked_causal_gb300", "csrc", KERNEL_SOURCES[kernel])
+    if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != d.get("source_sha256_16"):
+        return None
+    return float(d["bytes_per_launch"])
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pa_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def replica_seed(base_seed: int, rank: int) -> int:
+    """Each rank processes its own independent batch of the same shape."""
+    return base_seed + 7919 * rank
+
+
+def reduce_max(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ------------------------------------------------------------------ the GPU arm
+class Runner:
+    def __init__(self, w: synth.Workload, dev, seed: int):
+        import torch
+        import segment_masked_causal_gb300 as pa
+        self.pa, self.torch, self.w, self.dev = pa, torch, w, dev
+        w2 = synth.Workload(w.name, w.B, w.Hq, w.Hkv, w.N, w.D, seed, w.seg, w.lengths, w.pad)
+        t = w2.tensors()
+        self.host = t
+        to = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(dev)
+        self.q, self.k, self.v, self.do = (to(t[x]) for x in ("q", "k", "v", "do"))
+        self.seg = torch.from_numpy(w.seg).to(dev)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
+        self.dq = torch.empty_like(self.q)
+        self.dk = torch.empty_like(self.k)
+        self.dv = torch.empty_like(self.v)
+        self.ws = pa.workspace(self.q, self.k)
+        self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush(self):
+        self.flush_buf.zero_()
+
+    def step(self, events=None, causal=False):
+        """The kernels of pa_fwd + pa_bwd, one call per kernel, events between."""
+        pa, seg = self.pa, (None if causal else self.seg)
+        q, k, v, do = self.q, self.k, self.v, self.do
+        ev = events or [None] * 7
+        rec = lambda e: e is not None and e.record()
+        rec(ev[0])
+        pa.pa_build_tile_table(q, k, seg, self.ws)
+        rec(ev[1])
+        pa.pa_fwd_tiles(q, k, v, seg, self.out, self.lse, self.ws)
+        rec(ev[2])
+        pa.pa_build_tile_table(q, k, seg, self.ws)
+        rec(ev[3])
+        pa.pa_bwd_delta(q, k, self.out, do, self.ws)
+        rec(ev[4])
+        pa.pa_bwd_dq(q, k, v, do, self.lse, seg, self.dq, self.ws)
+        rec(ev[5])
+        pa.pa_bwd_dkv(q, k, v, do, self.lse, seg, self.dk, self.dv, self.ws)
+        rec(ev[6])
+
+    def timed(self, steps: int, warmup: int, causal=False, sampler=None):
+        torch = self.torch
+        for _ in range(warmup):
+            self.step(causal=causal)
+            self.flush()
+        torch.cuda.synchronize()
+        barrier(self.dev)
+        if sampler:
+            sampler.start()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+        for i in range(steps):
+            self.flush()
+            self.step(evs[i], causal=causal)
+        torch.cuda.synchronize()
+        barrier(self.dev)
+        clocks = sampler.stop() if sampler else None
+        status = self.pa.pa_device_status(self.ws)
+        if status != 0:
+            raise RuntimeError(f"device status {status:#x}")
+        per = {"table_fwd": [], "fwd": [], "table_bwd": [], "delta": [], "dq": [], "dkv": [], "step": []}
+        keys = ["table_fwd", "fwd", "table_bwd", "delta", "dq", "dkv"]
+        for e in evs:
+            for n, key in enumerate(keys):
+                per[key].append(e[n].elapsed_time(e[n + 1]))
+            per["step"].append(e[0].elapsed_time(e[6]))
+        return {k: statistics.mean(v) for k, v in per.items()}, clocks
+
+    def e2e(self, steps: int, warmup: int):
+        """Public pa_fwd + pa_bwd with pinned host inputs/outputs: H2D of q, k,
+        v, dO, seg and D2H of O, lse, dQ, dK, dV inside the timed region."""
+        torch, pa = self.torch, self.pa
+        pin = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory()
+        h_in = {x: pin(self.host[x]) for x in ("q", "k", "v", "do")}
+        h_seg = torch.from_numpy(self.w.seg).pin_memory()
+        h_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                 for n, t in (("o", self.out), ("lse", self.lse), ("dq", self.dq), ("dk", self.dk), ("dv", self.dv))}
+        d_in = {"q": self.q, "k": self.k, "v": self.v, "do": self.do}
+
+        def one():
+            for x in d_in:
+                d_in[x].copy_(h_in[x], non_blocking=True)
+            self.seg.copy_(h_seg, non_blocking=True)
+            pa.pa_fwd(self.q, self.k, self.v, self.seg, self.out, self.lse, self.ws)
+            pa.pa_bwd(self.q, self.k, self.v, self.out, self.do, self.lse, self.seg, self.dq, self.dk, self.dv,
+                      self.ws)
+            for n, t in (("o", self.out), ("lse", self.lse), ("dq", self.dq), ("dk", self.dk), ("dv", self.dv)):
+                h_out[n].copy_(t, non_blocking=True)
+
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        barrier(self.dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            one()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(self.dev)
+        ms = e0.elapsed_time(e1) / steps
+        h2d = sum(t.numel() * t.element_size() for t in h_in.values()) + h_seg.numel() * 4
+        d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+        return ms, h2d, d2h
+
+
+def cpu_baseline(w: synth.Workload, seconds: float = 12.0, max_heads: int = 8):
+    """The oracle, as it stands, on a bounded sample: complete fwd+bwd of one
+    query head against its kv head (the per-head share of dK/dV), repeated over
+    heads until `seconds` have passed."""
+    import oracle
+    t = w.tensors()
+    done, elapsed = 0, 0.0
+    G = w.Hq // w.Hkv
+    while done < min(max_heads, w.Hq) and (elapsed < seconds or done == 0):
+        h = (done * 5) % w.Hq
+        hk = h // G
+        q = synth.bf16_bits_to_f64(t["q"][:, h:h + 1])
+        k = synth.bf16_bits_to_f64(t["k"][:, hk:hk + 1])
+        v = synth.bf16_bits_to_f64(t["v"][:, hk:hk + 1])
+        do = synth.bf16_bits_to_f64(t["do"][:, h:h + 1])
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, w.seg, w.scale, do)
+        elapsed += time.perf_counter() - t0
+        done += 1
+    flops = 14.0 * w.D * visible_pairs_per_head(w) * done
+    return {"value": flops / elapsed / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{done} of {w.Hq} query heads of {w.name}, each a complete fp64 forward+backward against "
+                      f"its kv head ({elapsed:.1f} s)"}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    world, rank, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    if local == 0:
+        import __graft_entry__
+        __graft_entry__.build()
+    barrier(dev)
+    import segment_masked_causal_gb300 as pa
+    pa.lib()
+
+    w = synth.workload(args.workload)
+    r = Runner(w, dev, replica_seed(w.seed, rank))
+    sampler = ClockSampler(local) if rank == 0 else None
+    t, clocks = r.timed(args.steps, args.warmup, sampler=sampler)
+    step_ms = reduce_max(t["step"], dev)
+    kern = {k: reduce_max(t[k], dev) for k in ("table_fwd", "fwd", "table_bwd", "delta", "dq", "dkv")}
+    flops = useful_flops(w)
+    value = flops * world / (step_ms * 1e-3) / 1e12
+    pk = peaks()
+    pairs = visible_pairs_per_head(w) * w.Hq
+    dom = max(("fwd", "dq", "dkv"), key=lambda k: kern[k])
+    achieved = FLOPS_PER_PAIR[dom] * w.D * pairs / (kern[dom] * 1e-3) / 1e12
+    traffic = kernel_traffic(dom, w.name)
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": traffic,
+                "peak_source": pk["source"] + " bf16 burst (MEASURED_PEAKS.json)" if pk["source"] == "measured"
+                else "fallback 1.9 PFLOP/s"}
+    delta_bytes = 2 * 2 * w.B * w.Hq * w.N * w.D + 4 * w.B * w.Hq * w.N
+    kernels = {k: {"ms": round(v, 4)} for k, v in kern.items()}
+    for k in ("fwd", "dq", "dkv"):
+        kernels[k]["tflops"] = round(FLOPS_PER_PAIR[k] * w.D * pairs / (kern[k] * 1e-3) / 1e12, 2)
+    kernels["delta"]["gbs"] = round(delta_bytes / (kern["delta"] * 1e-3) / 1e9, 1)
+    kernels["delta"]["hbm_frac"] = round(kernels["delta"]["gbs"] / pk["hbm_gbs"], 4)
+
+    e2e_ms, h2d, d2h = r.e2e(max(3, min(args.steps, 10)), 2)
+    e2e_ms = reduce_max(e2e_ms, dev)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "segments": sum(len(l) for l in w.lengths), "seed": w.seed,
+                   "l2": "flushed between timed steps (256 MiB write, outside the events)",
+                   "parallelism": "replicas" if world == 1 else f"replicas x{world} (no data-path collective)"},
+        "frac_of_peak": round(value / world / pk["bf16_tflops"], 4),
+        "useful_tflop_per_step": round(flops / 1e12, 4),
+        "executed_tile_pairs_per_head": executed_tile_pairs(w),
+        "kernels": kernels,
+        "roofline": roofline,
+        "gpu_launches": 6 * args.steps,
+        "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "clocks": clocks,
+    }
+    if not args.no_extras and w.name == "8k_one_segment":
+        line["packed"] = packed_extras(dev, rank, args)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def packed_extras(dev, rank, args):
+    """The 8k row in packed segments, and the causal entry points on the
+    one-segment row: per-kernel times for the skip speedup (packed vs causal on
+    the same length) and the identical-work overhead (packed kernels with one
+    segment vs the causal ones)."""
+    steps = max(3, min(args.steps, 10))
+    one = synth.workload("8k_one_segment")
+    pk = synth.workload("8k_packed")
+    r1 = Runner(one, dev, replica_seed(one.seed, rank))
+    t_packed1, _ = r1.timed(steps, 2)
+    t_causal, _ = r1.timed(steps, 2, causal=True)
+    del r1
+    r2 = Runner(pk, dev, replica_seed(pk.seed, rank))
+    t_multi, _ = r2.timed(steps, 2)
+    del r2
+    flops = useful_flops(pk)
+    out = {"workload": pk.name, "segments": len(pk.lengths[0]),
+           "useful_tflops": round(flops / (t_multi["step"] * 1e-3) / 1e12, 3),
+           "ms_per_step": round(t_multi["step"], 4),
+           "visible_fraction_of_causal": round(visible_pairs_per_head(pk) / visible_pairs_per_head(one), 4),
+           "executed_tile_fraction_of_causal": round(executed_tile_pairs(pk) / executed_tile_pairs(one), 4)}
+    for k in ("fwd", "dq", "dkv", "step"):
+        out[k] = {"causal_ms": round(t_causal[k], 4), "packed_one_segment_ms": round(t_packed1[k], 4),
+                  "packed_multi_ms": round(t_multi[k], 4),
+                  "skip_speedup_vs_causal": round(t_causal[k] / t_multi[k], 3),
+                  "one_segment_overhead_vs_causal": round(t_packed1[k] / t_causal[k] - 1.0, 4)}
+    return out
+
+
+# ------------------------------------------------------------------ the reference arm
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = synth.workload(args.workload)
+    t = w.tensors()
+    G = w.Hq // w.Hkv
+    pairs = visible_pairs_per_head(w)
+
+    def one(i):
+        h = (i * 5) % w.Hq
+        hk = h // G
+        f = lambda x, a, b: synth.bf16_bits_to_f64(t[x][:, a:b])
+        oracle.attention(f("q", h, h + 1), f("k", hk, hk + 1), f("v", hk, hk + 1), w.seg, w.scale, f("do", h, h + 1))
+
+    for i in range(args.warmup):
+        one(i)
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        one(args.warmup + i)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    value = 14.0 * w.D * pairs / (ms * 1e-3) / 1e12
+    sample = f"one query head (rotating) of {w.Hq} of {w.name} per step, complete fp64 forward+backward"
+    line = {"metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                       "sample": "1 query head per step"},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="8k_one_segment", choices=synth.WORKLOADS)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="skip the packed / causal comparison runs")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 warm-up steps, whatever was asked
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,147 @@
+/*
+ * pa.h -- C ABI of libpa: packed (block-diagonal causal) attention on GB300.
+ *
+ * The operation (mlx-train-perf changelog, entry adding
+ * `flash_attention(segments=...)` and the PACKED forward, dQ and dK/dV
+ * kernels; mlx-train-perf 0.5.1 README, "Sequence packing" and
+ * "Flash-attention training path"): several sequences are packed into one
+ * row; a per-token int32 segment id says which sequence each token belongs
+ * to, and token i attends token j iff j <= i and seg[i] == seg[j]. No (N, N)
+ * mask exists anywhere. The forward saves only the output and its
+ * log-sum-exp; the backward recomputes attention tile by tile.
+ *
+ *   S_ij  = scale * <q_i, k_j>           over visible (i, j) only
+ *   lse_i = ln sum_j exp(S_ij)
+ *   o_i   = sum_j exp(S_ij - lse_i) v_j
+ *   and the gradients of o with respect to q, k and v.
+ *
+ * Layouts (all contiguous, row-major; same README, "If you maintain a
+ * trainer": q/k/v are (B, H, N, D), grouped-query heads mapped contiguously):
+ *   q, out, dout, dq : (B, Hq,  N, D) bf16
+ *   k, v, dk, dv     : (B, Hkv, N, D) bf16;  query head h reads kv head h / (Hq/Hkv)
+ *   lse              : (B, Hq,  N)    fp32, natural log
+ *   seg              : (B, N)         int32, shared by all heads. Ids are
+ *                      compared for equality only: any values are valid.
+ *                      Tile skipping is fastest when each id forms one
+ *                      contiguous run, which is what packing produces.
+ *
+ * Ownership: every pointer is device memory owned by the caller. The library
+ * allocates no device memory and keeps no pointer after a call returns. The
+ * workspace `ws` (pa_workspace_bytes) holds the per-tile segment-range table,
+ * the backward's delta = rowsum(dO * O) and a device status word.
+ *
+ * Execution: every call validates its arguments synchronously and returns an
+ * error before launching anything; otherwise it enqueues its kernels on
+ * `stream` and returns PA_OK without synchronising. Outputs are overwritten,
+ * never accumulated into. There is no fallback path: an unsupported shape or
+ * device is refused with a typed status (same README, "When it refuses":
+ * typed refusals, never silent fallbacks).
+ *
+ * Device-side waits are bounded; a pipeline that stalls for ~2 s ends its
+ * kernel and sets bits in the workspace status word (pa_device_status).
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pa_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef struct {
+  int32_t B;    /* rows (independent packed rows)                    */
+  int32_t Hq;   /* query heads                                       */
+  int32_t Hkv;  /* key/value heads; Hq % Hkv == 0                    */
+  int32_t N;    /* tokens per row; multiple of 128                   */
+  int32_t D;    /* head dim: 64 or 128                               */
+  float scale;  /* softmax scale; <= 0 selects 1/sqrt(D)             */
+} pa_dims;
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_NULL = 1,      /* a required pointer is NULL                          */
+  PA_ERR_HEAD_DIM = 2,  /* D not in {64, 128}                                  */
+  PA_ERR_GQA = 3,       /* Hq % Hkv != 0                                       */
+  PA_ERR_SHAPE = 4,     /* B, H, N <= 0, N % 128 != 0, or sizes overflow int32 */
+  PA_ERR_ALIGN = 5,     /* a pointer is not 16-byte aligned                    */
+  PA_ERR_WORKSPACE = 6, /* ws_bytes < pa_workspace_bytes(dims)                 */
+  PA_ERR_ARCH = 7,      /* current device is not compute capability 10.3       */
+  PA_ERR_CUDA = 8       /* a CUDA runtime / driver call or launch failed       */
+} pa_status;
+
+/* Device status bits (pa_device_status). */
+#define PA_DEVERR_TIMEOUT 0x1u /* a bounded wait expired; bits 8.. name the site */
+#define PA_DEVERR_DRAIN 0x2u   /* teardown after a timeout could not drain       */
+
+/* Workspace size in bytes for `dims` (0 if dims are invalid). */
+size_t pa_workspace_bytes(const pa_dims* dims);
+
+/*
+ * Forward. Writes out (B,Hq,N,D) bf16 and lse (B,Hq,N) fp32.
+ * seg (B,N) int32 must not be NULL (use pa_fwd_causal for plain causal).
+ */
+pa_status pa_fwd(const pa_dims* dims, const void* q, const void* k, const void* v, const int32_t* seg,
+                 void* out, float* lse, void* ws, size_t ws_bytes, pa_stream_t stream);
+
+/*
+ * Backward. Inputs: q, k, v, the forward's out and lse, dout = dL/d(out) and
+ * seg. Writes dq (B,Hq,N,D), dk and dv (B,Hkv,N,D), bf16. The gradients of all
+ * query heads of a group are summed into their kv head's dk/dv.
+ */
+pa_status pa_bwd(const pa_dims* dims, const void* q, const void* k, const void* v, const void* out,
+                 const void* dout, const float* lse, const int32_t* seg, void* dq, void* dk, void* dv,
+                 void* ws, size_t ws_bytes, pa_stream_t stream);
+
+/*
+ * Plain causal variants (mlx-train-perf 0.5.1 README, "If you maintain a
+ * trainer": flash_attention(q, k, v, scale=..., causal=True)). They run the
+ * same kernels with every token in one segment, so their results are
+ * bit-identical to pa_fwd / pa_bwd on an all-equal seg (the changelog states
+ * single-segment packed output is bit-identical to the causal kernels).
+ */
+pa_status pa_fwd_causal(const pa_dims* dims, const void* q, const void* k, const void* v, void* out,
+                        float* lse, void* ws, size_t ws_bytes, pa_stream_t stream);
+pa_status pa_bwd_causal(const pa_dims* dims, const void* q, const void* k, const void* v, const void* out,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv, void* ws,
+                        size_t ws_bytes, pa_stream_t stream);
+
+/*
+ * The steps of the path, one kernel each, for callers that schedule or time
+ * them individually. pa_fwd is pa_build_tile_table + pa_fwd_tiles; pa_bwd is
+ * pa_build_tile_table + pa_bwd_delta + pa_bwd_dq + pa_bwd_dkv, all on one
+ * stream, in that order. The later steps read the tile table (and the bwd
+ * steps the delta) from `ws`, so they must follow the steps that write it
+ * with the same dims and the same seg (NULL seg = plain causal throughout).
+ * pa_build_tile_table also clears the workspace status word.
+ */
+pa_status pa_build_tile_table(const pa_dims* dims, const int32_t* seg, void* ws, size_t ws_bytes,
+                              pa_stream_t stream);
+pa_status pa_fwd_tiles(const pa_dims* dims, const void* q, const void* k, const void* v, const int32_t* seg,
+                       void* out, float* lse, void* ws, size_t ws_bytes, pa_stream_t stream);
+pa_status pa_bwd_delta(const pa_dims* dims, const void* out, const void* dout, void* ws, size_t ws_bytes,
+                       pa_stream_t stream);
+pa_status pa_bwd_dq(const pa_dims* dims, const void* q, const void* k, const void* v, const void* dout,
+                    const float* lse, const int32_t* seg, void* dq, void* ws, size_t ws_bytes, pa_stream_t stream);
+pa_status pa_bwd_dkv(const pa_dims* dims, const void* q, const void* k, const void* v, const void* dout,
+                     const float* lse, const int32_t* seg, void* dk, void* dv, void* ws, size_t ws_bytes,
+                     pa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns the workspace's device status word
+ * (0 = healthy; PA_DEVERR_* bits otherwise) and clears it. Returns
+ * 0xFFFFFFFF if the read itself fails.
+ */
+uint32_t pa_device_status(const void* ws, pa_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* pa_status_string(pa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

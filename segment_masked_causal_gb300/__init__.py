@@ -1,0 +1,245 @@
+"""Packed (block-diagonal causal) attention on GB300: Python binding of libpa.
+
+Thin ctypes marshalling over the C ABI in include/pa.h: every function here
+has the same name as its C entry point, checks that the torch tensors it is
+given have the layout the ABI expects, and passes their device pointers and
+the current CUDA stream through. All computation happens in the CUDA kernels
+of libpa.so; there is no other code path. If the library has not been built
+(``python -m segment_masked_causal_gb300.build``), importing works but every
+call raises ``LibraryMissing``.
+
+Semantics (mlx-train-perf changelog, PACKED kernels; 0.5.1 README,
+"Sequence packing"): token i attends token j iff j <= i and seg[i] == seg[j].
+q/out/dout/dq are (B, Hq, N, D) bf16; k/v/dk/dv are (B, Hkv, N, D) bf16; lse
+is (B, Hq, N) fp32; seg is (B, N) int32; D in {64, 128}; N % 128 == 0.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpa.so")
+
+PA_OK = 0
+STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_NULL", 2: "PA_ERR_HEAD_DIM", 3: "PA_ERR_GQA", 4: "PA_ERR_SHAPE",
+                5: "PA_ERR_ALIGN", 6: "PA_ERR_WORKSPACE", 7: "PA_ERR_ARCH", 8: "PA_ERR_CUDA"}
+EXPORTS = ["pa_workspace_bytes", "pa_fwd", "pa_bwd", "pa_fwd_causal", "pa_bwd_causal", "pa_build_tile_table",
+           "pa_fwd_tiles", "pa_bwd_delta", "pa_bwd_dq", "pa_bwd_dkv", "pa_device_status", "pa_status_string"]
+
+
+class LibraryMissing(RuntimeError):
+    pass
+
+
+class PAError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+class pa_dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("N", ctypes.c_int32), ("D", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """The loaded libpa.so (ctypes), with argument types declared."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise LibraryMissing(f"{LIB_PATH} not built; run python -m segment_masked_causal_gb300.build")
+            L = ctypes.CDLL(LIB_PATH)
+            P, S = ctypes.c_void_p, ctypes.c_size_t
+            D = ctypes.POINTER(pa_dims)
+            L.pa_workspace_bytes.argtypes = [D]
+            L.pa_workspace_bytes.restype = S
+            L.pa_fwd.argtypes = [D, P, P, P, P, P, P, P, S, P]
+            L.pa_fwd_causal.argtypes = [D, P, P, P, P, P, P, S, P]
+            L.pa_bwd.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P, S, P]
+            L.pa_bwd_causal.argtypes = [D, P, P, P, P, P, P, P, P, P, P, S, P]
+            L.pa_build_tile_table.argtypes = [D, P, P, S, P]
+            L.pa_fwd_tiles.argtypes = [D, P, P, P, P, P, P, P, S, P]
+            L.pa_bwd_delta.argtypes = [D, P, P, P, S, P]
+            L.pa_bwd_dq.argtypes = [D, P, P, P, P, P, P, P, P, S, P]
+            L.pa_bwd_dkv.argtypes = [D, P, P, P, P, P, P, P, P, P, S, P]
+            for f in ("pa_fwd", "pa_fwd_causal", "pa_bwd", "pa_bwd_causal", "pa_build_tile_table", "pa_fwd_tiles",
+                      "pa_bwd_delta", "pa_bwd_dq", "pa_bwd_dkv"):
+                getattr(L, f).restype = ctypes.c_int
+            L.pa_device_status.argtypes = [P, P]
+            L.pa_device_status.restype = ctypes.c_uint32
+            L.pa_status_string.argtypes = [ctypes.c_int]
+            L.pa_status_string.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def make_dims(B, Hq, Hkv, N, D, scale=0.0) -> pa_dims:
+    return pa_dims(int(B), int(Hq), int(Hkv), int(N), int(D), float(scale))
+
+
+def _check(code: int):
+    if code != PA_OK:
+        raise PAError(code, lib().pa_status_string(code).decode())
+
+
+def _ptr(t, dtype=None, name=""):
+    """Device pointer of a contiguous CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def _dims_of(q, k, scale):
+    B, Hq, N, D = q.shape
+    return make_dims(B, Hq, k.shape[1], N, D, scale)
+
+
+def pa_workspace_bytes(B, Hq, Hkv, N, D) -> int:
+    d = make_dims(B, Hq, Hkv, N, D)
+    return int(lib().pa_workspace_bytes(ctypes.byref(d)))
+
+
+def workspace(q, k, device=None):
+    """A device workspace sized for q/k (caller-owned torch uint8 tensor)."""
+    import torch
+    B, Hq, N, D = q.shape
+    n = pa_workspace_bytes(B, Hq, k.shape[1], N, D)
+    if n == 0:
+        raise PAError(4, "invalid dims")
+    return torch.empty(n, dtype=torch.uint8, device=device or q.device)
+
+
+def pa_fwd(q, k, v, seg, out, lse, ws, scale=0.0, stream=None):
+    import torch
+    bf = torch.bfloat16
+    d = _dims_of(q, k, scale)
+    _check(lib().pa_fwd(ctypes.byref(d), _ptr(q, bf, "q"), _ptr(k, bf, "k"), _ptr(v, bf, "v"),
+                        _ptr(seg, torch.int32, "seg"), _ptr(out, bf, "out"), _ptr(lse, torch.float32, "lse"),
+                        _ptr(ws, None, "ws"), ws.numel() if hasattr(ws, "numel") else 0, _stream(stream)))
+
+
+def pa_fwd_causal(q, k, v, out, lse, ws, scale=0.0, stream=None):
+    import torch
+    bf = torch.bfloat16
+    d = _dims_of(q, k, scale)
+    _check(lib().pa_fwd_causal(ctypes.byref(d), _ptr(q, bf, "q"), _ptr(k, bf, "k"), _ptr(v, bf, "v"),
+                               _ptr(out, bf, "out"), _ptr(lse, torch.float32, "lse"), _ptr(ws, None, "ws"),
+                               ws.numel(), _stream(stream)))
+
+
+def pa_bwd(q, k, v, out, dout, lse, seg, dq, dk, dv, ws, scale=0.0, stream=None):
+    import torch
+    bf = torch.bfloat16
+    d = _dims_of(q, k, scale)
+    _check(lib().pa_bwd(ctypes.byref(d), _ptr(q, bf, "q"), _ptr(k, bf, "k"), _ptr(v, bf, "v"),
+                        _ptr(out, bf, "out"), _ptr(dout, bf, "dout"), _ptr(lse, torch.float32, "lse"),
+                        _ptr(seg, torch.int32, "seg"), _ptr(dq, bf, "dq"), _ptr(dk, bf, "dk"), _ptr(dv, bf, "dv"),
+                        _ptr(ws, None, "ws"), ws.numel(), _stream(stream)))
+
+
+def pa_bwd_causal(q, k, v, out, dout, lse, dq, dk, dv, ws, scale=0.0, stream=None):
+    import torch
+    bf = torch.bfloat16
+    d = _dims_of(q, k, scale)
+    _check(lib().pa_bwd_causal(ctypes.byref(d), _ptr(q, bf, "q"), _ptr(k, bf, "k"), _ptr(v, bf, "v"),
+                               _ptr(out, bf, "out"), _ptr(dout, bf, "dout"), _ptr(lse, torch.float32, "lse"),
+                               _ptr(dq, bf, "dq"), _ptr(dk, bf, "dk"), _ptr(dv, bf, "dv"), _ptr(ws, None, "ws"),
+                               ws.numel(), _stream(stream)))
+
+
+def pa_build_tile_table(q, k, seg, ws, scale=0.0, stream=None):
+    import torch
+    d = _dims_of(q, k, scale)
+    _check(lib().pa_build_tile_table(ctypes.byref(d), _ptr(seg, torch.int32, "seg"), _ptr(ws, None, "ws"),
+                                     ws.numel(), _stream(stream)))
+
+
+def pa_fwd_tiles(q, k, v, seg, out, lse, ws, scale=0.0, stream=None):
+    import torch
+    bf = torch.bfloat16
+    d = _dims_of(q, k, scale)
+    _check(lib().pa_fwd_tiles(ctypes.byref(d), _ptr(q, bf, "q"), _ptr(k, bf, "k"), _ptr(v, bf, "v"),
+                              _ptr(seg, torch.int32, "seg"), _ptr(out, bf, "out"), _ptr(lse, torch.float32, "lse"),
+                              _ptr(ws, None, "ws"), ws.numel(), _stream(stream)))
+
+
+def pa_bwd_delta(q, k, out, dout, ws, scale=0.0, stream=None):
+    import torch
+    bf = torch.bfloat16
+    d = _dims_of(q, k, scale)
+    _check(lib().pa_bwd_delta(ctypes.byref(d), _ptr(out, bf, "out"), _ptr(dout, bf, "dout"), _ptr(ws, None, "ws"),
+                              ws.numel(), _stream(stream)))
+
+
+def pa_bwd_dq(q, k, v, dout, lse, seg, dq, ws, scale=0.0, stream=None):
+    import torch
+    bf = torch.bfloat16
+    d = _dims_of(q, k, scale)
+    _check(lib().pa_bwd_dq(ctypes.byref(d), _ptr(q, bf, "q"), _ptr(k, bf, "k"), _ptr(v, bf, "v"),
+                           _ptr(dout, bf, "dout"), _ptr(lse, torch.float32, "lse"), _ptr(seg, torch.int32, "seg"),
+                           _ptr(dq, bf, "dq"), _ptr(ws, None, "ws"), ws.numel(), _stream(stream)))
+
+
+def pa_bwd_dkv(q, k, v, dout, lse, seg, dk, dv, ws, scale=0.0, stream=None):
+    import torch
+    bf = torch.bfloat16
+    d = _dims_of(q, k, scale)
+    _check(lib().pa_bwd_dkv(ctypes.byref(d), _ptr(q, bf, "q"), _ptr(k, bf, "k"), _ptr(v, bf, "v"),
+                            _ptr(dout, bf, "dout"), _ptr(lse, torch.float32, "lse"), _ptr(seg, torch.int32, "seg"),
+                            _ptr(dk, bf, "dk"), _ptr(dv, bf, "dv"), _ptr(ws, None, "ws"), ws.numel(),
+                            _stream(stream)))
+
+
+def pa_device_status(ws, stream=None) -> int:
+    return int(lib().pa_device_status(_ptr(ws, None, "ws"), _stream(stream)))
+
+
+def pa_status_string(code: int) -> str:
+    return lib().pa_status_string(code).decode()
+
+
+# ---------------------------------------------------------------- conveniences
+def forward(q, k, v, seg=None, scale=0.0, ws=None):
+    """Allocate out/lse and run pa_fwd (seg given) or pa_fwd_causal (seg None)."""
+    import torch
+    B, Hq, N, D = q.shape
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    ws = workspace(q, k) if ws is None else ws
+    if seg is None:
+        pa_fwd_causal(q, k, v, out, lse, ws, scale)
+    else:
+        pa_fwd(q, k, v, seg, out, lse, ws, scale)
+    return out, lse
+
+
+def backward(q, k, v, out, dout, lse, seg=None, scale=0.0, ws=None):
+    """Allocate dq/dk/dv and run pa_bwd (seg given) or pa_bwd_causal (seg None)."""
+    import torch
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = workspace(q, k) if ws is None else ws
+    if seg is None:
+        pa_bwd_causal(q, k, v, out, dout, lse, dq, dk, dv, ws, scale)
+    else:
+        pa_bwd(q, k, v, out, dout, lse, seg, dq, dk, dv, ws, scale)
+    return dq, dk, dv

@@ -1,0 +1,266 @@
+// api.cu -- the extern "C" boundary of libpa (declared in include/pa.h).
+//
+// Every entry point validates its arguments on the host before touching the
+// device, refuses anything unsupported with a typed status (no fallback), and
+// otherwise enqueues the kernels on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <initializer_list>
+#include <mutex>
+
+#include "../../include/pa.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct WsLayout {
+  size_t status, tiles, delta, total;
+};
+
+bool dims_ok(const pa_dims* d, pa_status* why) {
+  if (!d) { *why = PA_ERR_NULL; return false; }
+  if (d->B <= 0 || d->Hq <= 0 || d->Hkv <= 0 || d->N <= 0 || (d->N % pa::kTile) != 0) {
+    *why = PA_ERR_SHAPE;
+    return false;
+  }
+  if (d->D != 64 && d->D != 128) { *why = PA_ERR_HEAD_DIM; return false; }
+  if (d->Hq % d->Hkv != 0) { *why = PA_ERR_GQA; return false; }
+  // tensor-map row coordinates and tile counts are 32-bit
+  const int64_t rows = (int64_t)d->B * d->Hq * d->N;
+  if (rows >= (int64_t(1) << 31) || (int64_t)d->N / pa::kTile > 65535 * 2) { *why = PA_ERR_SHAPE; return false; }
+  if (!(std::isfinite(d->scale))) { *why = PA_ERR_SHAPE; return false; }
+  return true;
+}
+
+WsLayout ws_layout(const pa_dims* d) {
+  WsLayout w;
+  const size_t T = (size_t)d->N / pa::kTile;
+  w.status = 0;
+  w.tiles = kAlign;
+  w.delta = w.tiles + round_up((size_t)d->B * T * sizeof(int4));
+  w.total = w.delta + round_up((size_t)d->B * d->Hq * d->N * sizeof(float));
+  return w;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Per-device: compute capability 10.3 and enough opt-in shared memory.
+pa_status device_ok() {
+  static std::mutex mu;
+  static int checked[64] = {0};  // 0 unknown, 1 ok, 2 refused
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return PA_ERR_ARCH;
+  std::lock_guard<std::mutex> lk(mu);
+  if (checked[dev] == 0) {
+    int maj = 0, min = 0, smem = 0;
+    if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return PA_ERR_CUDA;
+    checked[dev] = (maj == 10 && min == 3 && smem >= 232448) ? 1 : 2;
+  }
+  return checked[dev] == 1 ? PA_OK : PA_ERR_ARCH;
+}
+
+pa::AttnParams make_params(const pa_dims* d, const int32_t* seg, void* ws) {
+  pa::AttnParams p{};
+  p.B = d->B; p.Hq = d->Hq; p.Hkv = d->Hkv; p.N = d->N; p.T = d->N / pa::kTile; p.G = d->Hq / d->Hkv;
+  p.scale = d->scale > 0.f ? d->scale : 1.f / std::sqrt((float)d->D);
+  p.scale_log2 = p.scale * 1.4426950408889634f;
+  p.seg = seg;
+  const WsLayout w = ws_layout(d);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  p.status = reinterpret_cast<uint32_t*>(base + w.status);
+  p.tiles = reinterpret_cast<const int4*>(base + w.tiles);
+  p.delta = reinterpret_cast<float*>(base + w.delta);
+  return p;
+}
+
+pa_status common_checks(const pa_dims* d, void* ws, size_t ws_bytes) {
+  pa_status why = PA_OK;
+  if (!dims_ok(d, &why)) return why;
+  if (!ws) return PA_ERR_NULL;
+  if (!aligned16(ws)) return PA_ERR_ALIGN;
+  if (ws_bytes < ws_layout(d).total) return PA_ERR_WORKSPACE;
+  return PA_OK;
+}
+
+// Validation shared by every call: dims, workspace, then the given pointers
+// (all required, 16-byte aligned), then the device.
+pa_status check_call(const pa_dims* d, void* ws, size_t ws_bytes, std::initializer_list<const void*> required,
+                     const int32_t* seg) {
+  pa_status s = common_checks(d, ws, ws_bytes);
+  if (s != PA_OK) return s;
+  for (const void* x : required)
+    if (!x) return PA_ERR_NULL;
+  for (const void* x : required)
+    if (!aligned16(x)) return PA_ERR_ALIGN;
+  if (seg && !aligned16(seg)) return PA_ERR_ALIGN;
+  return device_ok();
+}
+
+inline cudaStream_t cu(pa_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+pa_status step_tile_table(const pa_dims* d, const int32_t* seg, void* ws, size_t ws_bytes, pa_stream_t stream) {
+  pa_status s = check_call(d, ws, ws_bytes, {}, seg);
+  if (s != PA_OK) return s;
+  pa::AttnParams p = make_params(d, seg, ws);
+  return pa::launch_tile_table(p, const_cast<int4*>(p.tiles), cu(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status step_fwd(const pa_dims* d, const void* q, const void* k, const void* v, const int32_t* seg, void* out,
+                   float* lse, void* ws, size_t ws_bytes, pa_stream_t stream) {
+  pa_status s = check_call(d, ws, ws_bytes, {q, k, v, out, lse}, seg);
+  if (s != PA_OK) return s;
+  pa::AttnParams p = make_params(d, seg, ws);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  return pa::launch_fwd(p, d->D, q, k, v, cu(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status step_delta(const pa_dims* d, const void* out, const void* dout, void* ws, size_t ws_bytes,
+                     pa_stream_t stream) {
+  pa_status s = check_call(d, ws, ws_bytes, {out, dout}, nullptr);
+  if (s != PA_OK) return s;
+  pa::AttnParams p = make_params(d, nullptr, ws);
+  p.o = static_cast<const __nv_bfloat16*>(out);
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  return pa::launch_delta(p, d->D, cu(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status step_dq(const pa_dims* d, const void* q, const void* k, const void* v, const void* dout,
+                  const float* lse, const int32_t* seg, void* dq, void* ws, size_t ws_bytes, pa_stream_t stream) {
+  pa_status s = check_call(d, ws, ws_bytes, {q, k, v, dout, lse, dq}, seg);
+  if (s != PA_OK) return s;
+  pa::AttnParams p = make_params(d, seg, ws);
+  p.lse_in = lse;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  return pa::launch_bwd_dq(p, d->D, q, k, v, dout, cu(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status step_dkv(const pa_dims* d, const void* q, const void* k, const void* v, const void* dout,
+                   const float* lse, const int32_t* seg, void* dk, void* dv, void* ws, size_t ws_bytes,
+                   pa_stream_t stream) {
+  pa_status s = check_call(d, ws, ws_bytes, {q, k, v, dout, lse, dk, dv}, seg);
+  if (s != PA_OK) return s;
+  pa::AttnParams p = make_params(d, seg, ws);
+  p.lse_in = lse;
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  return pa::launch_bwd_dkv(p, d->D, q, k, v, dout, cu(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status fwd_impl(const pa_dims* d, const void* q, const void* k, const void* v, const int32_t* seg, void* out,
+                   float* lse, void* ws, size_t ws_bytes, pa_stream_t stream) {
+  pa_status s = check_call(d, ws, ws_bytes, {q, k, v, out, lse}, seg);
+  if (s != PA_OK) return s;
+  if ((s = step_tile_table(d, seg, ws, ws_bytes, stream)) != PA_OK) return s;
+  return step_fwd(d, q, k, v, seg, out, lse, ws, ws_bytes, stream);
+}
+
+pa_status bwd_impl(const pa_dims* d, const void* q, const void* k, const void* v, const void* out,
+                   const void* dout, const float* lse, const int32_t* seg, void* dq, void* dk, void* dv, void* ws,
+                   size_t ws_bytes, pa_stream_t stream) {
+  pa_status s = check_call(d, ws, ws_bytes, {q, k, v, out, dout, lse, dq, dk, dv}, seg);
+  if (s != PA_OK) return s;
+  if ((s = step_tile_table(d, seg, ws, ws_bytes, stream)) != PA_OK) return s;
+  if ((s = step_delta(d, out, dout, ws, ws_bytes, stream)) != PA_OK) return s;
+  if ((s = step_dq(d, q, k, v, dout, lse, seg, dq, ws, ws_bytes, stream)) != PA_OK) return s;
+  return step_dkv(d, q, k, v, dout, lse, seg, dk, dv, ws, ws_bytes, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_workspace_bytes(const pa_dims* dims) {
+  pa_status why;
+  if (!dims_ok(dims, &why)) return 0;
+  return ws_layout(dims).total;
+}
+
+pa_status pa_fwd(const pa_dims* dims, const void* q, const void* k, const void* v, const int32_t* seg, void* out,
+                 float* lse, void* ws, size_t ws_bytes, pa_stream_t stream) {
+  if (!seg) return PA_ERR_NULL;
+  return fwd_impl(dims, q, k, v, seg, out, lse, ws, ws_bytes, stream);
+}
+
+pa_status pa_fwd_causal(const pa_dims* dims, const void* q, const void* k, const void* v, void* out, float* lse,
+                        void* ws, size_t ws_bytes, pa_stream_t stream) {
+  return fwd_impl(dims, q, k, v, nullptr, out, lse, ws, ws_bytes, stream);
+}
+
+pa_status pa_bwd(const pa_dims* dims, const void* q, const void* k, const void* v, const void* out,
+                 const void* dout, const float* lse, const int32_t* seg, void* dq, void* dk, void* dv, void* ws,
+                 size_t ws_bytes, pa_stream_t stream) {
+  if (!seg) return PA_ERR_NULL;
+  return bwd_impl(dims, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream);
+}
+
+pa_status pa_bwd_causal(const pa_dims* dims, const void* q, const void* k, const void* v, const void* out,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv, void* ws,
+                        size_t ws_bytes, pa_stream_t stream) {
+  return bwd_impl(dims, q, k, v, out, dout, lse, nullptr, dq, dk, dv, ws, ws_bytes, stream);
+}
+
+pa_status pa_build_tile_table(const pa_dims* dims, const int32_t* seg, void* ws, size_t ws_bytes,
+                              pa_stream_t stream) {
+  return step_tile_table(dims, seg, ws, ws_bytes, stream);
+}
+
+pa_status pa_fwd_tiles(const pa_dims* dims, const void* q, const void* k, const void* v, const int32_t* seg,
+                       void* out, float* lse, void* ws, size_t ws_bytes, pa_stream_t stream) {
+  return step_fwd(dims, q, k, v, seg, out, lse, ws, ws_bytes, stream);
+}
+
+pa_status pa_bwd_delta(const pa_dims* dims, const void* out, const void* dout, void* ws, size_t ws_bytes,
+                       pa_stream_t stream) {
+  return step_delta(dims, out, dout, ws, ws_bytes, stream);
+}
+
+pa_status pa_bwd_dq(const pa_dims* dims, const void* q, const void* k, const void* v, const void* dout,
+                    const float* lse, const int32_t* seg, void* dq, void* ws, size_t ws_bytes, pa_stream_t stream) {
+  return step_dq(dims, q, k, v, dout, lse, seg, dq, ws, ws_bytes, stream);
+}
+
+pa_status pa_bwd_dkv(const pa_dims* dims, const void* q, const void* k, const void* v, const void* dout,
+                     const float* lse, const int32_t* seg, void* dk, void* dv, void* ws, size_t ws_bytes,
+                     pa_stream_t stream) {
+  return step_dkv(dims, q, k, v, dout, lse, seg, dk, dv, ws, ws_bytes, stream);
+}
+
+uint32_t pa_device_status(const void* ws, pa_stream_t stream) {
+  if (!ws) return 0xFFFFFFFFu;
+  uint32_t h = 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return 0xFFFFFFFFu;
+  if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return 0xFFFFFFFFu;
+  const uint32_t zero = 0;
+  if (cudaMemcpy(const_cast<void*>(ws), &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return 0xFFFFFFFFu;
+  return h;
+}
+
+const char* pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "ok";
+    case PA_ERR_NULL: return "a required pointer is NULL";
+    case PA_ERR_HEAD_DIM: return "head dim must be 64 or 128";
+    case PA_ERR_GQA: return "Hq must be a multiple of Hkv";
+    case PA_ERR_SHAPE: return "bad shape (B, H, N > 0; N % 128 == 0; B*Hq*N < 2^31; finite scale)";
+    case PA_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case PA_ERR_WORKSPACE: return "workspace too small (see pa_workspace_bytes)";
+    case PA_ERR_ARCH: return "device is not compute capability 10.3 (GB300)";
+    case PA_ERR_CUDA: return "a CUDA call or kernel launch failed";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

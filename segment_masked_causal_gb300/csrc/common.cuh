@@ -1,0 +1,85 @@
+// common.cuh -- definitions shared by the packed-attention kernels.
+//
+// Tiles are 128 tokens. For every (row b, tile t) the prologue kernel writes
+// one int4 {smin, smax, kv_lo, q_hi}:
+//   smin/smax  smallest / largest segment id inside the tile,
+//   kv_lo      first key tile <= t whose id range overlaps tile t's,
+//   q_hi       last query tile >= t whose id range overlaps tile t's.
+// A (query tile, key tile) pair can hold a visible pair only if the key tile
+// is not after the query tile and the two id ranges overlap; every other pair
+// is skipped without being computed (the changelog entry for the PACKED
+// kernels: cross-segment blocks are skipped; the 0.5.0 note in the README's
+// "Sequence packing": dK/dV ends its query walk at the key block's segment
+// end). Range overlap is a conservative test, so any id values stay correct;
+// contiguous runs (what packing produces) make it exact at tile granularity.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+
+namespace pa {
+
+constexpr int kTile = 128;
+
+struct AttnParams {
+  int B, Hq, Hkv, N, T, G;
+  float scale;       // softmax scale
+  float scale_log2;  // scale * log2(e)
+  const int32_t* seg;   // (B, N) or null (every token in one segment)
+  const int4* tiles;    // (B, T) table written by the prologue
+  uint32_t* status;     // device status word
+  // forward outputs
+  __nv_bfloat16* out;
+  float* lse;
+  // backward
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* dout;
+  const float* lse_in;
+  float* delta;  // (B, Hq, N), written by the delta kernel
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+};
+
+__device__ __forceinline__ bool tiles_overlap(int4 a, int4 b) { return a.x <= b.y && b.x <= a.y; }
+
+// Every element of the (query tile, key tile) pair is visible: strictly below
+// the diagonal and both tiles inside one and the same segment.
+__device__ __forceinline__ bool tile_pair_full(int tq, int4 q, int tk, int4 k) {
+  return tk < tq && q.x == q.y && k.x == k.y && q.x == k.x;
+}
+
+// Key tiles a query tile visits, in increasing order.
+struct KvWalk {
+  const int4* row;  // tiles of this batch row
+  int tq;
+  int4 qt;
+  __device__ __forceinline__ KvWalk(const int4* r, int tq_) : row(r), tq(tq_), qt(r[tq_]) {}
+  __device__ __forceinline__ int first() const { return next(qt.z - 1); }
+  __device__ __forceinline__ int next(int tk) const {
+    for (++tk; tk < tq; ++tk)
+      if (tiles_overlap(row[tk], qt)) return tk;
+    return tk;  // tq itself: the diagonal tile always holds visible pairs
+  }
+  __device__ __forceinline__ int count() const {
+    int n = 0;
+    for (int tk = first(); tk <= tq; tk = next(tk)) ++n;
+    return n;
+  }
+};
+
+// Query tiles a key tile is visited by, in increasing order.
+struct QWalk {
+  const int4* row;
+  int tk;
+  int4 kt;
+  __device__ __forceinline__ QWalk(const int4* r, int tk_) : row(r), tk(tk_), kt(r[tk_]) {}
+  __device__ __forceinline__ int first() const { return tk; }
+  __device__ __forceinline__ int next(int tq) const {
+    for (++tq; tq <= kt.w; ++tq)
+      if (tiles_overlap(row[tq], kt)) return tq;
+    return kt.w + 1;
+  }
+  __device__ __forceinline__ int end() const { return kt.w + 1; }
+};
+
+}  // namespace pa

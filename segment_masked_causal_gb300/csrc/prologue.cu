@@ -1,0 +1,111 @@
+// prologue.cu -- the segment-range tile table and the delta preprocess.
+//
+// Tile table: for each 128-token tile of each batch row, the smallest and
+// largest segment id it holds, the first key tile whose id range overlaps it
+// (the first key tile a query tile must visit) and the last query tile whose
+// range overlaps it (where a key tile's query walk ends: mlx-train-perf 0.5.1
+// README, "Sequence packing", the 0.5.0 dK/dV change). With seg == null every
+// token is in segment 0.
+//
+// Delta: D_i = <dO_i, O_i>, the per-row term of the softmax backward
+// (dS = P * (dP - D)); one fp32 value per query row, read by both backward
+// kernels. Bandwidth-bound: 16-byte loads, rows split over D/8 lanes and
+// reduced with shuffles.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pa {
+
+namespace {
+
+__global__ void __launch_bounds__(256) tile_table_kernel(const int32_t* __restrict__ seg, int N, int T,
+                                                         int4* __restrict__ tiles, uint32_t* status) {
+  extern __shared__ int2 mm[];  // T entries {min, max}
+  const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (b == 0 && threadIdx.x == 0 && status) *status = 0u;
+  for (int t = warp; t < T; t += blockDim.x >> 5) {
+    int lo = 0, hi = 0;
+    if (seg) {
+      const int4 v = reinterpret_cast<const int4*>(seg + (size_t)b * N + (size_t)t * kTile)[lane];
+      lo = min(min(v.x, v.y), min(v.z, v.w));
+      hi = max(max(v.x, v.y), max(v.z, v.w));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(~0u, lo, o));
+        hi = max(hi, __shfl_xor_sync(~0u, hi, o));
+      }
+    }
+    if (lane == 0) mm[t] = make_int2(lo, hi);
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {
+    const int2 me = mm[t];
+    int lo = t, hi = t;
+    for (int u = 0; u < t; ++u)
+      if (mm[u].x <= me.y && me.x <= mm[u].y) { lo = u; break; }
+    for (int u = T - 1; u > t; --u)
+      if (mm[u].x <= me.y && me.x <= mm[u].y) { hi = u; break; }
+    tiles[(size_t)b * T + t] = make_int4(me.x, me.y, lo, hi);
+  }
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <int D>
+__global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restrict__ o,
+                                                    const __nv_bfloat16* __restrict__ dout,
+                                                    float* __restrict__ delta, size_t rows) {
+  constexpr int LPR = D / 8;  // lanes per row
+  const size_t gtid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  const int sub = threadIdx.x % LPR;
+  for (size_t t = gtid; t < rows * LPR; t += stride) {
+    const size_t row = t / LPR;
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + row * D) + sub);
+    const uint4 c = __ldg(reinterpret_cast<const uint4*>(dout + row * D) + sub);
+    float acc = bf16lo(a.x) * bf16lo(c.x);
+    acc = fmaf(bf16hi(a.x), bf16hi(c.x), acc);
+    acc = fmaf(bf16lo(a.y), bf16lo(c.y), acc);
+    acc = fmaf(bf16hi(a.y), bf16hi(c.y), acc);
+    acc = fmaf(bf16lo(a.z), bf16lo(c.z), acc);
+    acc = fmaf(bf16hi(a.z), bf16hi(c.z), acc);
+    acc = fmaf(bf16lo(a.w), bf16lo(c.w), acc);
+    acc = fmaf(bf16hi(a.w), bf16hi(c.w), acc);
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(~0u, acc, off);
+    if (sub == 0) delta[row] = acc;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_tile_table(const AttnParams& p, int4* tiles, cudaStream_t st) {
+  const size_t smem = (size_t)p.T * sizeof(int2);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(tile_table_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  tile_table_kernel<<<p.B, 256, smem, st>>>(p.seg, p.N, p.T, tiles, p.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_delta(const AttnParams& p, int D, cudaStream_t st) {
+  const size_t rows = (size_t)p.B * p.Hq * p.N;
+  const size_t threads = rows * (size_t)(D / 8);
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  size_t blocks = (threads + 255) / 256;
+  const size_t cap = (size_t)sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (D == 128)
+    delta_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.delta, rows);
+  else
+    delta_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.delta, rows);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,230 @@
+"""Helpers shared by the GPU tests: move a seeded workload to the device, run
+the library through its C ABI, and compare with the fp64 oracle on full
+tensors or on sampled rows."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import segment_masked_causal_gb300 as pa
+import synth
+
+# the benchmark spec tolerances for the path
+O_MAXABS = 1e-2
+GRAD_RELL2 = 2e-2
+LSE_MAXABS = 1e-3
+
+
+def bits_to_torch(bits: np.ndarray, dev) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+class Case:
+    """A workload with its bf16 inputs on the device and fp64 copies on the host."""
+
+    def __init__(self, w: synth.Workload, dev, host64: bool = True):
+        self.w = w
+        t = w.tensors()
+        self.bits = t
+        self.q, self.k, self.v, self.do = (bits_to_torch(t[x], dev) for x in ("q", "k", "v", "do"))
+        self.seg = torch.from_numpy(w.seg).to(dev)
+        self.ws = pa.workspace(self.q, self.k)
+        self._h = None
+        self.host64 = host64
+
+    @property
+    def h(self):
+        if self._h is None:
+            self._h = {x: synth.bf16_bits_to_f64(self.bits[x]) for x in ("q", "k", "v", "do")}
+        return self._h
+
+    def run(self, causal: bool = False):
+        q, k, v, do = self.q, self.k, self.v, self.do
+        seg = None if causal else self.seg
+        out, lse = pa.forward(q, k, v, seg, ws=self.ws)
+        dq, dk, dv = pa.backward(q, k, v, out, do, lse, seg, ws=self.ws)
+        torch.cuda.synchronize()
+        st = pa.pa_device_status(self.ws)
+        assert st == 0, f"device status {st:#x}"
+        return {"o": out, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+
+    def oracle_full(self, causal: bool = False):
+        h = self.h
+        return oracle.attention(h["q"], h["k"], h["v"], None if causal else self.w.seg, self.w.scale, h["do"])
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def rel_l2(a: np.ndarray, b: np.ndarray) -> float:
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def assert_full_parity(gpu: dict, ref: dict, tag: str = ""):
+    o_err = np.abs(f64(gpu["o"]) - ref["o"]).max()
+    l_err = np.abs(f64(gpu["lse"]) - ref["lse"]).max()
+    errs = {n: rel_l2(f64(gpu[n]), ref[n]) for n in ("dq", "dk", "dv")}
+    msg = f"{tag} o_maxabs={o_err:.3e} lse_maxabs={l_err:.3e} " + " ".join(f"{n}={e:.3e}" for n, e in errs.items())
+    assert o_err <= O_MAXABS, msg
+    assert l_err <= LSE_MAXABS, msg
+    for n, e in errs.items():
+        assert e <= GRAD_RELL2, msg
+    return msg
+
+
+# ------------------------------------------------------------------ sampling
+def sample_query_rows(w: synth.Workload, n_random: int = 48, heads=None, seed: int = 0) -> np.ndarray:
+    """Flat (b, h, i) rows: segment starts and ends, tile edges, first/last
+    rows, plus random rows, over a few heads."""
+    rng = np.random.default_rng(seed)
+    heads = heads if heads is not None else sorted({0, w.Hq // 2, w.Hq - 1})
+    rows = set()
+    for b in range(w.B):
+        starts = np.concatenate([[0], np.cumsum(w.lengths[b])[:-1]])
+        ends = np.cumsum(w.lengths[b]) - 1
+        pos = set(starts[:8].tolist()) | set(ends[:8].tolist()) | set(starts[-4:].tolist()) | set(ends[-4:].tolist())
+        pos |= {0, 1, 127, 128, 129, w.N - 129, w.N - 128, w.N - 1}
+        pos |= set(rng.integers(0, w.N, n_random).tolist())
+        for h in heads:
+            for i in pos:
+                if 0 <= i < w.N:
+                    rows.add((b * w.Hq + h) * w.N + int(i))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def sample_key_rows(w: synth.Workload, n: int = 24, max_walk: int = 700, seed: int = 1) -> np.ndarray:
+    """Flat (b, hk, j) key rows whose oracle needs at most `max_walk` query
+    rows of its own segment (i >= j): segment ends and a few rows before them."""
+    rng = np.random.default_rng(seed)
+    rows = set()
+    heads = sorted({0, w.Hkv - 1})
+    for b in range(w.B):
+        starts = np.concatenate([[0], np.cumsum(w.lengths[b])[:-1]])
+        ends = np.cumsum(w.lengths[b])  # exclusive
+        for s, e in zip(starts, ends):
+            cand = [e - 1, max(s, e - 2), max(s, e - 129), max(s, e - 128)]
+            if e - s <= max_walk:
+                cand.append(s)
+            cand += list(rng.integers(max(s, e - max_walk), e, 2))
+            for j in cand:
+                for g in heads:
+                    rows.add((b * w.Hkv + g) * w.N + int(j))
+    rows = np.array(sorted(rows), dtype=np.int64)
+    if len(rows) > n * w.B * len(heads):
+        rows = np.sort(rng.choice(rows, n * w.B * len(heads), replace=False))
+    return rows
+
+
+def needed_query_rows(w: synth.Workload, krows: np.ndarray) -> np.ndarray:
+    G = w.Hq // w.Hkv
+    out = set()
+    for r in krows:
+        j = int(r % w.N)
+        bg = int(r // w.N)
+        g, b = bg % w.Hkv, bg // w.Hkv
+        idx = np.nonzero(w.seg[b, j:] == w.seg[b, j])[0] + j
+        for h in range(g * G, (g + 1) * G):
+            out.update(((b * w.Hq + h) * w.N + idx).tolist())
+    return np.array(sorted(out), dtype=np.int64)
+
+
+def assert_sampled_parity(case: Case, gpu: dict, causal: bool = False, tag: str = "", qrows=None, krows=None):
+    w, h = case.w, case.h
+    seg = None if causal else w.seg
+    D = w.D
+    qrows = sample_query_rows(w) if qrows is None else qrows
+    krows = sample_key_rows(w) if krows is None else krows
+    need = np.union1d(qrows, needed_query_rows(w, krows) if not causal else _needed_causal(w, krows))
+    o, lse, delta = oracle.forward(h["q"], h["k"], h["v"], seg, w.scale, h["do"], rows=need)
+    lse_full = np.full(w.B * w.Hq * w.N, np.nan)
+    dl_full = np.full(w.B * w.Hq * w.N, np.nan)
+    lse_full[need] = lse
+    dl_full[need] = delta
+    pos = np.searchsorted(need, qrows)
+    go = f64(gpu["o"]).reshape(-1, D)[qrows]
+    o_err = np.abs(go - o[pos]).max()
+    l_err = np.abs(f64(gpu["lse"]).reshape(-1)[qrows] - lse[pos]).max()
+    dq = oracle.dq(h["q"], h["k"], h["v"], seg, w.scale, h["do"], lse_full.reshape(w.B, w.Hq, w.N),
+                   dl_full.reshape(w.B, w.Hq, w.N), rows=qrows)
+    dq_err = rel_l2(f64(gpu["dq"]).reshape(-1, D)[qrows], dq)
+    dk, dv = oracle.dkv(h["q"], h["k"], h["v"], seg, w.scale, h["do"], lse_full.reshape(w.B, w.Hq, w.N),
+                        dl_full.reshape(w.B, w.Hq, w.N), rows=krows)
+    assert np.isfinite(dk).all() and np.isfinite(dv).all(), "oracle read an lse/delta it was not given"
+    dk_err = rel_l2(f64(gpu["dk"]).reshape(-1, D)[krows], dk)
+    dv_err = rel_l2(f64(gpu["dv"]).reshape(-1, D)[krows], dv)
+    msg = (f"{tag} rows={len(qrows)}/{len(krows)} o_maxabs={o_err:.3e} lse_maxabs={l_err:.3e} "
+           f"dq={dq_err:.3e} dk={dk_err:.3e} dv={dv_err:.3e}")
+    assert o_err <= O_MAXABS, msg
+    assert l_err <= LSE_MAXABS, msg
+    assert dq_err <= GRAD_RELL2 and dk_err <= GRAD_RELL2 and dv_err <= GRAD_RELL2, msg
+    return msg
+
+
+def _needed_causal(w, krows):
+    G = w.Hq // w.Hkv
+    out = set()
+    for r in krows:
+        j = int(r % w.N)
+        bg = int(r // w.N)
+        g, b = bg % w.Hkv, bg // w.Hkv
+        idx = np.arange(j, w.N)
+        for h in range(g * G, (g + 1) * G):
+            out.update(((b * w.Hq + h) * w.N + idx).tolist())
+    return np.array(sorted(out), dtype=np.int64)
+
+
+def assert_segment_sums(case: Case, gpu: dict, tol: float = 1e-2, min_len: int = 16):
+    """Rows of P sum to 1 and rows of dS to 0, so over each segment
+    sum_j dk_j = 0 and sum_j dv_j = sum over the group's heads of sum_i dO_i.
+    Bound: each bf16 output is within ~1e-2 of its exact value relative to the
+    typical magnitude, so the sum's error is below tol times the segment's L1
+    mass plus L times the tensor's mean magnitude (the floor keeps segments
+    whose gradients are ~0, such as length-1 ones, from dividing 0 by 0).
+    Segments shorter than `min_len` are skipped: there the exact sums cancel so
+    far that the known rounding terms dominate (delta uses the bf16 output, so
+    each row's sum of dS is off by dO.(o - bf16(o)); simulated with every bf16
+    rounding of the path, the ratio reaches 5e-2 at length 2, 9e-3 at 4 and
+    stays below 3e-3 from 13 on). Short segments are covered element by
+    element elsewhere."""
+    w = case.w
+    G = w.Hq // w.Hkv
+    dk = gpu["dk"].float()
+    dv = gpu["dv"].float()
+    do = case.do.float()
+    worst = 0.0
+    gk = float(dk.abs().mean())
+    for b in range(w.B):
+        start = 0
+        for L in w.lengths[b]:
+            sl = slice(start, start + L)
+            sk = dk[b, :, sl].sum(1)
+            mk = dk[b, :, sl].abs().sum(1) + L * gk + 1e-30
+            sv = dv[b, :, sl].sum(1)
+            ref = do[b, :, sl].sum(1).reshape(w.Hkv, G, w.D).sum(1)
+            mv = dv[b, :, sl].abs().sum(1) + do[b, :, sl].abs().sum(1).reshape(w.Hkv, G, w.D).sum(1) + 1e-6
+            worst = max(worst, float((sk.abs() / mk).max()), float(((sv - ref).abs() / mv).max()))
+            start += L
+    assert worst <= tol, f"segment-sum invariant violated: {worst:.3e}"
+    return worst
+
+
+def assert_group_parity(case: Case, gpu: dict, hk: int, tag: str = ""):
+    """Every output element of one kv group (its G query heads for o, lse, dq;
+    the kv head for dk, dv) against the oracle, all batch rows."""
+    w, h = case.w, case.h
+    G = w.Hq // w.Hkv
+    sl = slice(hk * G, (hk + 1) * G)
+    sub = {x: h[x][:, sl] for x in ("q", "do")}
+    kv = {x: h[x][:, hk:hk + 1] for x in ("k", "v")}
+    ref = oracle.attention(sub["q"], kv["k"], kv["v"], w.seg, w.scale, sub["do"])
+    got = {"o": gpu["o"][:, sl], "lse": gpu["lse"][:, sl], "dq": gpu["dq"][:, sl],
+           "dk": gpu["dk"][:, hk:hk + 1], "dv": gpu["dv"][:, hk:hk + 1]}
+    msg = assert_full_parity(got, ref, tag)
+    # no single key row may be far off even if the tensor-wide norm is fine
+    for n in ("dk", "dv"):
+        a, b = f64(got[n]).reshape(-1, w.D), ref[n].reshape(-1, w.D)
+        row_err = np.linalg.norm(a - b, axis=1) / (np.linalg.norm(b, axis=1) + np.sqrt(w.D) * np.abs(b).mean())
+        assert row_err.max() <= 0.1, f"{tag} worst {n} row {row_err.argmax()} err {row_err.max():.3e}"
+    return msg

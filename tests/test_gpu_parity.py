@@ -1,0 +1,131 @@
+"""GPU results against the fp64 oracle (through the C ABI).
+
+Tolerances (the target's): O max-abs <= 1e-2 over every compared element;
+dQ/dK/dV relative L2 <= 2e-2 over every compared element; lse max-abs 1e-3.
+Small cases compare every element; the full-size workloads compare rows the
+oracle computes one by one (segment starts/ends, tile edges, random rows) and
+check per-segment gradient sums, which hold at any size. The packed kernels
+with a single segment must be bit-identical to the causal kernels (changelog
+entry adding the PACKED kernels). Dropping the segment mask must fail the
+tolerance (mlx-train-perf 0.5.1 README, "Sequence packing": contamination
+test).
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from _gpu_common import (Case, assert_full_parity, assert_group_parity, assert_sampled_parity,
+                         assert_segment_sums, f64, O_MAXABS)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from segment_masked_causal_gb300 import build
+    build.build()
+
+
+SMALL = [
+    ("tiny_3seg", synth.workload("tiny_3seg")),
+    ("tiny_fixed_1_100_155", synth.workload("tiny_fixed_1_100_155")),
+    ("ragged_gqa_d128", synth.custom(2, 4, 2, 512, 128, [[1, 130, 5, 120, 256], [512]], seed=21)),
+    ("many_len3_d64", synth.custom(1, 2, 1, 384, 64, [[3] * 128], seed=22)),
+    ("len1_runs_d128", synth.custom(1, 2, 2, 256, 128, [[1] * 40 + [88, 128]], seed=23)),
+    ("gqa8_d64", synth.custom(1, 8, 1, 640, 64, [[300, 213, 127]], seed=24)),
+]
+
+
+@pytest.mark.parametrize("name,w", SMALL, ids=[n for n, _ in SMALL])
+def test_small_full_parity(name, w, cuda_dev):
+    c = Case(w, cuda_dev)
+    print(assert_full_parity(c.run(), c.oracle_full(), name))
+
+
+def test_causal_entry_points_full_parity(cuda_dev):
+    w = synth.custom(1, 4, 1, 384, 128, [[384]], seed=25)
+    c = Case(w, cuda_dev)
+    print(assert_full_parity(c.run(causal=True), c.oracle_full(causal=True), "causal"))
+
+
+def test_non_contiguous_ids_full_parity(cuda_dev):
+    """Ids are compared for equality only: a sequence id may reappear later
+    in the row and its tokens still see each other."""
+    w = synth.custom(1, 2, 2, 512, 128, [[100, 100, 100, 212]], seed=26)
+    w.seg[0] = np.array([5] * 100 + [9] * 100 + [5] * 100 + [-3] * 212, np.int32)
+    c = Case(w, cuda_dev)
+    print(assert_full_parity(c.run(), c.oracle_full(), "noncontig"))
+
+
+def test_causal_2k_gqa(cuda_dev):
+    w = synth.workload("causal_2k_gqa")
+    c = Case(w, cuda_dev)
+    g = c.run()
+    print(assert_sampled_parity(c, g, tag=w.name))
+    assert_segment_sums(c, g)
+
+
+def test_packed_4x4096_short(cuda_dev):
+    w = synth.workload("packed_4x4096_short")
+    c = Case(w, cuda_dev)
+    g = c.run()
+    print(assert_sampled_parity(c, g, tag=w.name))
+    assert_segment_sums(c, g)
+    # every element of two whole kv groups (short segments make this cheap)
+    for hk in (0, w.Hkv - 1):
+        print(assert_group_parity(c, g, hk, tag=f"{w.name} group {hk}"))
+
+
+def test_8k_packed_group_full(cuda_dev):
+    w = synth.workload("8k_packed")
+    c = Case(w, cuda_dev)
+    print(assert_group_parity(c, c.run(), 3, tag="8k_packed group 3"))
+
+
+@pytest.mark.parametrize("name", ["8k_one_segment", "8k_packed"])
+def test_8k(name, cuda_dev):
+    w = synth.workload(name)
+    c = Case(w, cuda_dev)
+    g = c.run()
+    print(assert_sampled_parity(c, g, tag=name))
+    assert_segment_sums(c, g)
+
+
+@pytest.mark.parametrize("name", ["long_32k_one_segment", "long_32k_packed", "long_64k_one_segment",
+                                  "long_64k_packed"])
+def test_long_context(name, cuda_dev):
+    w = synth.workload(name)
+    c = Case(w, cuda_dev)
+    g = c.run()
+    print(assert_sampled_parity(c, g, tag=name))
+    assert_segment_sums(c, g)
+
+
+@pytest.mark.parametrize("name", ["causal_2k_gqa", "8k_one_segment", "long_32k_one_segment"])
+def test_single_segment_bit_identical_to_causal(name, cuda_dev):
+    w = synth.workload(name)
+    c = Case(w, cuda_dev)
+    packed = c.run()
+    causal = c.run(causal=True)
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        assert torch.equal(packed[n].view(torch.int16) if packed[n].dtype == torch.bfloat16 else packed[n].view(torch.int32),
+                           causal[n].view(torch.int16) if causal[n].dtype == torch.bfloat16 else causal[n].view(torch.int32)), n
+
+
+def test_runs_are_deterministic(cuda_dev):
+    c = Case(synth.workload("packed_4x4096_short"), cuda_dev)
+    a, b = c.run(), c.run()
+    for n in a:
+        assert torch.equal(a[n], b[n]), n
+
+
+def test_dropping_the_mask_fails_parity(cuda_dev):
+    """Negative control: the causal kernel on a packed row must miss the
+    packed oracle by far more than the tolerance."""
+    w = synth.workload("tiny_3seg")
+    c = Case(w, cuda_dev)
+    ref = c.oracle_full()
+    wrong = c.run(causal=True)
+    err = np.abs(f64(wrong["o"]) - ref["o"]).max()
+    assert err > 10 * O_MAXABS, err
