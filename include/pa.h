@@ -131,6 +131,34 @@ pa_status pa_bwd_dkv(const pa_dims* dims, const void* q, const void* k, const vo
                      pa_stream_t stream);
 
 /*
+ * Backward without a caller workspace, for callers that cannot allocate device
+ * memory when they run it: code inside a region where its allocator or memory
+ * pool forbids new allocations, or a host runtime that only hands out its own
+ * tensors. The pages have no counterpart; this is a deployment convenience.
+ *
+ * Same arguments and results as pa_bwd (seg may be NULL for plain causal, as
+ * in pa_bwd_causal), minus the workspace: the scratch lives in one static
+ * device array of PA_NOALLOC_SCRATCH_BYTES (8 MiB) inside the library, held by
+ * every GPU that loads the library until the process exits. The call makes no
+ * allocation of any kind.
+ *   - Limit: dims whose pa_workspace_bytes exceeds PA_NOALLOC_SCRATCH_BYTES
+ *     (about B*Hq*N > 2 million query rows) are refused with PA_ERR_WORKSPACE.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last call's
+ *     contents (the call itself resets what must start at zero). Calls whose
+ *     kernels overlap on the GPU -- on different streams, or from different
+ *     threads -- race on it and corrupt each other's results: serialise them.
+ *   - device_status: if not NULL, the call waits for its kernels and stores
+ *     the device status word there (0 = healthy, else PA_DEVERR_* bits);
+ *     if NULL, the call returns without synchronising.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+pa_status pa_bwd_noalloc(const pa_dims* dims, const void* q, const void* k, const void* v, const void* out,
+                         const void* dout, const float* lse, const int32_t* seg, void* dq, void* dk, void* dv,
+                         uint32_t* device_status, pa_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns the workspace's device status word
  * (0 = healthy; PA_DEVERR_* bits otherwise) and clears it. Returns
  * 0xFFFFFFFF if the read itself fails.

@@ -26,7 +26,8 @@ PA_OK = 0
 STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_NULL", 2: "PA_ERR_HEAD_DIM", 3: "PA_ERR_GQA", 4: "PA_ERR_SHAPE",
                 5: "PA_ERR_ALIGN", 6: "PA_ERR_WORKSPACE", 7: "PA_ERR_ARCH", 8: "PA_ERR_CUDA"}
 EXPORTS = ["pa_workspace_bytes", "pa_fwd", "pa_bwd", "pa_fwd_causal", "pa_bwd_causal", "pa_build_tile_table",
-           "pa_fwd_tiles", "pa_bwd_delta", "pa_bwd_dq", "pa_bwd_dkv", "pa_device_status", "pa_status_string"]
+           "pa_fwd_tiles", "pa_bwd_delta", "pa_bwd_dq", "pa_bwd_dkv", "pa_bwd_noalloc", "pa_device_status",
+           "pa_status_string"]
 
 
 class LibraryMissing(RuntimeError):
@@ -72,6 +73,8 @@ def lib():
             for f in ("pa_fwd", "pa_fwd_causal", "pa_bwd", "pa_bwd_causal", "pa_build_tile_table", "pa_fwd_tiles",
                       "pa_bwd_delta", "pa_bwd_dq", "pa_bwd_dkv"):
                 getattr(L, f).restype = ctypes.c_int
+            L.pa_bwd_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P, P, ctypes.POINTER(ctypes.c_uint32), P]
+            L.pa_bwd_noalloc.restype = ctypes.c_int
             L.pa_device_status.argtypes = [P, P]
             L.pa_device_status.restype = ctypes.c_uint32
             L.pa_status_string.argtypes = [ctypes.c_int]
@@ -208,6 +211,22 @@ def pa_bwd_dkv(q, k, v, dout, lse, seg, dk, dv, ws, scale=0.0, stream=None):
                             _ptr(dout, bf, "dout"), _ptr(lse, torch.float32, "lse"), _ptr(seg, torch.int32, "seg"),
                             _ptr(dk, bf, "dk"), _ptr(dv, bf, "dv"), _ptr(ws, None, "ws"), ws.numel(),
                             _stream(stream)))
+
+
+def pa_bwd_noalloc(q, k, v, out, dout, lse, seg, dq, dk, dv, scale=0.0, stream=None, wait_status=False):
+    """pa_bwd without a workspace, for callers that cannot allocate device
+    memory (the scratch is a fixed 8 MiB array inside the library). Returns the
+    device status word when wait_status is true (the call then synchronises),
+    else None. Calls that overlap on the GPU share that array and race."""
+    import torch
+    bf = torch.bfloat16
+    d = _dims_of(q, k, scale)
+    st = ctypes.c_uint32(0xFFFFFFFF)
+    _check(lib().pa_bwd_noalloc(ctypes.byref(d), _ptr(q, bf, "q"), _ptr(k, bf, "k"), _ptr(v, bf, "v"),
+                                _ptr(out, bf, "out"), _ptr(dout, bf, "dout"), _ptr(lse, torch.float32, "lse"),
+                                _ptr(seg, torch.int32, "seg"), _ptr(dq, bf, "dq"), _ptr(dk, bf, "dk"),
+                                _ptr(dv, bf, "dv"), ctypes.byref(st) if wait_status else None, _stream(stream)))
+    return int(st.value) if wait_status else None
 
 
 def pa_device_status(ws, stream=None) -> int:
