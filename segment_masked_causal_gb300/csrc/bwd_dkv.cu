@@ -5,16 +5,23 @@
 // the last tile whose segment range overlaps the key tile's -- the query walk
 // ends at the key block's segment end instead of masking the rest
 // (mlx-train-perf 0.5.1 README, "Sequence packing", the 0.5.0 dK/dV change).
-// Per visited (query head, query tile), with K and V resident:
-//   S^T  = K Q^T   (TMEM)        P^T  = exp(scale * S^T - lse)      (bf16 smem)
-//   dP^T = V dO^T  (TMEM)        dS^T = P^T * (dP^T - delta)         (bf16 smem)
-//   dV += P^T dO   dK += dS^T Q  (TMEM accumulators)
+// Every query tile is processed as two 64-row halves ("steps"). Per step, with
+// K and V resident in shared memory:
+//   S^T  = K Q^T   (TMEM, 64 columns)   P^T  = exp(scale * S^T - lse)
+//   dP^T = V dO^T  (TMEM, 64 columns)   dS^T = P^T * (dP^T - delta)
+//   dV += P^T dO   dK += dS^T Q         (TMEM accumulators; P^T and dS^T are
+//                                        written back as bf16 over S^T and fed
+//                                        to the MMA straight from TMEM)
 // and finally dK *= scale. The group's heads are summed inside the CTA in a
 // fixed order, so dK/dV need no atomics and are deterministic.
 //
-// Warp roles: warp 0 TMA producer (Q, dO tiles plus the query tile's lse,
-// delta and segment ids), warp 1 MMA issuer and TMEM owner, warps 2..5 one
-// key row per thread.
+// Pipelining: S^T/dP^T of a step live in one of two TMEM buffers, so the MMA
+// issuer starts step i+1's S^T and dP^T before step i's gradient MMAs and the
+// tensor core runs while the softmax warps work on step i.
+//
+// Warp roles: warp 0 TMA producer (Q, dO halves plus their lse, delta and
+// segment ids through a 4-stage ring), warp 1 MMA issuer and TMEM owner,
+// warps 2..9 softmax: two threads per key row, 32 query columns each.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -28,39 +35,40 @@ namespace {
 
 template <int D>
 struct DkvLayout {
-  static constexpr int NSQ = (D == 128) ? 1 : 2;
-  static constexpr uint32_t KV_BYTES = 128 * D * 2;
-  static constexpr uint32_t Q_BYTES = 128 * D * 2;
-  static constexpr uint32_t PT_BYTES = 128 * 128 * 2;
+  static constexpr int NS = 4;                           // Q/dO half-tile stages
+  static constexpr uint32_t KV_BYTES = 128 * D * 2;      // one K or V tile
+  static constexpr uint32_t QH_BYTES = 64 * D * 2;       // one 64-row half tile of Q or dO
+  static constexpr uint32_t KV_CHUNK = 128 * 128;        // one 64-column chunk of a 128-row tile
+  static constexpr uint32_t QH_CHUNK = 64 * 128;         // one 64-column chunk of a 64-row tile
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
   static constexpr uint32_t OFF_Q = OFF_V + KV_BYTES;
-  static constexpr uint32_t OFF_DO = OFF_Q + NSQ * Q_BYTES;
-  static constexpr uint32_t OFF_P = OFF_DO + NSQ * Q_BYTES;
-  static constexpr uint32_t OFF_DS = OFF_P + PT_BYTES;
-  static constexpr uint32_t TILE_BYTES = OFF_DS + PT_BYTES;
+  static constexpr uint32_t OFF_DO = OFF_Q + NS * QH_BYTES;
+  static constexpr uint32_t TILE_BYTES = OFF_DO + NS * QH_BYTES;
   static constexpr uint32_t MISC_BYTES = 4096;
   static constexpr uint32_t SMEM = TILE_BYTES + MISC_BYTES + 1024;
-  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D, TMEM_COLS = 512;
+  // TMEM: dV, dK accumulators, then two step buffers of 128 columns each
+  // (S^T in the first 64, dP^T in the second 64)
+  static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_BUF = 2 * D, TMEM_COLS = 512;
 };
 
 struct DkvMisc {
-  uint64_t kv_full, q_full[2], q_empty[2];
-  uint64_t s_full, s_empty, pds_full, grad_done, mma_final;
+  uint64_t kv_full, q_full[4], q_empty[4];
+  uint64_t s_full[2], pds_full[2], grad_done[2], mma_final;
   uint32_t tmem_base;
   int abort_flag;
-  alignas(16) float lse[2][128];
-  alignas(16) float dl[2][128];
-  alignas(16) int32_t segq[2][128];
+  alignas(16) float lse[4][64];
+  alignas(16) float dl[4][64];
+  alignas(16) int32_t segq[4][64];
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const AttnParams p) {
   using L = DkvLayout<D>;
-  constexpr int NSQ = L::NSQ;
+  constexpr int NS = L::NS;
   static_assert(sizeof(DkvMisc) <= L::MISC_BYTES, "misc region");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   DkvMisc& m = *reinterpret_cast<DkvMisc*>(smem_raw);
@@ -68,13 +76,12 @@ __global__ void __launch_bounds__(192, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + sizeof(DkvMisc) + 1023) & ~uintptr_t(1023));
   const uint32_t sK = smem_u32(base + L::OFF_K), sV = smem_u32(base + L::OFF_V);
   const uint32_t sQ = smem_u32(base + L::OFF_Q), sDO = smem_u32(base + L::OFF_DO);
-  const uint32_t sP = smem_u32(base + L::OFF_P), sDS = smem_u32(base + L::OFF_DS);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // key tiles near the end of a row have the shortest causal walks: start the
-  // longest ones first
-  const int tk = (int)blockIdx.x;
-  const int hk = blockIdx.y, b = blockIdx.z;
+  // heaviest causal walks (smallest key tile index) first, across all heads
+  const int per_tile = p.Hkv * p.B;
+  const int tk = (int)blockIdx.x / per_tile;
+  const int hk = (int)blockIdx.x % p.Hkv, b = ((int)blockIdx.x / p.Hkv) % p.B;
   const int4* trow = p.tiles + (size_t)b * p.T;
   const Guard g{&m.abort_flag, p.status};
   const QWalk walk(trow, tk);
@@ -83,19 +90,20 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     m.abort_flag = 0;
     mbar_init(&m.kv_full, 1);
-    for (int s = 0; s < NSQ; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&m.q_full[s], 1);
       mbar_init(&m.q_empty[s], 1);
     }
-    mbar_init(&m.s_full, 1);
-    mbar_init(&m.s_empty, 128);
-    mbar_init(&m.pds_full, 128);
-    mbar_init(&m.grad_done, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&m.s_full[s], 1);
+      mbar_init(&m.pds_full[s], 256);
+      mbar_init(&m.grad_done[s], 1);
+    }
     mbar_init(&m.mma_final, 1);
     fence_mbar_init();
   }
   if (!p.seg)  // every token in one segment: the query-tile ids are all 0
-    for (int x = threadIdx.x; x < 2 * 128; x += blockDim.x) (&m.segq[0][0])[x] = 0;
+    for (int x = threadIdx.x; x < NS * 64; x += blockDim.x) (&m.segq[0][0])[x] = 0;
   if (warp == 1) {
     tmem_alloc(&m.tmem_base, L::TMEM_COLS);
     tmem_relinquish();
@@ -106,6 +114,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = m.tmem_base;
 
   if (warp == 0) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmDO);
@@ -114,75 +123,80 @@ __global__ void __launch_bounds__(192, 1)
       const int krow = (b * p.Hkv + hk) * p.N + tk * kTile;
       mbar_expect_tx(&m.kv_full, 2 * L::KV_BYTES);
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_2d(base + L::OFF_K + c * 16384, &tmK, &m.kv_full, c * 64, krow);
-        tma_load_2d(base + L::OFF_V + c * 16384, &tmV, &m.kv_full, c * 64, krow);
+        tma_load_2d(base + L::OFF_K + c * L::KV_CHUNK, &tmK, &m.kv_full, c * 64, krow);
+        tma_load_2d(base + L::OFF_V + c * L::KV_CHUNK, &tmV, &m.kv_full, c * 64, krow);
       }
-      const uint32_t qbytes = 2 * L::Q_BYTES + 1024 + (p.seg ? 512 : 0);
+      const uint32_t qbytes = 2 * L::QH_BYTES + 512 + (p.seg ? 256 : 0);
       int i = 0;
       bool ok = true;
       for (int hq = h0; ok && hq < h1; ++hq) {
-        for (int tq = walk.first(); tq < walk.end(); tq = walk.next(tq), ++i) {
-          const int st = i % NSQ;
-          if (!g.wait(&m.q_empty[st], ((i / NSQ) & 1) ^ 1, 1)) { ok = false; break; }
-          const int qrow = (b * p.Hq + hq) * p.N + tq * kTile;
-          mbar_expect_tx(&m.q_full[st], qbytes);
-          for (int c = 0; c < D / 64; ++c) {
-            tma_load_2d(base + L::OFF_Q + st * L::Q_BYTES + c * 16384, &tmQ, &m.q_full[st], c * 64, qrow);
-            tma_load_2d(base + L::OFF_DO + st * L::Q_BYTES + c * 16384, &tmDO, &m.q_full[st], c * 64, qrow);
+        for (int tq = walk.first(); ok && tq < walk.end(); tq = walk.next(tq)) {
+          for (int half = 0; half < 2; ++half, ++i) {
+            const int st = i % NS;
+            if (!g.wait(&m.q_empty[st], ((i / NS) & 1) ^ 1, 1)) { ok = false; break; }
+            const int qrow = (b * p.Hq + hq) * p.N + tq * kTile + half * 64;
+            mbar_expect_tx(&m.q_full[st], qbytes);
+            for (int c = 0; c < D / 64; ++c) {
+              tma_load_2d(base + L::OFF_Q + st * L::QH_BYTES + c * L::QH_CHUNK, &tmQ, &m.q_full[st], c * 64, qrow);
+              tma_load_2d(base + L::OFF_DO + st * L::QH_BYTES + c * L::QH_CHUNK, &tmDO, &m.q_full[st], c * 64,
+                          qrow);
+            }
+            bulk_load(m.lse[st], p.lse_in + qrow, 256, &m.q_full[st]);
+            bulk_load(m.dl[st], p.delta + qrow, 256, &m.q_full[st]);
+            if (p.seg) bulk_load(m.segq[st], p.seg + (size_t)b * p.N + tq * kTile + half * 64, 256, &m.q_full[st]);
           }
-          bulk_load(m.lse[st], p.lse_in + qrow, 512, &m.q_full[st]);
-          bulk_load(m.dl[st], p.delta + qrow, 512, &m.q_full[st]);
-          if (p.seg) bulk_load(m.segq[st], p.seg + (size_t)b * p.N + tq * kTile, 512, &m.q_full[st]);
         }
       }
       g.drain(&m.kv_full, 0);
-      for (int k = (i > NSQ ? i - NSQ : 0); k < i; ++k) g.drain(&m.q_full[k % NSQ], (k / NSQ) & 1);
+      for (int k = (i > NS ? i - NS : 0); k < i; ++k) g.drain(&m.q_full[k % NS], (k / NS) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idS = idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);
       auto issue_grad = [&](int i) -> bool {
-        const int st = i % NSQ;
-        if (!g.wait(&m.pds_full, i & 1, 2)) return false;
+        const int bb = i & 1, st = i % NS;
+        if (!g.wait(&m.pds_full[bb], (i >> 1) & 1, 2)) return false;
         tc_fence_after();
-        const uint32_t qa = sQ + st * L::Q_BYTES, da = sDO + st * L::Q_BYTES;
+        const uint32_t buf = tmem + L::TM_BUF + bb * 128;
+        const uint32_t qa = sQ + st * L::QH_BYTES, da = sDO + st * L::QH_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+        for (int kk = 0; kk < 4; ++kk) {
+          // thread-half kk>>1 keeps P^T in its columns [0,16) and dS^T in [16,32)
+          const uint32_t pcol = buf + (kk >> 1) * 32 + (kk & 1) * 8;
           const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          umma_bf16(tmem + L::TM_DV, sdesc_sw128(sP + aoff, 16, 1024), sdesc_sw128(da + kk * 2048, 16384, 1024),
-                    idG, acc);
-          umma_bf16(tmem + L::TM_DK, sdesc_sw128(sDS + aoff, 16, 1024), sdesc_sw128(qa + kk * 2048, 16384, 1024),
-                    idG, acc);
+          umma_bf16_ta(tmem + L::TM_DV, pcol, sdesc_sw128(da + kk * 2048, L::QH_CHUNK, 1024), idG, acc);
+          umma_bf16_ta(tmem + L::TM_DK, pcol + 16, sdesc_sw128(qa + kk * 2048, L::QH_CHUNK, 1024), idG, acc);
         }
-        umma_commit(&m.grad_done);
+        umma_commit(&m.grad_done[bb]);
         umma_commit(&m.q_empty[st]);
         return true;
       };
       bool ok = g.wait(&m.kv_full, 0, 3);
       int i = 0;
       for (int hq = h0; ok && hq < h1; ++hq) {
-        for (int tq = walk.first(); tq < walk.end(); tq = walk.next(tq), ++i) {
-          const int st = i % NSQ;
-          if (NSQ == 1 && i > 0 && !issue_grad(i - 1)) { ok = false; break; }
-          if (!g.wait(&m.q_full[st], (i / NSQ) & 1, 4) || !g.wait(&m.s_empty, (i & 1) ^ 1, 5)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t qa = sQ + st * L::Q_BYTES, da = sDO + st * L::Q_BYTES;
+        for (int tq = walk.first(); ok && tq < walk.end(); tq = walk.next(tq)) {
+          for (int half = 0; half < 2; ++half, ++i) {
+            const int bb = i & 1, st = i % NS;
+            if (!g.wait(&m.q_full[st], (i / NS) & 1, 4)) { ok = false; break; }
+            // buffer bb is free once the gradient MMAs of step i-2 have read it
+            if (i >= 2 && !g.wait(&m.grad_done[bb], ((i - 2) >> 1) & 1, 5)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t buf = tmem + L::TM_BUF + bb * 128;
+            const uint32_t qa = sQ + st * L::QH_BYTES, da = sDO + st * L::QH_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-            umma_bf16(tmem + L::TM_S, sdesc_sw128(sK + koff, 16, 1024), sdesc_sw128(qa + koff, 16, 1024), idS,
-                      kk > 0 ? 1u : 0u);
-            umma_bf16(tmem + L::TM_DP, sdesc_sw128(sV + koff, 16, 1024), sdesc_sw128(da + koff, 16, 1024), idS,
-                      kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t ko = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
+              const uint32_t qo = (kk >> 2) * L::QH_CHUNK + (kk & 3) * 32;
+              umma_bf16(buf, sdesc_sw128(sK + ko, 16, 1024), sdesc_sw128(qa + qo, 16, 1024), idS, kk > 0 ? 1u : 0u);
+              umma_bf16(buf + 64, sdesc_sw128(sV + ko, 16, 1024), sdesc_sw128(da + qo, 16, 1024), idS,
+                        kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&m.s_full[bb]);
+            if (i > 0 && !issue_grad(i - 1)) { ok = false; break; }
           }
-          umma_commit(&m.s_full);
-          if (NSQ > 1 && i > 0 && !issue_grad(i - 1)) { ok = false; break; }
         }
       }
       if (ok && i > 0) issue_grad(i - 1);
@@ -191,68 +205,58 @@ __global__ void __launch_bounds__(192, 1)
     }
     __syncwarp();
   } else {
-    const int wq = warp & 3;
-    const int r = wq * 32 + lane;
+    // ------------------------------------------------------------ softmax
+    const int quarter = warp & 3;
+    const int hsel = (warp - 2) >> 2;  // which 32 of the step's 64 query columns
+    const int r = quarter * 32 + lane;
     const int kvidx = tk * kTile + r;
     const int32_t segk = p.seg ? p.seg[(size_t)b * p.N + kvidx] : 0;
-    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
     const int4 kt = trow[tk];
     bool ok = true;
     int i = 0;
     for (int hq = h0; ok && hq < h1; ++hq) {
-      for (int tq = walk.first(); tq < walk.end(); tq = walk.next(tq), ++i) {
-        const int st = i % NSQ;
-        ok = g.wait(&m.q_full[st], (i / NSQ) & 1, 6);
-        if (!__all_sync(~0u, ok)) { ok = false; break; }
-        ok = g.wait(&m.s_full, i & 1, 7);
-        if (!__all_sync(~0u, ok)) { ok = false; break; }
-        tc_fence_after();
+      for (int tq = walk.first(); ok && tq < walk.end(); tq = walk.next(tq)) {
         const bool masked = !tile_pair_full(tq, trow[tq], tk, kt);
-        const int qbase = tq * kTile;
-        float pr[128];
+        for (int half = 0; half < 2; ++half, ++i) {
+          const int bb = i & 1, st = i % NS;
+          ok = g.wait(&m.q_full[st], (i / NS) & 1, 6);
+          if (!__all_sync(~0u, ok)) { ok = false; break; }
+          ok = g.wait(&m.s_full[bb], (i >> 1) & 1, 7);
+          if (!__all_sync(~0u, ok)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t buf = tmem + lane_base + L::TM_BUF + bb * 128 + hsel * 32;
+          uint32_t sv[32], dp[32];
+          tmem_ld32(buf, sv);
+          tmem_ld32(buf + 64, dp);  // this thread's dP^T columns
+          const int c0 = hsel * 32;
+          const int q0 = tq * kTile + half * 64 + c0;
+          uint32_t pw[16], dw[16];
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + L::TM_S + c0, v);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int c = c0 + e;
-            float s = __uint_as_float(v[e]);
+          for (int e = 0; e < 32; e += 2) {
+            float s0 = __uint_as_float(sv[e]), s1 = __uint_as_float(sv[e + 1]);
             if (masked) {
-              const bool vis = (qbase + c >= kvidx) && (m.segq[st][c] == segk);
-              s = vis ? s : -INFINITY;
+              s0 = (q0 + e >= kvidx && m.segq[st][c0 + e] == segk) ? s0 : -INFINITY;
+              s1 = (q0 + e + 1 >= kvidx && m.segq[st][c0 + e + 1] == segk) ? s1 : -INFINITY;
             }
-            pr[c] = ex2(fmaf(s, sl2, -m.lse[st][c] * 1.4426950408889634f));
+            const float p0 = ex2(fmaf(s0, sl2, -m.lse[st][c0 + e] * 1.4426950408889634f));
+            const float p1 = ex2(fmaf(s1, sl2, -m.lse[st][c0 + e + 1] * 1.4426950408889634f));
+            const float d0 = p0 * (__uint_as_float(dp[e]) - m.dl[st][c0 + e]);
+            const float d1 = p1 * (__uint_as_float(dp[e + 1]) - m.dl[st][c0 + e + 1]);
+            pw[e >> 1] = pack_bf16x2(p0, p1);
+            dw[e >> 1] = pack_bf16x2(d0, d1);
           }
+          // P^T and dS^T go over this thread's own S^T columns
+          tmem_st16(buf, pw);
+          tmem_st16(buf + 16, dw);
+          tc_fence_before();
+          mbar_arrive(&m.pds_full[bb]);
         }
-        // P^T / dS^T tiles are free once the previous step's gradient MMAs finished
-        if (i > 0) ok = g.wait(&m.grad_done, (i - 1) & 1, 8);
-        if (!__all_sync(~0u, ok)) { ok = false; break; }
-#pragma unroll
-        for (int c8 = 0; c8 < 128; c8 += 8)
-          st_shared_v4(sP + sw128_offset(r, c8), pack_bf16x2(pr[c8], pr[c8 + 1]), pack_bf16x2(pr[c8 + 2], pr[c8 + 3]),
-                       pack_bf16x2(pr[c8 + 4], pr[c8 + 5]), pack_bf16x2(pr[c8 + 6], pr[c8 + 7]));
-#pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + L::TM_DP + c0, v);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) pr[c0 + e] = pr[c0 + e] * (__uint_as_float(v[e]) - m.dl[st][c0 + e]);
-#pragma unroll
-          for (int c8 = c0; c8 < c0 + 32; c8 += 8)
-            st_shared_v4(sDS + sw128_offset(r, c8), pack_bf16x2(pr[c8], pr[c8 + 1]),
-                         pack_bf16x2(pr[c8 + 2], pr[c8 + 3]), pack_bf16x2(pr[c8 + 4], pr[c8 + 5]),
-                         pack_bf16x2(pr[c8 + 6], pr[c8 + 7]));
-        }
-        tc_fence_before();
-        mbar_arrive(&m.s_empty);
-        fence_async_smem();
-        mbar_arrive(&m.pds_full);
       }
     }
     if (ok && i > 0) {
-      ok = g.wait(&m.grad_done, (i - 1) & 1, 9);
+      ok = g.wait(&m.grad_done[(i - 1) & 1], ((i - 1) >> 1) & 1, 9);
       ok = __all_sync(~0u, ok);
     }
     if (ok && i > 0) {
@@ -262,7 +266,7 @@ __global__ void __launch_bounds__(192, 1)
       uint4* krow = reinterpret_cast<uint4*>(p.dk + row * D);
       const float sc = p.scale;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = hsel * (D / 2); c0 < (hsel + 1) * (D / 2); c0 += 32) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + L::TM_DV + c0, v);
 #pragma unroll
@@ -301,13 +305,13 @@ cudaError_t launch_dkv_d(const AttnParams& p, const void* q, const void* k, cons
   using L = DkvLayout<D>;
   CUtensorMap tq, tdo, tk, tv;
   const uint64_t qrows = (uint64_t)p.B * p.Hq * p.N, krows = (uint64_t)p.B * p.Hkv * p.N;
-  if (!tmap_bf16_2d_sw128(&tq, q, D, qrows, 128) || !tmap_bf16_2d_sw128(&tdo, dout, D, qrows, 128) ||
+  if (!tmap_bf16_2d_sw128(&tq, q, D, qrows, 64) || !tmap_bf16_2d_sw128(&tdo, dout, D, qrows, 64) ||
       !tmap_bf16_2d_sw128(&tk, k, D, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, D, krows, 128))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(dkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.T, p.Hkv, p.B);
-  dkv_kernel<D><<<grid, 192, L::SMEM, st>>>(tq, tdo, tk, tv, p);
+  dim3 grid(p.T * p.Hkv * p.B);
+  dkv_kernel<D><<<grid, 320, L::SMEM, st>>>(tq, tdo, tk, tv, p);
   return cudaGetLastError();
 }
 
