@@ -2,16 +2,23 @@
 //
 // One CTA per (query tile of 128 rows, query head, batch row); it visits the
 // same key tiles as the forward (the changelog's PACKED dQ kernel: cross-
-// segment blocks skipped). Per key tile:
-//   S  = Q K^T           (TMEM)     P  = exp(scale * S - lse)
-//   dP = dO V^T          (TMEM)     dS = P * (dP - delta)      (bf16, smem)
-//   dQ += dS K           (TMEM accumulator)
+// segment blocks skipped). Every key tile is processed as two 64-column
+// halves ("steps"):
+//   S  = Q K^T   (TMEM, 64 columns)   P  = exp(scale * S - lse)
+//   dP = dO V^T  (TMEM, 64 columns)   dS = P * (dP - delta)   (bf16, over S)
+//   dQ += dS K   (TMEM accumulator, dS read straight from TMEM)
 // and finally dQ *= scale. The probabilities are recomputed from the saved
 // log-sum-exp (mlx-train-perf 0.5.1 README, "Flash-attention training path":
 // the backward recomputes the tiles it needs from O(N) saved state).
 //
-// Warp roles as in the forward: warp 0 TMA producer, warp 1 MMA issuer and
-// TMEM owner, warps 2..5 one query row per thread.
+// Q and dO stay in TMEM for the whole CTA (each row thread stores its own row
+// once), so the S and dP MMAs read only K and V from shared memory. S/dP of
+// consecutive steps alternate between two TMEM buffers: the MMA issuer starts
+// step i+1 while the softmax warps work on step i.
+//
+// Warp roles: warp 0 TMA producer (K/V tiles, 3-stage ring), warp 1 MMA
+// issuer and TMEM owner, warps 2..9 two threads per query row, 32 key columns
+// each.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -25,66 +32,60 @@ namespace {
 
 template <int D>
 struct DqLayout {
-  static constexpr int NS = (D == 128) ? 2 : 3;
-  static constexpr uint32_t Q_BYTES = 128 * D * 2;
+  static constexpr int NS = 3;
   static constexpr uint32_t KV_BYTES = 128 * D * 2;
-  static constexpr uint32_t DS_BYTES = 128 * 128 * 2;
-  static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_DO = OFF_Q + Q_BYTES;
-  static constexpr uint32_t OFF_K = OFF_DO + Q_BYTES;
+  static constexpr uint32_t KV_CHUNK = 128 * 128;  // one 64-column chunk of a 128-row tile
+  static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + NS * KV_BYTES;
-  static constexpr uint32_t OFF_DS = OFF_V + NS * KV_BYTES;
-  static constexpr uint32_t TILE_BYTES = OFF_DS + DS_BYTES;
+  static constexpr uint32_t TILE_BYTES = OFF_V + NS * KV_BYTES;
   static constexpr uint32_t MISC_BYTES = 2048;
   static constexpr uint32_t SMEM = TILE_BYTES + MISC_BYTES + 1024;
-  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256, TMEM_COLS = 512;
+  // TMEM: Q and dO as bf16 (D/2 columns each), dQ accumulator, two step buffers
+  // of 128 columns (S in the first 64, dP in the second 64)
+  static constexpr uint32_t TM_Q = 0, TM_DO = D / 2, TM_DQ = D, TM_BUF = 2 * D, TMEM_COLS = 512;
 };
 
 struct DqMisc {
-  uint64_t q_full;
   uint64_t kv_full[3], kv_empty[3];
-  uint64_t s_full, s_empty, ds_full, dq_done, seg_ready[2];
-  uint64_t mma_final;
+  uint64_t qdo_ready, s_full[2], ds_full[2], dq_done[2], mma_final;
   uint32_t tmem_base;
   int abort_flag;
-  int32_t segkv[2][128];
+  alignas(16) int32_t segkv[3][128];
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
-    dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-              const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-              const AttnParams p) {
+__global__ void __launch_bounds__(320, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+              const __nv_bfloat16* __restrict__ q, const AttnParams p) {
   using L = DqLayout<D>;
   constexpr int NS = L::NS;
   static_assert(sizeof(DqMisc) <= L::MISC_BYTES, "misc region");
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   DqMisc& m = *reinterpret_cast<DqMisc*>(smem_raw);
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + sizeof(DqMisc) + 1023) & ~uintptr_t(1023));
-  const uint32_t sQ = smem_u32(base + L::OFF_Q), sDO = smem_u32(base + L::OFF_DO);
   const uint32_t sK = smem_u32(base + L::OFF_K), sV = smem_u32(base + L::OFF_V);
-  const uint32_t sDS = smem_u32(base + L::OFF_DS);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tq = p.T - 1 - (int)blockIdx.x;
-  const int h = blockIdx.y, b = blockIdx.z, hk = h / p.G;
+  // longest causal rows first, across all heads and batch rows
+  const int per_tile = p.Hq * p.B;
+  const int tq = p.T - 1 - (int)blockIdx.x / per_tile;
+  const int h = (int)blockIdx.x % p.Hq, b = ((int)blockIdx.x / p.Hq) % p.B, hk = h / p.G;
   const int4* trow = p.tiles + (size_t)b * p.T;
   const Guard g{&m.abort_flag, p.status};
 
   if (threadIdx.x == 0) {
     m.abort_flag = 0;
-    mbar_init(&m.q_full, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&m.kv_full[s], 1);
       mbar_init(&m.kv_empty[s], 1);
     }
-    mbar_init(&m.s_full, 1);
-    mbar_init(&m.s_empty, 128);
-    mbar_init(&m.ds_full, 128);
-    mbar_init(&m.dq_done, 1);
-    mbar_init(&m.seg_ready[0], 128);
-    mbar_init(&m.seg_ready[1], 128);
+    mbar_init(&m.qdo_ready, 256);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&m.s_full[s], 1);
+      mbar_init(&m.ds_full[s], 256);
+      mbar_init(&m.dq_done[s], 1);
+    }
     mbar_init(&m.mma_final, 1);
     fence_mbar_init();
   }
@@ -99,149 +100,155 @@ __global__ void __launch_bounds__(192, 1)
   const KvWalk walk(trow, tq);
 
   if (warp == 0) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmDO);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      const int qrow = (b * p.Hq + h) * p.N + tq * kTile;
       const int krow0 = (b * p.Hkv + hk) * p.N;
-      mbar_expect_tx(&m.q_full, 2 * L::Q_BYTES);
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_2d(base + L::OFF_Q + c * 16384, &tmQ, &m.q_full, c * 64, qrow);
-        tma_load_2d(base + L::OFF_DO + c * 16384, &tmDO, &m.q_full, c * 64, qrow);
-      }
       int j = 0;
       for (int tk = walk.first(); tk <= tq; tk = walk.next(tk), ++j) {
         const int st = j % NS;
         if (!g.wait(&m.kv_empty[st], ((j / NS) & 1) ^ 1, 1)) break;
-        mbar_expect_tx(&m.kv_full[st], 2 * L::KV_BYTES);
+        mbar_expect_tx(&m.kv_full[st], 2 * L::KV_BYTES + (p.seg ? 512 : 0));
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_2d(base + L::OFF_K + st * L::KV_BYTES + c * 16384, &tmK, &m.kv_full[st], c * 64,
+          tma_load_2d(base + L::OFF_K + st * L::KV_BYTES + c * L::KV_CHUNK, &tmK, &m.kv_full[st], c * 64,
                       krow0 + tk * kTile);
-          tma_load_2d(base + L::OFF_V + st * L::KV_BYTES + c * 16384, &tmV, &m.kv_full[st], c * 64,
+          tma_load_2d(base + L::OFF_V + st * L::KV_BYTES + c * L::KV_CHUNK, &tmV, &m.kv_full[st], c * 64,
                       krow0 + tk * kTile);
         }
+        if (p.seg) bulk_load(m.segkv[st], p.seg + (size_t)b * p.N + tk * kTile, 512, &m.kv_full[st]);
       }
-      g.drain(&m.q_full, 0);
       for (int i = (j > NS ? j - NS : 0); i < j; ++i) g.drain(&m.kv_full[i % NS], (i / NS) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idS = idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, true);
+      // dQ += dS_i K_half(i): dS from TMEM, K rows of the half as the K dimension
       auto issue_dq = [&](int i) -> bool {
-        const int st = i % NS;
-        if (!g.wait(&m.ds_full, i & 1, 2)) return false;
+        const int bb = i & 1, st = (i >> 1) % NS, half = i & 1;
+        if (!g.wait(&m.ds_full[bb], (i >> 1) & 1, 2)) return false;
         tc_fence_after();
-        const uint32_t ka = sK + st * L::KV_BYTES;
+        const uint32_t buf = tmem + L::TM_BUF + bb * 128;
+        const uint32_t ka = sK + st * L::KV_BYTES + half * 64 * 128;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16(tmem + L::TM_DQ, sdesc_sw128(sDS + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                    sdesc_sw128(ka + kk * 2048, 16384, 1024), idQ, (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&m.dq_done);
-        umma_commit(&m.kv_empty[st]);
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_ta(tmem + L::TM_DQ, buf + (kk >> 1) * 32 + (kk & 1) * 8,
+                       sdesc_sw128(ka + kk * 2048, L::KV_CHUNK, 1024), idQ, (i > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&m.dq_done[bb]);
+        if (half == 1) umma_commit(&m.kv_empty[st]);
         return true;
       };
-      bool ok = g.wait(&m.q_full, 0, 3);
-      int j = 0;
+      bool ok = g.wait(&m.qdo_ready, 0, 3);
+      tc_fence_after();
+      int i = 0, j = 0;
       for (int tk = walk.first(); ok && tk <= tq; tk = walk.next(tk), ++j) {
         const int st = j % NS;
-        ok = g.wait(&m.kv_full[st], (j / NS) & 1, 4) && g.wait(&m.s_empty, (j & 1) ^ 1, 5);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t ka = sK + st * L::KV_BYTES, va = sV + st * L::KV_BYTES;
+        if (!g.wait(&m.kv_full[st], (j / NS) & 1, 4)) { ok = false; break; }
+        for (int half = 0; half < 2; ++half, ++i) {
+          const int bb = i & 1;
+          if (i >= 2 && !g.wait(&m.dq_done[bb], ((i - 2) >> 1) & 1, 5)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t buf = tmem + L::TM_BUF + bb * 128;
+          const uint32_t ka = sK + st * L::KV_BYTES + half * 64 * 128;
+          const uint32_t va = sV + st * L::KV_BYTES + half * 64 * 128;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_bf16(tmem + L::TM_S, sdesc_sw128(sQ + koff, 16, 1024), sdesc_sw128(ka + koff, 16, 1024), idS,
-                    kk > 0 ? 1u : 0u);
-          umma_bf16(tmem + L::TM_DP, sdesc_sw128(sDO + koff, 16, 1024), sdesc_sw128(va + koff, 16, 1024), idS,
-                    kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ko = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
+            umma_bf16_ta(buf, tmem + L::TM_Q + kk * 8, sdesc_sw128(ka + ko, 16, 1024), idS, kk > 0 ? 1u : 0u);
+            umma_bf16_ta(buf + 64, tmem + L::TM_DO + kk * 8, sdesc_sw128(va + ko, 16, 1024), idS,
+                         kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&m.s_full[bb]);
+          if (i > 0 && !issue_dq(i - 1)) { ok = false; break; }
         }
-        umma_commit(&m.s_full);
-        if (j > 0) ok = issue_dq(j - 1);
       }
-      if (ok && j > 0) issue_dq(j - 1);
+      if (ok && i > 0) issue_dq(i - 1);
       umma_commit(&m.mma_final);
       g.drain(&m.mma_final, 0);
     }
     __syncwarp();
   } else {
-    const int wq = warp & 3;
-    const int r = wq * 32 + lane;
+    // ------------------------------------------------------------ softmax
+    const int quarter = warp & 3;
+    const int hsel = (warp - 2) >> 2;
+    const int r = quarter * 32 + lane;
     const int qidx = tq * kTile + r;
     const size_t row = (size_t)(b * p.Hq + h) * p.N + qidx;
     const int32_t segq = p.seg ? p.seg[(size_t)b * p.N + qidx] : 0;
     const float lse2 = p.lse_in[row] * 1.4426950408889634f;
     const float dlt = p.delta[row];
-    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
-    bool ok = true;
-    int j = 0;
-    uint32_t nseg0 = 0, nseg1 = 0;
-    for (int tk = walk.first(); tk <= tq; tk = walk.next(tk), ++j) {
-      const int sb = j & 1;
-      // segkv[sb] was last read in tile j-2; this thread already saw dq_done
-      // for tile j-2 (before writing dS in tile j-1), and that MMA needed the
-      // ds_full arrivals every thread made after its tile j-2 mask reads.
-      const bool masked = !tile_pair_full(tq, walk.qt, tk, trow[tk]);
-      if (masked) {
-        m.segkv[sb][r] = p.seg ? p.seg[(size_t)b * p.N + tk * kTile + r] : 0;
-        mbar_arrive(&m.seg_ready[sb]);
-        const uint32_t use = sb ? nseg1++ : nseg0++;
-        ok = g.wait(&m.seg_ready[sb], use & 1, 7);
-        if (!__all_sync(~0u, ok)) { ok = false; break; }
-      }
-      ok = g.wait(&m.s_full, j & 1, 8);
-      if (!__all_sync(~0u, ok)) { ok = false; break; }
-      tc_fence_after();
-      float pr[128];
+    // this thread's half of its Q and dO rows into TMEM, as bf16 pairs
+    {
+      const uint32_t* qsrc = reinterpret_cast<const uint32_t*>(q + row * D) + hsel * (D / 4);
+      const uint32_t* dsrc = reinterpret_cast<const uint32_t*>(p.dout + row * D) + hsel * (D / 4);
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + L::TM_S + c0, v);
+      for (int c0 = 0; c0 < D / 4; c0 += 16) {
+        uint32_t a[16], d[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = c0 + i;
-          float s = __uint_as_float(v[i]);
-          if (masked) {
-            const bool vis = (tk * kTile + c <= qidx) && (m.segkv[sb][c] == segq);
-            s = vis ? s : -INFINITY;
-          }
-          pr[c] = ex2(fmaf(s, sl2, -lse2));
+        for (int e = 0; e < 16; e += 4) {
+          const uint4 x = __ldg(reinterpret_cast<const uint4*>(qsrc + c0 + e));
+          const uint4 y = __ldg(reinterpret_cast<const uint4*>(dsrc + c0 + e));
+          a[e] = x.x; a[e + 1] = x.y; a[e + 2] = x.z; a[e + 3] = x.w;
+          d[e] = y.x; d[e + 1] = y.y; d[e + 2] = y.z; d[e + 3] = y.w;
         }
-      }
-#pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + L::TM_DP + c0, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pr[c0 + i] = pr[c0 + i] * (__uint_as_float(v[i]) - dlt);
+        tmem_st16(tmem + lane_base + L::TM_Q + hsel * (D / 4) + c0, a);
+        tmem_st16(tmem + lane_base + L::TM_DO + hsel * (D / 4) + c0, d);
       }
       tc_fence_before();
-      mbar_arrive(&m.s_empty);
-      // the dS tile is free once the previous dQ MMA has read it
-      if (j >= 1) ok = g.wait(&m.dq_done, (j - 1) & 1, 9);
-      if (!__all_sync(~0u, ok)) { ok = false; break; }
-#pragma unroll
-      for (int c8 = 0; c8 < 128; c8 += 8)
-        st_shared_v4(sDS + sw128_offset(r, c8), pack_bf16x2(pr[c8], pr[c8 + 1]), pack_bf16x2(pr[c8 + 2], pr[c8 + 3]),
-                     pack_bf16x2(pr[c8 + 4], pr[c8 + 5]), pack_bf16x2(pr[c8 + 6], pr[c8 + 7]));
-      fence_async_smem();
-      mbar_arrive(&m.ds_full);
+      mbar_arrive(&m.qdo_ready);
     }
-    if (ok && j > 0) {
-      ok = g.wait(&m.dq_done, (j - 1) & 1, 10);
+    bool ok = true;
+    int i = 0, j = 0;
+    for (int tk = walk.first(); ok && tk <= tq; tk = walk.next(tk), ++j) {
+      const int st = j % NS;
+      const bool masked = !tile_pair_full(tq, walk.qt, tk, trow[tk]);
+      if (masked && p.seg) {  // segment ids of this key tile arrived with it
+        ok = g.wait(&m.kv_full[st], (j / NS) & 1, 6);
+        if (!__all_sync(~0u, ok)) { ok = false; break; }
+      }
+      for (int half = 0; half < 2; ++half, ++i) {
+        const int bb = i & 1;
+        ok = g.wait(&m.s_full[bb], (i >> 1) & 1, 7);
+        if (!__all_sync(~0u, ok)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t buf = tmem + lane_base + L::TM_BUF + bb * 128 + hsel * 32;
+        uint32_t sv[32], dp[32];
+        tmem_ld32(buf, sv);
+        tmem_ld32(buf + 64, dp);
+        const int c0 = half * 64 + hsel * 32;  // key column within the tile
+        const int k0 = tk * kTile + c0;
+        uint32_t dw[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float s0 = __uint_as_float(sv[e]), s1 = __uint_as_float(sv[e + 1]);
+          if (masked) {
+            const int32_t g0 = p.seg ? m.segkv[st][c0 + e] : 0, g1 = p.seg ? m.segkv[st][c0 + e + 1] : 0;
+            s0 = (k0 + e <= qidx && g0 == segq) ? s0 : -INFINITY;
+            s1 = (k0 + e + 1 <= qidx && g1 == segq) ? s1 : -INFINITY;
+          }
+          const float p0 = ex2(fmaf(s0, sl2, -lse2)), p1 = ex2(fmaf(s1, sl2, -lse2));
+          dw[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - dlt), p1 * (__uint_as_float(dp[e + 1]) - dlt));
+        }
+        tmem_st16(buf, dw);  // dS over this thread's own S columns
+        tc_fence_before();
+        mbar_arrive(&m.ds_full[bb]);
+      }
+    }
+    if (ok && i > 0) {
+      ok = g.wait(&m.dq_done[(i - 1) & 1], ((i - 1) >> 1) & 1, 10);
       ok = __all_sync(~0u, ok);
     }
-    if (ok && j > 0) {
+    if (ok && i > 0) {
       tc_fence_after();
       uint4* drow = reinterpret_cast<uint4*>(p.dq + row * D);
       const float sc = p.scale;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = hsel * (D / 2); c0 < (hsel + 1) * (D / 2); c0 += 32) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + L::TM_DQ + c0, v);
 #pragma unroll
@@ -268,15 +275,16 @@ template <int D>
 cudaError_t launch_dq_d(const AttnParams& p, const void* q, const void* k, const void* v, const void* dout,
                         cudaStream_t st) {
   using L = DqLayout<D>;
-  CUtensorMap tq, tdo, tk, tv;
-  const uint64_t qrows = (uint64_t)p.B * p.Hq * p.N, krows = (uint64_t)p.B * p.Hkv * p.N;
-  if (!tmap_bf16_2d_sw128(&tq, q, D, qrows, 128) || !tmap_bf16_2d_sw128(&tdo, dout, D, qrows, 128) ||
-      !tmap_bf16_2d_sw128(&tk, k, D, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, D, krows, 128))
+  CUtensorMap tk, tv;
+  const uint64_t krows = (uint64_t)p.B * p.Hkv * p.N;
+  if (!tmap_bf16_2d_sw128(&tk, k, D, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, D, krows, 128))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.T, p.Hq, p.B);
-  dq_kernel<D><<<grid, 192, L::SMEM, st>>>(tq, tdo, tk, tv, p);
+  AttnParams pp = p;
+  pp.dout = static_cast<const __nv_bfloat16*>(dout);
+  dim3 grid(p.T * p.Hq * p.B);
+  dq_kernel<D><<<grid, 320, L::SMEM, st>>>(tk, tv, static_cast<const __nv_bfloat16*>(q), pp);
   return cudaGetLastError();
 }
 
