@@ -17,7 +17,10 @@
 //
 // Pipelining: S^T/dP^T of a step live in one of two TMEM buffers, so the MMA
 // issuer starts step i+1's S^T and dP^T before step i's gradient MMAs and the
-// tensor core runs while the softmax warps work on step i.
+// tensor core runs while the softmax warps work on step i. Within a buffer the
+// S^T and dP^T halves swap roles on every use, so a step's S^T never waits and
+// its dP^T waits only for gradient MMAs already queued ahead of that S^T: the
+// single MMA-issuing thread never stalls on work it has just issued.
 //
 // Warp roles: warp 0 TMA producer (Q, dO halves plus their lse, delta and
 // segment ids through a 4-stage ring), warp 1 MMA issuer and TMEM owner,
@@ -47,8 +50,8 @@ struct DkvLayout {
   static constexpr uint32_t TILE_BYTES = OFF_DO + NS * QH_BYTES;
   static constexpr uint32_t MISC_BYTES = 4096;
   static constexpr uint32_t SMEM = TILE_BYTES + MISC_BYTES + 1024;
-  // TMEM: dV, dK accumulators, then two step buffers of 128 columns each
-  // (S^T in the first 64, dP^T in the second 64)
+  // TMEM: dV, dK accumulators, then two step buffers of 128 columns each;
+  // a buffer's 64-column halves hold S^T and dP^T and swap roles on every use
   static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_BUF = 2 * D, TMEM_COLS = 512;
 };
 
@@ -160,20 +163,23 @@ __global__ void __launch_bounds__(320, 1)
         const int bb = i & 1, st = i % NS;
         if (!g.wait(&m.pds_full[bb], (i >> 1) & 1, 2)) return false;
         tc_fence_after();
-        const uint32_t buf = tmem + L::TM_BUF + bb * 128;
-        const uint32_t qa = sQ + st * L::QH_BYTES, da = sDO + st * L::QH_BYTES;
+        const uint32_t buf = tmem + L::TM_BUF + bb * 128 + (((i >> 1) & 1) ? 64 : 0);  // step i's S^T half
+        const uint64_t gq = sdesc_sw128(sQ + st * L::QH_BYTES, L::QH_CHUNK, 1024);
+        const uint64_t gd = sdesc_sw128(sDO + st * L::QH_BYTES, L::QH_CHUNK, 1024);
+        const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           // thread-half kk>>1 keeps P^T in its columns [0,16) and dS^T in [16,32)
           const uint32_t pcol = buf + (kk >> 1) * 32 + (kk & 1) * 8;
-          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          umma_bf16_ta(tmem + L::TM_DV, pcol, sdesc_sw128(da + kk * 2048, L::QH_CHUNK, 1024), idG, acc);
-          umma_bf16_ta(tmem + L::TM_DK, pcol + 16, sdesc_sw128(qa + kk * 2048, L::QH_CHUNK, 1024), idG, acc);
+          const uint32_t acc = kk > 0 ? 1u : acc0;
+          umma_bf16_ta(tmem + L::TM_DV, pcol, sdesc_add(gd, kk * 2048), idG, acc);
+          umma_bf16_ta(tmem + L::TM_DK, pcol + 16, sdesc_add(gq, kk * 2048), idG, acc);
         }
         umma_commit(&m.grad_done[bb]);
         umma_commit(&m.q_empty[st]);
         return true;
       };
+      const uint64_t dk0 = sdesc_sw128(sK, 16, 1024), dv0 = sdesc_sw128(sV, 16, 1024);
       bool ok = g.wait(&m.kv_full, 0, 3);
       int i = 0;
       for (int hq = h0; ok && hq < h1; ++hq) {
@@ -181,18 +187,28 @@ __global__ void __launch_bounds__(320, 1)
           for (int half = 0; half < 2; ++half, ++i) {
             const int bb = i & 1, st = i % NS;
             if (!g.wait(&m.q_full[st], (i / NS) & 1, 4)) { ok = false; break; }
-            // buffer bb is free once the gradient MMAs of step i-2 have read it
-            if (i >= 2 && !g.wait(&m.grad_done[bb], ((i - 2) >> 1) & 1, 5)) { ok = false; break; }
-            tc_fence_after();
+            // Buffer bb's two halves swap roles on every use: S^T of step i goes
+            // where dP^T of step i-2 was (free once that softmax read it), dP^T
+            // where step i-2's P^T/dS^T was (free once its gradient MMAs ran).
             const uint32_t buf = tmem + L::TM_BUF + bb * 128;
-            const uint32_t qa = sQ + st * L::QH_BYTES, da = sDO + st * L::QH_BYTES;
+            const uint32_t sO = ((i >> 1) & 1) ? 64 : 0, dO_ = 64 - sO;
+            const uint64_t dq0 = sdesc_sw128(sQ + st * L::QH_BYTES, 16, 1024);
+            const uint64_t do0 = sdesc_sw128(sDO + st * L::QH_BYTES, 16, 1024);
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t ko = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
               const uint32_t qo = (kk >> 2) * L::QH_CHUNK + (kk & 3) * 32;
-              umma_bf16(buf, sdesc_sw128(sK + ko, 16, 1024), sdesc_sw128(qa + qo, 16, 1024), idS, kk > 0 ? 1u : 0u);
-              umma_bf16(buf + 64, sdesc_sw128(sV + ko, 16, 1024), sdesc_sw128(da + qo, 16, 1024), idS,
-                        kk > 0 ? 1u : 0u);
+              umma_bf16(buf + sO, sdesc_add(dk0, ko), sdesc_add(dq0, qo), idS, kk > 0 ? 1u : 0u);
+            }
+            // only now wait for step i-2's gradient MMAs: S^T of step i is queued behind them
+            if (i >= 2 && !g.wait(&m.grad_done[bb], ((i - 2) >> 1) & 1, 5)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t ko = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
+              const uint32_t qo = (kk >> 2) * L::QH_CHUNK + (kk & 3) * 32;
+              umma_bf16(buf + dO_, sdesc_add(dv0, ko), sdesc_add(do0, qo), idS, kk > 0 ? 1u : 0u);
             }
             umma_commit(&m.s_full[bb]);
             if (i > 0 && !issue_grad(i - 1)) { ok = false; break; }
@@ -226,30 +242,42 @@ __global__ void __launch_bounds__(320, 1)
           ok = g.wait(&m.s_full[bb], (i >> 1) & 1, 7);
           if (!__all_sync(~0u, ok)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t buf = tmem + lane_base + L::TM_BUF + bb * 128 + hsel * 32;
+          const uint32_t sO = ((i >> 1) & 1) ? 64 : 0;
+          const uint32_t buf = tmem + lane_base + L::TM_BUF + bb * 128 + sO + hsel * 32;
+          const uint32_t dbuf = tmem + lane_base + L::TM_BUF + bb * 128 + (64 - sO) + hsel * 32;
           uint32_t sv[32], dp[32];
-          tmem_ld32(buf, sv);
-          tmem_ld32(buf + 64, dp);  // this thread's dP^T columns
+          tmem_ld32x2(buf, dbuf, sv, dp);  // this thread's S^T and dP^T columns
           const int c0 = hsel * 32;
           const int q0 = tq * kTile + half * 64 + c0;
+          const float4* l4 = reinterpret_cast<const float4*>(&m.lse[st][c0]);
+          const float4* d4 = reinterpret_cast<const float4*>(&m.dl[st][c0]);
+          const int4* g4 = reinterpret_cast<const int4*>(&m.segq[st][c0]);
           uint32_t pw[16], dw[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float s0 = __uint_as_float(sv[e]), s1 = __uint_as_float(sv[e + 1]);
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 lv = l4[e4], dv = d4[e4];
+            const float lz[4] = {lv.x, lv.y, lv.z, lv.w}, dz[4] = {dv.x, dv.y, dv.z, dv.w};
+            float pz[4], sz[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sz[e] = __uint_as_float(sv[e4 * 4 + e]);
             if (masked) {
-              s0 = (q0 + e >= kvidx && m.segq[st][c0 + e] == segk) ? s0 : -INFINITY;
-              s1 = (q0 + e + 1 >= kvidx && m.segq[st][c0 + e + 1] == segk) ? s1 : -INFINITY;
+              const int4 gv = g4[e4];
+              const int32_t gz[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                sz[e] = (q0 + e4 * 4 + e >= kvidx && gz[e] == segk) ? sz[e] : -INFINITY;
             }
-            const float p0 = ex2(fmaf(s0, sl2, -m.lse[st][c0 + e] * 1.4426950408889634f));
-            const float p1 = ex2(fmaf(s1, sl2, -m.lse[st][c0 + e + 1] * 1.4426950408889634f));
-            const float d0 = p0 * (__uint_as_float(dp[e]) - m.dl[st][c0 + e]);
-            const float d1 = p1 * (__uint_as_float(dp[e + 1]) - m.dl[st][c0 + e + 1]);
-            pw[e >> 1] = pack_bf16x2(p0, p1);
-            dw[e >> 1] = pack_bf16x2(d0, d1);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pz[e] = ex2(fmaf(sz[e], sl2, -lz[e] * 1.4426950408889634f));
+            pw[e4 * 2] = pack_bf16x2(pz[0], pz[1]);
+            pw[e4 * 2 + 1] = pack_bf16x2(pz[2], pz[3]);
+            dw[e4 * 2] = pack_bf16x2(pz[0] * (__uint_as_float(dp[e4 * 4]) - dz[0]),
+                                     pz[1] * (__uint_as_float(dp[e4 * 4 + 1]) - dz[1]));
+            dw[e4 * 2 + 1] = pack_bf16x2(pz[2] * (__uint_as_float(dp[e4 * 4 + 2]) - dz[2]),
+                                         pz[3] * (__uint_as_float(dp[e4 * 4 + 3]) - dz[3]));
           }
           // P^T and dS^T go over this thread's own S^T columns
-          tmem_st16(buf, pw);
-          tmem_st16(buf + 16, dw);
+          tmem_st16x2(buf, buf + 16, pw, dw);
           tc_fence_before();
           mbar_arrive(&m.pds_full[bb]);
         }

@@ -41,7 +41,7 @@ struct DqLayout {
   static constexpr uint32_t MISC_BYTES = 2048;
   static constexpr uint32_t SMEM = TILE_BYTES + MISC_BYTES + 1024;
   // TMEM: Q and dO as bf16 (D/2 columns each), dQ accumulator, two step buffers
-  // of 128 columns (S in the first 64, dP in the second 64)
+  // of 128 columns whose 64-column halves hold S and dP and swap roles on every use
   static constexpr uint32_t TM_Q = 0, TM_DO = D / 2, TM_DQ = D, TM_BUF = 2 * D, TMEM_COLS = 512;
 };
 
@@ -131,12 +131,13 @@ __global__ void __launch_bounds__(320, 1)
         const int bb = i & 1, st = (i >> 1) % NS, half = i & 1;
         if (!g.wait(&m.ds_full[bb], (i >> 1) & 1, 2)) return false;
         tc_fence_after();
-        const uint32_t buf = tmem + L::TM_BUF + bb * 128;
-        const uint32_t ka = sK + st * L::KV_BYTES + half * 64 * 128;
+        const uint32_t buf = tmem + L::TM_BUF + bb * 128 + (((i >> 1) & 1) ? 64 : 0);  // step i's S half
+        const uint64_t kd = sdesc_sw128(sK + st * L::KV_BYTES + half * 64 * 128, L::KV_CHUNK, 1024);
+        const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_ta(tmem + L::TM_DQ, buf + (kk >> 1) * 32 + (kk & 1) * 8,
-                       sdesc_sw128(ka + kk * 2048, L::KV_CHUNK, 1024), idQ, (i > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ta(tmem + L::TM_DQ, buf + (kk >> 1) * 32 + (kk & 1) * 8, sdesc_add(kd, kk * 2048), idQ,
+                       kk > 0 ? 1u : acc0);
         umma_commit(&m.dq_done[bb]);
         if (half == 1) umma_commit(&m.kv_empty[st]);
         return true;
@@ -149,17 +150,26 @@ __global__ void __launch_bounds__(320, 1)
         if (!g.wait(&m.kv_full[st], (j / NS) & 1, 4)) { ok = false; break; }
         for (int half = 0; half < 2; ++half, ++i) {
           const int bb = i & 1;
-          if (i >= 2 && !g.wait(&m.dq_done[bb], ((i - 2) >> 1) & 1, 5)) { ok = false; break; }
-          tc_fence_after();
+          // Buffer bb's halves swap roles on every use: S of step i goes where
+          // dP of step i-2 was (free once that softmax read it), dP where step
+          // i-2's dS was (free once its dQ MMAs ran).
           const uint32_t buf = tmem + L::TM_BUF + bb * 128;
-          const uint32_t ka = sK + st * L::KV_BYTES + half * 64 * 128;
-          const uint32_t va = sV + st * L::KV_BYTES + half * 64 * 128;
+          const uint32_t sO = ((i >> 1) & 1) ? 64 : 0, dO_ = 64 - sO;
+          const uint64_t kd = sdesc_sw128(sK + st * L::KV_BYTES + half * 64 * 128, 16, 1024);
+          const uint64_t vd = sdesc_sw128(sV + st * L::KV_BYTES + half * 64 * 128, 16, 1024);
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ko = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
-            umma_bf16_ta(buf, tmem + L::TM_Q + kk * 8, sdesc_sw128(ka + ko, 16, 1024), idS, kk > 0 ? 1u : 0u);
-            umma_bf16_ta(buf + 64, tmem + L::TM_DO + kk * 8, sdesc_sw128(va + ko, 16, 1024), idS,
-                         kk > 0 ? 1u : 0u);
+            umma_bf16_ta(buf + sO, tmem + L::TM_Q + kk * 8, sdesc_add(kd, ko), idS, kk > 0 ? 1u : 0u);
+          }
+          // only now wait for step i-2's dQ MMAs: S of step i is queued behind them
+          if (i >= 2 && !g.wait(&m.dq_done[bb], ((i - 2) >> 1) & 1, 5)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ko = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
+            umma_bf16_ta(buf + dO_, tmem + L::TM_DO + kk * 8, sdesc_add(vd, ko), idS, kk > 0 ? 1u : 0u);
           }
           umma_commit(&m.s_full[bb]);
           if (i > 0 && !issue_dq(i - 1)) { ok = false; break; }
@@ -216,22 +226,32 @@ __global__ void __launch_bounds__(320, 1)
         ok = g.wait(&m.s_full[bb], (i >> 1) & 1, 7);
         if (!__all_sync(~0u, ok)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t buf = tmem + lane_base + L::TM_BUF + bb * 128 + hsel * 32;
+        const uint32_t sO = ((i >> 1) & 1) ? 64 : 0;
+        const uint32_t buf = tmem + lane_base + L::TM_BUF + bb * 128 + sO + hsel * 32;
         uint32_t sv[32], dp[32];
-        tmem_ld32(buf, sv);
-        tmem_ld32(buf + 64, dp);
+        tmem_ld32x2(buf, tmem + lane_base + L::TM_BUF + bb * 128 + (64 - sO) + hsel * 32, sv, dp);
         const int c0 = half * 64 + hsel * 32;  // key column within the tile
         const int k0 = tk * kTile + c0;
         uint32_t dw[16];
+        float sz[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sz[e] = __uint_as_float(sv[e]);
+        if (masked) {
+          const int4* g4 = reinterpret_cast<const int4*>(&m.segkv[st][c0]);
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const int4 gv = p.seg ? g4[e4] : make_int4(0, 0, 0, 0);
+            const int32_t gz[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = e4 * 4 + e;
+              sz[c] = (k0 + c <= qidx && gz[e] == segq) ? sz[c] : -INFINITY;
+            }
+          }
+        }
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float s0 = __uint_as_float(sv[e]), s1 = __uint_as_float(sv[e + 1]);
-          if (masked) {
-            const int32_t g0 = p.seg ? m.segkv[st][c0 + e] : 0, g1 = p.seg ? m.segkv[st][c0 + e + 1] : 0;
-            s0 = (k0 + e <= qidx && g0 == segq) ? s0 : -INFINITY;
-            s1 = (k0 + e + 1 <= qidx && g1 == segq) ? s1 : -INFINITY;
-          }
-          const float p0 = ex2(fmaf(s0, sl2, -lse2)), p1 = ex2(fmaf(s1, sl2, -lse2));
+          const float p0 = ex2(fmaf(sz[e], sl2, -lse2)), p1 = ex2(fmaf(sz[e + 1], sl2, -lse2));
           dw[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - dlt), p1 * (__uint_as_float(dp[e + 1]) - dlt));
         }
         tmem_st16(buf, dw);  // dS over this thread's own S columns

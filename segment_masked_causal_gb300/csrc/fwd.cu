@@ -7,14 +7,16 @@
 // not entirely visible. The saved state is O and its log-sum-exp
 // (mlx-train-perf 0.5.1 README, "Flash-attention training path").
 //
-// Every key tile is split into two 64-key halves. Half h of every tile goes to
-// softmax warpgroup h, which keeps its own running maximum, sums and O
+// Every key tile is split into two 64-key halves ("steps"; step i = 2 * tile +
+// half). Half h of every tile goes to softmax warpgroup h, which keeps its own running maximum, sums and O
 // accumulator (TMEM); the two partial results are combined once at the end:
 //   O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / (l_0 2^(m_0 - m) + l_1 2^(m_1 - m)).
 // Per half:  S_h = Q K_h^T (TMEM, 64 columns; Q resident in TMEM as the A
 // operand), P_h = 2^(S_h log2e scale - m) written back as bf16 over S_h and
 // fed to O_h += P_h V_h straight from TMEM. Shared memory carries only the
-// K/V ring.
+// K/V ring. S buffers rotate over three 64-column slots and the MMA issuer
+// queues S_{i+1} before PV_i, so a slot it must wait for was freed by a PV
+// issued two groups earlier and the tensor pipe never drains.
 //
 // Online softmax works in log2 units of the scaled score and rescales an O
 // accumulator only when its running maximum rises by more than 8 (a factor
@@ -45,13 +47,13 @@ struct FwdLayout {
   static constexpr uint32_t TILE_BYTES = OFF_V + NS * KV_BYTES;
   static constexpr uint32_t MISC_BYTES = 8192;
   static constexpr uint32_t SMEM = TILE_BYTES + MISC_BYTES + 1024;
-  // TMEM: S_0, S_1 (64 columns each), Q as bf16 (D/2 columns), O_0, O_1
-  static constexpr uint32_t TM_S = 0, TM_Q = 128, TM_O = 256, TMEM_COLS = 512;
+  // TMEM: three rotating 64-column S buffers, Q as bf16 (D/2 columns), O_0, O_1
+  static constexpr uint32_t TM_S = 0, TM_Q = 192, TM_O = 256, TMEM_COLS = 512;
 };
 
 struct FwdMisc {
   uint64_t kv_full[4], kv_empty[4];
-  uint64_t q_ready, s_full[2], p_full[2], pv_done[2], comb_ready, mma_final;
+  uint64_t q_ready, s_full[3], p_full[3], pv_done[3], comb_ready, mma_final;
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) int32_t segkv[4][128];
@@ -86,7 +88,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&m.kv_empty[s], 1);
     }
     mbar_init(&m.q_ready, 256);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(&m.s_full[s], 1);
       mbar_init(&m.p_full[s], 128);
       mbar_init(&m.pv_done[s], 1);
@@ -132,17 +134,19 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
-      // O_w += P_w V_half: step i = 2 * tile + half, warpgroup w = half
+      // O_w += P_w V_half for step i = 2 * tile + half (warpgroup w = half);
+      // P_w sits in S slot i % 3
       auto issue_pv = [&](int i) -> bool {
-        const int w = i & 1, st = (i >> 1) % NS;
-        if (!g.wait(&m.p_full[w], (i >> 1) & 1, 2)) return false;
+        const int w = i & 1, st = (i >> 1) % NS, bi = i % 3;
+        if (!g.wait(&m.p_full[bi], (i / 3) & 1, 2)) return false;
         tc_fence_after();
-        const uint32_t va = sV + st * L::KV_BYTES + w * 64 * 128;
+        const uint64_t vd = sdesc_sw128(sV + st * L::KV_BYTES + w * 64 * 128, L::KV_CHUNK, 1024);
+        const uint32_t acc0 = i >= 2 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_ta(tmem + L::TM_O + w * D, tmem + L::TM_S + w * 64 + kk * 8,
-                       sdesc_sw128(va + kk * 2048, L::KV_CHUNK, 1024), idO, (i >= 2 || kk > 0) ? 1u : 0u);
-        umma_commit(&m.pv_done[w]);
+          umma_bf16_ta(tmem + L::TM_O + w * D, tmem + L::TM_S + bi * 64 + kk * 8, sdesc_add(vd, kk * 2048), idO,
+                       kk > 0 ? 1u : acc0);
+        umma_commit(&m.pv_done[bi]);
         if (w == 1) umma_commit(&m.kv_empty[st]);
         return true;
       };
@@ -153,20 +157,23 @@ __global__ void __launch_bounds__(320, 1)
         const int st = j % NS;
         if (!g.wait(&m.kv_full[st], (j / NS) & 1, 4)) { ok = false; break; }
         for (int w = 0; w < 2; ++w, ++i) {
-          // S_w is free once the PV of this warpgroup's previous half has read P_w
-          if (i >= 2 && !g.wait(&m.pv_done[w], ((i - 2) >> 1) & 1, 5)) { ok = false; break; }
+          const int bi = i % 3;
+          // slot bi is free once the PV of step i-3 has read the P it held
+          if (i >= 3 && !g.wait(&m.pv_done[bi], ((i - 3) / 3) & 1, 5)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t ka = sK + st * L::KV_BYTES + w * 64 * 128;
+          const uint64_t kd = sdesc_sw128(sK + st * L::KV_BYTES + w * 64 * 128, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            umma_bf16_ta(tmem + L::TM_S + w * 64, tmem + L::TM_Q + kk * 8,
-                         sdesc_sw128(ka + (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32, 16, 1024), idS,
-                         kk > 0 ? 1u : 0u);
-          umma_commit(&m.s_full[w]);
-          if (i > 0 && !issue_pv(i - 1)) { ok = false; break; }
+            umma_bf16_ta(tmem + L::TM_S + bi * 64, tmem + L::TM_Q + kk * 8,
+                         sdesc_add(kd, (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32), idS, kk > 0 ? 1u : 0u);
+          umma_commit(&m.s_full[bi]);
+          // PV one step behind S: the slot S_{i+1} needs was freed by PV_{i-2},
+          // issued two groups earlier, so the issuer never waits on the group
+          // it has just queued
+          if (i >= 1 && !issue_pv(i - 1)) { ok = false; break; }
         }
       }
-      if (ok && i > 0) issue_pv(i - 1);
+      if (ok && i >= 1) ok = issue_pv(i - 1);
       umma_commit(&m.mma_final);
       g.drain(&m.mma_final, 0);
     }
@@ -180,7 +187,6 @@ __global__ void __launch_bounds__(320, 1)
     const size_t row = (size_t)(b * p.Hq + h) * p.N + qidx;
     const int32_t segq = p.seg ? p.seg[(size_t)b * p.N + qidx] : 0;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_base + L::TM_S + w * 64;
     const uint32_t tO = tmem + lane_base + L::TM_O + w * D;
     const float sl2 = p.scale_log2;
     // this warpgroup's half of the query row into TMEM, as bf16 pairs
@@ -209,14 +215,15 @@ __global__ void __launch_bounds__(320, 1)
         ok = g.wait(&m.kv_full[st], (j / NS) & 1, 6);
         if (!__all_sync(~0u, ok)) { ok = false; break; }
       }
-      ok = g.wait(&m.s_full[w], j & 1, 7);
+      const int i = 2 * j + w, bi = i % 3;
+      const uint32_t tS = tmem + lane_base + L::TM_S + bi * 64;
+      ok = g.wait(&m.s_full[bi], (i / 3) & 1, 7);
       if (!__all_sync(~0u, ok)) { ok = false; break; }
       tc_fence_after();
       float s[64];
       {
         uint32_t v0[32], v1[32];
-        tmem_ld32(tS, v0);
-        tmem_ld32(tS + 32, v1);
+        tmem_ld32x2(tS, tS + 32, v0, v1);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           s[e] = __uint_as_float(v0[e]);
@@ -225,21 +232,28 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (masked) {
         const int k0 = tk * kTile + w * 64;
+        const int4* g4 = reinterpret_cast<const int4*>(&m.segkv[st][w * 64]);
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          const int32_t gk = p.seg ? m.segkv[st][w * 64 + e] : 0;
-          s[e] = (k0 + e <= qidx && gk == segq) ? s[e] : -INFINITY;
+        for (int e4 = 0; e4 < 16; ++e4) {
+          const int4 gv = p.seg ? g4[e4] : make_int4(0, 0, 0, 0);
+          const int32_t gz[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = e4 * 4 + e;
+            s[c] = (k0 + c <= qidx && gz[e] == segq) ? s[c] : -INFINITY;
+          }
         }
       }
-      float mt = -INFINITY;
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int e = 0; e < 64; ++e) mt = fmaxf(mt, s[e]);
+      for (int e = 0; e < 64; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], s[e]);
+      const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const float ms = mt * sl2;
       if (__any_sync(~0u, ms > m_used + 8.f)) {
         const float m_new = fmaxf(m_used, ms);
         const float alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_new);
         if (j > 0) {  // O_w holds earlier tiles: rescale it once their PV is done
-          ok = g.wait(&m.pv_done[w], (j - 1) & 1, 8);
+          ok = g.wait(&m.pv_done[(i - 2) % 3], ((i - 2) / 3) & 1, 8);
           if (!__all_sync(~0u, ok)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
@@ -258,35 +272,27 @@ __global__ void __launch_bounds__(320, 1)
       const float moff = (m_used == -INFINITY) ? 0.f : m_used;
       // l sums the exact fp32 weights (for lse); lr sums the bf16-rounded
       // weights the PV product uses, so O / lr is a convex combination
-      float lsum = 0.f, lrsum = 0.f;
-      uint32_t pw[32];
+      float ls4[4] = {0.f, 0.f, 0.f, 0.f}, lr4[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t lo[16], hi[16];
 #pragma unroll
       for (int e = 0; e < 64; e += 2) {
         const float e0 = ex2(fmaf(s[e], sl2, -moff));
         const float e1 = ex2(fmaf(s[e + 1], sl2, -moff));
-        lsum += e0 + e1;
         const uint32_t x = pack_bf16x2(e0, e1);
-        lrsum += __uint_as_float(x << 16) + __uint_as_float(x & 0xFFFF0000u);
-        pw[e >> 1] = x;
+        ls4[(e >> 1) & 3] += e0 + e1;
+        lr4[(e >> 1) & 3] += __uint_as_float(x << 16) + __uint_as_float(x & 0xFFFF0000u);
+        if (e < 32) lo[e >> 1] = x; else hi[(e - 32) >> 1] = x;
       }
-      l += lsum;
-      lr += lrsum;
-      {  // P_w over the first 32 columns of this row's S_w
-        uint32_t lo[16], hi[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          lo[e] = pw[e];
-          hi[e] = pw[16 + e];
-        }
-        tmem_st16(tS, lo);
-        tmem_st16(tS + 16, hi);
-      }
+      l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+      lr += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
+      tmem_st16x2(tS, tS + 16, lo, hi);  // P_w over the first 32 columns of this row's S slot
       tc_fence_before();
-      mbar_arrive(&m.p_full[w]);
+      mbar_arrive(&m.p_full[bi]);
     }
     // ------------------------------------------------------------ combine + epilogue
     if (ok && j > 0) {
-      ok = g.wait(&m.pv_done[w], (j - 1) & 1, 9);
+      const int il = 2 * (j - 1) + w;
+      ok = g.wait(&m.pv_done[il % 3], (il / 3) & 1, 9);
       ok = __all_sync(~0u, ok);
     }
     if (ok) {
