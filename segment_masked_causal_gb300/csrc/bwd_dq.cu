@@ -2,23 +2,23 @@
 //
 // One CTA per (query tile of 128 rows, query head, batch row); it visits the
 // same key tiles as the forward (the changelog's PACKED dQ kernel: cross-
-// segment blocks skipped). Every key tile is processed as two 64-column
-// halves ("steps"):
-//   S  = Q K^T   (TMEM, 64 columns)   P  = exp(scale * S - lse)
-//   dP = dO V^T  (TMEM, 64 columns)   dS = P * (dP - delta)   (bf16, over S)
+// segment blocks skipped). Per key tile j:
+//   S  = Q K^T   (TMEM, 128 columns)   P  = exp(scale * S - lse)
+//   dP = dO V^T  (TMEM, 128 columns)   dS = P * (dP - delta)   (bf16, over S)
 //   dQ += dS K   (TMEM accumulator, dS read straight from TMEM)
 // and finally dQ *= scale. The probabilities are recomputed from the saved
 // log-sum-exp (mlx-train-perf 0.5.1 README, "Flash-attention training path":
 // the backward recomputes the tiles it needs from O(N) saved state).
 //
-// Q and dO stay in TMEM for the whole CTA (each row thread stores its own row
-// once), so the S and dP MMAs read only K and V from shared memory. S/dP of
-// consecutive steps alternate between two TMEM buffers: the MMA issuer starts
-// step i+1 while the softmax warps work on step i.
+// Every MMA is 128 x 128 (or 128 x D) with K = 16: wide enough that the one
+// issuing thread keeps the tensor pipe busy. TMEM holds dQ, one dP region and
+// two S regions used by alternate key tiles. The softmax warps release the dP
+// region as soon as they have loaded it, so the next tile's S and dP run on
+// the tensor core while this tile's dS is being formed.
 //
-// Warp roles: warp 0 TMA producer (K/V tiles, 3-stage ring), warp 1 MMA
-// issuer and TMEM owner, warps 2..9 two threads per query row, 32 key columns
-// each.
+// Warp roles: warp 0 TMA producer (Q and dO once; K through a 3-stage ring,
+// V through a 2-stage ring), warp 1 MMA issuer and TMEM owner, warps 2..9
+// two threads per query row, 64 key columns each.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -32,22 +32,23 @@ namespace {
 
 template <int D>
 struct DqLayout {
-  static constexpr int NS = 3;
-  static constexpr uint32_t KV_BYTES = 128 * D * 2;
-  static constexpr uint32_t KV_CHUNK = 128 * 128;  // one 64-column chunk of a 128-row tile
-  static constexpr uint32_t OFF_K = 0;
-  static constexpr uint32_t OFF_V = OFF_K + NS * KV_BYTES;
-  static constexpr uint32_t TILE_BYTES = OFF_V + NS * KV_BYTES;
+  static constexpr int NSK = 3, NSV = 2;
+  static constexpr uint32_t TB = 128 * D * 2;     // one 128-row tile of Q, dO, K or V
+  static constexpr uint32_t CHUNK = 128 * 128;    // one 64-column chunk of a 128-row tile
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_DO = OFF_Q + TB;
+  static constexpr uint32_t OFF_K = OFF_DO + TB;
+  static constexpr uint32_t OFF_V = OFF_K + NSK * TB;
+  static constexpr uint32_t TILE_BYTES = OFF_V + NSV * TB;
   static constexpr uint32_t MISC_BYTES = 2048;
   static constexpr uint32_t SMEM = TILE_BYTES + MISC_BYTES + 1024;
-  // TMEM: Q and dO as bf16 (D/2 columns each), dQ accumulator, two step buffers
-  // of 128 columns whose 64-column halves hold S and dP and swap roles on every use
-  static constexpr uint32_t TM_Q = 0, TM_DO = D / 2, TM_DQ = D, TM_BUF = 2 * D, TMEM_COLS = 512;
+  // TMEM: dQ accumulator, then S for even tiles, dP, S for odd tiles (128 columns each)
+  static constexpr uint32_t TM_DQ = 0, TM_S0 = 128, TM_DP = 256, TM_S1 = 384, TMEM_COLS = 512;
 };
 
 struct DqMisc {
-  uint64_t kv_full[3], kv_empty[3];
-  uint64_t qdo_ready, s_full[2], ds_full[2], dq_done[2], mma_final;
+  uint64_t q_full, k_full[3], k_empty[3], v_full[2], v_empty[2];
+  uint64_t s_full[2], dp_free[2], ds_full[2], dq_done[2], mma_final;
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) int32_t segkv[3][128];
@@ -55,15 +56,18 @@ struct DqMisc {
 
 template <int D>
 __global__ void __launch_bounds__(320, 1)
-    dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-              const __nv_bfloat16* __restrict__ q, const AttnParams p) {
+    dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+              const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+              const AttnParams p) {
   using L = DqLayout<D>;
-  constexpr int NS = L::NS;
+  constexpr int NSK = L::NSK, NSV = L::NSV;
   static_assert(sizeof(DqMisc) <= L::MISC_BYTES, "misc region");
+  static_assert(L::SMEM <= 232448, "shared memory");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   DqMisc& m = *reinterpret_cast<DqMisc*>(smem_raw);
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + sizeof(DqMisc) + 1023) & ~uintptr_t(1023));
+  const uint32_t sQ = smem_u32(base + L::OFF_Q), sDO = smem_u32(base + L::OFF_DO);
   const uint32_t sK = smem_u32(base + L::OFF_K), sV = smem_u32(base + L::OFF_V);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -76,13 +80,18 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     m.abort_flag = 0;
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&m.kv_full[s], 1);
-      mbar_init(&m.kv_empty[s], 1);
+    mbar_init(&m.q_full, 1);
+    for (int s = 0; s < NSK; ++s) {
+      mbar_init(&m.k_full[s], 1);
+      mbar_init(&m.k_empty[s], 1);
     }
-    mbar_init(&m.qdo_ready, 256);
+    for (int s = 0; s < NSV; ++s) {
+      mbar_init(&m.v_full[s], 1);
+      mbar_init(&m.v_empty[s], 1);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&m.s_full[s], 1);
+      mbar_init(&m.dp_free[s], 256);
       mbar_init(&m.ds_full[s], 256);
       mbar_init(&m.dq_done[s], 1);
     }
@@ -102,80 +111,91 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmDO);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
+      const int qrow = (b * p.Hq + h) * p.N + tq * kTile;
       const int krow0 = (b * p.Hkv + hk) * p.N;
-      int j = 0;
-      for (int tk = walk.first(); tk <= tq; tk = walk.next(tk), ++j) {
-        const int st = j % NS;
-        if (!g.wait(&m.kv_empty[st], ((j / NS) & 1) ^ 1, 1)) break;
-        mbar_expect_tx(&m.kv_full[st], 2 * L::KV_BYTES + (p.seg ? 512 : 0));
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_2d(base + L::OFF_K + st * L::KV_BYTES + c * L::KV_CHUNK, &tmK, &m.kv_full[st], c * 64,
-                      krow0 + tk * kTile);
-          tma_load_2d(base + L::OFF_V + st * L::KV_BYTES + c * L::KV_CHUNK, &tmV, &m.kv_full[st], c * 64,
-                      krow0 + tk * kTile);
-        }
-        if (p.seg) bulk_load(m.segkv[st], p.seg + (size_t)b * p.N + tk * kTile, 512, &m.kv_full[st]);
+      mbar_expect_tx(&m.q_full, 2 * L::TB);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_2d(base + L::OFF_Q + c * L::CHUNK, &tmQ, &m.q_full, c * 64, qrow);
+        tma_load_2d(base + L::OFF_DO + c * L::CHUNK, &tmDO, &m.q_full, c * 64, qrow);
       }
-      for (int i = (j > NS ? j - NS : 0); i < j; ++i) g.drain(&m.kv_full[i % NS], (i / NS) & 1);
+      int jk = 0, jv = 0;  // K and V tiles issued
+      for (int tk = walk.first(); tk <= tq; tk = walk.next(tk)) {
+        const int sk = jk % NSK, sv = jv % NSV;
+        if (!g.wait(&m.k_empty[sk], ((jk / NSK) & 1) ^ 1, 1)) break;
+        mbar_expect_tx(&m.k_full[sk], L::TB + (p.seg ? 512 : 0));
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(base + L::OFF_K + sk * L::TB + c * L::CHUNK, &tmK, &m.k_full[sk], c * 64, krow0 + tk * kTile);
+        if (p.seg) bulk_load(m.segkv[sk], p.seg + (size_t)b * p.N + tk * kTile, 512, &m.k_full[sk]);
+        ++jk;
+        if (!g.wait(&m.v_empty[sv], ((jv / NSV) & 1) ^ 1, 2)) break;
+        mbar_expect_tx(&m.v_full[sv], L::TB);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(base + L::OFF_V + sv * L::TB + c * L::CHUNK, &tmV, &m.v_full[sv], c * 64, krow0 + tk * kTile);
+        ++jv;
+      }
+      // no copy may still be landing when the CTA exits
+      g.drain(&m.q_full, 0);
+      for (int i = (jk > NSK ? jk - NSK : 0); i < jk; ++i) g.drain(&m.k_full[i % NSK], (i / NSK) & 1);
+      for (int i = (jv > NSV ? jv - NSV : 0); i < jv; ++i) g.drain(&m.v_full[i % NSV], (i / NSV) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, true);
-      // dQ += dS_i K_half(i): dS from TMEM, K rows of the half as the K dimension
-      auto issue_dq = [&](int i) -> bool {
-        const int bb = i & 1, st = (i >> 1) % NS, half = i & 1;
-        if (!g.wait(&m.ds_full[bb], (i >> 1) & 1, 2)) return false;
+      const uint64_t qd = sdesc_sw128(sQ, 16, 1024), dod = sdesc_sw128(sDO, 16, 1024);
+      // dQ += dS_j K_j: dS from TMEM (thread-half h keeps the dS of its 64 key
+      // columns in S columns 64h..64h+31), K as the MN-major B operand
+      auto issue_dq = [&](int j) -> bool {
+        const int rs = j & 1, sk = j % NSK;
+        if (!g.wait(&m.ds_full[rs], (j >> 1) & 1, 3)) return false;
         tc_fence_after();
-        const uint32_t buf = tmem + L::TM_BUF + bb * 128 + (((i >> 1) & 1) ? 64 : 0);  // step i's S half
-        const uint64_t kd = sdesc_sw128(sK + st * L::KV_BYTES + half * 64 * 128, L::KV_CHUNK, 1024);
-        const uint32_t acc0 = i > 0 ? 1u : 0u;
+        const uint32_t sreg = tmem + (rs ? L::TM_S1 : L::TM_S0);
+        const uint64_t kmn = sdesc_sw128(sK + sk * L::TB, L::CHUNK, 1024);
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_ta(tmem + L::TM_DQ, buf + (kk >> 1) * 32 + (kk & 1) * 8, sdesc_add(kd, kk * 2048), idQ,
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_ta(tmem + L::TM_DQ, sreg + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(kmn, kk * 2048), idQ,
                        kk > 0 ? 1u : acc0);
-        umma_commit(&m.dq_done[bb]);
-        if (half == 1) umma_commit(&m.kv_empty[st]);
+        umma_commit(&m.dq_done[rs]);
+        umma_commit(&m.k_empty[sk]);
         return true;
       };
-      bool ok = g.wait(&m.qdo_ready, 0, 3);
-      tc_fence_after();
-      int i = 0, j = 0;
+      bool ok = g.wait(&m.q_full, 0, 4);
+      int j = 0;
       for (int tk = walk.first(); ok && tk <= tq; tk = walk.next(tk), ++j) {
-        const int st = j % NS;
-        if (!g.wait(&m.kv_full[st], (j / NS) & 1, 4)) { ok = false; break; }
-        for (int half = 0; half < 2; ++half, ++i) {
-          const int bb = i & 1;
-          // Buffer bb's halves swap roles on every use: S of step i goes where
-          // dP of step i-2 was (free once that softmax read it), dP where step
-          // i-2's dS was (free once its dQ MMAs ran).
-          const uint32_t buf = tmem + L::TM_BUF + bb * 128;
-          const uint32_t sO = ((i >> 1) & 1) ? 64 : 0, dO_ = 64 - sO;
-          const uint64_t kd = sdesc_sw128(sK + st * L::KV_BYTES + half * 64 * 128, 16, 1024);
-          const uint64_t vd = sdesc_sw128(sV + st * L::KV_BYTES + half * 64 * 128, 16, 1024);
-          tc_fence_after();
+        const int rs = j & 1, sk = j % NSK, sv = j % NSV;
+        // S_j goes into the S region of tile j-2, free once dQ of tile j-2 ran
+        if (!g.wait(&m.k_full[sk], (j / NSK) & 1, 5)) { ok = false; break; }
+        if (j >= 2 && !g.wait(&m.dq_done[rs], ((j - 2) >> 1) & 1, 6)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sreg = tmem + (rs ? L::TM_S1 : L::TM_S0);
+        const uint64_t kd = sdesc_sw128(sK + sk * L::TB, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
-            umma_bf16_ta(buf + sO, tmem + L::TM_Q + kk * 8, sdesc_add(kd, ko), idS, kk > 0 ? 1u : 0u);
-          }
-          // only now wait for step i-2's dQ MMAs: S of step i is queued behind them
-          if (i >= 2 && !g.wait(&m.dq_done[bb], ((i - 2) >> 1) & 1, 5)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
-            umma_bf16_ta(buf + dO_, tmem + L::TM_DO + kk * 8, sdesc_add(vd, ko), idS, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(&m.s_full[bb]);
-          if (i > 0 && !issue_dq(i - 1)) { ok = false; break; }
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
+          umma_bf16(sreg, sdesc_add(qd, ko), sdesc_add(kd, ko), idS, kk > 0 ? 1u : 0u);
         }
+        // dP_j into the dP region once the softmax of tile j-1 has read it
+        if (!g.wait(&m.v_full[sv], (j / NSV) & 1, 7)) { ok = false; break; }
+        if (j >= 1 && !g.wait(&m.dp_free[(j - 1) & 1], ((j - 1) >> 1) & 1, 8)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t vd = sdesc_sw128(sV + sv * L::TB, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
+          umma_bf16(tmem + L::TM_DP, sdesc_add(dod, ko), sdesc_add(vd, ko), idS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&m.s_full[rs]);
+        umma_commit(&m.v_empty[sv]);
+        if (j > 0 && !issue_dq(j - 1)) { ok = false; break; }
       }
-      if (ok && i > 0) issue_dq(i - 1);
+      if (ok && j > 0) issue_dq(j - 1);
       umma_commit(&m.mma_final);
       g.drain(&m.mma_final, 0);
     }
@@ -183,7 +203,7 @@ __global__ void __launch_bounds__(320, 1)
   } else {
     // ------------------------------------------------------------ softmax
     const int quarter = warp & 3;
-    const int hsel = (warp - 2) >> 2;
+    const int hsel = (warp - 2) >> 2;  // which 64 key columns of every tile
     const int r = quarter * 32 + lane;
     const int qidx = tq * kTile + r;
     const size_t row = (size_t)(b * p.Hq + h) * p.N + qidx;
@@ -192,78 +212,65 @@ __global__ void __launch_bounds__(320, 1)
     const float dlt = p.delta[row];
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
-    // this thread's half of its Q and dO rows into TMEM, as bf16 pairs
-    {
-      const uint32_t* qsrc = reinterpret_cast<const uint32_t*>(q + row * D) + hsel * (D / 4);
-      const uint32_t* dsrc = reinterpret_cast<const uint32_t*>(p.dout + row * D) + hsel * (D / 4);
-#pragma unroll
-      for (int c0 = 0; c0 < D / 4; c0 += 16) {
-        uint32_t a[16], d[16];
-#pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          const uint4 x = __ldg(reinterpret_cast<const uint4*>(qsrc + c0 + e));
-          const uint4 y = __ldg(reinterpret_cast<const uint4*>(dsrc + c0 + e));
-          a[e] = x.x; a[e + 1] = x.y; a[e + 2] = x.z; a[e + 3] = x.w;
-          d[e] = y.x; d[e + 1] = y.y; d[e + 2] = y.z; d[e + 3] = y.w;
-        }
-        tmem_st16(tmem + lane_base + L::TM_Q + hsel * (D / 4) + c0, a);
-        tmem_st16(tmem + lane_base + L::TM_DO + hsel * (D / 4) + c0, d);
-      }
-      tc_fence_before();
-      mbar_arrive(&m.qdo_ready);
-    }
     bool ok = true;
-    int i = 0, j = 0;
-    for (int tk = walk.first(); ok && tk <= tq; tk = walk.next(tk), ++j) {
-      const int st = j % NS;
+    int j = 0;
+    for (int tk = walk.first(); tk <= tq; tk = walk.next(tk), ++j) {
+      const int rs = j & 1, sk = j % NSK;
       const bool masked = !tile_pair_full(tq, walk.qt, tk, trow[tk]);
-      if (masked && p.seg) {  // segment ids of this key tile arrived with it
-        ok = g.wait(&m.kv_full[st], (j / NS) & 1, 6);
+      if (masked && p.seg) {  // segment ids of this key tile arrived with K
+        ok = g.wait(&m.k_full[sk], (j / NSK) & 1, 9);
         if (!__all_sync(~0u, ok)) { ok = false; break; }
       }
-      for (int half = 0; half < 2; ++half, ++i) {
-        const int bb = i & 1;
-        ok = g.wait(&m.s_full[bb], (i >> 1) & 1, 7);
-        if (!__all_sync(~0u, ok)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t sO = ((i >> 1) & 1) ? 64 : 0;
-        const uint32_t buf = tmem + lane_base + L::TM_BUF + bb * 128 + sO + hsel * 32;
-        uint32_t sv[32], dp[32];
-        tmem_ld32x2(buf, tmem + lane_base + L::TM_BUF + bb * 128 + (64 - sO) + hsel * 32, sv, dp);
-        const int c0 = half * 64 + hsel * 32;  // key column within the tile
-        const int k0 = tk * kTile + c0;
-        uint32_t dw[16];
-        float sz[32];
+      ok = g.wait(&m.s_full[rs], (j >> 1) & 1, 10);
+      if (!__all_sync(~0u, ok)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sreg = tmem + lane_base + (rs ? L::TM_S1 : L::TM_S0) + hsel * 64;
+      const uint32_t dreg = tmem + lane_base + L::TM_DP + hsel * 64;
+      uint32_t s0[32], s1[32], d0[32], d1[32];
+      tmem_ld32x2(sreg, dreg, s0, d0);
+      tmem_ld32x2(sreg + 32, dreg + 32, s1, d1);
+      // the dP region may now take the next tile's dP
+      tc_fence_before();
+      mbar_arrive(&m.dp_free[rs]);
+      const int c0 = hsel * 64;
+      const int k0 = tk * kTile + c0;
+      float sz[64];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) sz[e] = __uint_as_float(sv[e]);
-        if (masked) {
-          const int4* g4 = reinterpret_cast<const int4*>(&m.segkv[st][c0]);
+      for (int e = 0; e < 32; ++e) {
+        sz[e] = __uint_as_float(s0[e]);
+        sz[32 + e] = __uint_as_float(s1[e]);
+      }
+      if (masked) {
+        const int4* g4 = reinterpret_cast<const int4*>(&m.segkv[sk][c0]);
 #pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const int4 gv = p.seg ? g4[e4] : make_int4(0, 0, 0, 0);
-            const int32_t gz[4] = {gv.x, gv.y, gv.z, gv.w};
+        for (int e4 = 0; e4 < 16; ++e4) {
+          const int4 gv = p.seg ? g4[e4] : make_int4(0, 0, 0, 0);
+          const int32_t gz[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = e4 * 4 + e;
-              sz[c] = (k0 + c <= qidx && gz[e] == segq) ? sz[c] : -INFINITY;
-            }
+          for (int e = 0; e < 4; ++e) {
+            const int c = e4 * 4 + e;
+            sz[c] = (k0 + c <= qidx && gz[e] == segq) ? sz[c] : -INFINITY;
           }
         }
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float p0 = ex2(fmaf(sz[e], sl2, -lse2)), p1 = ex2(fmaf(sz[e + 1], sl2, -lse2));
-          dw[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - dlt), p1 * (__uint_as_float(dp[e + 1]) - dlt));
-        }
-        tmem_st16(buf, dw);  // dS over this thread's own S columns
-        tc_fence_before();
-        mbar_arrive(&m.ds_full[bb]);
       }
+      uint32_t w0[16], w1[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        const float p0 = ex2(fmaf(sz[e], sl2, -lse2)), p1 = ex2(fmaf(sz[e + 1], sl2, -lse2));
+        w0[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(d0[e]) - dlt), p1 * (__uint_as_float(d0[e + 1]) - dlt));
+        const float p2 = ex2(fmaf(sz[32 + e], sl2, -lse2)), p3 = ex2(fmaf(sz[33 + e], sl2, -lse2));
+        w1[e >> 1] = pack_bf16x2(p2 * (__uint_as_float(d1[e]) - dlt), p3 * (__uint_as_float(d1[e + 1]) - dlt));
+      }
+      // dS over this thread's own (already read) S columns: 64 keys -> 32 columns
+      tmem_st16x2(sreg, sreg + 16, w0, w1);
+      tc_fence_before();
+      mbar_arrive(&m.ds_full[rs]);
     }
-    if (ok && i > 0) {
-      ok = g.wait(&m.dq_done[(i - 1) & 1], ((i - 1) >> 1) & 1, 10);
+    if (ok && j > 0) {
+      ok = g.wait(&m.dq_done[(j - 1) & 1], ((j - 1) >> 1) & 1, 11);
       ok = __all_sync(~0u, ok);
     }
-    if (ok && i > 0) {
+    if (ok && j > 0) {
       tc_fence_after();
       uint4* drow = reinterpret_cast<uint4*>(p.dq + row * D);
       const float sc = p.scale;
@@ -295,16 +302,15 @@ template <int D>
 cudaError_t launch_dq_d(const AttnParams& p, const void* q, const void* k, const void* v, const void* dout,
                         cudaStream_t st) {
   using L = DqLayout<D>;
-  CUtensorMap tk, tv;
-  const uint64_t krows = (uint64_t)p.B * p.Hkv * p.N;
-  if (!tmap_bf16_2d_sw128(&tk, k, D, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, D, krows, 128))
+  CUtensorMap tq, tdo, tk, tv;
+  const uint64_t qrows = (uint64_t)p.B * p.Hq * p.N, krows = (uint64_t)p.B * p.Hkv * p.N;
+  if (!tmap_bf16_2d_sw128(&tq, q, D, qrows, 128) || !tmap_bf16_2d_sw128(&tdo, dout, D, qrows, 128) ||
+      !tmap_bf16_2d_sw128(&tk, k, D, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, D, krows, 128))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
-  AttnParams pp = p;
-  pp.dout = static_cast<const __nv_bfloat16*>(dout);
   dim3 grid(p.T * p.Hq * p.B);
-  dq_kernel<D><<<grid, 320, L::SMEM, st>>>(tk, tv, static_cast<const __nv_bfloat16*>(q), pp);
+  dq_kernel<D><<<grid, 320, L::SMEM, st>>>(tq, tdo, tk, tv, p);
   return cudaGetLastError();
 }
 
