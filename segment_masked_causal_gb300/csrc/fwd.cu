@@ -7,25 +7,26 @@
 // not entirely visible. The saved state is O and its log-sum-exp
 // (mlx-train-perf 0.5.1 README, "Flash-attention training path").
 //
-// Every key tile is split into two 64-key halves ("steps"; step i = 2 * tile +
-// half). Half h of every tile goes to softmax warpgroup h, which keeps its own running maximum, sums and O
-// accumulator (TMEM); the two partial results are combined once at the end:
+// The visited key tiles alternate between two softmax warpgroups: warpgroup w
+// takes tiles w, w+2, w+4, ... and keeps its own S buffer, running maximum,
+// sums and O accumulator in TMEM; the two partial results are combined once
+// at the end:
 //   O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / (l_0 2^(m_0 - m) + l_1 2^(m_1 - m)).
-// Per half:  S_h = Q K_h^T (TMEM, 64 columns; Q resident in TMEM as the A
-// operand), P_h = 2^(S_h log2e scale - m) written back as bf16 over S_h and
-// fed to O_h += P_h V_h straight from TMEM. Shared memory carries only the
-// K/V ring. S buffers rotate over three 64-column slots and the MMA issuer
-// queues S_{i+1} before PV_i, so a slot it must wait for was freed by a PV
-// issued two groups earlier and the tensor pipe never drains.
+// Per tile: S = Q K^T (128 x 128, Q and K in shared memory), P = 2^(S log2e
+// scale - m) written back as bf16 over S and fed to O += P V straight from
+// TMEM. Every MMA is at least 128 x D x 16, wide enough that the one issuing
+// thread keeps the tensor pipe busy; while one warpgroup computes its P the
+// tensor core runs the other warpgroup's PV and S.
 //
 // Online softmax works in log2 units of the scaled score and rescales an O
 // accumulator only when its running maximum rises by more than 8 (a factor
 // 256); P is always computed against the maximum in use, so O and l stay
 // consistent and O / l is exact in real arithmetic.
 //
-// Warp roles: warp 0 TMA producer (K/V ring), warp 1 MMA issuer and TMEM
-// owner, warps 2..5 warpgroup 0 and warps 6..9 warpgroup 1 (one query row per
-// thread in each).
+// Warp roles: warp 0 TMA producer (Q once; K through a 3-stage ring, V and
+// the key tile's segment ids through a 2-stage ring), warp 1 MMA issuer and
+// TMEM owner, warps 2..5 warpgroup 0 and warps 6..9 warpgroup 1 (one query
+// row per thread in each).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -39,39 +40,41 @@ namespace {
 
 template <int D>
 struct FwdLayout {
-  static constexpr int NS = (D == 128) ? 3 : 4;   // K/V stages
-  static constexpr uint32_t KV_BYTES = 128 * D * 2;
-  static constexpr uint32_t KV_CHUNK = 128 * 128;  // one 64-column chunk of a 128-row tile
-  static constexpr uint32_t OFF_K = 0;
-  static constexpr uint32_t OFF_V = OFF_K + NS * KV_BYTES;
-  static constexpr uint32_t TILE_BYTES = OFF_V + NS * KV_BYTES;
+  static constexpr int NSK = 3, NSV = 2;
+  static constexpr uint32_t TB = 128 * D * 2;   // one 128-row tile of Q, K or V
+  static constexpr uint32_t CHUNK = 128 * 128;  // one 64-column chunk of a 128-row tile
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + TB;
+  static constexpr uint32_t OFF_V = OFF_K + NSK * TB;
+  static constexpr uint32_t TILE_BYTES = OFF_V + NSV * TB;
   static constexpr uint32_t MISC_BYTES = 8192;
   static constexpr uint32_t SMEM = TILE_BYTES + MISC_BYTES + 1024;
-  // TMEM: three rotating 64-column S buffers, Q as bf16 (D/2 columns), O_0, O_1
-  static constexpr uint32_t TM_S = 0, TM_Q = 192, TM_O = 256, TMEM_COLS = 512;
+  // TMEM: S_0, S_1 (128 columns each), O_0 at 256, O_1 at 384 (D columns each)
+  static constexpr uint32_t TM_S = 0, TM_O = 256, TMEM_COLS = 512;
 };
 
 struct FwdMisc {
-  uint64_t kv_full[4], kv_empty[4];
-  uint64_t q_ready, s_full[3], p_full[3], pv_done[3], comb_ready, mma_final;
+  uint64_t q_full, k_full[3], k_empty[3], v_full[2], v_empty[2];
+  uint64_t s_full[2], p_full[2], pv_done[2], comb_ready, mma_final;
   uint32_t tmem_base;
   int abort_flag;
-  alignas(16) int32_t segkv[4][128];
+  alignas(16) int32_t segkv[2][128];
   float mst[2][128], lst[2][128], lrst[2][128];  // per-warpgroup row statistics for the final combine
 };
 
 template <int D>
 __global__ void __launch_bounds__(320, 1)
-    fwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-               const __nv_bfloat16* __restrict__ q, const AttnParams p) {
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   using L = FwdLayout<D>;
-  constexpr int NS = L::NS;
+  constexpr int NSK = L::NSK, NSV = L::NSV;
   static_assert(sizeof(FwdMisc) <= L::MISC_BYTES, "misc region");
+  static_assert(L::SMEM <= 232448, "shared memory");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   FwdMisc& m = *reinterpret_cast<FwdMisc*>(smem_raw);
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + sizeof(FwdMisc) + 1023) & ~uintptr_t(1023));
-  const uint32_t sK = smem_u32(base + L::OFF_K), sV = smem_u32(base + L::OFF_V);
+  const uint32_t sQ = smem_u32(base + L::OFF_Q), sK = smem_u32(base + L::OFF_K), sV = smem_u32(base + L::OFF_V);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // longest causal rows first, across all heads and batch rows
@@ -83,12 +86,16 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     m.abort_flag = 0;
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&m.kv_full[s], 1);
-      mbar_init(&m.kv_empty[s], 1);
+    mbar_init(&m.q_full, 1);
+    for (int s = 0; s < NSK; ++s) {
+      mbar_init(&m.k_full[s], 1);
+      mbar_init(&m.k_empty[s], 1);
     }
-    mbar_init(&m.q_ready, 256);
-    for (int s = 0; s < 3; ++s) {
+    for (int s = 0; s < NSV; ++s) {
+      mbar_init(&m.v_full[s], 1);
+      mbar_init(&m.v_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&m.s_full[s], 1);
       mbar_init(&m.p_full[s], 128);
       mbar_init(&m.pv_done[s], 1);
@@ -110,70 +117,81 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
+      const int qrow = (b * p.Hq + h) * p.N + tq * kTile;
       const int krow0 = (b * p.Hkv + hk) * p.N;
-      int j = 0;
-      for (int tk = walk.first(); tk <= tq; tk = walk.next(tk), ++j) {
-        const int st = j % NS;
-        if (!g.wait(&m.kv_empty[st], ((j / NS) & 1) ^ 1, 1)) break;
-        mbar_expect_tx(&m.kv_full[st], 2 * L::KV_BYTES + (p.seg ? 512 : 0));
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_2d(base + L::OFF_K + st * L::KV_BYTES + c * L::KV_CHUNK, &tmK, &m.kv_full[st], c * 64,
-                      krow0 + tk * kTile);
-          tma_load_2d(base + L::OFF_V + st * L::KV_BYTES + c * L::KV_CHUNK, &tmV, &m.kv_full[st], c * 64,
-                      krow0 + tk * kTile);
-        }
-        if (p.seg) bulk_load(m.segkv[st], p.seg + (size_t)b * p.N + tk * kTile, 512, &m.kv_full[st]);
+      mbar_expect_tx(&m.q_full, L::TB);
+      for (int c = 0; c < D / 64; ++c) tma_load_2d(base + L::OFF_Q + c * L::CHUNK, &tmQ, &m.q_full, c * 64, qrow);
+      int jk = 0, jv = 0;
+      for (int tk = walk.first(); tk <= tq; tk = walk.next(tk)) {
+        const int sk = jk % NSK, sv = jv % NSV;
+        if (!g.wait(&m.k_empty[sk], ((jk / NSK) & 1) ^ 1, 1)) break;
+        mbar_expect_tx(&m.k_full[sk], L::TB);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(base + L::OFF_K + sk * L::TB + c * L::CHUNK, &tmK, &m.k_full[sk], c * 64, krow0 + tk * kTile);
+        ++jk;
+        if (!g.wait(&m.v_empty[sv], ((jv / NSV) & 1) ^ 1, 2)) break;
+        mbar_expect_tx(&m.v_full[sv], L::TB + (p.seg ? 512 : 0));
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(base + L::OFF_V + sv * L::TB + c * L::CHUNK, &tmV, &m.v_full[sv], c * 64, krow0 + tk * kTile);
+        if (p.seg) bulk_load(m.segkv[sv], p.seg + (size_t)b * p.N + tk * kTile, 512, &m.v_full[sv]);
+        ++jv;
       }
-      for (int i = (j > NS ? j - NS : 0); i < j; ++i) g.drain(&m.kv_full[i % NS], (i / NS) & 1);
+      // no copy may still be landing when the CTA exits
+      g.drain(&m.q_full, 0);
+      for (int i = (jk > NSK ? jk - NSK : 0); i < jk; ++i) g.drain(&m.k_full[i % NSK], (i / NSK) & 1);
+      for (int i = (jv > NSV ? jv - NSV : 0); i < jv; ++i) g.drain(&m.v_full[i % NSV], (i / NSV) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
-      // O_w += P_w V_half for step i = 2 * tile + half (warpgroup w = half);
-      // P_w sits in S slot i % 3
-      auto issue_pv = [&](int i) -> bool {
-        const int w = i & 1, st = (i >> 1) % NS, bi = i % 3;
-        if (!g.wait(&m.p_full[bi], (i / 3) & 1, 2)) return false;
+      const uint64_t qd = sdesc_sw128(sQ, 16, 1024);
+      const int n = walk.count();
+      // S_j = Q K_j^T into warpgroup (j & 1)'s S buffer
+      auto issue_s = [&](int j) -> bool {
+        const int w = j & 1, sk = j % NSK;
+        if (!g.wait(&m.k_full[sk], (j / NSK) & 1, 3)) return false;
         tc_fence_after();
-        const uint64_t vd = sdesc_sw128(sV + st * L::KV_BYTES + w * 64 * 128, L::KV_CHUNK, 1024);
-        const uint32_t acc0 = i >= 2 ? 1u : 0u;
+        const uint64_t kd = sdesc_sw128(sK + sk * L::TB, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_ta(tmem + L::TM_O + w * D, tmem + L::TM_S + bi * 64 + kk * 8, sdesc_add(vd, kk * 2048), idO,
-                       kk > 0 ? 1u : acc0);
-        umma_commit(&m.pv_done[bi]);
-        if (w == 1) umma_commit(&m.kv_empty[st]);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
+          umma_bf16(tmem + L::TM_S + w * 128, sdesc_add(qd, ko), sdesc_add(kd, ko), idS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&m.s_full[w]);
+        umma_commit(&m.k_empty[sk]);
         return true;
       };
-      bool ok = g.wait(&m.q_ready, 0, 3);
-      tc_fence_after();
-      int i = 0, j = 0;
-      for (int tk = walk.first(); ok && tk <= tq; tk = walk.next(tk), ++j) {
-        const int st = j % NS;
-        if (!g.wait(&m.kv_full[st], (j / NS) & 1, 4)) { ok = false; break; }
-        for (int w = 0; w < 2; ++w, ++i) {
-          const int bi = i % 3;
-          // slot bi is free once the PV of step i-3 has read the P it held
-          if (i >= 3 && !g.wait(&m.pv_done[bi], ((i - 3) / 3) & 1, 5)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t kd = sdesc_sw128(sK + st * L::KV_BYTES + w * 64 * 128, 16, 1024);
+      bool ok = g.wait(&m.q_full, 0, 4);
+      if (ok) ok = issue_s(0);
+      if (ok && n > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < n; ++j) {
+        const int w = j & 1, sv = j % NSV;
+        // O_w += P_j V_j, P_j read from warpgroup w's S buffer
+        if (!g.wait(&m.p_full[w], (j >> 1) & 1, 5) || !g.wait(&m.v_full[sv], (j / NSV) & 1, 6)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t vd = sdesc_sw128(sV + sv * L::TB, L::CHUNK, 1024);
+        const uint32_t acc0 = j >= 2 ? 1u : 0u;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_bf16_ta(tmem + L::TM_S + bi * 64, tmem + L::TM_Q + kk * 8,
-                         sdesc_add(kd, (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32), idS, kk > 0 ? 1u : 0u);
-          umma_commit(&m.s_full[bi]);
-          // PV one step behind S: the slot S_{i+1} needs was freed by PV_{i-2},
-          // issued two groups earlier, so the issuer never waits on the group
-          // it has just queued
-          if (i >= 1 && !issue_pv(i - 1)) { ok = false; break; }
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_ta(tmem + L::TM_O + w * 128, tmem + L::TM_S + w * 128 + kk * 8, sdesc_add(vd, kk * 2048), idO,
+                       kk > 0 ? 1u : acc0);
+        umma_commit(&m.pv_done[w]);
+        umma_commit(&m.v_empty[sv]);
+        // S_{j+2} reuses this S buffer: wait for the PV just queued to read P_j
+        if (j + 2 < n) {
+          if (!g.wait(&m.pv_done[w], (j >> 1) & 1, 7)) { ok = false; break; }
+          ok = issue_s(j + 2);
         }
       }
-      if (ok && i >= 1) ok = issue_pv(i - 1);
       umma_commit(&m.mma_final);
       g.drain(&m.mma_final, 0);
     }
@@ -181,79 +199,68 @@ __global__ void __launch_bounds__(320, 1)
   } else {
     // ------------------------------------------------------------ softmax
     const int quarter = warp & 3;
-    const int w = (warp - 2) >> 2;  // warpgroup: which 64-key half of every tile
+    const int w = (warp - 2) >> 2;  // warpgroup: takes every other visited key tile
     const int r = quarter * 32 + lane;
     const int qidx = tq * kTile + r;
     const size_t row = (size_t)(b * p.Hq + h) * p.N + qidx;
     const int32_t segq = p.seg ? p.seg[(size_t)b * p.N + qidx] : 0;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tO = tmem + lane_base + L::TM_O + w * D;
+    const uint32_t tS = tmem + lane_base + L::TM_S + w * 128;
+    const uint32_t tO = tmem + lane_base + L::TM_O + w * 128;
     const float sl2 = p.scale_log2;
-    // this warpgroup's half of the query row into TMEM, as bf16 pairs
-    {
-      const uint32_t* qsrc = reinterpret_cast<const uint32_t*>(q + row * D) + w * (D / 4);
-#pragma unroll
-      for (int c0 = 0; c0 < D / 4; c0 += 16) {
-        uint32_t a[16];
-#pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          const uint4 x = __ldg(reinterpret_cast<const uint4*>(qsrc + c0 + e));
-          a[e] = x.x; a[e + 1] = x.y; a[e + 2] = x.z; a[e + 3] = x.w;
-        }
-        tmem_st16(tmem + lane_base + L::TM_Q + w * (D / 4) + c0, a);
-      }
-      tc_fence_before();
-      mbar_arrive(&m.q_ready);
-    }
+    const int n = walk.count();
     float m_used = -INFINITY, l = 0.f, lr = 0.f;
     bool ok = true;
-    int j = 0;
-    for (int tk = walk.first(); tk <= tq; tk = walk.next(tk), ++j) {
-      const int st = j % NS;
+    int jj = 0, mine = 0, jlast = -1;
+    for (int tk = walk.first(); tk <= tq; tk = walk.next(tk), ++jj) {
+      if ((jj & 1) != w) continue;
       const bool masked = !tile_pair_full(tq, walk.qt, tk, trow[tk]);
-      if (masked && p.seg) {  // segment ids of this key tile arrived with it
-        ok = g.wait(&m.kv_full[st], (j / NS) & 1, 6);
+      if (masked && p.seg) {  // segment ids of this key tile arrived with V
+        ok = g.wait(&m.v_full[jj % NSV], (jj / NSV) & 1, 8);
         if (!__all_sync(~0u, ok)) { ok = false; break; }
       }
-      const int i = 2 * j + w, bi = i % 3;
-      const uint32_t tS = tmem + lane_base + L::TM_S + bi * 64;
-      ok = g.wait(&m.s_full[bi], (i / 3) & 1, 7);
+      ok = g.wait(&m.s_full[w], (jj >> 1) & 1, 9);
       if (!__all_sync(~0u, ok)) { ok = false; break; }
       tc_fence_after();
-      float s[64];
-      {
-        uint32_t v0[32], v1[32];
-        tmem_ld32x2(tS, tS + 32, v0, v1);
+      // Two passes over S in TMEM (the row never sits in registers whole):
+      // pass 1 finds the row maximum, pass 2 forms P 64 keys at a time.
+      const int k0 = tk * kTile;
+      const int4* g4 = reinterpret_cast<const int4*>(&m.segkv[jj % NSV][0]);
+      auto load64 = [&](int half, float (&x)[64]) {
+        uint32_t a0[32], a1[32];
+        tmem_ld32x2(tS + 64 * half, tS + 64 * half + 32, a0, a1);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          s[e] = __uint_as_float(v0[e]);
-          s[32 + e] = __uint_as_float(v1[e]);
+          x[e] = __uint_as_float(a0[e]);
+          x[32 + e] = __uint_as_float(a1[e]);
         }
-      }
-      if (masked) {
-        const int k0 = tk * kTile + w * 64;
-        const int4* g4 = reinterpret_cast<const int4*>(&m.segkv[st][w * 64]);
+        if (masked) {
 #pragma unroll
-        for (int e4 = 0; e4 < 16; ++e4) {
-          const int4 gv = p.seg ? g4[e4] : make_int4(0, 0, 0, 0);
-          const int32_t gz[4] = {gv.x, gv.y, gv.z, gv.w};
+          for (int e4 = 0; e4 < 16; ++e4) {
+            const int4 gv = p.seg ? g4[half * 16 + e4] : make_int4(0, 0, 0, 0);
+            const int32_t gz[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = e4 * 4 + e;
-            s[c] = (k0 + c <= qidx && gz[e] == segq) ? s[c] : -INFINITY;
+            for (int e = 0; e < 4; ++e) {
+              const int c = e4 * 4 + e;
+              x[c] = (k0 + 64 * half + c <= qidx && gz[e] == segq) ? x[c] : -INFINITY;
+            }
           }
         }
-      }
+      };
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int e = 0; e < 64; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], s[e]);
-      const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      const float ms = mt * sl2;
+      for (int hh = 0; hh < 2; ++hh) {
+        float x[64];
+        load64(hh, x);
+#pragma unroll
+        for (int e = 0; e < 64; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], x[e]);
+      }
+      const float ms = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
       if (__any_sync(~0u, ms > m_used + 8.f)) {
         const float m_new = fmaxf(m_used, ms);
         const float alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_new);
-        if (j > 0) {  // O_w holds earlier tiles: rescale it once their PV is done
-          ok = g.wait(&m.pv_done[(i - 2) % 3], ((i - 2) / 3) & 1, 8);
+        if (mine > 0) {  // O_w holds earlier tiles: rescale it once their PV is done
+          ok = g.wait(&m.pv_done[w], ((jj - 2) >> 1) & 1, 10);
           if (!__all_sync(~0u, ok)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
@@ -273,26 +280,32 @@ __global__ void __launch_bounds__(320, 1)
       // l sums the exact fp32 weights (for lse); lr sums the bf16-rounded
       // weights the PV product uses, so O / lr is a convex combination
       float ls4[4] = {0.f, 0.f, 0.f, 0.f}, lr4[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t lo[16], hi[16];
 #pragma unroll
-      for (int e = 0; e < 64; e += 2) {
-        const float e0 = ex2(fmaf(s[e], sl2, -moff));
-        const float e1 = ex2(fmaf(s[e + 1], sl2, -moff));
-        const uint32_t x = pack_bf16x2(e0, e1);
-        ls4[(e >> 1) & 3] += e0 + e1;
-        lr4[(e >> 1) & 3] += __uint_as_float(x << 16) + __uint_as_float(x & 0xFFFF0000u);
-        if (e < 32) lo[e >> 1] = x; else hi[(e - 32) >> 1] = x;
+      for (int hh = 0; hh < 2; ++hh) {  // 64 keys -> 32 packed columns, written over S already read
+        float x[64];
+        load64(hh, x);
+        uint32_t pw[2][16];
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          const float e0 = ex2(fmaf(x[e], sl2, -moff));
+          const float e1 = ex2(fmaf(x[e + 1], sl2, -moff));
+          const uint32_t y = pack_bf16x2(e0, e1);
+          ls4[(e >> 1) & 3] += e0 + e1;
+          lr4[(e >> 1) & 3] += __uint_as_float(y << 16) + __uint_as_float(y & 0xFFFF0000u);
+          pw[e >> 5][(e >> 1) & 15] = y;
+        }
+        tmem_st16x2(tS + 32 * hh, tS + 32 * hh + 16, pw[0], pw[1]);
       }
       l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       lr += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
-      tmem_st16x2(tS, tS + 16, lo, hi);  // P_w over the first 32 columns of this row's S slot
       tc_fence_before();
-      mbar_arrive(&m.p_full[bi]);
+      mbar_arrive(&m.p_full[w]);
+      ++mine;
+      jlast = jj;
     }
     // ------------------------------------------------------------ combine + epilogue
-    if (ok && j > 0) {
-      const int il = 2 * (j - 1) + w;
-      ok = g.wait(&m.pv_done[il % 3], (il / 3) & 1, 9);
+    if (ok && mine > 0) {
+      ok = g.wait(&m.pv_done[w], (jlast >> 1) & 1, 11);
       ok = __all_sync(~0u, ok);
     }
     if (ok) {
@@ -300,26 +313,34 @@ __global__ void __launch_bounds__(320, 1)
       m.lst[w][r] = l;
       m.lrst[w][r] = lr;
       mbar_arrive(&m.comb_ready);
-      ok = g.wait(&m.comb_ready, 0, 10);
+      ok = g.wait(&m.comb_ready, 0, 12);
       ok = __all_sync(~0u, ok);
     }
-    if (ok && j > 0) {
+    if (ok) {
       tc_fence_after();
+      const bool has1 = n > 1;  // warpgroup 1 saw at least one tile
       // both threads of a row evaluate the same expressions in the same order
-      const float m0 = m.mst[0][r], m1 = m.mst[1][r];
+      const float m0 = m.mst[0][r], m1 = has1 ? m.mst[1][r] : -INFINITY;
       const float mx = fmaxf(m0, m1);
       const float f0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - mx);
       const float f1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - mx);
-      const float lsum = m.lst[0][r] * f0 + m.lst[1][r] * f1;
-      const float inv = 1.f / (m.lrst[0][r] * f0 + m.lrst[1][r] * f1);
+      const float l0 = m.lst[0][r], l1 = has1 ? m.lst[1][r] : 0.f;
+      const float r0 = m.lrst[0][r], r1 = has1 ? m.lrst[1][r] : 0.f;
+      const float lsum = l0 * f0 + l1 * f1;
+      const float inv = 1.f / (r0 * f0 + r1 * f1);
       const float g0 = f0 * inv, g1 = f1 * inv;
       uint4* orow = reinterpret_cast<uint4*>(p.out + row * D);
-      const uint32_t tO0 = tmem + lane_base + L::TM_O, tO1 = tO0 + D;
+      const uint32_t tO0 = tmem + lane_base + L::TM_O, tO1 = tO0 + 128;
 #pragma unroll
       for (int c0 = w * (D / 2); c0 < (w + 1) * (D / 2); c0 += 32) {
         uint32_t a[32], bb[32];
-        tmem_ld32(tO0 + c0, a);
-        tmem_ld32(tO1 + c0, bb);
+        if (has1) {
+          tmem_ld32x2(tO0 + c0, tO1 + c0, a, bb);
+        } else {
+          tmem_ld32(tO0 + c0, a);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) bb[e] = 0u;
+        }
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           float o[8];
@@ -348,14 +369,15 @@ __global__ void __launch_bounds__(320, 1)
 template <int D>
 cudaError_t launch_fwd_d(const AttnParams& p, const void* q, const void* k, const void* v, cudaStream_t st) {
   using L = FwdLayout<D>;
-  CUtensorMap tk, tv;
-  const uint64_t krows = (uint64_t)p.B * p.Hkv * p.N;
-  if (!tmap_bf16_2d_sw128(&tk, k, D, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, D, krows, 128))
+  CUtensorMap tq, tk, tv;
+  const uint64_t qrows = (uint64_t)p.B * p.Hq * p.N, krows = (uint64_t)p.B * p.Hkv * p.N;
+  if (!tmap_bf16_2d_sw128(&tq, q, D, qrows, 128) || !tmap_bf16_2d_sw128(&tk, k, D, krows, 128) ||
+      !tmap_bf16_2d_sw128(&tv, v, D, krows, 128))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.T * p.Hq * p.B);
-  fwd_kernel<D><<<grid, 320, L::SMEM, st>>>(tk, tv, static_cast<const __nv_bfloat16*>(q), p);
+  fwd_kernel<D><<<grid, 320, L::SMEM, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
