@@ -76,6 +76,8 @@ typedef enum {
 /* Device status bits (pa_device_status). */
 #define PA_DEVERR_TIMEOUT 0x1u /* a bounded wait expired; bits 8.. name the site */
 #define PA_DEVERR_DRAIN 0x2u   /* teardown after a timeout could not drain       */
+#define PA_DEVERR_SMEM 0x4u    /* a kernel's shared memory was not 1 KiB aligned;
+                                  the kernel did no work                          */
 
 /* Workspace size in bytes for `dims` (0 if dims are invalid). */
 size_t pa_workspace_bytes(const pa_dims* dims);

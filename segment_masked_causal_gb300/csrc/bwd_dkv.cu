@@ -5,25 +5,32 @@
 // the last tile whose segment range overlaps the key tile's -- the query walk
 // ends at the key block's segment end instead of masking the rest
 // (mlx-train-perf 0.5.1 README, "Sequence packing", the 0.5.0 dK/dV change).
-// Per visited (query head, query tile) "step", with K and V resident in
+// Per visited (query head, query tile) step i, with K and V resident in
 // shared memory:
-//   S^T  = K Q^T   (TMEM, 128 columns)   P^T  = exp(scale * S^T - lse)
-//   dP^T = V dO^T  (TMEM, 128 columns)   dS^T = P^T * (dP^T - delta)
-//   dV += P^T dO   dK += dS^T Q          (TMEM accumulators; P^T and dS^T are
-//                                         written back as bf16 over S^T and fed
-//                                         to the MMA straight from TMEM)
-// and finally dK *= scale. The group's heads are summed inside the CTA in a
-// fixed order, so dK/dV need no atomics and are deterministic.
+//   S^T_i  = K Q_i^T   (TMEM)   P^T_i  = exp(scale * S^T_i - lse)   (rounded to bf16)
+//   dP^T_i = V dO_i^T  (TMEM)   dS^T_i = P^T_i * (dP^T_i - delta)
+//   dV += P^T_i dO_i   dK += dS^T_i Q_i
+// and finally dK *= scale. P^T_i and dS^T_i are written back as bf16 over
+// S^T_i and fed to the gradient MMAs straight from TMEM. The group's heads are
+// summed inside the CTA in a fixed order, so dK/dV need no atomics and are
+// deterministic.
 //
-// Every MMA is 128 x 128 (or 128 x D) x 16, wide enough that the one issuing
-// thread keeps the tensor pipe busy. Besides dV and dK, TMEM holds two
-// 128-column regions that swap roles every step: S^T of step i goes where dP^T
-// of step i-1 was (released by the softmax warps as soon as they have read
-// it), dP^T where step i-1's P^T/dS^T were (free once its gradient MMAs ran).
+// TMEM holds the dV and dK accumulators and two 128-column regions whose roles
+// swap every step: S^T_{i+1} goes where dP^T_i was as soon as the softmax
+// warps have read dP^T_i, and dP^T_{i+1} goes where P^T_i/dS^T_i were once
+// the gradient MMAs of step i have read them.
 //
-// Warp roles: warp 0 TMA producer (Q and dO tiles plus the query tile's lse,
-// delta and segment ids through a 2-stage ring), warp 1 MMA issuer and TMEM
-// owner, warps 2..9 softmax: two threads per key row, 64 query columns each.
+// Two warps issue MMAs, each in its own order, so neither waits behind the
+// other's dependencies: one issues S^T_i and dP^T_i (looking ahead), the
+// other dV_i and dK_i together once dS^T_i is ready. The
+// softmax warps run each step in two phases: phase A turns S^T_i into P^T_i,
+// phase B reads dP^T_i (releasing its region) and forms dS^T_i. Q rides a
+// 3-stage ring because each Q tile is read twice a step apart (by S^T_i and
+// by dK_i); dO rides a 2-stage ring.
+//
+// Warp roles: warp 0 TMA producer, warp 1 issues S^T/dP^T and owns TMEM,
+// warp 2 issues dV/dK, warps 3..10 softmax: two threads per key row (TMEM
+// lane quarter = warp index mod 4), 64 query columns each.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -35,45 +42,54 @@ namespace pa {
 
 namespace {
 
+constexpr int kDkvThreads = 352;
+constexpr int kQStages = 3, kDoStages = 2;
+
+struct DkvMisc {
+  uint64_t kv_full;
+  uint64_t q_full[kQStages], q_empty[kQStages];
+  uint64_t do_full[kDoStages], do_empty[kDoStages];
+  uint64_t s_full[2], dp_full[2], dp_free[2], ds_full[2], grad_done[2];
+  uint64_t final_sd, final_grad;
+  uint32_t tmem_base;
+  int abort_flag;
+  alignas(16) float lse[kQStages][128];
+  alignas(16) float dl[kDoStages][128];
+};
+
 template <int D>
 struct DkvLayout {
-  static constexpr int NS = 2;                   // Q/dO stages
   static constexpr uint32_t TB = 128 * D * 2;    // one 128-row tile of K, V, Q or dO
   static constexpr uint32_t CHUNK = 128 * 128;   // one 64-column chunk of a 128-row tile
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + TB;
   static constexpr uint32_t OFF_Q = OFF_V + TB;
-  static constexpr uint32_t OFF_DO = OFF_Q + NS * TB;
-  static constexpr uint32_t TILE_BYTES = OFF_DO + NS * TB;
-  static constexpr uint32_t MISC_BYTES = 4096;
-  static constexpr uint32_t SMEM = TILE_BYTES + MISC_BYTES + 1024;
-  // TMEM: dV, dK accumulators (D columns each), then two 128-column regions
+  static constexpr uint32_t OFF_DO = OFF_Q + kQStages * TB;
+  static constexpr uint32_t OFF_MISC = OFF_DO + kDoStages * TB;
+  static constexpr uint32_t SMEM = OFF_MISC + (uint32_t)((sizeof(DkvMisc) + 127) & ~size_t(127));
+  // TMEM: dV, dK accumulators (D columns each), then the two step regions
   static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_X = 256, TM_Y = 384, TMEM_COLS = 512;
-};
-
-struct DkvMisc {
-  uint64_t kv_full, q_full[2], q_empty[2];
-  uint64_t s_full[2], dp_free[2], pds_full[2], grad_done[2], mma_final;
-  uint32_t tmem_base;
-  int abort_flag;
-  alignas(16) float lse[2][128];
-  alignas(16) float dl[2][128];
-  alignas(16) int32_t segq[2][128];
+  // region holding S^T_i (then P^T_i and dS^T_i), and the one holding dP^T_i
+  static __device__ __forceinline__ uint32_t reg_s(int i) { return (i & 1) ? TM_Y : TM_X; }
+  static __device__ __forceinline__ uint32_t reg_dp(int i) { return (i & 1) ? TM_X : TM_Y; }
 };
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(kDkvThreads, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const AttnParams p) {
   using L = DkvLayout<D>;
-  constexpr int NS = L::NS;
-  static_assert(sizeof(DkvMisc) <= L::MISC_BYTES, "misc region");
   static_assert(L::SMEM <= 232448, "shared memory");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  DkvMisc& m = *reinterpret_cast<DkvMisc*>(smem_raw);
-  uint8_t* base = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + sizeof(DkvMisc) + 1023) & ~uintptr_t(1023));
+  // The 128-byte-swizzled tiles sit at fixed offsets from the start of dynamic
+  // shared memory, which must therefore be 1 KiB aligned; otherwise do nothing.
+  if (smem_u32_runtime(smem_raw) & 1023u) {
+    if (threadIdx.x == 0 && p.status) atomicOr(p.status, PA_DEVERR_SMEM);
+    return;
+  }
+  uint8_t* base = smem_raw;
+  DkvMisc& m = *reinterpret_cast<DkvMisc*>(base + L::OFF_MISC);
   const uint32_t sK = smem_u32(base + L::OFF_K), sV = smem_u32(base + L::OFF_V);
   const uint32_t sQ = smem_u32(base + L::OFF_Q), sDO = smem_u32(base + L::OFF_DO);
 
@@ -90,21 +106,25 @@ __global__ void __launch_bounds__(320, 1)
   if (threadIdx.x == 0) {
     m.abort_flag = 0;
     mbar_init(&m.kv_full, 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < kQStages; ++s) {
       mbar_init(&m.q_full[s], 1);
       mbar_init(&m.q_empty[s], 1);
     }
+    for (int s = 0; s < kDoStages; ++s) {
+      mbar_init(&m.do_full[s], 1);
+      mbar_init(&m.do_empty[s], 2);  // released by the dP^T and by the dV MMAs
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&m.s_full[s], 1);
+      mbar_init(&m.dp_full[s], 1);
       mbar_init(&m.dp_free[s], 256);
-      mbar_init(&m.pds_full[s], 256);
+      mbar_init(&m.ds_full[s], 256);
       mbar_init(&m.grad_done[s], 1);
     }
-    mbar_init(&m.mma_final, 1);
+    mbar_init(&m.final_sd, 1);
+    mbar_init(&m.final_grad, 1);
     fence_mbar_init();
   }
-  if (!p.seg)  // every token in one segment: the query-tile ids are all 0
-    for (int x = threadIdx.x; x < NS * 128; x += blockDim.x) (&m.segq[0][0])[x] = 0;
   if (warp == 1) {
     tmem_alloc(&m.tmem_base, L::TMEM_COLS);
     tmem_relinquish();
@@ -127,95 +147,127 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_2d(base + L::OFF_K + c * L::CHUNK, &tmK, &m.kv_full, c * 64, krow);
         tma_load_2d(base + L::OFF_V + c * L::CHUNK, &tmV, &m.kv_full, c * 64, krow);
       }
-      const uint32_t qbytes = 2 * L::TB + 1024 + (p.seg ? 512 : 0);
-      int i = 0;
+      int i = 0, nq = 0, nd = 0;  // steps, Q loads and dO loads issued
       bool ok = true;
       for (int hq = h0; ok && hq < h1; ++hq) {
         for (int tq = walk.first(); tq < walk.end(); tq = walk.next(tq), ++i) {
-          const int st = i % NS;
-          if (!g.wait(&m.q_empty[st], ((i / NS) & 1) ^ 1, 1)) { ok = false; break; }
+          const int qs = i % kQStages, ds = i % kDoStages;
           const int qrow = (b * p.Hq + hq) * p.N + tq * kTile;
-          mbar_expect_tx(&m.q_full[st], qbytes);
-          for (int c = 0; c < D / 64; ++c) {
-            tma_load_2d(base + L::OFF_Q + st * L::TB + c * L::CHUNK, &tmQ, &m.q_full[st], c * 64, qrow);
-            tma_load_2d(base + L::OFF_DO + st * L::TB + c * L::CHUNK, &tmDO, &m.q_full[st], c * 64, qrow);
-          }
-          bulk_load(m.lse[st], p.lse_in + qrow, 512, &m.q_full[st]);
-          bulk_load(m.dl[st], p.delta + qrow, 512, &m.q_full[st]);
-          if (p.seg) bulk_load(m.segq[st], p.seg + (size_t)b * p.N + tq * kTile, 512, &m.q_full[st]);
+          if (!g.wait(&m.q_empty[qs], ((i / kQStages) & 1) ^ 1, 1)) { ok = false; break; }
+          mbar_expect_tx(&m.q_full[qs], L::TB + 512);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(base + L::OFF_Q + qs * L::TB + c * L::CHUNK, &tmQ, &m.q_full[qs], c * 64, qrow);
+          bulk_load(m.lse[qs], p.lse_in + qrow, 512, &m.q_full[qs]);
+          ++nq;
+          if (!g.wait(&m.do_empty[ds], ((i / kDoStages) & 1) ^ 1, 2)) { ok = false; break; }
+          mbar_expect_tx(&m.do_full[ds], L::TB + 512);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(base + L::OFF_DO + ds * L::TB + c * L::CHUNK, &tmDO, &m.do_full[ds], c * 64, qrow);
+          bulk_load(m.dl[ds], p.delta + qrow, 512, &m.do_full[ds]);
+          ++nd;
         }
       }
+      // no copy may still be landing when the CTA exits
       g.drain(&m.kv_full, 0);
-      for (int k = (i > NS ? i - NS : 0); k < i; ++k) g.drain(&m.q_full[k % NS], (k / NS) & 1);
+      for (int k = (nq > kQStages ? nq - kQStages : 0); k < nq; ++k) g.drain(&m.q_full[k % kQStages], (k / kQStages) & 1);
+      for (int k = (nd > kDoStages ? nd - kDoStages : 0); k < nd; ++k)
+        g.drain(&m.do_full[k % kDoStages], (k / kDoStages) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);
-      const uint64_t kd = sdesc_sw128(sK, 16, 1024), vd = sdesc_sw128(sV, 16, 1024);
-      // dV += P^T dO, dK += dS^T Q for step i: thread-half h keeps P^T of its 64
-      // query columns in region columns 64h..64h+31 and dS^T in 64h+32..64h+63
-      auto issue_grad = [&](int i) -> bool {
-        const int bb = i & 1, st = i % NS;
-        if (!g.wait(&m.pds_full[bb], (i >> 1) & 1, 2)) return false;
+    // ------------------------------------------------------------ S^T / dP^T issuer
+    // The whole warp runs the issue loop and every wait; lane 0 alone issues
+    // the tcgen05 instructions.
+    const bool leader = lane == 0;
+    constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+    const uint64_t kd = sdesc_sw128(sK, 16, 1024), vd = sdesc_sw128(sV, 16, 1024);
+    bool ok = g.wait_warp(&m.kv_full, 0, 3);
+    int i = 0;
+    for (int hq = h0; ok && hq < h1; ++hq) {
+      for (int tq = walk.first(); tq < walk.end(); tq = walk.next(tq), ++i) {
+        const int qs = i % kQStages, ds = i % kDoStages;
+        if (!g.wait_warp(&m.q_full[qs], (i / kQStages) & 1, 4)) { ok = false; break; }
+        // S^T_i where dP^T_{i-1} was: free once the softmax has read it
+        if (i >= 1 && !g.wait_warp(&m.dp_free[(i - 1) & 1], ((i - 1) >> 1) & 1, 5)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sreg = tmem + (bb ? L::TM_Y : L::TM_X);
-        const uint64_t gq = sdesc_sw128(sQ + st * L::TB, L::CHUNK, 1024);
-        const uint64_t gd = sdesc_sw128(sDO + st * L::TB, L::CHUNK, 1024);
-        const uint32_t acc0 = i > 0 ? 1u : 0u;
+        const uint64_t qd = sdesc_sw128(sQ + qs * L::TB, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
+          if (leader) umma_bf16(tmem + L::reg_s(i), sdesc_add(kd, ko), sdesc_add(qd, ko), idS, kk > 0 ? 1u : 0u);
+        }
+        if (leader) umma_commit(&m.s_full[i & 1]);
+        __syncwarp();
+        // dP^T_i where P^T_{i-1}/dS^T_{i-1} were: free once their MMAs ran
+        if (!g.wait_warp(&m.do_full[ds], (i / kDoStages) & 1, 6)) { ok = false; break; }
+        if (i >= 1 && !g.wait_warp(&m.grad_done[(i - 1) & 1], ((i - 1) >> 1) & 1, 7)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t dod = sdesc_sw128(sDO + ds * L::TB, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
+          if (leader) umma_bf16(tmem + L::reg_dp(i), sdesc_add(vd, ko), sdesc_add(dod, ko), idS, kk > 0 ? 1u : 0u);
+        }
+        if (leader) {
+          umma_commit(&m.dp_full[i & 1]);
+          umma_commit(&m.do_empty[ds]);
+        }
+        __syncwarp();
+      }
+    }
+    if (leader) {
+      umma_commit(&m.final_sd);
+      g.drain(&m.final_sd, 0);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ dV / dK issuer
+    // thread-half h keeps P^T of its 64 query columns in columns 64h..64h+31
+    // of step j's S region and dS^T in columns 64h+32..64h+63
+    const bool leader = lane == 0;
+    constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);
+    bool ok = true;
+    int j = 0;
+    for (int hq = h0; ok && hq < h1; ++hq) {
+      for (int tq = walk.first(); tq < walk.end(); tq = walk.next(tq), ++j) {
+        const int qs = j % kQStages, ds = j % kDoStages;
+        const uint32_t sreg = tmem + L::reg_s(j);
+        // both gradient products of step j as one uninterrupted group of 16
+        // MMAs once dS^T_j is in place (the softmax threads wrote P^T_j before
+        // dS^T_j): an mbarrier wait right behind a short group starves the
+        // tensor pipe, and nothing waits on dV_j alone
+        if (!g.wait_warp(&m.do_full[ds], (j / kDoStages) & 1, 8)) { ok = false; break; }
+        if (!g.wait_warp(&m.q_full[qs], (j / kQStages) & 1, 9)) { ok = false; break; }
+        if (!g.wait_warp(&m.ds_full[j & 1], (j >> 1) & 1, 11)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t gd = sdesc_sw128(sDO + ds * L::TB, L::CHUNK, 1024);
+        const uint64_t gq = sdesc_sw128(sQ + qs * L::TB, L::CHUNK, 1024);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
           const uint32_t pcol = sreg + (kk >> 2) * 64 + (kk & 3) * 8;
-          const uint32_t acc = kk > 0 ? 1u : acc0;
-          umma_bf16_ta(tmem + L::TM_DV, pcol, sdesc_add(gd, kk * 2048), idG, acc);
-          umma_bf16_ta(tmem + L::TM_DK, pcol + 32, sdesc_add(gq, kk * 2048), idG, acc);
+          if (leader) {
+            umma_bf16_ta(tmem + L::TM_DV, pcol, sdesc_add(gd, kk * 2048), idG, acc);
+            umma_bf16_ta(tmem + L::TM_DK, pcol + 32, sdesc_add(gq, kk * 2048), idG, acc);
+          }
         }
-        umma_commit(&m.grad_done[bb]);
-        umma_commit(&m.q_empty[st]);
-        return true;
-      };
-      bool ok = g.wait(&m.kv_full, 0, 3);
-      int i = 0;
-      for (int hq = h0; ok && hq < h1; ++hq) {
-        for (int tq = walk.first(); tq < walk.end(); tq = walk.next(tq), ++i) {
-          const int bb = i & 1, st = i % NS;
-          const uint32_t sreg = tmem + (bb ? L::TM_Y : L::TM_X), dreg = tmem + (bb ? L::TM_X : L::TM_Y);
-          if (!g.wait(&m.q_full[st], (i / NS) & 1, 4)) { ok = false; break; }
-          // S^T_i where dP^T_{i-1} was: free once that softmax has read it
-          if (i >= 1 && !g.wait(&m.dp_free[(i - 1) & 1], ((i - 1) >> 1) & 1, 5)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t qd = sdesc_sw128(sQ + st * L::TB, 16, 1024);
-          const uint64_t dod = sdesc_sw128(sDO + st * L::TB, 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-            umma_bf16(sreg, sdesc_add(kd, ko), sdesc_add(qd, ko), idS, kk > 0 ? 1u : 0u);
-          }
-          if (i >= 1) {
-            // gradient MMAs of step i-1, then dP^T_i into the region they read
-            if (!issue_grad(i - 1)) { ok = false; break; }
-            if (!g.wait(&m.grad_done[(i - 1) & 1], ((i - 1) >> 1) & 1, 6)) { ok = false; break; }
-            tc_fence_after();
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-            umma_bf16(dreg, sdesc_add(vd, ko), sdesc_add(dod, ko), idS, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(&m.s_full[bb]);
+        if (leader) {
+          umma_commit(&m.grad_done[j & 1]);
+          umma_commit(&m.do_empty[ds]);
+          umma_commit(&m.q_empty[qs]);
         }
+        __syncwarp();
       }
-      if (ok && i > 0) issue_grad(i - 1);
-      umma_commit(&m.mma_final);
-      g.drain(&m.mma_final, 0);
+    }
+    if (leader) {
+      umma_commit(&m.final_grad);
+      g.drain(&m.final_grad, 0);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
     const int quarter = warp & 3;
-    const int hsel = (warp - 2) >> 2;  // which 64 query columns of every step
+    const int hsel = (warp - 3) >> 2;  // which 64 query columns of every step
     const int r = quarter * 32 + lane;
     const int kvidx = tk * kTile + r;
     const int32_t segk = p.seg ? p.seg[(size_t)b * p.N + kvidx] : 0;
@@ -226,63 +278,91 @@ __global__ void __launch_bounds__(320, 1)
     int i = 0;
     for (int hq = h0; ok && hq < h1; ++hq) {
       for (int tq = walk.first(); tq < walk.end(); tq = walk.next(tq), ++i) {
-        const int bb = i & 1, st = i % NS;
-        ok = g.wait(&m.q_full[st], (i / NS) & 1, 7);
+        const int qs = i % kQStages, ds = i % kDoStages;
+        // this step's lse and delta vectors (waited here, before this thread
+        // releases anything of the step, so neither ring can run ahead)
+        ok = g.wait(&m.q_full[qs], (i / kQStages) & 1, 12) && g.wait(&m.do_full[ds], (i / kDoStages) & 1, 13);
         if (!__all_sync(~0u, ok)) { ok = false; break; }
-        ok = g.wait(&m.s_full[bb], (i >> 1) & 1, 8);
+        ok = g.wait(&m.s_full[i & 1], (i >> 1) & 1, 14);
         if (!__all_sync(~0u, ok)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sreg = tmem + lane_base + (bb ? L::TM_Y : L::TM_X) + hsel * 64;
-        const uint32_t dreg = tmem + lane_base + (bb ? L::TM_X : L::TM_Y) + hsel * 64;
+        const uint32_t sreg = tmem + lane_base + L::reg_s(i) + hsel * 64;
+        const uint32_t dreg = tmem + lane_base + L::reg_dp(i) + hsel * 64;
         const bool masked = !tile_pair_full(tq, trow[tq], tk, kt);
-        uint32_t sv[2][32];
-        tmem_ld32x2(sreg, sreg + 32, sv[0], sv[1]);
-#pragma unroll
+        const int c0 = hsel * 64;        // first query column of this thread within the tile
+        const int q0 = tq * kTile + c0;  // its token index
+        // ---- phase A: P^T = exp2(S^T * scale*log2e - lse*log2e), bf16 over S^T.
+        // Two 32-column chunks in a rolled loop (the softmax code must stay
+        // small: instruction fetch, not arithmetic, limits these warps).
+#pragma unroll 1
         for (int c = 0; c < 2; ++c) {
-          uint32_t dp[32];
-          tmem_ld32(dreg + 32 * c, dp);
-          if (c == 1) {  // dP^T fully read: the region may take the next step's S^T
-            tc_fence_before();
-            mbar_arrive(&m.dp_free[bb]);
-          }
-          const int c0 = hsel * 64 + 32 * c;  // query column within the tile
-          const int q0 = tq * kTile + c0;
-          const float4* l4 = reinterpret_cast<const float4*>(&m.lse[st][c0]);
-          const float4* d4 = reinterpret_cast<const float4*>(&m.dl[st][c0]);
-          const int4* g4 = reinterpret_cast<const int4*>(&m.segq[st][c0]);
-          uint32_t pw[16], dw[16];
+          uint32_t sv[32];
+          tmem_ld32(sreg + 32 * c, sv);
+          const float4* l4 = reinterpret_cast<const float4*>(&m.lse[qs][c0 + 32 * c]);
+          const int qc = q0 + 32 * c;
+          uint32_t pw[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 lv = l4[e4], dv = d4[e4];
-            const float lz[4] = {lv.x, lv.y, lv.z, lv.w}, dz[4] = {dv.x, dv.y, dv.z, dv.w};
-            float sz[4], pz[4];
+            const float4 lv = l4[e4];
+            const float lz[4] = {lv.x, lv.y, lv.z, lv.w};
+            float sz[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sz[e] = __uint_as_float(sv[c][e4 * 4 + e]);
+            for (int e = 0; e < 4; ++e) sz[e] = __uint_as_float(sv[e4 * 4 + e]);
             if (masked) {
-              const int4 gv = g4[e4];
+              const int4 gv = p.seg ? __ldg(reinterpret_cast<const int4*>(p.seg + (size_t)b * p.N + qc) + e4)
+                                    : make_int4(0, 0, 0, 0);
               const int32_t gz[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                sz[e] = (q0 + e4 * 4 + e >= kvidx && gz[e] == segk) ? sz[e] : -INFINITY;
+                sz[e] = (qc + e4 * 4 + e >= kvidx && gz[e] == segk) ? sz[e] : -INFINITY;
             }
+            float pz[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) pz[e] = ex2(fmaf(sz[e], sl2, -lz[e] * 1.4426950408889634f));
             pw[e4 * 2] = pack_bf16x2(pz[0], pz[1]);
             pw[e4 * 2 + 1] = pack_bf16x2(pz[2], pz[3]);
-            dw[e4 * 2] = pack_bf16x2(pz[0] * (__uint_as_float(dp[e4 * 4]) - dz[0]),
-                                     pz[1] * (__uint_as_float(dp[e4 * 4 + 1]) - dz[1]));
-            dw[e4 * 2 + 1] = pack_bf16x2(pz[2] * (__uint_as_float(dp[e4 * 4 + 2]) - dz[2]),
-                                         pz[3] * (__uint_as_float(dp[e4 * 4 + 3]) - dz[3]));
           }
-          // P^T and dS^T over this thread's own S^T columns (all read above)
-          tmem_st16x2(sreg + 16 * c, sreg + 32 + 16 * c, pw, dw);
+          // packed columns 16c..16c+15: S^T columns this thread has already read
+          tmem_st16_nowait(sreg + 16 * c, pw);
         }
+        tmem_wait_st();
+        // ---- phase B: dS^T = P^T * (dP^T - delta), bf16 next to P^T. P^T is read
+        // back as the bf16 values the dV product uses, so dS^T is formed from
+        // the same rounded probabilities
+        ok = g.wait(&m.dp_full[i & 1], (i >> 1) & 1, 15);
+        if (!__all_sync(~0u, ok)) { ok = false; break; }
+        tc_fence_after();
+        const float4* d4 = reinterpret_cast<const float4*>(&m.dl[ds][c0]);
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          uint32_t dp[32], pb[16];
+          tmem_ld32_ld16(dreg + 32 * c, sreg + 16 * c, dp, pb);
+          if (c == 1) {  // dP^T fully read: its region may take the next S^T
+            tc_fence_before();
+            mbar_arrive(&m.dp_free[i & 1]);
+          }
+          uint32_t dw[16];
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 dv = d4[c * 8 + e4];
+            const float pp[4] = {__uint_as_float(pb[e4 * 2] << 16), __uint_as_float(pb[e4 * 2] & 0xFFFF0000u),
+                                 __uint_as_float(pb[e4 * 2 + 1] << 16),
+                                 __uint_as_float(pb[e4 * 2 + 1] & 0xFFFF0000u)};
+            dw[e4 * 2] = pack_bf16x2(pp[0] * (__uint_as_float(dp[e4 * 4]) - dv.x),
+                                     pp[1] * (__uint_as_float(dp[e4 * 4 + 1]) - dv.y));
+            dw[e4 * 2 + 1] = pack_bf16x2(pp[2] * (__uint_as_float(dp[e4 * 4 + 2]) - dv.z),
+                                         pp[3] * (__uint_as_float(dp[e4 * 4 + 3]) - dv.w));
+          }
+          // over this thread's own S^T columns 32..63 (read in phase A)
+          tmem_st16_nowait(sreg + 32 + 16 * c, dw);
+        }
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&m.pds_full[bb]);
+        mbar_arrive(&m.ds_full[i & 1]);
       }
     }
     if (ok && i > 0) {
-      ok = g.wait(&m.grad_done[(i - 1) & 1], ((i - 1) >> 1) & 1, 9);
+      ok = g.wait(&m.final_grad, 0, 16);
       ok = __all_sync(~0u, ok);
     }
     if (ok && i > 0) {
@@ -332,7 +412,7 @@ cudaError_t launch_dkv_d(const AttnParams& p, const void* q, const void* k, cons
   cudaError_t e = cudaFuncSetAttribute(dkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.T * p.Hkv * p.B);
-  dkv_kernel<D><<<grid, 320, L::SMEM, st>>>(tq, tdo, tk, tv, p);
+  dkv_kernel<D><<<grid, kDkvThreads, L::SMEM, st>>>(tq, tdo, tk, tv, p);
   return cudaGetLastError();
 }
 

@@ -145,57 +145,68 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, true);
-      const uint64_t qd = sdesc_sw128(sQ, 16, 1024), dod = sdesc_sw128(sDO, 16, 1024);
-      // dQ += dS_j K_j: dS from TMEM (thread-half h keeps the dS of its 64 key
-      // columns in S columns 64h..64h+31), K as the MN-major B operand
-      auto issue_dq = [&](int j) -> bool {
-        const int rs = j & 1, sk = j % NSK;
-        if (!g.wait(&m.ds_full[rs], (j >> 1) & 1, 3)) return false;
-        tc_fence_after();
-        const uint32_t sreg = tmem + (rs ? L::TM_S1 : L::TM_S0);
-        const uint64_t kmn = sdesc_sw128(sK + sk * L::TB, L::CHUNK, 1024);
-        const uint32_t acc0 = j > 0 ? 1u : 0u;
+    // The whole warp runs the issue loop and every wait; lane 0 alone issues
+    // the tcgen05 instructions.
+    const bool leader = lane == 0;
+    constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, true);
+    const uint64_t qd = sdesc_sw128(sQ, 16, 1024), dod = sdesc_sw128(sDO, 16, 1024);
+    // dQ += dS_j K_j: dS from TMEM (thread-half h keeps the dS of its 64 key
+    // columns in S columns 64h..64h+31), K as the MN-major B operand
+    auto issue_dq = [&](int j) -> bool {
+      const int rs = j & 1, sk = j % NSK;
+      if (!g.wait_warp(&m.ds_full[rs], (j >> 1) & 1, 3)) return false;
+      tc_fence_after();
+      const uint32_t sreg = tmem + (rs ? L::TM_S1 : L::TM_S0);
+      const uint64_t kmn = sdesc_sw128(sK + sk * L::TB, L::CHUNK, 1024);
+      const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
+      for (int kk = 0; kk < 8; ++kk)
+        if (leader)
           umma_bf16_ta(tmem + L::TM_DQ, sreg + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(kmn, kk * 2048), idQ,
                        kk > 0 ? 1u : acc0);
+      if (leader) {
         umma_commit(&m.dq_done[rs]);
         umma_commit(&m.k_empty[sk]);
-        return true;
-      };
-      bool ok = g.wait(&m.q_full, 0, 4);
-      int j = 0;
-      for (int tk = walk.first(); ok && tk <= tq; tk = walk.next(tk), ++j) {
-        const int rs = j & 1, sk = j % NSK, sv = j % NSV;
-        // S_j goes into the S region of tile j-2, free once dQ of tile j-2 ran
-        if (!g.wait(&m.k_full[sk], (j / NSK) & 1, 5)) { ok = false; break; }
-        if (j >= 2 && !g.wait(&m.dq_done[rs], ((j - 2) >> 1) & 1, 6)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t sreg = tmem + (rs ? L::TM_S1 : L::TM_S0);
-        const uint64_t kd = sdesc_sw128(sK + sk * L::TB, 16, 1024);
+      }
+      __syncwarp();
+      return true;
+    };
+    bool ok = g.wait_warp(&m.q_full, 0, 4);
+    int j = 0;
+    for (int tk = walk.first(); ok && tk <= tq; tk = walk.next(tk), ++j) {
+      const int rs = j & 1, sk = j % NSK, sv = j % NSV;
+      // S_j goes into the S region of tile j-2, free once dQ of tile j-2 ran
+      if (!g.wait_warp(&m.k_full[sk], (j / NSK) & 1, 5)) { ok = false; break; }
+      if (j >= 2 && !g.wait_warp(&m.dq_done[rs], ((j - 2) >> 1) & 1, 6)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sreg = tmem + (rs ? L::TM_S1 : L::TM_S0);
+      const uint64_t kd = sdesc_sw128(sK + sk * L::TB, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-          umma_bf16(sreg, sdesc_add(qd, ko), sdesc_add(kd, ko), idS, kk > 0 ? 1u : 0u);
-        }
-        // dP_j into the dP region once the softmax of tile j-1 has read it
-        if (!g.wait(&m.v_full[sv], (j / NSV) & 1, 7)) { ok = false; break; }
-        if (j >= 1 && !g.wait(&m.dp_free[(j - 1) & 1], ((j - 1) >> 1) & 1, 8)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t vd = sdesc_sw128(sV + sv * L::TB, 16, 1024);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
+        if (leader) umma_bf16(sreg, sdesc_add(qd, ko), sdesc_add(kd, ko), idS, kk > 0 ? 1u : 0u);
+      }
+      __syncwarp();
+      // dP_j into the dP region once the softmax of tile j-1 has read it
+      if (!g.wait_warp(&m.v_full[sv], (j / NSV) & 1, 7)) { ok = false; break; }
+      if (j >= 1 && !g.wait_warp(&m.dp_free[(j - 1) & 1], ((j - 1) >> 1) & 1, 8)) { ok = false; break; }
+      tc_fence_after();
+      const uint64_t vd = sdesc_sw128(sV + sv * L::TB, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-          umma_bf16(tmem + L::TM_DP, sdesc_add(dod, ko), sdesc_add(vd, ko), idS, kk > 0 ? 1u : 0u);
-        }
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
+        if (leader) umma_bf16(tmem + L::TM_DP, sdesc_add(dod, ko), sdesc_add(vd, ko), idS, kk > 0 ? 1u : 0u);
+      }
+      if (leader) {
         umma_commit(&m.s_full[rs]);
         umma_commit(&m.v_empty[sv]);
-        if (j > 0 && !issue_dq(j - 1)) { ok = false; break; }
       }
-      if (ok && j > 0) issue_dq(j - 1);
+      __syncwarp();
+      if (j > 0 && !issue_dq(j - 1)) { ok = false; break; }
+    }
+    if (ok && j > 0) issue_dq(j - 1);
+    if (leader) {
       umma_commit(&m.mma_final);
       g.drain(&m.mma_final, 0);
     }

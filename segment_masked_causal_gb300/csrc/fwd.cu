@@ -147,51 +147,61 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
-      const uint64_t qd = sdesc_sw128(sQ, 16, 1024);
-      const int n = walk.count();
-      // S_j = Q K_j^T into warpgroup (j & 1)'s S buffer
-      auto issue_s = [&](int j) -> bool {
-        const int w = j & 1, sk = j % NSK;
-        if (!g.wait(&m.k_full[sk], (j / NSK) & 1, 3)) return false;
-        tc_fence_after();
-        const uint64_t kd = sdesc_sw128(sK + sk * L::TB, 16, 1024);
+    // The whole warp runs the issue loop and every wait; lane 0 alone issues
+    // the tcgen05 instructions.
+    const bool leader = lane == 0;
+    constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
+    const uint64_t qd = sdesc_sw128(sQ, 16, 1024);
+    const int n = walk.count();
+    // S_j = Q K_j^T into warpgroup (j & 1)'s S buffer
+    auto issue_s = [&](int j) -> bool {
+      const int w = j & 1, sk = j % NSK;
+      if (!g.wait_warp(&m.k_full[sk], (j / NSK) & 1, 3)) return false;
+      tc_fence_after();
+      const uint64_t kd = sdesc_sw128(sK + sk * L::TB, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-          umma_bf16(tmem + L::TM_S + w * 128, sdesc_add(qd, ko), sdesc_add(kd, ko), idS, kk > 0 ? 1u : 0u);
-        }
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
+        if (leader) umma_bf16(tmem + L::TM_S + w * 128, sdesc_add(qd, ko), sdesc_add(kd, ko), idS, kk > 0 ? 1u : 0u);
+      }
+      if (leader) {
         umma_commit(&m.s_full[w]);
         umma_commit(&m.k_empty[sk]);
-        return true;
-      };
-      bool ok = g.wait(&m.q_full, 0, 4);
-      if (ok) ok = issue_s(0);
-      if (ok && n > 1) ok = issue_s(1);
-      for (int j = 0; ok && j < n; ++j) {
-        const int w = j & 1, sv = j % NSV;
-        // O_w += P_j V_j, P_j read from warpgroup w's S buffer
-        if (!g.wait(&m.p_full[w], (j >> 1) & 1, 5) || !g.wait(&m.v_full[sv], (j / NSV) & 1, 6)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint64_t vd = sdesc_sw128(sV + sv * L::TB, L::CHUNK, 1024);
-        const uint32_t acc0 = j >= 2 ? 1u : 0u;
+      }
+      __syncwarp();
+      return true;
+    };
+    bool ok = g.wait_warp(&m.q_full, 0, 4);
+    if (ok) ok = issue_s(0);
+    if (ok && n > 1) ok = issue_s(1);
+    for (int j = 0; ok && j < n; ++j) {
+      const int w = j & 1, sv = j % NSV;
+      // O_w += P_j V_j, P_j read from warpgroup w's S buffer
+      if (!g.wait_warp(&m.p_full[w], (j >> 1) & 1, 5) || !g.wait_warp(&m.v_full[sv], (j / NSV) & 1, 6)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t vd = sdesc_sw128(sV + sv * L::TB, L::CHUNK, 1024);
+      const uint32_t acc0 = j >= 2 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
+      for (int kk = 0; kk < 8; ++kk)
+        if (leader)
           umma_bf16_ta(tmem + L::TM_O + w * 128, tmem + L::TM_S + w * 128 + kk * 8, sdesc_add(vd, kk * 2048), idO,
                        kk > 0 ? 1u : acc0);
+      if (leader) {
         umma_commit(&m.pv_done[w]);
         umma_commit(&m.v_empty[sv]);
-        // S_{j+2} reuses this S buffer: wait for the PV just queued to read P_j
-        if (j + 2 < n) {
-          if (!g.wait(&m.pv_done[w], (j >> 1) & 1, 7)) { ok = false; break; }
-          ok = issue_s(j + 2);
-        }
       }
+      __syncwarp();
+      // S_{j+2} reuses this S buffer: wait for the PV just queued to read P_j
+      if (j + 2 < n) {
+        if (!g.wait_warp(&m.pv_done[w], (j >> 1) & 1, 7)) { ok = false; break; }
+        ok = issue_s(j + 2);
+      }
+    }
+    if (leader) {
       umma_commit(&m.mma_final);
       g.drain(&m.mma_final, 0);
     }

@@ -20,6 +20,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Shared-space address of a generic pointer, computed in inline assembly so
+// that the compiler cannot fold alignment checks on it from the declared
+// alignment of the array it points into.
+__device__ __forceinline__ uint32_t smem_u32_runtime(const void* p) {
+  uint64_t a;
+  asm volatile("cvta.to.shared.u64 %0, %1;" : "=l"(a) : "l"(reinterpret_cast<uint64_t>(p)));
+  return static_cast<uint32_t>(a);
+}
+
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -52,6 +61,25 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Polling loop of a bounded wait, kept out of line: every wait site inlines
+// only its first test, so the hot loops of the kernels stay small enough for
+// the instruction cache.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint32_t site, volatile int* abort_flag,
+                                            uint32_t* status) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        if (status) atomicOr(status, PA_DEVERR_TIMEOUT | (site << 8));
+        return false;
+      }
+    }
+  }
+}
+
 // Shared per-CTA abort flag + the caller's global status word. A wait gives up
 // when its own limit expires or when another role of the CTA has already
 // given up; both cases return false.
@@ -66,20 +94,17 @@ struct Guard {
   // Wait for the phase of `bar` with parity `parity` to complete.
   __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, uint32_t site) const {
     if (mbar_test(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-      if (mbar_test(bar, parity)) return true;
-      if ((it & 63u) == 0) {
-        if (*abort_flag) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
-          fail(PA_DEVERR_TIMEOUT | (site << 8));
-          return false;
-        }
-      }
-    }
+    return mbar_wait_slow(bar, parity, site, abort_flag, status);
+  }
+  // The same wait made by every lane of a converged warp; the result is the
+  // same on all lanes. An MMA-issuing warp waits this way so that its issue
+  // loop stays warp-uniform and only the tcgen05 instructions are predicated
+  // on one lane, which keeps the tensor pipe fed after each wait.
+  __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, uint32_t site) const {
+    return __all_sync(0xffffffffu, wait(bar, parity, site));
   }
   // Bounded wait used only during teardown after an abort: never sets the flag.
-  __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) const {
+  __device__ __noinline__ void drain(uint64_t* bar, uint32_t parity) const {
     const uint64_t t0 = globaltimer();
     while (!mbar_test(bar, parity)) {
       if (globaltimer() - t0 > kWaitLimitNs) {
@@ -244,6 +269,26 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t a0, uint32_t a1, uint32_t (
       : "memory");
 }
 
+// A 32-column load (from a0) and a 16-column load (from a1) under a single wait.
+__device__ __forceinline__ void tmem_ld32_ld16(uint32_t a0, uint32_t a1, uint32_t (&r)[32], uint32_t (&s)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%48];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47}, [%49];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(s[0]), "=r"(s[1]), "=r"(s[2]), "=r"(s[3]), "=r"(s[4]),
+        "=r"(s[5]), "=r"(s[6]), "=r"(s[7]), "=r"(s[8]), "=r"(s[9]), "=r"(s[10]), "=r"(s[11]), "=r"(s[12]),
+        "=r"(s[13]), "=r"(s[14]), "=r"(s[15])
+      : "r"(a0), "r"(a1)
+      : "memory");
+}
+
 // Two 16-column stores (to a0 and a1) under a single wait.
 __device__ __forceinline__ void tmem_st16x2(uint32_t a0, uint32_t a1, const uint32_t (&r)[16],
                                             const uint32_t (&s)[16]) {
@@ -259,6 +304,17 @@ __device__ __forceinline__ void tmem_st16x2(uint32_t a0, uint32_t a1, const uint
       "r"(s[10]), "r"(s[11]), "r"(s[12]), "r"(s[13]), "r"(s[14]), "r"(s[15])
       : "memory");
 }
+
+// 16-column store without the wait; tmem_wait_st() completes all such stores.
+__device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
