@@ -237,43 +237,42 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const uint32_t sreg = tmem + lane_base + (rs ? L::TM_S1 : L::TM_S0) + hsel * 64;
       const uint32_t dreg = tmem + lane_base + L::TM_DP + hsel * 64;
-      uint32_t s0[32], s1[32], d0[32], d1[32];
-      tmem_ld32x2(sreg, dreg, s0, d0);
-      tmem_ld32x2(sreg + 32, dreg + 32, s1, d1);
-      // the dP region may now take the next tile's dP
-      tc_fence_before();
-      mbar_arrive(&m.dp_free[rs]);
       const int c0 = hsel * 64;
-      const int k0 = tk * kTile + c0;
-      float sz[64];
+      // Two 32-key chunks in a rolled loop (the softmax code must stay small:
+      // instruction fetch, not arithmetic, limits these warps). dS goes over
+      // this thread's own S columns, which the chunk has already read.
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sv[32], dp[32];
+        tmem_ld32x2(sreg + 32 * c, dreg + 32 * c, sv, dp);
+        if (c == 1) {  // the dP region may now take the next tile's dP
+          tc_fence_before();
+          mbar_arrive(&m.dp_free[rs]);
+        }
+        const int k0 = tk * kTile + c0 + 32 * c;
+        if (masked) {
+          const int4* g4 = reinterpret_cast<const int4*>(&m.segkv[sk][c0 + 32 * c]);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        sz[e] = __uint_as_float(s0[e]);
-        sz[32 + e] = __uint_as_float(s1[e]);
-      }
-      if (masked) {
-        const int4* g4 = reinterpret_cast<const int4*>(&m.segkv[sk][c0]);
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const int4 gv = p.seg ? g4[e4] : make_int4(0, 0, 0, 0);
+            const int32_t gz[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
-        for (int e4 = 0; e4 < 16; ++e4) {
-          const int4 gv = p.seg ? g4[e4] : make_int4(0, 0, 0, 0);
-          const int32_t gz[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = e4 * 4 + e;
-            sz[c] = (k0 + c <= qidx && gz[e] == segq) ? sz[c] : -INFINITY;
+            for (int e = 0; e < 4; ++e) {
+              const int cc = e4 * 4 + e;
+              sv[cc] = (k0 + cc <= qidx && gz[e] == segq) ? sv[cc] : __float_as_uint(-INFINITY);
+            }
           }
         }
-      }
-      uint32_t w0[16], w1[16];
+        uint32_t w[16];
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const float p0 = ex2(fmaf(sz[e], sl2, -lse2)), p1 = ex2(fmaf(sz[e + 1], sl2, -lse2));
-        w0[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(d0[e]) - dlt), p1 * (__uint_as_float(d0[e + 1]) - dlt));
-        const float p2 = ex2(fmaf(sz[32 + e], sl2, -lse2)), p3 = ex2(fmaf(sz[33 + e], sl2, -lse2));
-        w1[e >> 1] = pack_bf16x2(p2 * (__uint_as_float(d1[e]) - dlt), p3 * (__uint_as_float(d1[e + 1]) - dlt));
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2));
+          const float p1 = ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2));
+          w[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - dlt), p1 * (__uint_as_float(dp[e + 1]) - dlt));
+        }
+        tmem_st16_nowait(sreg + 16 * c, w);
       }
-      // dS over this thread's own (already read) S columns: 64 keys -> 32 columns
-      tmem_st16x2(sreg, sreg + 16, w0, w1);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&m.ds_full[rs]);
     }

@@ -233,37 +233,33 @@ __global__ void __launch_bounds__(320, 1)
       if (!__all_sync(~0u, ok)) { ok = false; break; }
       tc_fence_after();
       // Two passes over S in TMEM (the row never sits in registers whole):
-      // pass 1 finds the row maximum, pass 2 forms P 64 keys at a time.
+      // pass 1 finds the row maximum, pass 2 forms P. Both walk the 128 keys
+      // as four 32-column chunks in rolled loops: instruction fetch, not
+      // arithmetic, limits these warps, so the code must stay small.
       const int k0 = tk * kTile;
       const int4* g4 = reinterpret_cast<const int4*>(&m.segkv[jj % NSV][0]);
-      auto load64 = [&](int half, float (&x)[64]) {
-        uint32_t a0[32], a1[32];
-        tmem_ld32x2(tS + 64 * half, tS + 64 * half + 32, a0, a1);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          x[e] = __uint_as_float(a0[e]);
-          x[32 + e] = __uint_as_float(a1[e]);
-        }
+      auto load32 = [&](int c, uint32_t (&x)[32]) {
+        tmem_ld32(tS + 32 * c, x);
         if (masked) {
 #pragma unroll
-          for (int e4 = 0; e4 < 16; ++e4) {
-            const int4 gv = p.seg ? g4[half * 16 + e4] : make_int4(0, 0, 0, 0);
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const int4 gv = p.seg ? g4[c * 8 + e4] : make_int4(0, 0, 0, 0);
             const int32_t gz[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int c = e4 * 4 + e;
-              x[c] = (k0 + 64 * half + c <= qidx && gz[e] == segq) ? x[c] : -INFINITY;
+              const int cc = e4 * 4 + e;
+              x[cc] = (k0 + 32 * c + cc <= qidx && gz[e] == segq) ? x[cc] : __float_as_uint(-INFINITY);
             }
           }
         }
       };
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t x[32];
+        load32(c, x);
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float x[64];
-        load64(hh, x);
-#pragma unroll
-        for (int e = 0; e < 64; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], x[e]);
+        for (int e = 0; e < 32; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(x[e]));
       }
       const float ms = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
       if (__any_sync(~0u, ms > m_used + 8.f)) {
@@ -273,7 +269,7 @@ __global__ void __launch_bounds__(320, 1)
           ok = g.wait(&m.pv_done[w], ((jj - 2) >> 1) & 1, 10);
           if (!__all_sync(~0u, ok)) { ok = false; break; }
           tc_fence_after();
-#pragma unroll
+#pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t v[32];
             tmem_ld32(tO + c0, v);
@@ -290,22 +286,23 @@ __global__ void __launch_bounds__(320, 1)
       // l sums the exact fp32 weights (for lse); lr sums the bf16-rounded
       // weights the PV product uses, so O / lr is a convex combination
       float ls4[4] = {0.f, 0.f, 0.f, 0.f}, lr4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {  // 32 keys -> 16 packed columns, over S columns already read
+        uint32_t x[32];
+        load32(c, x);
+        uint32_t pw[16];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {  // 64 keys -> 32 packed columns, written over S already read
-        float x[64];
-        load64(hh, x);
-        uint32_t pw[2][16];
-#pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          const float e0 = ex2(fmaf(x[e], sl2, -moff));
-          const float e1 = ex2(fmaf(x[e + 1], sl2, -moff));
+        for (int e = 0; e < 32; e += 2) {
+          const float e0 = ex2(fmaf(__uint_as_float(x[e]), sl2, -moff));
+          const float e1 = ex2(fmaf(__uint_as_float(x[e + 1]), sl2, -moff));
           const uint32_t y = pack_bf16x2(e0, e1);
           ls4[(e >> 1) & 3] += e0 + e1;
           lr4[(e >> 1) & 3] += __uint_as_float(y << 16) + __uint_as_float(y & 0xFFFF0000u);
-          pw[e >> 5][(e >> 1) & 15] = y;
+          pw[e >> 1] = y;
         }
-        tmem_st16x2(tS + 32 * hh, tS + 32 * hh + 16, pw[0], pw[1]);
+        tmem_st16_nowait(tS + 16 * c, pw);
       }
+      tmem_wait_st();
       l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       lr += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
       tc_fence_before();
