@@ -174,20 +174,11 @@ __global__ void __launch_bounds__(320, 1)
     };
     bool ok = g.wait_warp(&m.q_full, 0, 4);
     int j = 0;
+    // Per tile j: dP_j, S_j, then dQ_{j-1}. S_j reuses the S region that
+    // dQ_{j-2} read; with dP_j issued in between, waiting for dQ_{j-2} never
+    // leaves the tensor pipe empty.
     for (int tk = walk.first(); ok && tk <= tq; tk = walk.next(tk), ++j) {
       const int rs = j & 1, sk = j % NSK, sv = j % NSV;
-      // S_j goes into the S region of tile j-2, free once dQ of tile j-2 ran
-      if (!g.wait_warp(&m.k_full[sk], (j / NSK) & 1, 5)) { ok = false; break; }
-      if (j >= 2 && !g.wait_warp(&m.dq_done[rs], ((j - 2) >> 1) & 1, 6)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t sreg = tmem + (rs ? L::TM_S1 : L::TM_S0);
-      const uint64_t kd = sdesc_sw128(sK + sk * L::TB, 16, 1024);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-        if (leader) umma_bf16(sreg, sdesc_add(qd, ko), sdesc_add(kd, ko), idS, kk > 0 ? 1u : 0u);
-      }
-      __syncwarp();
       // dP_j into the dP region once the softmax of tile j-1 has read it
       if (!g.wait_warp(&m.v_full[sv], (j / NSV) & 1, 7)) { ok = false; break; }
       if (j >= 1 && !g.wait_warp(&m.dp_free[(j - 1) & 1], ((j - 1) >> 1) & 1, 8)) { ok = false; break; }
@@ -198,10 +189,20 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
         if (leader) umma_bf16(tmem + L::TM_DP, sdesc_add(dod, ko), sdesc_add(vd, ko), idS, kk > 0 ? 1u : 0u);
       }
-      if (leader) {
-        umma_commit(&m.s_full[rs]);
-        umma_commit(&m.v_empty[sv]);
+      if (leader) umma_commit(&m.v_empty[sv]);
+      __syncwarp();
+      // S_j into the S region of tile j-2, free once dQ of tile j-2 ran
+      if (!g.wait_warp(&m.k_full[sk], (j / NSK) & 1, 5)) { ok = false; break; }
+      if (j >= 2 && !g.wait_warp(&m.dq_done[rs], ((j - 2) >> 1) & 1, 6)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sreg = tmem + (rs ? L::TM_S1 : L::TM_S0);
+      const uint64_t kd = sdesc_sw128(sK + sk * L::TB, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
+        if (leader) umma_bf16(sreg, sdesc_add(qd, ko), sdesc_add(kd, ko), idS, kk > 0 ? 1u : 0u);
       }
+      if (leader) umma_commit(&m.s_full[rs]);
       __syncwarp();
       if (j > 0 && !issue_dq(j - 1)) { ok = false; break; }
     }
