@@ -10,15 +10,17 @@
 // log-sum-exp (mlx-train-perf 0.5.1 README, "Flash-attention training path":
 // the backward recomputes the tiles it needs from O(N) saved state).
 //
-// Every MMA is 128 x 128 (or 128 x D) with K = 16: wide enough that the one
-// issuing thread keeps the tensor pipe busy. TMEM holds dQ, one dP region and
+// Every MMA is 128 x 128 (or 128 x D) with K = 16. Two warps issue them: one
+// issues dP and S, the other dQ as soon as each tile's dS is ready, so neither
+// waits behind the other's dependencies. TMEM holds dQ, one dP region and
 // two S regions used by alternate key tiles. The softmax warps release the dP
 // region as soon as they have loaded it, so the next tile's S and dP run on
 // the tensor core while this tile's dS is being formed.
 //
 // Warp roles: warp 0 TMA producer (Q and dO once; K through a 3-stage ring,
-// V through a 2-stage ring), warp 1 MMA issuer and TMEM owner, warps 2..9
-// two threads per query row, 64 key columns each.
+// V through a 2-stage ring), warp 1 dP/S issuer and TMEM owner, warp 2 dQ
+// issuer, warps 3..10 softmax: two threads per query row (TMEM lane quarter
+// = warp index mod 4), 64 key columns each.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -48,14 +50,14 @@ struct DqLayout {
 
 struct DqMisc {
   uint64_t q_full, k_full[3], k_empty[3], v_full[2], v_empty[2];
-  uint64_t s_full[2], dp_free[2], ds_full[2], dq_done[2], mma_final;
+  uint64_t s_full[2], dp_free[2], ds_full[2], dq_done[2], mma_final[2];
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) int32_t segkv[3][128];
 };
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const AttnParams p) {
@@ -95,7 +97,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&m.ds_full[s], 256);
       mbar_init(&m.dq_done[s], 1);
     }
-    mbar_init(&m.mma_final, 1);
+    mbar_init(&m.mma_final[0], 1);
+    mbar_init(&m.mma_final[1], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -144,39 +147,16 @@ __global__ void __launch_bounds__(320, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ dP / S issuer
+    // Per tile j: dP_j, then S_j. S_j reuses the S region that dQ_{j-2} read;
+    // with dP_j issued in between, that wait never empties the tensor pipe.
     // The whole warp runs the issue loop and every wait; lane 0 alone issues
     // the tcgen05 instructions.
     const bool leader = lane == 0;
     constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-    constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, true);
     const uint64_t qd = sdesc_sw128(sQ, 16, 1024), dod = sdesc_sw128(sDO, 16, 1024);
-    // dQ += dS_j K_j: dS from TMEM (thread-half h keeps the dS of its 64 key
-    // columns in S columns 64h..64h+31), K as the MN-major B operand
-    auto issue_dq = [&](int j) -> bool {
-      const int rs = j & 1, sk = j % NSK;
-      if (!g.wait_warp(&m.ds_full[rs], (j >> 1) & 1, 3)) return false;
-      tc_fence_after();
-      const uint32_t sreg = tmem + (rs ? L::TM_S1 : L::TM_S0);
-      const uint64_t kmn = sdesc_sw128(sK + sk * L::TB, L::CHUNK, 1024);
-      const uint32_t acc0 = j > 0 ? 1u : 0u;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        if (leader)
-          umma_bf16_ta(tmem + L::TM_DQ, sreg + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(kmn, kk * 2048), idQ,
-                       kk > 0 ? 1u : acc0);
-      if (leader) {
-        umma_commit(&m.dq_done[rs]);
-        umma_commit(&m.k_empty[sk]);
-      }
-      __syncwarp();
-      return true;
-    };
     bool ok = g.wait_warp(&m.q_full, 0, 4);
     int j = 0;
-    // Per tile j: dP_j, S_j, then dQ_{j-1}. S_j reuses the S region that
-    // dQ_{j-2} read; with dP_j issued in between, waiting for dQ_{j-2} never
-    // leaves the tensor pipe empty.
     for (int tk = walk.first(); ok && tk <= tq; tk = walk.next(tk), ++j) {
       const int rs = j & 1, sk = j % NSK, sv = j % NSV;
       // dP_j into the dP region once the softmax of tile j-1 has read it
@@ -204,18 +184,47 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (leader) umma_commit(&m.s_full[rs]);
       __syncwarp();
-      if (j > 0 && !issue_dq(j - 1)) { ok = false; break; }
     }
-    if (ok && j > 0) issue_dq(j - 1);
     if (leader) {
-      umma_commit(&m.mma_final);
-      g.drain(&m.mma_final, 0);
+      umma_commit(&m.mma_final[0]);
+      g.drain(&m.mma_final[0], 0);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ dQ issuer
+    // dQ += dS_j K_j as soon as dS_j is in TMEM: thread-half h keeps the dS of
+    // its 64 key columns in S columns 64h..64h+31; K is the MN-major B operand.
+    const bool leader = lane == 0;
+    constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, true);
+    bool ok = true;
+    int j = 0;
+    for (int tk = walk.first(); ok && tk <= tq; tk = walk.next(tk), ++j) {
+      const int rs = j & 1, sk = j % NSK;
+      if (!g.wait_warp(&m.k_full[sk], (j / NSK) & 1, 2)) { ok = false; break; }
+      if (!g.wait_warp(&m.ds_full[rs], (j >> 1) & 1, 3)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sreg = tmem + (rs ? L::TM_S1 : L::TM_S0);
+      const uint64_t kmn = sdesc_sw128(sK + sk * L::TB, L::CHUNK, 1024);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        if (leader)
+          umma_bf16_ta(tmem + L::TM_DQ, sreg + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(kmn, kk * 2048), idQ,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+      if (leader) {
+        umma_commit(&m.dq_done[rs]);
+        umma_commit(&m.k_empty[sk]);
+      }
+      __syncwarp();
+    }
+    if (leader) {
+      umma_commit(&m.mma_final[1]);
+      g.drain(&m.mma_final[1], 0);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
     const int quarter = warp & 3;
-    const int hsel = (warp - 2) >> 2;  // which 64 key columns of every tile
+    const int hsel = (warp - 3) >> 2;  // which 64 key columns of every tile
     const int r = quarter * 32 + lane;
     const int qidx = tq * kTile + r;
     const size_t row = (size_t)(b * p.Hq + h) * p.N + qidx;
@@ -321,7 +330,7 @@ cudaError_t launch_dq_d(const AttnParams& p, const void* q, const void* k, const
   cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.T * p.Hq * p.B);
-  dq_kernel<D><<<grid, 320, L::SMEM, st>>>(tq, tdo, tk, tv, p);
+  dq_kernel<D><<<grid, 352, L::SMEM, st>>>(tq, tdo, tk, tv, p);
   return cudaGetLastError();
 }
 

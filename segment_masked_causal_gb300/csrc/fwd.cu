@@ -14,9 +14,9 @@
 //   O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / (l_0 2^(m_0 - m) + l_1 2^(m_1 - m)).
 // Per tile: S = Q K^T (128 x 128, Q and K in shared memory), P = 2^(S log2e
 // scale - m) written back as bf16 over S and fed to O += P V straight from
-// TMEM. Every MMA is at least 128 x D x 16, wide enough that the one issuing
-// thread keeps the tensor pipe busy; while one warpgroup computes its P the
-// tensor core runs the other warpgroup's PV and S.
+// TMEM. Every MMA is at least 128 x D x 16. Each warpgroup has its own
+// MMA-issuing warp, so while one warpgroup computes its P the tensor core
+// runs the other warpgroup's PV and S.
 //
 // Online softmax works in log2 units of the scaled score and rescales an O
 // accumulator only when its running maximum rises by more than 8 (a factor
@@ -24,9 +24,10 @@
 // consistent and O / l is exact in real arithmetic.
 //
 // Warp roles: warp 0 TMA producer (Q once; K through a 3-stage ring, V and
-// the key tile's segment ids through a 2-stage ring), warp 1 MMA issuer and
-// TMEM owner, warps 2..5 warpgroup 0 and warps 6..9 warpgroup 1 (one query
-// row per thread in each).
+// the key tile's segment ids through a 2-stage ring), warps 1 and 2 the MMA
+// issuers of warpgroups 0 and 1 (warp 1 also owns TMEM), warps 3..6
+// warpgroup 0 and warps 7..10 warpgroup 1 (one query row per thread in each;
+// TMEM lane quarter = warp index mod 4).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -55,7 +56,7 @@ struct FwdLayout {
 
 struct FwdMisc {
   uint64_t q_full, k_full[3], k_empty[3], v_full[2], v_empty[2];
-  uint64_t s_full[2], p_full[2], pv_done[2], comb_ready, mma_final;
+  uint64_t s_full[2], p_full[2], pv_done[2], comb_ready, mma_final[2];
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) int32_t segkv[2][128];
@@ -63,7 +64,7 @@ struct FwdMisc {
 };
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   using L = FwdLayout<D>;
@@ -101,7 +102,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&m.pv_done[s], 1);
     }
     mbar_init(&m.comb_ready, 256);
-    mbar_init(&m.mma_final, 1);
+    mbar_init(&m.mma_final[0], 1);
+    mbar_init(&m.mma_final[1], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -145,18 +147,22 @@ __global__ void __launch_bounds__(320, 1)
       for (int i = (jv > NSV ? jv - NSV : 0); i < jv; ++i) g.drain(&m.v_full[i % NSV], (i / NSV) & 1);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp <= 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 1 issues warpgroup 0's tiles and warp 2 warpgroup 1's, each in its
+    // own order: while one waits for its PV to finish reading P before the
+    // next S may overwrite that buffer, the other keeps the tensor pipe fed.
     // The whole warp runs the issue loop and every wait; lane 0 alone issues
     // the tcgen05 instructions.
+    const int w = warp - 1;
     const bool leader = lane == 0;
     constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
     const uint64_t qd = sdesc_sw128(sQ, 16, 1024);
     const int n = walk.count();
-    // S_j = Q K_j^T into warpgroup (j & 1)'s S buffer
+    // S_j = Q K_j^T into this warpgroup's S buffer
     auto issue_s = [&](int j) -> bool {
-      const int w = j & 1, sk = j % NSK;
+      const int sk = j % NSK;
       if (!g.wait_warp(&m.k_full[sk], (j / NSK) & 1, 3)) return false;
       tc_fence_after();
       const uint64_t kd = sdesc_sw128(sK + sk * L::TB, 16, 1024);
@@ -173,11 +179,10 @@ __global__ void __launch_bounds__(320, 1)
       return true;
     };
     bool ok = g.wait_warp(&m.q_full, 0, 4);
-    if (ok) ok = issue_s(0);
-    if (ok && n > 1) ok = issue_s(1);
-    for (int j = 0; ok && j < n; ++j) {
-      const int w = j & 1, sv = j % NSV;
-      // O_w += P_j V_j, P_j read from warpgroup w's S buffer
+    if (ok && w < n) ok = issue_s(w);
+    for (int j = w; ok && j < n; j += 2) {
+      const int sv = j % NSV;  // == w: each warpgroup has its own V stage
+      // O_w += P_j V_j, P_j read from this warpgroup's S buffer
       if (!g.wait_warp(&m.p_full[w], (j >> 1) & 1, 5) || !g.wait_warp(&m.v_full[sv], (j / NSV) & 1, 6)) {
         ok = false;
         break;
@@ -202,14 +207,14 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     if (leader) {
-      umma_commit(&m.mma_final);
-      g.drain(&m.mma_final, 0);
+      umma_commit(&m.mma_final[w]);
+      g.drain(&m.mma_final[w], 0);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
     const int quarter = warp & 3;
-    const int w = (warp - 2) >> 2;  // warpgroup: takes every other visited key tile
+    const int w = (warp - 3) >> 2;  // warpgroup: takes every other visited key tile
     const int r = quarter * 32 + lane;
     const int qidx = tq * kTile + r;
     const size_t row = (size_t)(b * p.Hq + h) * p.N + qidx;
@@ -384,7 +389,7 @@ cudaError_t launch_fwd_d(const AttnParams& p, const void* q, const void* k, cons
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.T * p.Hq * p.B);
-  fwd_kernel<D><<<grid, 320, L::SMEM, st>>>(tq, tk, tv, p);
+  fwd_kernel<D><<<grid, 352, L::SMEM, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
