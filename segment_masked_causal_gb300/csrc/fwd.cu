@@ -7,27 +7,26 @@
 // not entirely visible. The saved state is O and its log-sum-exp
 // (mlx-train-perf 0.5.1 README, "Flash-attention training path").
 //
-// The visited key tiles alternate between two softmax warpgroups: warpgroup w
-// takes tiles w, w+2, w+4, ... and keeps its own S buffer, running maximum,
-// sums and O accumulator in TMEM; the two partial results are combined once
-// at the end:
-//   O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / (l_0 2^(m_0 - m) + l_1 2^(m_1 - m)).
-// Per tile: S = Q K^T (128 x 128, Q and K in shared memory), P = 2^(S log2e
-// scale - m) written back as bf16 over S and fed to O += P V straight from
-// TMEM. Every MMA is at least 128 x D x 16. Each warpgroup has its own
-// MMA-issuing warp, so while one warpgroup computes its P the tensor core
-// runs the other warpgroup's PV and S.
+// Per visited key tile j: S_j = Q K_j^T (128 x 128, Q and K in shared memory)
+// into one of three TMEM S buffers, P_j = 2^(S_j log2e scale - m) written back
+// as bf16 over S_j, and O += P_j V_j with P_j fed straight from TMEM into one
+// O accumulator. With three S buffers, S_{j+3} waits only for PV_j, which
+// finishes while the softmax is still on tiles j+1 and j+2: the softmax warps
+// never wait for their own PV. All eight softmax warps work on every tile, two
+// threads per query row (64 keys each); the two halves of a row exchange their
+// maxima through shared memory. One warp issues the S products, another the
+// PV products, each waiting only on its own dependencies.
 //
-// Online softmax works in log2 units of the scaled score and rescales an O
-// accumulator only when its running maximum rises by more than 8 (a factor
-// 256); P is always computed against the maximum in use, so O and l stay
-// consistent and O / l is exact in real arithmetic.
+// Online softmax works in log2 units of the scaled score and rescales O only
+// when a row's maximum rises by more than 8 (a factor 256); P is always
+// computed against the maximum in use, so O and l stay consistent and O / l
+// is exact in real arithmetic. O is divided by the sum of the bf16-rounded
+// weights the PV product used; lse uses the exact fp32 sum.
 //
 // Warp roles: warp 0 TMA producer (Q once; K through a 3-stage ring, V and
-// the key tile's segment ids through a 2-stage ring), warps 1 and 2 the MMA
-// issuers of warpgroups 0 and 1 (warp 1 also owns TMEM), warps 3..6
-// warpgroup 0 and warps 7..10 warpgroup 1 (one query row per thread in each;
-// TMEM lane quarter = warp index mod 4).
+// the key tile's segment ids through a 2-stage ring), warp 1 S issuer and
+// TMEM owner, warp 2 PV issuer, warps 3..10 softmax (TMEM lane quarter =
+// warp index mod 4; warps w and w+4 share a quarter and split its rows' keys).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -41,7 +40,7 @@ namespace {
 
 template <int D>
 struct FwdLayout {
-  static constexpr int NSK = 3, NSV = 2;
+  static constexpr int NSK = 3, NSV = 2, NSB = 3;  // K stages, V stages, TMEM S buffers
   static constexpr uint32_t TB = 128 * D * 2;   // one 128-row tile of Q, K or V
   static constexpr uint32_t CHUNK = 128 * 128;  // one 64-column chunk of a 128-row tile
   static constexpr uint32_t OFF_Q = 0;
@@ -50,17 +49,18 @@ struct FwdLayout {
   static constexpr uint32_t TILE_BYTES = OFF_V + NSV * TB;
   static constexpr uint32_t MISC_BYTES = 8192;
   static constexpr uint32_t SMEM = TILE_BYTES + MISC_BYTES + 1024;
-  // TMEM: S_0, S_1 (128 columns each), O_0 at 256, O_1 at 384 (D columns each)
-  static constexpr uint32_t TM_S = 0, TM_O = 256, TMEM_COLS = 512;
+  // TMEM: O (D columns) at 0, S buffers of 128 columns at 128, 256, 384
+  static constexpr uint32_t TM_O = 0, TM_S = 128, TMEM_COLS = 512;
 };
 
 struct FwdMisc {
   uint64_t q_full, k_full[3], k_empty[3], v_full[2], v_empty[2];
-  uint64_t s_full[2], p_full[2], pv_done[2], comb_ready, mma_final[2];
+  uint64_t s_full[3], p_full[3], pv_done[3], xbar[2][4], fin_s, fin_pv;
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) int32_t segkv[2][128];
-  float mst[2][128], lst[2][128], lrst[2][128];  // per-warpgroup row statistics for the final combine
+  float xmax[2][2][128];  // [tile parity][key half][row]: half-row maxima of the two threads of a row
+  float xsum[2][2][128];  // [l, lr][key half][row]: half-row sums for the epilogue
 };
 
 template <int D>
@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(352, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   using L = FwdLayout<D>;
-  constexpr int NSK = L::NSK, NSV = L::NSV;
+  constexpr int NSK = L::NSK, NSV = L::NSV, NSB = L::NSB;
   static_assert(sizeof(FwdMisc) <= L::MISC_BYTES, "misc region");
   static_assert(L::SMEM <= 232448, "shared memory");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -96,14 +96,15 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(&m.v_full[s], 1);
       mbar_init(&m.v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < L::NSB; ++s) {
       mbar_init(&m.s_full[s], 1);
-      mbar_init(&m.p_full[s], 128);
+      mbar_init(&m.p_full[s], 256);
       mbar_init(&m.pv_done[s], 1);
     }
-    mbar_init(&m.comb_ready, 256);
-    mbar_init(&m.mma_final[0], 1);
-    mbar_init(&m.mma_final[1], 1);
+    for (int s = 0; s < 2; ++s)
+      for (int q = 0; q < 4; ++q) mbar_init(&m.xbar[s][q], 64);  // the two warps of a lane quarter
+    mbar_init(&m.fin_s, 1);
+    mbar_init(&m.fin_pv, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -147,135 +148,136 @@ __global__ void __launch_bounds__(352, 1)
       for (int i = (jv > NSV ? jv - NSV : 0); i < jv; ++i) g.drain(&m.v_full[i % NSV], (i / NSV) & 1);
     }
     __syncwarp();
-  } else if (warp <= 2) {
-    // ------------------------------------------------------------ MMA issuers
-    // Warp 1 issues warpgroup 0's tiles and warp 2 warpgroup 1's, each in its
-    // own order: while one waits for its PV to finish reading P before the
-    // next S may overwrite that buffer, the other keeps the tensor pipe fed.
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ S issuer
     // The whole warp runs the issue loop and every wait; lane 0 alone issues
     // the tcgen05 instructions.
-    const int w = warp - 1;
     const bool leader = lane == 0;
     constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-    constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
     const uint64_t qd = sdesc_sw128(sQ, 16, 1024);
-    const int n = walk.count();
-    // S_j = Q K_j^T into this warpgroup's S buffer
-    auto issue_s = [&](int j) -> bool {
-      const int sk = j % NSK;
-      if (!g.wait_warp(&m.k_full[sk], (j / NSK) & 1, 3)) return false;
+    bool ok = g.wait_warp(&m.q_full, 0, 3);
+    int j = 0;
+    for (int tk = walk.first(); ok && tk <= tq; tk = walk.next(tk), ++j) {
+      const int sb = j % NSB, sk = j % NSK;
+      // S_j into buffer sb once PV_{j-3} has read the P that was there
+      if (j >= NSB && !g.wait_warp(&m.pv_done[sb], ((j - NSB) / NSB) & 1, 4)) { ok = false; break; }
+      if (!g.wait_warp(&m.k_full[sk], (j / NSK) & 1, 5)) { ok = false; break; }
       tc_fence_after();
       const uint64_t kd = sdesc_sw128(sK + sk * L::TB, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-        if (leader) umma_bf16(tmem + L::TM_S + w * 128, sdesc_add(qd, ko), sdesc_add(kd, ko), idS, kk > 0 ? 1u : 0u);
+        if (leader) umma_bf16(tmem + L::TM_S + sb * 128, sdesc_add(qd, ko), sdesc_add(kd, ko), idS, kk > 0 ? 1u : 0u);
       }
       if (leader) {
-        umma_commit(&m.s_full[w]);
+        umma_commit(&m.s_full[sb]);
         umma_commit(&m.k_empty[sk]);
       }
       __syncwarp();
-      return true;
-    };
-    bool ok = g.wait_warp(&m.q_full, 0, 4);
-    if (ok && w < n) ok = issue_s(w);
-    for (int j = w; ok && j < n; j += 2) {
-      const int sv = j % NSV;  // == w: each warpgroup has its own V stage
-      // O_w += P_j V_j, P_j read from this warpgroup's S buffer
-      if (!g.wait_warp(&m.p_full[w], (j >> 1) & 1, 5) || !g.wait_warp(&m.v_full[sv], (j / NSV) & 1, 6)) {
-        ok = false;
-        break;
-      }
+    }
+    if (leader) {
+      umma_commit(&m.fin_s);
+      g.drain(&m.fin_s, 0);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ PV issuer
+    // O += P_j V_j with P_j (bf16, packed in the first 64 columns of its S
+    // buffer) as the A operand straight from TMEM and V MN-major.
+    const bool leader = lane == 0;
+    constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
+    bool ok = true;
+    int j = 0;
+    for (int tk = walk.first(); ok && tk <= tq; tk = walk.next(tk), ++j) {
+      const int sb = j % NSB, sv = j % NSV;
+      if (!g.wait_warp(&m.v_full[sv], (j / NSV) & 1, 6)) { ok = false; break; }
+      if (!g.wait_warp(&m.p_full[sb], (j / NSB) & 1, 7)) { ok = false; break; }
       tc_fence_after();
       const uint64_t vd = sdesc_sw128(sV + sv * L::TB, L::CHUNK, 1024);
-      const uint32_t acc0 = j >= 2 ? 1u : 0u;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         if (leader)
-          umma_bf16_ta(tmem + L::TM_O + w * 128, tmem + L::TM_S + w * 128 + kk * 8, sdesc_add(vd, kk * 2048), idO,
-                       kk > 0 ? 1u : acc0);
+          umma_bf16_ta(tmem + L::TM_O, tmem + L::TM_S + sb * 128 + kk * 8, sdesc_add(vd, kk * 2048), idO,
+                       (j > 0 || kk > 0) ? 1u : 0u);
       if (leader) {
-        umma_commit(&m.pv_done[w]);
+        umma_commit(&m.pv_done[sb]);
         umma_commit(&m.v_empty[sv]);
       }
       __syncwarp();
-      // S_{j+2} reuses this S buffer: wait for the PV just queued to read P_j
-      if (j + 2 < n) {
-        if (!g.wait_warp(&m.pv_done[w], (j >> 1) & 1, 7)) { ok = false; break; }
-        ok = issue_s(j + 2);
-      }
     }
     if (leader) {
-      umma_commit(&m.mma_final[w]);
-      g.drain(&m.mma_final[w], 0);
+      umma_commit(&m.fin_pv);
+      g.drain(&m.fin_pv, 0);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
     const int quarter = warp & 3;
-    const int w = (warp - 3) >> 2;  // warpgroup: takes every other visited key tile
+    const int hsel = (warp - 3) >> 2;  // which 64 keys of every tile (and which half of the O row)
     const int r = quarter * 32 + lane;
     const int qidx = tq * kTile + r;
     const size_t row = (size_t)(b * p.Hq + h) * p.N + qidx;
     const int32_t segq = p.seg ? p.seg[(size_t)b * p.N + qidx] : 0;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_base + L::TM_S + w * 128;
-    const uint32_t tO = tmem + lane_base + L::TM_O + w * 128;
+    const uint32_t tO = tmem + lane_base + L::TM_O + hsel * (D / 2);
     const float sl2 = p.scale_log2;
-    const int n = walk.count();
-    float m_used = -INFINITY, l = 0.f, lr = 0.f;
+    float m_used = -INFINITY, l = 0.f, lr = 0.f;  // l and lr over this thread's half of the keys
     bool ok = true;
-    int jj = 0, mine = 0, jlast = -1;
+    int jj = 0;
     for (int tk = walk.first(); tk <= tq; tk = walk.next(tk), ++jj) {
-      if ((jj & 1) != w) continue;
+      const int sb = jj % NSB, xs = jj & 1;
       const bool masked = !tile_pair_full(tq, walk.qt, tk, trow[tk]);
       if (masked && p.seg) {  // segment ids of this key tile arrived with V
         ok = g.wait(&m.v_full[jj % NSV], (jj / NSV) & 1, 8);
         if (!__all_sync(~0u, ok)) { ok = false; break; }
       }
-      ok = g.wait(&m.s_full[w], (jj >> 1) & 1, 9);
+      ok = g.wait(&m.s_full[sb], (jj / NSB) & 1, 9);
       if (!__all_sync(~0u, ok)) { ok = false; break; }
       tc_fence_after();
-      // Two passes over S in TMEM (the row never sits in registers whole):
-      // pass 1 finds the row maximum, pass 2 forms P. Both walk the 128 keys
-      // as four 32-column chunks in rolled loops: instruction fetch, not
-      // arithmetic, limits these warps, so the code must stay small.
-      const int k0 = tk * kTile;
-      const int4* g4 = reinterpret_cast<const int4*>(&m.segkv[jj % NSV][0]);
-      auto load32 = [&](int c, uint32_t (&x)[32]) {
-        tmem_ld32(tS + 32 * c, x);
-        if (masked) {
+      const uint32_t tS = tmem + lane_base + L::TM_S + sb * 128;
+      uint32_t xa[32], xb[32];  // this thread's 64 scores (keys 64*hsel ..)
+      tmem_ld32x2(tS + 64 * hsel, tS + 64 * hsel + 32, xa, xb);
+      if (masked) {
+        const int k0 = tk * kTile + 64 * hsel;
+        const int4* g4 = reinterpret_cast<const int4*>(&m.segkv[jj % NSV][64 * hsel]);
 #pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const int4 gv = p.seg ? g4[c * 8 + e4] : make_int4(0, 0, 0, 0);
-            const int32_t gz[4] = {gv.x, gv.y, gv.z, gv.w};
+        for (int e4 = 0; e4 < 16; ++e4) {
+          const int4 gv = p.seg ? g4[e4] : make_int4(0, 0, 0, 0);
+          const int32_t gz[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int cc = e4 * 4 + e;
-              x[cc] = (k0 + 32 * c + cc <= qidx && gz[e] == segq) ? x[cc] : __float_as_uint(-INFINITY);
-            }
+          for (int e = 0; e < 4; ++e) {
+            const int c = e4 * 4 + e;
+            uint32_t& x = c < 32 ? xa[c] : xb[c - 32];
+            x = (k0 + c <= qidx && gz[e] == segq) ? x : __float_as_uint(-INFINITY);
           }
         }
-      };
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t x[32];
-        load32(c, x);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(x[e]));
       }
-      const float ms = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(xa[e]));
+        mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(xb[e]));
+      }
+      // exchange the half-row maxima with the other thread of the row
+      const float mloc = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      m.xmax[xs][hsel][r] = mloc;
+      tc_fence_before();  // this thread's S reads are done before the other half overwrites them with P
+      mbar_arrive(&m.xbar[xs][quarter]);
+      ok = g.wait(&m.xbar[xs][quarter], (jj >> 1) & 1, 10);
+      if (!__all_sync(~0u, ok)) { ok = false; break; }
+      tc_fence_after();
+      const float ms = fmaxf(mloc, m.xmax[xs][hsel ^ 1][r]) * sl2;
+      // both threads of a row hold the same ms and m_used, so they take the
+      // same decisions; both warps of a quarter hold the same rows
       if (__any_sync(~0u, ms > m_used + 8.f)) {
         const float m_new = fmaxf(m_used, ms);
         const float alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_new);
-        if (mine > 0) {  // O_w holds earlier tiles: rescale it once their PV is done
-          ok = g.wait(&m.pv_done[w], ((jj - 2) >> 1) & 1, 10);
+        if (jj > 0) {  // O holds earlier tiles: rescale this half of it once their PV is done
+          ok = g.wait(&m.pv_done[(jj - 1) % NSB], ((jj - 1) / NSB) & 1, 11);
           if (!__all_sync(~0u, ok)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
+          for (int c0 = 0; c0 < D / 2; c0 += 32) {
             uint32_t v[32];
             tmem_ld32(tO + c0, v);
 #pragma unroll
@@ -291,83 +293,61 @@ __global__ void __launch_bounds__(352, 1)
       // l sums the exact fp32 weights (for lse); lr sums the bf16-rounded
       // weights the PV product uses, so O / lr is a convex combination
       float ls4[4] = {0.f, 0.f, 0.f, 0.f}, lr4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {  // 32 keys -> 16 packed columns, over S columns already read
-        uint32_t x[32];
-        load32(c, x);
-        uint32_t pw[16];
+      uint32_t pa[16], pb[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float e0 = ex2(fmaf(__uint_as_float(x[e]), sl2, -moff));
-          const float e1 = ex2(fmaf(__uint_as_float(x[e + 1]), sl2, -moff));
-          const uint32_t y = pack_bf16x2(e0, e1);
-          ls4[(e >> 1) & 3] += e0 + e1;
-          lr4[(e >> 1) & 3] += __uint_as_float(y << 16) + __uint_as_float(y & 0xFFFF0000u);
-          pw[e >> 1] = y;
-        }
-        tmem_st16_nowait(tS + 16 * c, pw);
+      for (int e = 0; e < 32; e += 2) {
+        const float e0 = ex2(fmaf(__uint_as_float(xa[e]), sl2, -moff));
+        const float e1 = ex2(fmaf(__uint_as_float(xa[e + 1]), sl2, -moff));
+        const float f0 = ex2(fmaf(__uint_as_float(xb[e]), sl2, -moff));
+        const float f1 = ex2(fmaf(__uint_as_float(xb[e + 1]), sl2, -moff));
+        const uint32_t y = pack_bf16x2(e0, e1), z = pack_bf16x2(f0, f1);
+        ls4[(e >> 1) & 3] += (e0 + e1) + (f0 + f1);
+        lr4[(e >> 1) & 3] += (__uint_as_float(y << 16) + __uint_as_float(y & 0xFFFF0000u)) +
+                             (__uint_as_float(z << 16) + __uint_as_float(z & 0xFFFF0000u));
+        pa[e >> 1] = y;
+        pb[e >> 1] = z;
       }
-      tmem_wait_st();
+      // P for keys 64*hsel .. 64*hsel+63 -> packed columns 32*hsel .. 32*hsel+31
+      // (S columns both threads of the row have read before the exchange)
+      tmem_st16x2(tS + 32 * hsel, tS + 32 * hsel + 16, pa, pb);
       l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       lr += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
       tc_fence_before();
-      mbar_arrive(&m.p_full[w]);
-      ++mine;
-      jlast = jj;
+      mbar_arrive(&m.p_full[sb]);
     }
-    // ------------------------------------------------------------ combine + epilogue
-    if (ok && mine > 0) {
-      ok = g.wait(&m.pv_done[w], (jlast >> 1) & 1, 11);
+    // ------------------------------------------------------------ epilogue
+    if (ok && jj > 0) {
+      ok = g.wait(&m.pv_done[(jj - 1) % NSB], ((jj - 1) / NSB) & 1, 12);
       ok = __all_sync(~0u, ok);
     }
-    if (ok) {
-      m.mst[w][r] = m_used;
-      m.lst[w][r] = l;
-      m.lrst[w][r] = lr;
-      mbar_arrive(&m.comb_ready);
-      ok = g.wait(&m.comb_ready, 0, 12);
+    if (ok) {  // add up the two halves' sums
+      m.xsum[0][hsel][r] = l;
+      m.xsum[1][hsel][r] = lr;
+      mbar_arrive(&m.xbar[jj & 1][quarter]);
+      ok = g.wait(&m.xbar[jj & 1][quarter], (jj >> 1) & 1, 13);
       ok = __all_sync(~0u, ok);
     }
     if (ok) {
       tc_fence_after();
-      const bool has1 = n > 1;  // warpgroup 1 saw at least one tile
-      // both threads of a row evaluate the same expressions in the same order
-      const float m0 = m.mst[0][r], m1 = has1 ? m.mst[1][r] : -INFINITY;
-      const float mx = fmaxf(m0, m1);
-      const float f0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - mx);
-      const float f1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - mx);
-      const float l0 = m.lst[0][r], l1 = has1 ? m.lst[1][r] : 0.f;
-      const float r0 = m.lrst[0][r], r1 = has1 ? m.lrst[1][r] : 0.f;
-      const float lsum = l0 * f0 + l1 * f1;
-      const float inv = 1.f / (r0 * f0 + r1 * f1);
-      const float g0 = f0 * inv, g1 = f1 * inv;
-      uint4* orow = reinterpret_cast<uint4*>(p.out + row * D);
-      const uint32_t tO0 = tmem + lane_base + L::TM_O, tO1 = tO0 + 128;
-#pragma unroll
-      for (int c0 = w * (D / 2); c0 < (w + 1) * (D / 2); c0 += 32) {
-        uint32_t a[32], bb[32];
-        if (has1) {
-          tmem_ld32x2(tO0 + c0, tO1 + c0, a, bb);
-        } else {
-          tmem_ld32(tO0 + c0, a);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) bb[e] = 0u;
-        }
+      // both threads of a row add the halves in the same order
+      const float lt = m.xsum[0][0][r] + m.xsum[0][1][r];
+      const float inv = 1.f / (m.xsum[1][0][r] + m.xsum[1][1][r]);
+      uint4* orow = reinterpret_cast<uint4*>(p.out + row * D + hsel * (D / 2));
+#pragma unroll 1
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
+        uint32_t a[32];
+        tmem_ld32(tO + c0, a);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          float o[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            o[e] = __uint_as_float(a[q4 * 8 + e]) * g0 + __uint_as_float(bb[q4 * 8 + e]) * g1;
           uint4 x;
-          x.x = pack_bf16x2(o[0], o[1]);
-          x.y = pack_bf16x2(o[2], o[3]);
-          x.z = pack_bf16x2(o[4], o[5]);
-          x.w = pack_bf16x2(o[6], o[7]);
+          x.x = pack_bf16x2(__uint_as_float(a[q4 * 8 + 0]) * inv, __uint_as_float(a[q4 * 8 + 1]) * inv);
+          x.y = pack_bf16x2(__uint_as_float(a[q4 * 8 + 2]) * inv, __uint_as_float(a[q4 * 8 + 3]) * inv);
+          x.z = pack_bf16x2(__uint_as_float(a[q4 * 8 + 4]) * inv, __uint_as_float(a[q4 * 8 + 5]) * inv);
+          x.w = pack_bf16x2(__uint_as_float(a[q4 * 8 + 6]) * inv, __uint_as_float(a[q4 * 8 + 7]) * inv);
           orow[(c0 >> 3) + q4] = x;
         }
       }
-      if (w == 0) p.lse[row] = mx * 0.6931471805599453f + logf(lsum);
+      if (hsel == 0) p.lse[row] = m_used * 0.6931471805599453f + logf(lt);
     }
   }
   tc_fence_before();
