@@ -22,7 +22,7 @@
 //
 // Two warps issue MMAs, each in its own order, so neither waits behind the
 // other's dependencies: one issues S^T_i and dP^T_i (looking ahead), the
-// other dV_i and dK_i together once dS^T_i is ready. The
+// other dV_i as soon as P^T_i is ready and dK_i once dS^T_i is. The
 // softmax warps run each step in two phases: phase A turns S^T_i into P^T_i,
 // phase B reads dP^T_i (releasing its region) and forms dS^T_i. Q rides a
 // 3-stage ring because each Q tile is read twice a step apart (by S^T_i and
@@ -49,7 +49,7 @@ struct DkvMisc {
   uint64_t kv_full;
   uint64_t q_full[kQStages], q_empty[kQStages];
   uint64_t do_full[kDoStages], do_empty[kDoStages];
-  uint64_t s_full[2], dp_full[2], dp_free[2], ds_full[2], grad_done[2];
+  uint64_t s_full[2], dp_full[2], p_full[2], dp_free[2], ds_full[2], grad_done[2];
   uint64_t final_sd, final_grad;
   uint32_t tmem_base;
   int abort_flag;
@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&m.s_full[s], 1);
       mbar_init(&m.dp_full[s], 1);
+      mbar_init(&m.p_full[s], 256);
       mbar_init(&m.dp_free[s], 256);
       mbar_init(&m.ds_full[s], 256);
       mbar_init(&m.grad_done[s], 1);
@@ -232,28 +233,31 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
       for (int tq = walk.first(); tq < walk.end(); tq = walk.next(tq), ++j) {
         const int qs = j % kQStages, ds = j % kDoStages;
         const uint32_t sreg = tmem + L::reg_s(j);
-        // both gradient products of step j as one uninterrupted group of 16
-        // MMAs once dS^T_j is in place (the softmax threads wrote P^T_j before
-        // dS^T_j): an mbarrier wait right behind a short group starves the
-        // tensor pipe, and nothing waits on dV_j alone
+        // dV_j as soon as P^T_j is in place, dK_j once dS^T_j is: dP^T_{j+1}
+        // waits for both, and only dK_j then stands between the end of the
+        // softmax and the next dP^T
         if (!g.wait_warp(&m.do_full[ds], (j / kDoStages) & 1, 8)) { ok = false; break; }
-        if (!g.wait_warp(&m.q_full[qs], (j / kQStages) & 1, 9)) { ok = false; break; }
-        if (!g.wait_warp(&m.ds_full[j & 1], (j >> 1) & 1, 11)) { ok = false; break; }
+        if (!g.wait_warp(&m.p_full[j & 1], (j >> 1) & 1, 9)) { ok = false; break; }
         tc_fence_after();
         const uint64_t gd = sdesc_sw128(sDO + ds * L::TB, L::CHUNK, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          if (leader)
+            umma_bf16_ta(tmem + L::TM_DV, sreg + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(gd, kk * 2048), idG,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+        if (leader) umma_commit(&m.do_empty[ds]);
+        __syncwarp();
+        if (!g.wait_warp(&m.q_full[qs], (j / kQStages) & 1, 10)) { ok = false; break; }
+        if (!g.wait_warp(&m.ds_full[j & 1], (j >> 1) & 1, 11)) { ok = false; break; }
+        tc_fence_after();
         const uint64_t gq = sdesc_sw128(sQ + qs * L::TB, L::CHUNK, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-          const uint32_t pcol = sreg + (kk >> 2) * 64 + (kk & 3) * 8;
-          if (leader) {
-            umma_bf16_ta(tmem + L::TM_DV, pcol, sdesc_add(gd, kk * 2048), idG, acc);
-            umma_bf16_ta(tmem + L::TM_DK, pcol + 32, sdesc_add(gq, kk * 2048), idG, acc);
-          }
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          if (leader)
+            umma_bf16_ta(tmem + L::TM_DK, sreg + (kk >> 2) * 64 + 32 + (kk & 3) * 8, sdesc_add(gq, kk * 2048), idG,
+                         (j > 0 || kk > 0) ? 1u : 0u);
         if (leader) {
           umma_commit(&m.grad_done[j & 1]);
-          umma_commit(&m.do_empty[ds]);
           umma_commit(&m.q_empty[qs]);
         }
         __syncwarp();
@@ -326,6 +330,8 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
           tmem_st16_nowait(sreg + 16 * c, pw);
         }
         tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&m.p_full[i & 1]);
         // ---- phase B: dS^T = P^T * (dP^T - delta), bf16 next to P^T. P^T is read
         // back as the bf16 values the dV product uses, so dS^T is formed from
         // the same rounded probabilities
