@@ -12,10 +12,11 @@
 //
 // Every MMA is 128 x 128 (or 128 x D) with K = 16. Two warps issue them: one
 // issues dP and S, the other dQ as soon as each tile's dS is ready, so neither
-// waits behind the other's dependencies. TMEM holds dQ, one dP region and
-// two S regions used by alternate key tiles. The softmax warps release the dP
-// region as soon as they have loaded it, so the next tile's S and dP run on
-// the tensor core while this tile's dS is being formed.
+// waits behind the other's dependencies. TMEM holds dQ, one S region and two
+// dP regions used by alternate key tiles; dS is written over its tile's dP.
+// The softmax warps release the S region as soon as they have loaded it, and
+// a dP region is needed again only two tiles later, so the next tile's S and
+// dP run on the tensor core while this tile's dS is being formed.
 //
 // Warp roles: warp 0 TMA producer (Q and dO once; K through a 3-stage ring,
 // V through a 2-stage ring), warp 1 dP/S issuer and TMEM owner, warp 2 dQ
@@ -44,13 +45,15 @@ struct DqLayout {
   static constexpr uint32_t TILE_BYTES = OFF_V + NSV * TB;
   static constexpr uint32_t MISC_BYTES = 2048;
   static constexpr uint32_t SMEM = TILE_BYTES + MISC_BYTES + 1024;
-  // TMEM: dQ accumulator, then S for even tiles, dP, S for odd tiles (128 columns each)
-  static constexpr uint32_t TM_DQ = 0, TM_S0 = 128, TM_DP = 256, TM_S1 = 384, TMEM_COLS = 512;
+  // TMEM: dQ accumulator, one S region, and two dP regions (128 columns each)
+  // used by alternate tiles; dS is written over its tile's dP
+  static constexpr uint32_t TM_DQ = 0, TM_S = 128, TM_P0 = 256, TM_P1 = 384, TMEM_COLS = 512;
+  static __device__ __forceinline__ uint32_t reg_p(int j) { return (j & 1) ? TM_P1 : TM_P0; }
 };
 
 struct DqMisc {
   uint64_t q_full, k_full[3], k_empty[3], v_full[2], v_empty[2];
-  uint64_t s_full[2], dp_free[2], ds_full[2], dq_done[2], mma_final[2];
+  uint64_t s_full, s_free, ds_full[2], dq_done[2], mma_final[2];
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) int32_t segkv[3][128];
@@ -91,9 +94,9 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(&m.v_full[s], 1);
       mbar_init(&m.v_empty[s], 1);
     }
+    mbar_init(&m.s_full, 1);
+    mbar_init(&m.s_free, 256);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&m.s_full[s], 1);
-      mbar_init(&m.dp_free[s], 256);
       mbar_init(&m.ds_full[s], 256);
       mbar_init(&m.dq_done[s], 1);
     }
@@ -159,30 +162,29 @@ __global__ void __launch_bounds__(352, 1)
     int j = 0;
     for (int tk = walk.first(); ok && tk <= tq; tk = walk.next(tk), ++j) {
       const int rs = j & 1, sk = j % NSK, sv = j % NSV;
-      // dP_j into the dP region once the softmax of tile j-1 has read it
+      // dP_j into dP region rs once dQ_{j-2} has read the dS that was there
       if (!g.wait_warp(&m.v_full[sv], (j / NSV) & 1, 7)) { ok = false; break; }
-      if (j >= 1 && !g.wait_warp(&m.dp_free[(j - 1) & 1], ((j - 1) >> 1) & 1, 8)) { ok = false; break; }
+      if (j >= 2 && !g.wait_warp(&m.dq_done[rs], ((j - 2) >> 1) & 1, 8)) { ok = false; break; }
       tc_fence_after();
       const uint64_t vd = sdesc_sw128(sV + sv * L::TB, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-        if (leader) umma_bf16(tmem + L::TM_DP, sdesc_add(dod, ko), sdesc_add(vd, ko), idS, kk > 0 ? 1u : 0u);
+        if (leader) umma_bf16(tmem + L::reg_p(j), sdesc_add(dod, ko), sdesc_add(vd, ko), idS, kk > 0 ? 1u : 0u);
       }
       if (leader) umma_commit(&m.v_empty[sv]);
       __syncwarp();
-      // S_j into the S region of tile j-2, free once dQ of tile j-2 ran
+      // S_j into the S region once the softmax has read S_{j-1}
       if (!g.wait_warp(&m.k_full[sk], (j / NSK) & 1, 5)) { ok = false; break; }
-      if (j >= 2 && !g.wait_warp(&m.dq_done[rs], ((j - 2) >> 1) & 1, 6)) { ok = false; break; }
+      if (j >= 1 && !g.wait_warp(&m.s_free, (j - 1) & 1, 6)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t sreg = tmem + (rs ? L::TM_S1 : L::TM_S0);
       const uint64_t kd = sdesc_sw128(sK + sk * L::TB, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-        if (leader) umma_bf16(sreg, sdesc_add(qd, ko), sdesc_add(kd, ko), idS, kk > 0 ? 1u : 0u);
+        if (leader) umma_bf16(tmem + L::TM_S, sdesc_add(qd, ko), sdesc_add(kd, ko), idS, kk > 0 ? 1u : 0u);
       }
-      if (leader) umma_commit(&m.s_full[rs]);
+      if (leader) umma_commit(&m.s_full);  // also covers dP_j, issued before
       __syncwarp();
     }
     if (leader) {
@@ -193,7 +195,8 @@ __global__ void __launch_bounds__(352, 1)
   } else if (warp == 2) {
     // ------------------------------------------------------------ dQ issuer
     // dQ += dS_j K_j as soon as dS_j is in TMEM: thread-half h keeps the dS of
-    // its 64 key columns in S columns 64h..64h+31; K is the MN-major B operand.
+    // its 64 key columns in columns 64h..64h+31 of the tile's dP region; K is
+    // the MN-major B operand.
     const bool leader = lane == 0;
     constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, true);
     bool ok = true;
@@ -203,12 +206,12 @@ __global__ void __launch_bounds__(352, 1)
       if (!g.wait_warp(&m.k_full[sk], (j / NSK) & 1, 2)) { ok = false; break; }
       if (!g.wait_warp(&m.ds_full[rs], (j >> 1) & 1, 3)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t sreg = tmem + (rs ? L::TM_S1 : L::TM_S0);
+      const uint32_t preg = tmem + L::reg_p(j);
       const uint64_t kmn = sdesc_sw128(sK + sk * L::TB, L::CHUNK, 1024);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         if (leader)
-          umma_bf16_ta(tmem + L::TM_DQ, sreg + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(kmn, kk * 2048), idQ,
+          umma_bf16_ta(tmem + L::TM_DQ, preg + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(kmn, kk * 2048), idQ,
                        (j > 0 || kk > 0) ? 1u : 0u);
       if (leader) {
         umma_commit(&m.dq_done[rs]);
@@ -242,22 +245,22 @@ __global__ void __launch_bounds__(352, 1)
         ok = g.wait(&m.k_full[sk], (j / NSK) & 1, 9);
         if (!__all_sync(~0u, ok)) { ok = false; break; }
       }
-      ok = g.wait(&m.s_full[rs], (j >> 1) & 1, 10);
+      ok = g.wait(&m.s_full, j & 1, 10);
       if (!__all_sync(~0u, ok)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t sreg = tmem + lane_base + (rs ? L::TM_S1 : L::TM_S0) + hsel * 64;
-      const uint32_t dreg = tmem + lane_base + L::TM_DP + hsel * 64;
+      const uint32_t sreg = tmem + lane_base + L::TM_S + hsel * 64;
+      const uint32_t preg = tmem + lane_base + L::reg_p(j) + hsel * 64;
       const int c0 = hsel * 64;
       // Two 32-key chunks in a rolled loop (the softmax code must stay small:
       // instruction fetch, not arithmetic, limits these warps). dS goes over
-      // this thread's own S columns, which the chunk has already read.
+      // this thread's own dP columns, which the chunk has already read.
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t sv[32], dp[32];
-        tmem_ld32x2(sreg + 32 * c, dreg + 32 * c, sv, dp);
-        if (c == 1) {  // the dP region may now take the next tile's dP
+        tmem_ld32x2(sreg + 32 * c, preg + 32 * c, sv, dp);
+        if (c == 1) {  // S fully read: the S region may take the next tile's S
           tc_fence_before();
-          mbar_arrive(&m.dp_free[rs]);
+          mbar_arrive(&m.s_free);
         }
         const int k0 = tk * kTile + c0 + 32 * c;
         if (masked) {
@@ -280,7 +283,7 @@ __global__ void __launch_bounds__(352, 1)
           const float p1 = ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2));
           w[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - dlt), p1 * (__uint_as_float(dp[e + 1]) - dlt));
         }
-        tmem_st16_nowait(sreg + 16 * c, w);
+        tmem_st16_nowait(preg + 16 * c, w);
       }
       tmem_wait_st();
       tc_fence_before();
