@@ -28,7 +28,8 @@
 // 3-stage ring because each Q tile is read twice a step apart (by S^T_i and
 // by dK_i); dO rides a 2-stage ring.
 //
-// Warp roles: warp 0 TMA producer, warp 1 issues S^T/dP^T and owns TMEM,
+// Warp roles: warp 0 TMA producer (lane 0 the Q ring, lane 1 the dO ring),
+// warp 1 issues S^T/dP^T and owns TMEM,
 // warp 2 issues dV/dK, warps 3..10 softmax: two threads per key row (TMEM
 // lane quarter = warp index mod 4), 64 query columns each.
 #include <cuda_runtime.h>
@@ -137,9 +138,10 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Lane 0 loads K, V and the Q ring (with lse), lane 1 the dO ring (with
+    // delta): each ring refills as soon as its own stage is released.
     if (lane == 0) {
       prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmDO);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       const int krow = (b * p.Hkv + hk) * p.N + tk * kTile;
@@ -148,30 +150,38 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
         tma_load_2d(base + L::OFF_K + c * L::CHUNK, &tmK, &m.kv_full, c * 64, krow);
         tma_load_2d(base + L::OFF_V + c * L::CHUNK, &tmV, &m.kv_full, c * 64, krow);
       }
-      int i = 0, nq = 0, nd = 0;  // steps, Q loads and dO loads issued
+      int i = 0;
       bool ok = true;
       for (int hq = h0; ok && hq < h1; ++hq) {
         for (int tq = walk.first(); tq < walk.end(); tq = walk.next(tq), ++i) {
-          const int qs = i % kQStages, ds = i % kDoStages;
+          const int qs = i % kQStages;
           const int qrow = (b * p.Hq + hq) * p.N + tq * kTile;
           if (!g.wait(&m.q_empty[qs], ((i / kQStages) & 1) ^ 1, 1)) { ok = false; break; }
           mbar_expect_tx(&m.q_full[qs], L::TB + 512);
           for (int c = 0; c < D / 64; ++c)
             tma_load_2d(base + L::OFF_Q + qs * L::TB + c * L::CHUNK, &tmQ, &m.q_full[qs], c * 64, qrow);
           bulk_load(m.lse[qs], p.lse_in + qrow, 512, &m.q_full[qs]);
-          ++nq;
+        }
+      }
+      // no copy may still be landing when the CTA exits
+      g.drain(&m.kv_full, 0);
+      for (int k = (i > kQStages ? i - kQStages : 0); k < i; ++k) g.drain(&m.q_full[k % kQStages], (k / kQStages) & 1);
+    } else if (lane == 1) {
+      prefetch_tmap(&tmDO);
+      int i = 0;
+      bool ok = true;
+      for (int hq = h0; ok && hq < h1; ++hq) {
+        for (int tq = walk.first(); tq < walk.end(); tq = walk.next(tq), ++i) {
+          const int ds = i % kDoStages;
+          const int qrow = (b * p.Hq + hq) * p.N + tq * kTile;
           if (!g.wait(&m.do_empty[ds], ((i / kDoStages) & 1) ^ 1, 2)) { ok = false; break; }
           mbar_expect_tx(&m.do_full[ds], L::TB + 512);
           for (int c = 0; c < D / 64; ++c)
             tma_load_2d(base + L::OFF_DO + ds * L::TB + c * L::CHUNK, &tmDO, &m.do_full[ds], c * 64, qrow);
           bulk_load(m.dl[ds], p.delta + qrow, 512, &m.do_full[ds]);
-          ++nd;
         }
       }
-      // no copy may still be landing when the CTA exits
-      g.drain(&m.kv_full, 0);
-      for (int k = (nq > kQStages ? nq - kQStages : 0); k < nq; ++k) g.drain(&m.q_full[k % kQStages], (k / kQStages) & 1);
-      for (int k = (nd > kDoStages ? nd - kDoStages : 0); k < nd; ++k)
+      for (int k = (i > kDoStages ? i - kDoStages : 0); k < i; ++k)
         g.drain(&m.do_full[k % kDoStages], (k / kDoStages) & 1);
     }
     __syncwarp();

@@ -116,36 +116,41 @@ __global__ void __launch_bounds__(352, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Lane 0 loads Q, dO and the K ring (with the key tiles' segment ids),
+    // lane 1 the V ring: each ring refills as soon as its own stage is released.
+    const int krow0 = (b * p.Hkv + hk) * p.N;
     if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmDO);
       prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
       const int qrow = (b * p.Hq + h) * p.N + tq * kTile;
-      const int krow0 = (b * p.Hkv + hk) * p.N;
       mbar_expect_tx(&m.q_full, 2 * L::TB);
       for (int c = 0; c < D / 64; ++c) {
         tma_load_2d(base + L::OFF_Q + c * L::CHUNK, &tmQ, &m.q_full, c * 64, qrow);
         tma_load_2d(base + L::OFF_DO + c * L::CHUNK, &tmDO, &m.q_full, c * 64, qrow);
       }
-      int jk = 0, jv = 0;  // K and V tiles issued
-      for (int tk = walk.first(); tk <= tq; tk = walk.next(tk)) {
-        const int sk = jk % NSK, sv = jv % NSV;
+      int jk = 0;
+      for (int tk = walk.first(); tk <= tq; tk = walk.next(tk), ++jk) {
+        const int sk = jk % NSK;
         if (!g.wait(&m.k_empty[sk], ((jk / NSK) & 1) ^ 1, 1)) break;
         mbar_expect_tx(&m.k_full[sk], L::TB + (p.seg ? 512 : 0));
         for (int c = 0; c < D / 64; ++c)
           tma_load_2d(base + L::OFF_K + sk * L::TB + c * L::CHUNK, &tmK, &m.k_full[sk], c * 64, krow0 + tk * kTile);
         if (p.seg) bulk_load(m.segkv[sk], p.seg + (size_t)b * p.N + tk * kTile, 512, &m.k_full[sk]);
-        ++jk;
-        if (!g.wait(&m.v_empty[sv], ((jv / NSV) & 1) ^ 1, 2)) break;
-        mbar_expect_tx(&m.v_full[sv], L::TB);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_2d(base + L::OFF_V + sv * L::TB + c * L::CHUNK, &tmV, &m.v_full[sv], c * 64, krow0 + tk * kTile);
-        ++jv;
       }
       // no copy may still be landing when the CTA exits
       g.drain(&m.q_full, 0);
       for (int i = (jk > NSK ? jk - NSK : 0); i < jk; ++i) g.drain(&m.k_full[i % NSK], (i / NSK) & 1);
+    } else if (lane == 1) {
+      prefetch_tmap(&tmV);
+      int jv = 0;
+      for (int tk = walk.first(); tk <= tq; tk = walk.next(tk), ++jv) {
+        const int sv = jv % NSV;
+        if (!g.wait(&m.v_empty[sv], ((jv / NSV) & 1) ^ 1, 2)) break;
+        mbar_expect_tx(&m.v_full[sv], L::TB);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(base + L::OFF_V + sv * L::TB + c * L::CHUNK, &tmV, &m.v_full[sv], c * 64, krow0 + tk * kTile);
+      }
       for (int i = (jv > NSV ? jv - NSV : 0); i < jv; ++i) g.drain(&m.v_full[i % NSV], (i / NSV) & 1);
     }
     __syncwarp();
