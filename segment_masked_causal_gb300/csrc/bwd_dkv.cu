@@ -153,7 +153,9 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
       int i = 0;
       bool ok = true;
       for (int hq = h0; ok && hq < h1; ++hq) {
-        for (int tq = walk.first(); tq < walk.end(); tq = walk.next(tq), ++i) {
+        int4 te = walk.kt, te_next;  // table entries of this and the next visited query tile
+        for (int tq = walk.first(), tq_next; tq < walk.end(); tq = tq_next, te = te_next, ++i) {
+          tq_next = walk.next(tq, te_next);  // loaded now, used after this tile's work
           const int qs = i % kQStages;
           const int qrow = (b * p.Hq + hq) * p.N + tq * kTile;
           if (!g.wait(&m.q_empty[qs], ((i / kQStages) & 1) ^ 1, 1)) { ok = false; break; }
@@ -171,7 +173,9 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
       int i = 0;
       bool ok = true;
       for (int hq = h0; ok && hq < h1; ++hq) {
-        for (int tq = walk.first(); tq < walk.end(); tq = walk.next(tq), ++i) {
+        int4 te = walk.kt, te_next;  // table entries of this and the next visited query tile
+        for (int tq = walk.first(), tq_next; tq < walk.end(); tq = tq_next, te = te_next, ++i) {
+          tq_next = walk.next(tq, te_next);  // loaded now, used after this tile's work
           const int ds = i % kDoStages;
           const int qrow = (b * p.Hq + hq) * p.N + tq * kTile;
           if (!g.wait(&m.do_empty[ds], ((i / kDoStages) & 1) ^ 1, 2)) { ok = false; break; }
@@ -195,7 +199,9 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
     bool ok = g.wait_warp(&m.kv_full, 0, 3);
     int i = 0;
     for (int hq = h0; ok && hq < h1; ++hq) {
-      for (int tq = walk.first(); tq < walk.end(); tq = walk.next(tq), ++i) {
+      int4 te = walk.kt, te_next;  // table entries of this and the next visited query tile
+      for (int tq = walk.first(), tq_next; tq < walk.end(); tq = tq_next, te = te_next, ++i) {
+        tq_next = walk.next(tq, te_next);  // loaded now, used after this tile's work
         const int qs = i % kQStages, ds = i % kDoStages;
         if (!g.wait_warp(&m.q_full[qs], (i / kQStages) & 1, 4)) { ok = false; break; }
         // S^T_i where dP^T_{i-1} was: free once the softmax has read it
@@ -240,7 +246,9 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
     bool ok = true;
     int j = 0;
     for (int hq = h0; ok && hq < h1; ++hq) {
-      for (int tq = walk.first(); tq < walk.end(); tq = walk.next(tq), ++j) {
+      int4 te = walk.kt, te_next;  // table entries of this and the next visited query tile
+      for (int tq = walk.first(), tq_next; tq < walk.end(); tq = tq_next, te = te_next, ++j) {
+        tq_next = walk.next(tq, te_next);  // loaded now, used after this tile's work
         const int qs = j % kQStages, ds = j % kDoStages;
         const uint32_t sreg = tmem + L::reg_s(j);
         // dV_j as soon as P^T_j is in place, dK_j once dS^T_j is: dP^T_{j+1}
@@ -291,7 +299,9 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
     bool ok = true;
     int i = 0;
     for (int hq = h0; ok && hq < h1; ++hq) {
-      for (int tq = walk.first(); tq < walk.end(); tq = walk.next(tq), ++i) {
+      int4 te = walk.kt, te_next;  // table entries of this and the next visited query tile
+      for (int tq = walk.first(), tq_next; tq < walk.end(); tq = tq_next, te = te_next, ++i) {
+        tq_next = walk.next(tq, te_next);  // loaded now, used after this tile's work
         const int qs = i % kQStages, ds = i % kDoStages;
         // this step's lse and delta vectors (waited here, before this thread
         // releases anything of the step, so neither ring can run ahead)
@@ -302,7 +312,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
         tc_fence_after();
         const uint32_t sreg = tmem + lane_base + L::reg_s(i) + hsel * 64;
         const uint32_t dreg = tmem + lane_base + L::reg_dp(i) + hsel * 64;
-        const bool masked = !tile_pair_full(tq, trow[tq], tk, kt);
+        const bool masked = !tile_pair_full(tq, te, tk, kt);
         const int c0 = hsel * 64;        // first query column of this thread within the tile
         const int q0 = tq * kTile + c0;  // its token index
         // ---- phase A: P^T = exp2(S^T * scale*log2e - lse*log2e), bf16 over S^T.

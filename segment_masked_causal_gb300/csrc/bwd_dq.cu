@@ -130,7 +130,9 @@ __global__ void __launch_bounds__(352, 1)
         tma_load_2d(base + L::OFF_DO + c * L::CHUNK, &tmDO, &m.q_full, c * 64, qrow);
       }
       int jk = 0;
-      for (int tk = walk.first(); tk <= tq; tk = walk.next(tk), ++jk) {
+      int4 te, te_next;  // table entries of this and the next visited key tile
+      for (int tk = walk.first(te), tk_next; tk <= tq; tk = tk_next, te = te_next, ++jk) {
+        tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
         const int sk = jk % NSK;
         if (!g.wait(&m.k_empty[sk], ((jk / NSK) & 1) ^ 1, 1)) break;
         mbar_expect_tx(&m.k_full[sk], L::TB + (p.seg ? 512 : 0));
@@ -144,7 +146,9 @@ __global__ void __launch_bounds__(352, 1)
     } else if (lane == 1) {
       prefetch_tmap(&tmV);
       int jv = 0;
-      for (int tk = walk.first(); tk <= tq; tk = walk.next(tk), ++jv) {
+      int4 te, te_next;  // table entries of this and the next visited key tile
+      for (int tk = walk.first(te), tk_next; tk <= tq; tk = tk_next, te = te_next, ++jv) {
+        tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
         const int sv = jv % NSV;
         if (!g.wait(&m.v_empty[sv], ((jv / NSV) & 1) ^ 1, 2)) break;
         mbar_expect_tx(&m.v_full[sv], L::TB);
@@ -165,7 +169,9 @@ __global__ void __launch_bounds__(352, 1)
     const uint64_t qd = sdesc_sw128(sQ, 16, 1024), dod = sdesc_sw128(sDO, 16, 1024);
     bool ok = g.wait_warp(&m.q_full, 0, 4);
     int j = 0;
-    for (int tk = walk.first(); ok && tk <= tq; tk = walk.next(tk), ++j) {
+    int4 te, te_next;  // table entries of this and the next visited key tile
+    for (int tk = walk.first(te), tk_next; ok && tk <= tq; tk = tk_next, te = te_next, ++j) {
+      tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
       const int rs = j & 1, sk = j % NSK, sv = j % NSV;
       // dP_j into dP region rs once dQ_{j-2} has read the dS that was there
       if (!g.wait_warp(&m.v_full[sv], (j / NSV) & 1, 7)) { ok = false; break; }
@@ -206,7 +212,9 @@ __global__ void __launch_bounds__(352, 1)
     constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, true);
     bool ok = true;
     int j = 0;
-    for (int tk = walk.first(); ok && tk <= tq; tk = walk.next(tk), ++j) {
+    int4 te, te_next;  // table entries of this and the next visited key tile
+    for (int tk = walk.first(te), tk_next; ok && tk <= tq; tk = tk_next, te = te_next, ++j) {
+      tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
       const int rs = j & 1, sk = j % NSK;
       if (!g.wait_warp(&m.k_full[sk], (j / NSK) & 1, 2)) { ok = false; break; }
       if (!g.wait_warp(&m.ds_full[rs], (j >> 1) & 1, 3)) { ok = false; break; }
@@ -243,9 +251,11 @@ __global__ void __launch_bounds__(352, 1)
     const float sl2 = p.scale_log2;
     bool ok = true;
     int j = 0;
-    for (int tk = walk.first(); tk <= tq; tk = walk.next(tk), ++j) {
+    int4 te, te_next;  // table entries of this and the next visited key tile
+    for (int tk = walk.first(te), tk_next; tk <= tq; tk = tk_next, te = te_next, ++j) {
+      tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
       const int rs = j & 1, sk = j % NSK;
-      const bool masked = !tile_pair_full(tq, walk.qt, tk, trow[tk]);
+      const bool masked = !tile_pair_full(tq, walk.qt, tk, te);
       if (masked && p.seg) {  // segment ids of this key tile arrived with K
         ok = g.wait(&m.k_full[sk], (j / NSK) & 1, 9);
         if (!__all_sync(~0u, ok)) { ok = false; break; }

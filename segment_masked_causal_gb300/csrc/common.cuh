@@ -65,6 +65,18 @@ struct KvWalk {
     for (int tk = first(); tk <= tq; tk = next(tk)) ++n;
     return n;
   }
+  // The same walk, also returning the table entry of the tile it lands on
+  // (loaded once). Callers ask for the next tile at the start of their work
+  // on the current one, so the load's latency hides behind that work.
+  __device__ __forceinline__ int next(int tk, int4& e) const {
+    for (++tk; tk < tq; ++tk) {
+      e = row[tk];
+      if (tiles_overlap(e, qt)) return tk;
+    }
+    e = qt;
+    return tk;
+  }
+  __device__ __forceinline__ int first(int4& e) const { return next(qt.z - 1, e); }
 };
 
 // Query tiles a key tile is visited by, in increasing order.
@@ -80,6 +92,16 @@ struct QWalk {
     return kt.w + 1;
   }
   __device__ __forceinline__ int end() const { return kt.w + 1; }
+  // The same walk, also returning the table entry of the tile it lands on
+  // (see KvWalk::next(int, int4&)).
+  __device__ __forceinline__ int next(int tq, int4& e) const {
+    for (++tq; tq <= kt.w; ++tq) {
+      e = row[tq];
+      if (tiles_overlap(e, kt)) return tq;
+    }
+    e = kt;
+    return kt.w + 1;
+  }
 };
 
 }  // namespace pa

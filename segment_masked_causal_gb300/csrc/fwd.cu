@@ -129,7 +129,9 @@ __global__ void __launch_bounds__(352, 1)
       mbar_expect_tx(&m.q_full, L::TB);
       for (int c = 0; c < D / 64; ++c) tma_load_2d(base + L::OFF_Q + c * L::CHUNK, &tmQ, &m.q_full, c * 64, qrow);
       int jk = 0;
-      for (int tk = walk.first(); tk <= tq; tk = walk.next(tk), ++jk) {
+      int4 te, te_next;  // table entries of this and the next visited key tile
+      for (int tk = walk.first(te), tk_next; tk <= tq; tk = tk_next, te = te_next, ++jk) {
+        tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
         const int sk = jk % NSK;
         if (!g.wait(&m.k_empty[sk], ((jk / NSK) & 1) ^ 1, 1)) break;
         mbar_expect_tx(&m.k_full[sk], L::TB);
@@ -142,7 +144,9 @@ __global__ void __launch_bounds__(352, 1)
     } else if (lane == 1) {
       prefetch_tmap(&tmV);
       int jv = 0;
-      for (int tk = walk.first(); tk <= tq; tk = walk.next(tk), ++jv) {
+      int4 te, te_next;  // table entries of this and the next visited key tile
+      for (int tk = walk.first(te), tk_next; tk <= tq; tk = tk_next, te = te_next, ++jv) {
+        tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
         const int sv = jv % NSV;
         if (!g.wait(&m.v_empty[sv], ((jv / NSV) & 1) ^ 1, 2)) break;
         mbar_expect_tx(&m.v_full[sv], L::TB + (p.seg ? 512 : 0));
@@ -162,7 +166,9 @@ __global__ void __launch_bounds__(352, 1)
     const uint64_t qd = sdesc_sw128(sQ, 16, 1024);
     bool ok = g.wait_warp(&m.q_full, 0, 3);
     int j = 0;
-    for (int tk = walk.first(); ok && tk <= tq; tk = walk.next(tk), ++j) {
+    int4 te, te_next;  // table entries of this and the next visited key tile
+    for (int tk = walk.first(te), tk_next; ok && tk <= tq; tk = tk_next, te = te_next, ++j) {
+      tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
       const int sb = j % NSB, sk = j % NSK;
       // S_j into buffer sb once PV_{j-3} has read the P that was there
       if (j >= NSB && !g.wait_warp(&m.pv_done[sb], ((j - NSB) / NSB) & 1, 4)) { ok = false; break; }
@@ -193,7 +199,9 @@ __global__ void __launch_bounds__(352, 1)
     constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
     bool ok = true;
     int j = 0;
-    for (int tk = walk.first(); ok && tk <= tq; tk = walk.next(tk), ++j) {
+    int4 te, te_next;  // table entries of this and the next visited key tile
+    for (int tk = walk.first(te), tk_next; ok && tk <= tq; tk = tk_next, te = te_next, ++j) {
+      tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
       const int sb = j % NSB, sv = j % NSV;
       if (!g.wait_warp(&m.v_full[sv], (j / NSV) & 1, 6)) { ok = false; break; }
       if (!g.wait_warp(&m.p_full[sb], (j / NSB) & 1, 7)) { ok = false; break; }
@@ -229,9 +237,11 @@ __global__ void __launch_bounds__(352, 1)
     float m_used = -INFINITY, l = 0.f, lr = 0.f;  // l and lr over this thread's half of the keys
     bool ok = true;
     int jj = 0;
-    for (int tk = walk.first(); tk <= tq; tk = walk.next(tk), ++jj) {
+    int4 te, te_next;  // table entries of this and the next visited key tile
+    for (int tk = walk.first(te), tk_next; tk <= tq; tk = tk_next, te = te_next, ++jj) {
+      tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
       const int sb = jj % NSB, xs = jj & 1;
-      const bool masked = !tile_pair_full(tq, walk.qt, tk, trow[tk]);
+      const bool masked = !tile_pair_full(tq, walk.qt, tk, te);
       if (masked && p.seg) {  // segment ids of this key tile arrived with V
         ok = g.wait(&m.v_full[jj % NSV], (jj / NSV) & 1, 8);
         if (!__all_sync(~0u, ok)) { ok = false; break; }
