@@ -359,21 +359,22 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
         if (!__all_sync(~0u, ok)) { ok = false; break; }
         tc_fence_after();
         const float4* d4 = reinterpret_cast<const float4*>(&m.dl[ds][c0]);
-#pragma unroll 1
+        // all of dP^T (64 columns) and P^T (32 packed columns) first, so the
+        // dP^T region is released before any arithmetic
+        uint32_t dpa[32], dpb[32], pb[32];
+        tmem_ld32x3(dreg, dreg + 32, sreg, dpa, dpb, pb);
+        tc_fence_before();
+        mbar_arrive(&m.dp_free[i & 1]);
+#pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t dp[32], pb[16];
-          tmem_ld32_ld16(dreg + 32 * c, sreg + 16 * c, dp, pb);
-          if (c == 1) {  // dP^T fully read: its region may take the next S^T
-            tc_fence_before();
-            mbar_arrive(&m.dp_free[i & 1]);
-          }
           uint32_t dw[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
             const float4 dv = d4[c * 8 + e4];
-            const float pp[4] = {__uint_as_float(pb[e4 * 2] << 16), __uint_as_float(pb[e4 * 2] & 0xFFFF0000u),
-                                 __uint_as_float(pb[e4 * 2 + 1] << 16),
-                                 __uint_as_float(pb[e4 * 2 + 1] & 0xFFFF0000u)};
+            const uint32_t w0 = pb[c * 16 + e4 * 2], w1 = pb[c * 16 + e4 * 2 + 1];
+            const float pp[4] = {__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u),
+                                 __uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u)};
+            const uint32_t* dp = c ? dpb : dpa;
             dw[e4 * 2] = pack_bf16x2(pp[0] * (__uint_as_float(dp[e4 * 4]) - dv.x),
                                      pp[1] * (__uint_as_float(dp[e4 * 4 + 1]) - dv.y));
             dw[e4 * 2 + 1] = pack_bf16x2(pp[2] * (__uint_as_float(dp[e4 * 4 + 2]) - dv.z),
