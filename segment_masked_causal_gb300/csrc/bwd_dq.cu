@@ -266,17 +266,19 @@ __global__ void __launch_bounds__(352, 1)
       const uint32_t sreg = tmem + lane_base + L::TM_S + hsel * 64;
       const uint32_t preg = tmem + lane_base + L::reg_p(j) + hsel * 64;
       const int c0 = hsel * 64;
-      // Two 32-key chunks in a rolled loop (the softmax code must stay small:
-      // instruction fetch, not arithmetic, limits these warps). dS goes over
-      // this thread's own dP columns, which the chunk has already read.
-#pragma unroll 1
+      // S (64 columns) and the first dP chunk first, so the S region is
+      // released before any arithmetic; dS goes over this thread's own dP
+      // columns, which have been read by then.
+      uint32_t sa[32], sb[32], dpa[32];
+      tmem_ld32x3(sreg, sreg + 32, preg, sa, sb, dpa);
+      tc_fence_before();
+      mbar_arrive(&m.s_free);
+#pragma unroll
       for (int c = 0; c < 2; ++c) {
-        uint32_t sv[32], dp[32];
-        tmem_ld32x2(sreg + 32 * c, preg + 32 * c, sv, dp);
-        if (c == 1) {  // S fully read: the S region may take the next tile's S
-          tc_fence_before();
-          mbar_arrive(&m.s_free);
-        }
+        uint32_t dpb[32];
+        if (c == 1) tmem_ld32(preg + 32, dpb);
+        uint32_t* sv = c ? sb : sa;
+        const uint32_t* dp = c ? dpb : dpa;
         const int k0 = tk * kTile + c0 + 32 * c;
         if (masked) {
           const int4* g4 = reinterpret_cast<const int4*>(&m.segkv[sk][c0 + 32 * c]);
