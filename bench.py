@@ -223,7 +223,7 @@ class Runner:
         rec(ev[2])
         pa.pa_build_tile_table(q, k, seg, self.ws)
         rec(ev[3])
-        pa.pa_bwd_delta(q, k, self.out, do, self.ws)
+        pa.pa_bwd_delta(q, k, self.out, do, self.lse, self.ws)
         rec(ev[4])
         pa.pa_bwd_dq(q, k, v, do, self.lse, seg, self.dq, self.ws)
         rec(ev[5])
@@ -352,7 +352,8 @@ def run_ours(args):
                 "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": traffic,
                 "peak_source": pk["source"] + " bf16 burst (MEASURED_PEAKS.json)" if pk["source"] == "measured"
                 else "fallback 1.9 PFLOP/s"}
-    delta_bytes = 2 * 2 * w.B * w.Hq * w.N * w.D + 4 * w.B * w.Hq * w.N
+    # per query row: read O and dO (bf16) and lse; write delta and lse*log2(e)
+    delta_bytes = 2 * 2 * w.B * w.Hq * w.N * w.D + 3 * 4 * w.B * w.Hq * w.N
     kernels = {k: {"ms": round(v, 4)} for k, v in kern.items()}
     for k in ("fwd", "dq", "dkv"):
         kernels[k]["tflops"] = round(FLOPS_PER_PAIR[k] * w.D * pairs / (kern[k] * 1e-3) / 1e12, 2)

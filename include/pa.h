@@ -28,7 +28,8 @@
  * Ownership: every pointer is device memory owned by the caller. The library
  * allocates no device memory and keeps no pointer after a call returns. The
  * workspace `ws` (pa_workspace_bytes) holds the per-tile segment-range table,
- * the backward's delta = rowsum(dO * O) and a device status word.
+ * the backward's per-row delta = rowsum(dO * O) and lse * log2(e), and a
+ * device status word.
  *
  * Execution: every call validates its arguments synchronously and returns an
  * error before launching anything; otherwise it enqueues its kernels on
@@ -116,16 +117,19 @@ pa_status pa_bwd_causal(const pa_dims* dims, const void* q, const void* k, const
  * them individually. pa_fwd is pa_build_tile_table + pa_fwd_tiles; pa_bwd is
  * pa_build_tile_table + pa_bwd_delta + pa_bwd_dq + pa_bwd_dkv, all on one
  * stream, in that order. The later steps read the tile table (and the bwd
- * steps the delta) from `ws`, so they must follow the steps that write it
- * with the same dims and the same seg (NULL seg = plain causal throughout).
- * pa_build_tile_table also clears the workspace status word.
+ * steps the per-row values of pa_bwd_delta) from `ws`, so they must follow
+ * the steps that write it with the same dims and the same seg (NULL seg =
+ * plain causal throughout). pa_build_tile_table also clears the workspace
+ * status word. pa_bwd_delta takes the forward's out and lse and stores, per
+ * query row, delta = rowsum(dO * O) and lse * log2(e) (the dK/dV step reads
+ * that copy; pa_bwd_dkv still validates its lse argument).
  */
 pa_status pa_build_tile_table(const pa_dims* dims, const int32_t* seg, void* ws, size_t ws_bytes,
                               pa_stream_t stream);
 pa_status pa_fwd_tiles(const pa_dims* dims, const void* q, const void* k, const void* v, const int32_t* seg,
                        void* out, float* lse, void* ws, size_t ws_bytes, pa_stream_t stream);
-pa_status pa_bwd_delta(const pa_dims* dims, const void* out, const void* dout, void* ws, size_t ws_bytes,
-                       pa_stream_t stream);
+pa_status pa_bwd_delta(const pa_dims* dims, const void* out, const void* dout, const float* lse, void* ws,
+                       size_t ws_bytes, pa_stream_t stream);
 pa_status pa_bwd_dq(const pa_dims* dims, const void* q, const void* k, const void* v, const void* dout,
                     const float* lse, const int32_t* seg, void* dq, void* ws, size_t ws_bytes, pa_stream_t stream);
 pa_status pa_bwd_dkv(const pa_dims* dims, const void* q, const void* k, const void* v, const void* dout,
@@ -144,7 +148,7 @@ pa_status pa_bwd_dkv(const pa_dims* dims, const void* q, const void* k, const vo
  * every GPU that loads the library until the process exits. The call makes no
  * allocation of any kind.
  *   - Limit: dims whose pa_workspace_bytes exceeds PA_NOALLOC_SCRATCH_BYTES
- *     (about B*Hq*N > 2 million query rows) are refused with PA_ERR_WORKSPACE.
+ *     (about B*Hq*N > 1 million query rows) are refused with PA_ERR_WORKSPACE.
  *   - The first call on each device looks up the array's device address with
  *     that device current; make that first call before any stream capture.
  *   - Every call on a device shares the one array, which keeps the last call's

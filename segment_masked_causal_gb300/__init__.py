@@ -67,7 +67,7 @@ def lib():
             L.pa_bwd_causal.argtypes = [D, P, P, P, P, P, P, P, P, P, P, S, P]
             L.pa_build_tile_table.argtypes = [D, P, P, S, P]
             L.pa_fwd_tiles.argtypes = [D, P, P, P, P, P, P, P, S, P]
-            L.pa_bwd_delta.argtypes = [D, P, P, P, S, P]
+            L.pa_bwd_delta.argtypes = [D, P, P, P, P, S, P]
             L.pa_bwd_dq.argtypes = [D, P, P, P, P, P, P, P, P, S, P]
             L.pa_bwd_dkv.argtypes = [D, P, P, P, P, P, P, P, P, P, S, P]
             for f in ("pa_fwd", "pa_fwd_causal", "pa_bwd", "pa_bwd_causal", "pa_build_tile_table", "pa_fwd_tiles",
@@ -186,12 +186,12 @@ def pa_fwd_tiles(q, k, v, seg, out, lse, ws, scale=0.0, stream=None):
                               _ptr(ws, None, "ws"), ws.numel(), _stream(stream)))
 
 
-def pa_bwd_delta(q, k, out, dout, ws, scale=0.0, stream=None):
+def pa_bwd_delta(q, k, out, dout, lse, ws, scale=0.0, stream=None):
     import torch
     bf = torch.bfloat16
     d = _dims_of(q, k, scale)
-    _check(lib().pa_bwd_delta(ctypes.byref(d), _ptr(out, bf, "out"), _ptr(dout, bf, "dout"), _ptr(ws, None, "ws"),
-                              ws.numel(), _stream(stream)))
+    _check(lib().pa_bwd_delta(ctypes.byref(d), _ptr(out, bf, "out"), _ptr(dout, bf, "dout"),
+                              _ptr(lse, torch.float32, "lse"), _ptr(ws, None, "ws"), ws.numel(), _stream(stream)))
 
 
 def pa_bwd_dq(q, k, v, dout, lse, seg, dq, ws, scale=0.0, stream=None):

@@ -20,7 +20,7 @@ constexpr size_t kAlign = 256;
 inline size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct WsLayout {
-  size_t status, tiles, delta, total;
+  size_t status, tiles, delta, lse2, total;
 };
 
 bool dims_ok(const pa_dims* d, pa_status* why) {
@@ -44,7 +44,8 @@ WsLayout ws_layout(const pa_dims* d) {
   w.status = 0;
   w.tiles = kAlign;
   w.delta = w.tiles + round_up((size_t)d->B * T * sizeof(int4));
-  w.total = w.delta + round_up((size_t)d->B * d->Hq * d->N * sizeof(float));
+  w.lse2 = w.delta + round_up((size_t)d->B * d->Hq * d->N * sizeof(float));
+  w.total = w.lse2 + round_up((size_t)d->B * d->Hq * d->N * sizeof(float));
   return w;
 }
 
@@ -80,6 +81,7 @@ pa::AttnParams make_params(const pa_dims* d, const int32_t* seg, void* ws) {
   p.status = reinterpret_cast<uint32_t*>(base + w.status);
   p.tiles = reinterpret_cast<const int4*>(base + w.tiles);
   p.delta = reinterpret_cast<float*>(base + w.delta);
+  p.lse2 = reinterpret_cast<float*>(base + w.lse2);
   return p;
 }
 
@@ -125,11 +127,12 @@ pa_status step_fwd(const pa_dims* d, const void* q, const void* k, const void* v
   return pa::launch_fwd(p, d->D, q, k, v, cu(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-pa_status step_delta(const pa_dims* d, const void* out, const void* dout, void* ws, size_t ws_bytes,
-                     pa_stream_t stream) {
-  pa_status s = check_call(d, ws, ws_bytes, {out, dout}, nullptr);
+pa_status step_delta(const pa_dims* d, const void* out, const void* dout, const float* lse, void* ws,
+                     size_t ws_bytes, pa_stream_t stream) {
+  pa_status s = check_call(d, ws, ws_bytes, {out, dout, lse}, nullptr);
   if (s != PA_OK) return s;
   pa::AttnParams p = make_params(d, nullptr, ws);
+  p.lse_in = lse;
   p.o = static_cast<const __nv_bfloat16*>(out);
   p.dout = static_cast<const __nv_bfloat16*>(dout);
   return pa::launch_delta(p, d->D, cu(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -171,7 +174,7 @@ pa_status bwd_impl(const pa_dims* d, const void* q, const void* k, const void* v
   pa_status s = check_call(d, ws, ws_bytes, {q, k, v, out, dout, lse, dq, dk, dv}, seg);
   if (s != PA_OK) return s;
   if ((s = step_tile_table(d, seg, ws, ws_bytes, stream)) != PA_OK) return s;
-  if ((s = step_delta(d, out, dout, ws, ws_bytes, stream)) != PA_OK) return s;
+  if ((s = step_delta(d, out, dout, lse, ws, ws_bytes, stream)) != PA_OK) return s;
   if ((s = step_dq(d, q, k, v, dout, lse, seg, dq, ws, ws_bytes, stream)) != PA_OK) return s;
   return step_dkv(d, q, k, v, dout, lse, seg, dk, dv, ws, ws_bytes, stream);
 }
@@ -220,9 +223,9 @@ pa_status pa_fwd_tiles(const pa_dims* dims, const void* q, const void* k, const 
   return step_fwd(dims, q, k, v, seg, out, lse, ws, ws_bytes, stream);
 }
 
-pa_status pa_bwd_delta(const pa_dims* dims, const void* out, const void* dout, void* ws, size_t ws_bytes,
-                       pa_stream_t stream) {
-  return step_delta(dims, out, dout, ws, ws_bytes, stream);
+pa_status pa_bwd_delta(const pa_dims* dims, const void* out, const void* dout, const float* lse, void* ws,
+                       size_t ws_bytes, pa_stream_t stream) {
+  return step_delta(dims, out, dout, lse, ws, ws_bytes, stream);
 }
 
 pa_status pa_bwd_dq(const pa_dims* dims, const void* q, const void* k, const void* v, const void* dout,

@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
           mbar_expect_tx(&m.q_full[qs], L::TB + 512);
           for (int c = 0; c < D / 64; ++c)
             tma_load_2d(base + L::OFF_Q + qs * L::TB + c * L::CHUNK, &tmQ, &m.q_full[qs], c * 64, qrow);
-          bulk_load(m.lse[qs], p.lse_in + qrow, 512, &m.q_full[qs]);
+          bulk_load(m.lse[qs], p.lse2 + qrow, 512, &m.q_full[qs]);  // lse * log2(e), from the delta step
         }
       }
       // no copy may still be landing when the CTA exits
@@ -315,7 +315,8 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
         const bool masked = !tile_pair_full(tq, te, tk, kt);
         const int c0 = hsel * 64;        // first query column of this thread within the tile
         const int q0 = tq * kTile + c0;  // its token index
-        // ---- phase A: P^T = exp2(S^T * scale*log2e - lse*log2e), bf16 over S^T.
+        // ---- phase A: P^T = exp2(S^T * scale*log2e - lse*log2e), bf16 over S^T
+        // (the delta step stored lse*log2e).
         // Two 32-column chunks in a rolled loop (the softmax code must stay
         // small: instruction fetch, not arithmetic, limits these warps).
 #pragma unroll 1
@@ -342,7 +343,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
             }
             float pz[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) pz[e] = ex2(fmaf(sz[e], sl2, -lz[e] * 1.4426950408889634f));
+            for (int e = 0; e < 4; ++e) pz[e] = ex2(fmaf(sz[e], sl2, -lz[e]));
             pw[e4 * 2] = pack_bf16x2(pz[0], pz[1]);
             pw[e4 * 2 + 1] = pack_bf16x2(pz[2], pz[3]);
           }

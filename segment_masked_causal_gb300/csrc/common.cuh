@@ -35,6 +35,7 @@ struct AttnParams {
   const __nv_bfloat16* dout;
   const float* lse_in;
   float* delta;  // (B, Hq, N), written by the delta kernel
+  float* lse2;   // (B, Hq, N) lse * log2(e), written by the delta kernel
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;

@@ -8,7 +8,7 @@ namespace pa {
 
 // Tile table (B, T) x {smin, smax, kv_lo, q_hi}; also clears the status word.
 cudaError_t launch_tile_table(const AttnParams& p, int4* tiles, cudaStream_t st);
-// delta[b, h, i] = sum_c dO[b, h, i, c] * O[b, h, i, c] (fp32).
+// delta[b, h, i] = sum_c dO[b, h, i, c] * O[b, h, i, c] (fp32), and lse2 = lse * log2(e).
 cudaError_t launch_delta(const AttnParams& p, int D, cudaStream_t st);
 cudaError_t launch_fwd(const AttnParams& p, int D, const void* q, const void* k, const void* v, cudaStream_t st);
 cudaError_t launch_bwd_dq(const AttnParams& p, int D, const void* q, const void* k, const void* v,

@@ -57,7 +57,8 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 template <int D>
 __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restrict__ o,
                                                     const __nv_bfloat16* __restrict__ dout,
-                                                    float* __restrict__ delta, size_t rows) {
+                                                    const float* __restrict__ lse, float* __restrict__ delta,
+                                                    float* __restrict__ lse2, size_t rows) {
   constexpr int LPR = D / 8;  // lanes per row
   const size_t gtid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
@@ -76,7 +77,10 @@ __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restr
     acc = fmaf(bf16hi(a.w), bf16hi(c.w), acc);
 #pragma unroll
     for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(~0u, acc, off);
-    if (sub == 0) delta[row] = acc;
+    if (sub == 0) {
+      delta[row] = acc;
+      lse2[row] = lse[row] * 1.4426950408889634f;  // for the dK/dV softmax, which works in base 2
+    }
   }
 }
 
@@ -102,9 +106,9 @@ cudaError_t launch_delta(const AttnParams& p, int D, cudaStream_t st) {
   const size_t cap = (size_t)sms * 8;
   if (blocks > cap) blocks = cap;
   if (D == 128)
-    delta_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.delta, rows);
+    delta_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, rows);
   else
-    delta_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.delta, rows);
+    delta_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, rows);
   return cudaGetLastError();
 }
 
