@@ -11,22 +11,27 @@
 // into one of three TMEM S buffers, P_j = 2^(S_j log2e scale - m) written back
 // as bf16 over S_j, and O += P_j V_j with P_j fed straight from TMEM into one
 // O accumulator. With three S buffers, S_{j+3} waits only for PV_j, which
-// finishes while the softmax is still on tiles j+1 and j+2: the softmax warps
-// never wait for their own PV. All eight softmax warps work on every tile, two
-// threads per query row (64 keys each); the two halves of a row exchange their
-// maxima through shared memory. One warp issues the S products, another the
-// PV products, each waiting only on its own dependencies.
+// finishes while the softmax is still on later tiles. The softmax runs in two
+// warpgroups, one thread per query row holding the row's 128 scores: group 0
+// takes the even visited tiles and group 1 the odd ones, so two tiles'
+// exponentials are in flight at once. The only step that passes from tile to
+// tile is the row maximum in use, which each group hands to the other through
+// shared memory as soon as it has its tile's maximum. One warp issues the S
+// products, another the PV products, each waiting only on its own
+// dependencies.
 //
 // Online softmax works in log2 units of the scaled score and rescales O only
 // when a row's maximum rises by more than 8 (a factor 256); P is always
 // computed against the maximum in use, so O and l stay consistent and O / l
-// is exact in real arithmetic. O is divided by the sum of the bf16-rounded
-// weights the PV product used; lse uses the exact fp32 sum.
+// is exact in real arithmetic. Each group keeps its own partial sums against
+// the maximum it last used; the epilogue brings both to the final maximum and
+// adds them. O is divided by the sum of the bf16-rounded weights the PV
+// product used; lse uses the exact fp32 sum.
 //
 // Warp roles: warp 0 TMA producer (Q once; K through a 3-stage ring, V and
 // the key tile's segment ids through a 2-stage ring), warp 1 S issuer and
-// TMEM owner, warp 2 PV issuer, warps 3..10 softmax (TMEM lane quarter =
-// warp index mod 4; warps w and w+4 share a quarter and split its rows' keys).
+// TMEM owner, warp 2 PV issuer, warps 3..6 softmax group 0 and warps 7..10
+// softmax group 1 (TMEM lane quarter = warp index mod 4).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -55,13 +60,63 @@ struct FwdLayout {
 
 struct FwdMisc {
   uint64_t q_full, k_full[3], k_empty[3], v_full[2], v_empty[2];
-  uint64_t s_full[3], p_full[3], pv_done[3], xbar[2][4], fin_s, fin_pv;
+  uint64_t s_full[3], p_full[3], pv_done[3], mh_full[2][4], sums_full, fin_s, fin_pv;
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) int32_t segkv[2][128];
-  float xmax[2][2][128];  // [tile parity][key half][row]: half-row maxima of the two threads of a row
-  float xsum[2][2][128];  // [l, lr][key half][row]: half-row sums for the epilogue
+  float mh[2][128];       // [tile parity][row]: row maximum in use after the tile
+  float sums[2][2][128];  // [group][l, lr][row]: each group's sums at the final maximum
 };
+
+// Mask 32 scores of keys k0 .. k0+31 for query row qidx (segment segq): a
+// score stays only where the key is not after the query (checked when causal
+// is set) and lies in the same segment. The keys' segment ids come from sg,
+// or are all segk when sg is null.
+__device__ __forceinline__ void mask32(uint32_t (&x)[32], const int32_t* sg, int32_t segk, int k0, int qidx,
+                                       int32_t segq, bool causal) {
+  const int4* g4 = reinterpret_cast<const int4*>(sg);
+#pragma unroll
+  for (int e4 = 0; e4 < 8; ++e4) {
+    const int4 gv = sg ? g4[e4] : make_int4(segk, segk, segk, segk);
+    const int32_t gz[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = e4 * 4 + e;
+      x[c] = ((!causal || k0 + c <= qidx) && gz[e] == segq) ? x[c] : __float_as_uint(-INFINITY);
+    }
+  }
+}
+
+__device__ __forceinline__ float max32(const uint32_t (&x)[32]) {
+  float a = __uint_as_float(x[0]), b = __uint_as_float(x[1]);
+#pragma unroll
+  for (int e = 2; e < 30; e += 4) {
+    a = fmax3(a, __uint_as_float(x[e]), __uint_as_float(x[e + 1]));
+    b = fmax3(b, __uint_as_float(x[e + 2]), __uint_as_float(x[e + 3]));
+  }
+  return fmax3(a, b, fmaxf(__uint_as_float(x[30]), __uint_as_float(x[31])));
+}
+
+// P for 32 keys: 2^(s sl2 - moff) packed to bf16 pairs into 16 TMEM columns
+// (not waited); adds the exact weights to ls and the bf16-rounded ones to lr.
+// The scaling and both sums run two keys per instruction (packed FP32).
+__device__ __forceinline__ void exp_store32(const uint32_t (&x)[32], uint64_t sc, uint64_t off, uint32_t taddr,
+                                            uint64_t& ls, uint64_t& lr) {
+  uint64_t s2[2] = {0ull, 0ull}, r2[2] = {0ull, 0ull};
+  uint32_t pk[16];
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    const float2 t = f2_split(fma2(f2(__uint_as_float(x[e]), __uint_as_float(x[e + 1])), sc, off));
+    const float e0 = ex2(t.x), e1 = ex2(t.y);
+    const uint32_t y = pack_bf16x2(e0, e1);
+    s2[(e >> 1) & 1] = add2(s2[(e >> 1) & 1], f2(e0, e1));
+    r2[(e >> 1) & 1] = add2(r2[(e >> 1) & 1], f2(__uint_as_float(y << 16), __uint_as_float(y & 0xFFFF0000u)));
+    pk[e >> 1] = y;
+  }
+  tmem_st16_nowait(taddr, pk);
+  ls = add2(ls, add2(s2[0], s2[1]));
+  lr = add2(lr, add2(r2[0], r2[1]));
+}
 
 template <int D>
 __global__ void __launch_bounds__(352, 1)
@@ -98,11 +153,12 @@ __global__ void __launch_bounds__(352, 1)
     }
     for (int s = 0; s < L::NSB; ++s) {
       mbar_init(&m.s_full[s], 1);
-      mbar_init(&m.p_full[s], 256);
+      mbar_init(&m.p_full[s], 128);  // the softmax group that owns the tile
       mbar_init(&m.pv_done[s], 1);
     }
     for (int s = 0; s < 2; ++s)
-      for (int q = 0; q < 4; ++q) mbar_init(&m.xbar[s][q], 64);  // the two warps of a lane quarter
+      for (int q = 0; q < 4; ++q) mbar_init(&m.mh_full[s][q], 32);  // one warp: 32 rows
+    mbar_init(&m.sums_full, 256);
     mbar_init(&m.fin_s, 1);
     mbar_init(&m.fin_pv, 1);
     fence_mbar_init();
@@ -225,144 +281,141 @@ __global__ void __launch_bounds__(352, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
+    // Group 0 (warps 3..6) takes the even visited tiles, group 1 (warps
+    // 7..10) the odd ones; thread r of a group owns query row r (TMEM lane r).
+    const int grp = (warp - 3) >> 2;
     const int quarter = warp & 3;
-    const int hsel = (warp - 3) >> 2;  // which 64 keys of every tile (and which half of the O row)
     const int r = quarter * 32 + lane;
     const int qidx = tq * kTile + r;
     const size_t row = (size_t)(b * p.Hq + h) * p.N + qidx;
     const int32_t segq = p.seg ? p.seg[(size_t)b * p.N + qidx] : 0;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tO = tmem + lane_base + L::TM_O + hsel * (D / 2);
+    const uint32_t tO = tmem + lane_base + L::TM_O;
     const float sl2 = p.scale_log2;
-    float m_used = -INFINITY, l = 0.f, lr = 0.f;  // l and lr over this thread's half of the keys
+    float m_w = -INFINITY;           // the maximum this group's sums are taken against
+    uint64_t l2 = 0ull, lr2 = 0ull;  // exact and bf16-rounded weight sums, two partial sums each
     bool ok = true;
-    int jj = 0;
+    int jj = 0;  // visited tiles
     int4 te, te_next;  // table entries of this and the next visited key tile
     for (int tk = walk.first(te), tk_next; tk <= tq; tk = tk_next, te = te_next, ++jj) {
       tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
-      const int sb = jj % NSB, xs = jj & 1;
+      if ((jj & 1) != grp) continue;
+      const int sb = jj % NSB;
       const bool masked = !tile_pair_full(tq, walk.qt, tk, te);
-      if (masked && p.seg) {  // segment ids of this key tile arrived with V
-        ok = g.wait(&m.v_full[jj % NSV], (jj / NSV) & 1, 8);
+      if (masked && p.seg && te.x != te.y) {
+        // Per-key segment ids arrive with V. This V stage last held tile
+        // jj - NSV, whose copy may still be landing (S_jj only waited for
+        // PV_{jj-3}): wait for it first, so that the parity wait for tile jj
+        // cannot match the phase of the copy before it.
+        ok = jj < NSV || g.wait(&m.v_full[jj % NSV], ((jj - NSV) / NSV) & 1, 8);
+        ok = ok && g.wait(&m.v_full[jj % NSV], (jj / NSV) & 1, 8);
         if (!__all_sync(~0u, ok)) { ok = false; break; }
       }
       ok = g.wait(&m.s_full[sb], (jj / NSB) & 1, 9);
       if (!__all_sync(~0u, ok)) { ok = false; break; }
       tc_fence_after();
       const uint32_t tS = tmem + lane_base + L::TM_S + sb * 128;
-      uint32_t xa[32], xb[32];  // this thread's 64 scores (keys 64*hsel ..)
-      tmem_ld32x2(tS + 64 * hsel, tS + 64 * hsel + 32, xa, xb);
+      uint32_t x0[32], x1[32], x2[32], x3[32];
+      tmem_ld128(tS, x0, x1, x2, x3);
       if (masked) {
-        const int k0 = tk * kTile + 64 * hsel;
-        const int4* g4 = reinterpret_cast<const int4*>(&m.segkv[jj % NSV][64 * hsel]);
-#pragma unroll
-        for (int e4 = 0; e4 < 16; ++e4) {
-          const int4 gv = p.seg ? g4[e4] : make_int4(0, 0, 0, 0);
-          const int32_t gz[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = e4 * 4 + e;
-            uint32_t& x = c < 32 ? xa[c] : xb[c - 32];
-            x = (k0 + c <= qidx && gz[e] == segq) ? x : __float_as_uint(-INFINITY);
-          }
-        }
+        // per-key segment ids only where the key tile spans several
+        // segments; otherwise the tile's one segment decides for all keys
+        const bool causal = tk == tq;
+        const int32_t* sg = (p.seg && te.x != te.y) ? m.segkv[jj % NSV] : nullptr;
+        const int k0 = tk * kTile;
+        mask32(x0, sg, te.x, k0, qidx, segq, causal);
+        mask32(x1, sg ? sg + 32 : sg, te.x, k0 + 32, qidx, segq, causal);
+        mask32(x2, sg ? sg + 64 : sg, te.x, k0 + 64, qidx, segq, causal);
+        mask32(x3, sg ? sg + 96 : sg, te.x, k0 + 96, qidx, segq, causal);
       }
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(xa[e]));
-        mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(xb[e]));
+      const float ms = fmax3(fmaxf(max32(x0), max32(x1)), max32(x2), max32(x3)) * sl2;
+      // the maximum in use after the previous tile, from the other group
+      float m_prev = -INFINITY;
+      if (jj > 0) {
+        ok = g.wait(&m.mh_full[(jj - 1) & 1][quarter], ((jj - 1) >> 1) & 1, 10);
+        if (!__all_sync(~0u, ok)) { ok = false; break; }
+        m_prev = m.mh[(jj - 1) & 1][r];
       }
-      // exchange the half-row maxima with the other thread of the row
-      const float mloc = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      m.xmax[xs][hsel][r] = mloc;
-      tc_fence_before();  // this thread's S reads are done before the other half overwrites them with P
-      mbar_arrive(&m.xbar[xs][quarter]);
-      ok = g.wait(&m.xbar[xs][quarter], (jj >> 1) & 1, 10);
-      if (!__all_sync(~0u, ok)) { ok = false; break; }
-      tc_fence_after();
-      const float ms = fmaxf(mloc, m.xmax[xs][hsel ^ 1][r]) * sl2;
-      // both threads of a row hold the same ms and m_used, so they take the
-      // same decisions; both warps of a quarter hold the same rows
-      if (__any_sync(~0u, ms > m_used + 8.f)) {
-        const float m_new = fmaxf(m_used, ms);
-        const float alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_new);
-        if (jj > 0) {  // O holds earlier tiles: rescale this half of it once their PV is done
-          ok = g.wait(&m.pv_done[(jj - 1) % NSB], ((jj - 1) / NSB) & 1, 11);
-          if (!__all_sync(~0u, ok)) { ok = false; break; }
-          tc_fence_after();
+      // the lanes of a warp take the rescale branch together
+      const bool rescale = __any_sync(~0u, ms > m_prev + 8.f);
+      const float m_new = rescale ? fmaxf(m_prev, ms) : m_prev;
+      m.mh[jj & 1][r] = m_new;
+      mbar_arrive(&m.mh_full[jj & 1][quarter]);
+      if (m_w != m_new) {  // this group's sums to the new maximum
+        const float a = (m_w == -INFINITY) ? 0.f : ex2(m_w - m_new);
+        l2 = mul2(l2, f2(a, a));
+        lr2 = mul2(lr2, f2(a, a));
+        m_w = m_new;
+      }
+      const float moff = (m_new == -INFINITY) ? 0.f : m_new;
+      const uint64_t sc = f2(sl2, sl2), off = f2(-moff, -moff);
+      // P for keys 32c .. 32c+31 -> packed columns 16c .. 16c+15 of the S
+      // buffer, all of whose scores this thread already holds
+      exp_store32(x0, sc, off, tS, l2, lr2);
+      exp_store32(x1, sc, off, tS + 16, l2, lr2);
+      exp_store32(x2, sc, off, tS + 32, l2, lr2);
+      exp_store32(x3, sc, off, tS + 48, l2, lr2);
+      if (rescale && jj > 0) {  // O holds earlier tiles: rescale it once their PV is done
+        const float alpha = (m_prev == -INFINITY) ? 0.f : ex2(m_prev - m_new);
+        ok = g.wait(&m.pv_done[(jj - 1) % NSB], ((jj - 1) / NSB) & 1, 11);
+        if (!__all_sync(~0u, ok)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll 1
-          for (int c0 = 0; c0 < D / 2; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tO + c0, v);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tO + c0, v);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            tmem_st32(tO + c0, v);
-          }
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+          tmem_st32(tO + c0, v);
         }
-        l *= alpha;
-        lr *= alpha;
-        m_used = m_new;
       }
-      const float moff = (m_used == -INFINITY) ? 0.f : m_used;
-      // l sums the exact fp32 weights (for lse); lr sums the bf16-rounded
-      // weights the PV product uses, so O / lr is a convex combination
-      float ls4[4] = {0.f, 0.f, 0.f, 0.f}, lr4[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pa[16], pb[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const float e0 = ex2(fmaf(__uint_as_float(xa[e]), sl2, -moff));
-        const float e1 = ex2(fmaf(__uint_as_float(xa[e + 1]), sl2, -moff));
-        const float f0 = ex2(fmaf(__uint_as_float(xb[e]), sl2, -moff));
-        const float f1 = ex2(fmaf(__uint_as_float(xb[e + 1]), sl2, -moff));
-        const uint32_t y = pack_bf16x2(e0, e1), z = pack_bf16x2(f0, f1);
-        ls4[(e >> 1) & 3] += (e0 + e1) + (f0 + f1);
-        lr4[(e >> 1) & 3] += (__uint_as_float(y << 16) + __uint_as_float(y & 0xFFFF0000u)) +
-                             (__uint_as_float(z << 16) + __uint_as_float(z & 0xFFFF0000u));
-        pa[e >> 1] = y;
-        pb[e >> 1] = z;
-      }
-      // P for keys 64*hsel .. 64*hsel+63 -> packed columns 32*hsel .. 32*hsel+31
-      // (S columns both threads of the row have read before the exchange)
-      tmem_st16x2(tS + 32 * hsel, tS + 32 * hsel + 16, pa, pb);
-      l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
-      lr += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&m.p_full[sb]);
     }
     // ------------------------------------------------------------ epilogue
+    // The final maximum is the one the last tile's group handed on; both
+    // groups take their sums to it, add them up and write half of O each.
+    float m_fin = -INFINITY;
     if (ok && jj > 0) {
-      ok = g.wait(&m.pv_done[(jj - 1) % NSB], ((jj - 1) / NSB) & 1, 12);
+      ok = g.wait(&m.mh_full[(jj - 1) & 1][quarter], ((jj - 1) >> 1) & 1, 12);
       ok = __all_sync(~0u, ok);
-    }
-    if (ok) {  // add up the two halves' sums
-      m.xsum[0][hsel][r] = l;
-      m.xsum[1][hsel][r] = lr;
-      mbar_arrive(&m.xbar[jj & 1][quarter]);
-      ok = g.wait(&m.xbar[jj & 1][quarter], (jj >> 1) & 1, 13);
-      ok = __all_sync(~0u, ok);
+      if (ok) m_fin = m.mh[(jj - 1) & 1][r];
     }
     if (ok) {
+      const float a = (m_w == m_fin) ? 1.f : (m_w == -INFINITY ? 0.f : ex2(m_w - m_fin));
+      const float2 lp = f2_split(l2), lrp = f2_split(lr2);
+      m.sums[grp][0][r] = (lp.x + lp.y) * a;
+      m.sums[grp][1][r] = (lrp.x + lrp.y) * a;
+      mbar_arrive(&m.sums_full);
+      ok = g.wait(&m.sums_full, 0, 13);
+      ok = __all_sync(~0u, ok);
+    }
+    if (ok && jj > 0) {  // the last PV has accumulated into O
+      ok = g.wait(&m.pv_done[(jj - 1) % NSB], ((jj - 1) / NSB) & 1, 14);
+      ok = __all_sync(~0u, ok);
+    }
+    if (ok && jj > 0) {
       tc_fence_after();
-      // both threads of a row add the halves in the same order
-      const float lt = m.xsum[0][0][r] + m.xsum[0][1][r];
-      const float inv = 1.f / (m.xsum[1][0][r] + m.xsum[1][1][r]);
-      uint4* orow = reinterpret_cast<uint4*>(p.out + row * D + hsel * (D / 2));
+      // both groups add the two groups' sums in the same order
+      const float lt = m.sums[0][0][r] + m.sums[1][0][r];
+      const float inv = 1.f / (m.sums[0][1][r] + m.sums[1][1][r]);
+      uint4* orow = reinterpret_cast<uint4*>(p.out + row * D + grp * (D / 2));
 #pragma unroll 1
       for (int c0 = 0; c0 < D / 2; c0 += 32) {
         uint32_t a[32];
-        tmem_ld32(tO + c0, a);
+        tmem_ld32(tO + grp * (D / 2) + c0, a);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 x;
-          x.x = pack_bf16x2(__uint_as_float(a[q4 * 8 + 0]) * inv, __uint_as_float(a[q4 * 8 + 1]) * inv);
-          x.y = pack_bf16x2(__uint_as_float(a[q4 * 8 + 2]) * inv, __uint_as_float(a[q4 * 8 + 3]) * inv);
-          x.z = pack_bf16x2(__uint_as_float(a[q4 * 8 + 4]) * inv, __uint_as_float(a[q4 * 8 + 5]) * inv);
-          x.w = pack_bf16x2(__uint_as_float(a[q4 * 8 + 6]) * inv, __uint_as_float(a[q4 * 8 + 7]) * inv);
-          orow[(c0 >> 3) + q4] = x;
+          uint4 y;
+          y.x = pack_bf16x2(__uint_as_float(a[q4 * 8 + 0]) * inv, __uint_as_float(a[q4 * 8 + 1]) * inv);
+          y.y = pack_bf16x2(__uint_as_float(a[q4 * 8 + 2]) * inv, __uint_as_float(a[q4 * 8 + 3]) * inv);
+          y.z = pack_bf16x2(__uint_as_float(a[q4 * 8 + 4]) * inv, __uint_as_float(a[q4 * 8 + 5]) * inv);
+          y.w = pack_bf16x2(__uint_as_float(a[q4 * 8 + 6]) * inv, __uint_as_float(a[q4 * 8 + 7]) * inv);
+          orow[(c0 >> 3) + q4] = y;
         }
       }
-      if (hsel == 0) p.lse[row] = m_used * 0.6931471805599453f + logf(lt);
+      if (grp == 0) p.lse[row] = m_fin * 0.6931471805599453f + logf(lt);
     }
   }
   tc_fence_before();

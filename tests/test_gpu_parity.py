@@ -34,6 +34,9 @@ SMALL = [
     ("many_len3_d64", synth.custom(1, 2, 1, 384, 64, [[3] * 128], seed=22)),
     ("len1_runs_d128", synth.custom(1, 2, 2, 256, 128, [[1] * 40 + [88, 128]], seed=23)),
     ("gqa8_d64", synth.custom(1, 8, 1, 640, 64, [[300, 213, 127]], seed=24)),
+    # odd group size and odd tile count: the forward pairs consecutive query
+    # tiles and the last pair has one tile only
+    ("g3_odd_tiles_d64", synth.custom(2, 3, 1, 384, 64, [[200, 184], [384]], seed=27)),
 ]
 
 
