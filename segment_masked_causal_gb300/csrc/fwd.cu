@@ -98,8 +98,10 @@ __device__ __forceinline__ float max32(const uint32_t (&x)[32]) {
 }
 
 // P for 32 keys: 2^(s sl2 - moff) packed to bf16 pairs into 16 TMEM columns
-// (not waited); adds the exact weights to ls and the bf16-rounded ones to lr.
-// The scaling and both sums run two keys per instruction (packed FP32).
+// (not waited); adds the exact weights to ls and, with ROUNDED, the
+// bf16-rounded ones to lr. The scaling and the sums run two keys per
+// instruction (packed FP32).
+template <bool ROUNDED>
 __device__ __forceinline__ void exp_store32(const uint32_t (&x)[32], uint64_t sc, uint64_t off, uint32_t taddr,
                                             uint64_t& ls, uint64_t& lr) {
   uint64_t s2[2] = {0ull, 0ull}, r2[2] = {0ull, 0ull};
@@ -110,12 +112,13 @@ __device__ __forceinline__ void exp_store32(const uint32_t (&x)[32], uint64_t sc
     const float e0 = ex2(t.x), e1 = ex2(t.y);
     const uint32_t y = pack_bf16x2(e0, e1);
     s2[(e >> 1) & 1] = add2(s2[(e >> 1) & 1], f2(e0, e1));
-    r2[(e >> 1) & 1] = add2(r2[(e >> 1) & 1], f2(__uint_as_float(y << 16), __uint_as_float(y & 0xFFFF0000u)));
+    if (ROUNDED)
+      r2[(e >> 1) & 1] = add2(r2[(e >> 1) & 1], f2(__uint_as_float(y << 16), __uint_as_float(y & 0xFFFF0000u)));
     pk[e >> 1] = y;
   }
   tmem_st16_nowait(taddr, pk);
   ls = add2(ls, add2(s2[0], s2[1]));
-  lr = add2(lr, add2(r2[0], r2[1]));
+  if (ROUNDED) lr = add2(lr, add2(r2[0], r2[1]));
 }
 
 template <int D>
@@ -351,10 +354,25 @@ __global__ void __launch_bounds__(352, 1)
       const uint64_t sc = f2(sl2, sl2), off = f2(-moff, -moff);
       // P for keys 32c .. 32c+31 -> packed columns 16c .. 16c+15 of the S
       // buffer, all of whose scores this thread already holds
-      exp_store32(x0, sc, off, tS, l2, lr2);
-      exp_store32(x1, sc, off, tS + 16, l2, lr2);
-      exp_store32(x2, sc, off, tS + 32, l2, lr2);
-      exp_store32(x3, sc, off, tS + 48, l2, lr2);
+      // The normaliser of O sums the bf16-rounded weights the PV product
+      // uses on masked tiles, where a row with few keys has all of them; on
+      // entirely visible tiles it takes the exact weights, whose rounding
+      // errors average out over the 128 keys of the tile.
+      uint64_t t2 = 0ull, tr2 = 0ull;
+      if (masked) {
+        exp_store32<true>(x0, sc, off, tS, t2, tr2);
+        exp_store32<true>(x1, sc, off, tS + 16, t2, tr2);
+        exp_store32<true>(x2, sc, off, tS + 32, t2, tr2);
+        exp_store32<true>(x3, sc, off, tS + 48, t2, tr2);
+      } else {
+        exp_store32<false>(x0, sc, off, tS, t2, tr2);
+        exp_store32<false>(x1, sc, off, tS + 16, t2, tr2);
+        exp_store32<false>(x2, sc, off, tS + 32, t2, tr2);
+        exp_store32<false>(x3, sc, off, tS + 48, t2, tr2);
+        tr2 = t2;
+      }
+      l2 = add2(l2, t2);
+      lr2 = add2(lr2, tr2);
       if (rescale && jj > 0) {  // O holds earlier tiles: rescale it once their PV is done
         const float alpha = (m_prev == -INFINITY) ? 0.f : ex2(m_prev - m_new);
         ok = g.wait(&m.pv_done[(jj - 1) % NSB], ((jj - 1) / NSB) & 1, 11);
