@@ -28,10 +28,11 @@
 // adds them. O is divided by the sum of the bf16-rounded weights the PV
 // product used; lse uses the exact fp32 sum.
 //
-// Warp roles: warp 0 TMA producer (Q once; K through a 3-stage ring, V and
-// the key tile's segment ids through a 2-stage ring), warp 1 S issuer and
-// TMEM owner, warp 2 PV issuer, warps 3..6 softmax group 0 and warps 7..10
-// softmax group 1 (TMEM lane quarter = warp index mod 4).
+// Warp roles: warp 0 TMA producer (Q once; K through a 3-stage ring, V
+// through a 2-stage ring, the key tiles' segment ids through a 4-stage ring
+// of their own), warp 1 S issuer and TMEM owner, warp 2 PV issuer, warps 3..6
+// softmax group 0 and warps 7..10 softmax group 1 (TMEM lane quarter = warp
+// index mod 4).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -61,9 +62,10 @@ struct FwdLayout {
 struct FwdMisc {
   uint64_t q_full, k_full[3], k_empty[3], v_full[2], v_empty[2];
   uint64_t s_full[3], p_full[3], pv_done[3], mh_full[2][4], sums_full, fin_s, fin_pv;
+  uint64_t seg_full[4], seg_empty[4];  // key tiles' segment ids: tile j in stage j mod 4
   uint32_t tmem_base;
   int abort_flag;
-  alignas(16) int32_t segkv[2][128];
+  alignas(16) int32_t segkv[4][128];
   float mh[2][128];       // [tile parity][row]: row maximum in use after the tile
   float sums[2][2][128];  // [group][l, lr][row]: each group's sums at the final maximum
 };
@@ -162,6 +164,10 @@ __global__ void __launch_bounds__(352, 1)
     for (int s = 0; s < 2; ++s)
       for (int q = 0; q < 4; ++q) mbar_init(&m.mh_full[s][q], 32);  // one warp: 32 rows
     mbar_init(&m.sums_full, 256);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&m.seg_full[s], 1);
+      mbar_init(&m.seg_empty[s], 128);  // the softmax group that owns the tile
+    }
     mbar_init(&m.fin_s, 1);
     mbar_init(&m.fin_pv, 1);
     fence_mbar_init();
@@ -178,8 +184,9 @@ __global__ void __launch_bounds__(352, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Lane 0 loads Q and the K ring, lane 1 the V ring (with the key tiles'
-    // segment ids): each ring refills as soon as its own stage is released.
+    // Lane 0 loads Q, then per key tile its segment ids (a 4-stage ring of
+    // their own) and K (a 3-stage ring); lane 1 the V ring: each ring refills
+    // as soon as its own stage is released.
     const int krow0 = (b * p.Hkv + hk) * p.N;
     if (lane == 0) {
       prefetch_tmap(&tmQ);
@@ -187,11 +194,18 @@ __global__ void __launch_bounds__(352, 1)
       const int qrow = (b * p.Hq + h) * p.N + tq * kTile;
       mbar_expect_tx(&m.q_full, L::TB);
       for (int c = 0; c < D / 64; ++c) tma_load_2d(base + L::OFF_Q + c * L::CHUNK, &tmQ, &m.q_full, c * 64, qrow);
-      int jk = 0;
+      int jk = 0, js = 0;  // K copies and segment-id copies issued
       int4 te, te_next;  // table entries of this and the next visited key tile
       for (int tk = walk.first(te), tk_next; tk <= tq; tk = tk_next, te = te_next, ++jk) {
         tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
         const int sk = jk % NSK;
+        if (p.seg) {  // the tile's segment ids, into stage jk mod 4 of their own ring
+          const int ss = jk & 3;
+          if (!g.wait(&m.seg_empty[ss], ((jk >> 2) & 1) ^ 1, 15)) break;
+          mbar_expect_tx(&m.seg_full[ss], 512);
+          bulk_load(m.segkv[ss], p.seg + (size_t)b * p.N + tk * kTile, 512, &m.seg_full[ss]);
+          ++js;
+        }
         if (!g.wait(&m.k_empty[sk], ((jk / NSK) & 1) ^ 1, 1)) break;
         mbar_expect_tx(&m.k_full[sk], L::TB);
         for (int c = 0; c < D / 64; ++c)
@@ -200,6 +214,7 @@ __global__ void __launch_bounds__(352, 1)
       // no copy may still be landing when the CTA exits
       g.drain(&m.q_full, 0);
       for (int i = (jk > NSK ? jk - NSK : 0); i < jk; ++i) g.drain(&m.k_full[i % NSK], (i / NSK) & 1);
+      for (int i = (js > 4 ? js - 4 : 0); i < js; ++i) g.drain(&m.seg_full[i & 3], (i >> 2) & 1);
     } else if (lane == 1) {
       prefetch_tmap(&tmV);
       int jv = 0;
@@ -208,10 +223,9 @@ __global__ void __launch_bounds__(352, 1)
         tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
         const int sv = jv % NSV;
         if (!g.wait(&m.v_empty[sv], ((jv / NSV) & 1) ^ 1, 2)) break;
-        mbar_expect_tx(&m.v_full[sv], L::TB + (p.seg ? 512 : 0));
+        mbar_expect_tx(&m.v_full[sv], L::TB);
         for (int c = 0; c < D / 64; ++c)
           tma_load_2d(base + L::OFF_V + sv * L::TB + c * L::CHUNK, &tmV, &m.v_full[sv], c * 64, krow0 + tk * kTile);
-        if (p.seg) bulk_load(m.segkv[sv], p.seg + (size_t)b * p.N + tk * kTile, 512, &m.v_full[sv]);
       }
       for (int i = (jv > NSV ? jv - NSV : 0); i < jv; ++i) g.drain(&m.v_full[i % NSV], (i / NSV) & 1);
     }
@@ -305,32 +319,31 @@ __global__ void __launch_bounds__(352, 1)
       if ((jj & 1) != grp) continue;
       const int sb = jj % NSB;
       const bool masked = !tile_pair_full(tq, walk.qt, tk, te);
-      if (masked && p.seg && te.x != te.y) {
-        // Per-key segment ids arrive with V. This V stage last held tile
-        // jj - NSV, whose copy may still be landing (S_jj only waited for
-        // PV_{jj-3}): wait for it first, so that the parity wait for tile jj
-        // cannot match the phase of the copy before it.
-        ok = jj < NSV || g.wait(&m.v_full[jj % NSV], ((jj - NSV) / NSV) & 1, 8);
-        ok = ok && g.wait(&m.v_full[jj % NSV], (jj / NSV) & 1, 8);
-        if (!__all_sync(~0u, ok)) { ok = false; break; }
-      }
       ok = g.wait(&m.s_full[sb], (jj / NSB) & 1, 9);
       if (!__all_sync(~0u, ok)) { ok = false; break; }
       tc_fence_after();
       const uint32_t tS = tmem + lane_base + L::TM_S + sb * 128;
       uint32_t x0[32], x1[32], x2[32], x3[32];
       tmem_ld128(tS, x0, x1, x2, x3);
+      if (p.seg) {
+        // the tile's segment ids: stage jj mod 4 belongs to this group, which
+        // waits every phase of it in turn (used only on masked tiles that
+        // span several segments; released once the mask is applied)
+        ok = g.wait(&m.seg_full[jj & 3], (jj >> 2) & 1, 8);
+        if (!__all_sync(~0u, ok)) { ok = false; break; }
+      }
       if (masked) {
         // per-key segment ids only where the key tile spans several
         // segments; otherwise the tile's one segment decides for all keys
         const bool causal = tk == tq;
-        const int32_t* sg = (p.seg && te.x != te.y) ? m.segkv[jj % NSV] : nullptr;
+        const int32_t* sg = (p.seg && te.x != te.y) ? m.segkv[jj & 3] : nullptr;
         const int k0 = tk * kTile;
         mask32(x0, sg, te.x, k0, qidx, segq, causal);
         mask32(x1, sg ? sg + 32 : sg, te.x, k0 + 32, qidx, segq, causal);
         mask32(x2, sg ? sg + 64 : sg, te.x, k0 + 64, qidx, segq, causal);
         mask32(x3, sg ? sg + 96 : sg, te.x, k0 + 96, qidx, segq, causal);
       }
+      if (p.seg) mbar_arrive(&m.seg_empty[jj & 3]);
       const float ms = fmax3(fmaxf(max32(x0), max32(x1)), max32(x2), max32(x3)) * sl2;
       // the maximum in use after the previous tile, from the other group
       float m_prev = -INFINITY;
