@@ -29,8 +29,9 @@
 // product used; lse uses the exact fp32 sum.
 //
 // Warp roles: warp 0 TMA producer (Q once; K through a 3-stage ring, V
-// through a 2-stage ring, the key tiles' segment ids through a 4-stage ring
-// of their own), warp 1 S issuer and TMEM owner, warp 2 PV issuer, warps 3..6
+// through a 2-stage ring, the per-key segment ids of key tiles that span
+// several segments through a ring of their own), warp 1 S issuer and TMEM
+// owner, warp 2 PV issuer, warps 3..6
 // softmax group 0 and warps 7..10 softmax group 1 (TMEM lane quarter = warp
 // index mod 4).
 #include <cuda_runtime.h>
@@ -62,7 +63,8 @@ struct FwdLayout {
 struct FwdMisc {
   uint64_t q_full, k_full[3], k_empty[3], v_full[2], v_empty[2];
   uint64_t s_full[3], p_full[3], pv_done[3], mh_full[2][4], sums_full, fin_s, fin_pv;
-  uint64_t seg_full[4], seg_empty[4];  // key tiles' segment ids: tile j in stage j mod 4
+  uint64_t seg_full[4], seg_empty[4];  // per-key segment ids of the tiles that need them (see seg_stage)
+  uint64_t o_staged;                   // O rows written to shared memory by all softmax threads
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) int32_t segkv[4][128];
@@ -123,10 +125,18 @@ __device__ __forceinline__ void exp_store32(const uint32_t (&x)[32], uint64_t sc
   if (ROUNDED) lr = add2(lr, add2(r2[0], r2[1]));
 }
 
+// Per-key segment ids travel only for key tiles that span several segments.
+// The n-th such tile of softmax group g (the group owning visited tile j is
+// j mod 2) uses stage g + 2 (n mod 2), phase n / 2: each group owns two
+// stages and waits every phase of them in order.
+__device__ __forceinline__ bool needs_ids(const AttnParams& p, int4 te) { return p.seg && te.x != te.y; }
+__device__ __forceinline__ int seg_stage(int g, int n) { return g + 2 * (n & 1); }
+
 template <int D>
 __global__ void __launch_bounds__(352, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-               const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+               const AttnParams p) {
   using L = FwdLayout<D>;
   constexpr int NSK = L::NSK, NSV = L::NSV, NSB = L::NSB;
   static_assert(sizeof(FwdMisc) <= L::MISC_BYTES, "misc region");
@@ -164,6 +174,7 @@ __global__ void __launch_bounds__(352, 1)
     for (int s = 0; s < 2; ++s)
       for (int q = 0; q < 4; ++q) mbar_init(&m.mh_full[s][q], 32);  // one warp: 32 rows
     mbar_init(&m.sums_full, 256);
+    mbar_init(&m.o_staged, 256);
     for (int s = 0; s < 4; ++s) {
       mbar_init(&m.seg_full[s], 1);
       mbar_init(&m.seg_empty[s], 128);  // the softmax group that owns the tile
@@ -184,9 +195,9 @@ __global__ void __launch_bounds__(352, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Lane 0 loads Q, then per key tile its segment ids (a 4-stage ring of
-    // their own) and K (a 3-stage ring); lane 1 the V ring: each ring refills
-    // as soon as its own stage is released.
+    // Lane 0 loads Q, then per key tile its per-key segment ids where the
+    // tile needs them (a ring of their own) and K (a 3-stage ring); lane 1
+    // the V ring: each ring refills as soon as its own stage is released.
     const int krow0 = (b * p.Hkv + hk) * p.N;
     if (lane == 0) {
       prefetch_tmap(&tmQ);
@@ -194,17 +205,18 @@ __global__ void __launch_bounds__(352, 1)
       const int qrow = (b * p.Hq + h) * p.N + tq * kTile;
       mbar_expect_tx(&m.q_full, L::TB);
       for (int c = 0; c < D / 64; ++c) tma_load_2d(base + L::OFF_Q + c * L::CHUNK, &tmQ, &m.q_full, c * 64, qrow);
-      int jk = 0, js = 0;  // K copies and segment-id copies issued
+      int jk = 0;
+      int ns[2] = {0, 0};  // segment-id copies issued for each softmax group's tiles
       int4 te, te_next;  // table entries of this and the next visited key tile
       for (int tk = walk.first(te), tk_next; tk <= tq; tk = tk_next, te = te_next, ++jk) {
         tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
         const int sk = jk % NSK;
-        if (p.seg) {  // the tile's segment ids, into stage jk mod 4 of their own ring
-          const int ss = jk & 3;
-          if (!g.wait(&m.seg_empty[ss], ((jk >> 2) & 1) ^ 1, 15)) break;
+        if (needs_ids(p, te)) {  // the tile's per-key segment ids, ahead of its K
+          const int grp = jk & 1, n = ns[grp], ss = seg_stage(grp, n);
+          if (!g.wait(&m.seg_empty[ss], ((n >> 1) & 1) ^ 1, 15)) break;
           mbar_expect_tx(&m.seg_full[ss], 512);
           bulk_load(m.segkv[ss], p.seg + (size_t)b * p.N + tk * kTile, 512, &m.seg_full[ss]);
-          ++js;
+          ++ns[grp];
         }
         if (!g.wait(&m.k_empty[sk], ((jk / NSK) & 1) ^ 1, 1)) break;
         mbar_expect_tx(&m.k_full[sk], L::TB);
@@ -214,7 +226,8 @@ __global__ void __launch_bounds__(352, 1)
       // no copy may still be landing when the CTA exits
       g.drain(&m.q_full, 0);
       for (int i = (jk > NSK ? jk - NSK : 0); i < jk; ++i) g.drain(&m.k_full[i % NSK], (i / NSK) & 1);
-      for (int i = (js > 4 ? js - 4 : 0); i < js; ++i) g.drain(&m.seg_full[i & 3], (i >> 2) & 1);
+      for (int grp = 0; grp < 2; ++grp)  // at most one copy per stage can be in flight: its last
+        for (int n = (ns[grp] > 2 ? ns[grp] - 2 : 0); n < ns[grp]; ++n) g.drain(&m.seg_full[seg_stage(grp, n)], (n >> 1) & 1);
     } else if (lane == 1) {
       prefetch_tmap(&tmV);
       int jv = 0;
@@ -312,7 +325,8 @@ __global__ void __launch_bounds__(352, 1)
     float m_w = -INFINITY;           // the maximum this group's sums are taken against
     uint64_t l2 = 0ull, lr2 = 0ull;  // exact and bf16-rounded weight sums, two partial sums each
     bool ok = true;
-    int jj = 0;  // visited tiles
+    int jj = 0;     // visited tiles
+    int n_ids = 0;  // this group's tiles that needed per-key segment ids
     int4 te, te_next;  // table entries of this and the next visited key tile
     for (int tk = walk.first(te), tk_next; tk <= tq; tk = tk_next, te = te_next, ++jj) {
       tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
@@ -325,25 +339,27 @@ __global__ void __launch_bounds__(352, 1)
       const uint32_t tS = tmem + lane_base + L::TM_S + sb * 128;
       uint32_t x0[32], x1[32], x2[32], x3[32];
       tmem_ld128(tS, x0, x1, x2, x3);
-      if (p.seg) {
-        // the tile's segment ids: stage jj mod 4 belongs to this group, which
-        // waits every phase of it in turn (used only on masked tiles that
-        // span several segments; released once the mask is applied)
-        ok = g.wait(&m.seg_full[jj & 3], (jj >> 2) & 1, 8);
+      const bool ids = needs_ids(p, te);  // then the tile is masked too
+      const int ss = seg_stage(grp, n_ids);
+      if (ids) {  // per-key segment ids, released once the mask is applied
+        ok = g.wait(&m.seg_full[ss], (n_ids >> 1) & 1, 8);
         if (!__all_sync(~0u, ok)) { ok = false; break; }
       }
       if (masked) {
         // per-key segment ids only where the key tile spans several
         // segments; otherwise the tile's one segment decides for all keys
         const bool causal = tk == tq;
-        const int32_t* sg = (p.seg && te.x != te.y) ? m.segkv[jj & 3] : nullptr;
+        const int32_t* sg = ids ? m.segkv[ss] : nullptr;
         const int k0 = tk * kTile;
         mask32(x0, sg, te.x, k0, qidx, segq, causal);
         mask32(x1, sg ? sg + 32 : sg, te.x, k0 + 32, qidx, segq, causal);
         mask32(x2, sg ? sg + 64 : sg, te.x, k0 + 64, qidx, segq, causal);
         mask32(x3, sg ? sg + 96 : sg, te.x, k0 + 96, qidx, segq, causal);
       }
-      if (p.seg) mbar_arrive(&m.seg_empty[jj & 3]);
+      if (ids) {
+        mbar_arrive(&m.seg_empty[ss]);
+        ++n_ids;
+      }
       const float ms = fmax3(fmaxf(max32(x0), max32(x1)), max32(x2), max32(x3)) * sl2;
       // the maximum in use after the previous tile, from the other group
       float m_prev = -INFINITY;
@@ -431,20 +447,33 @@ __global__ void __launch_bounds__(352, 1)
       // both groups add the two groups' sums in the same order
       const float lt = m.sums[0][0][r] + m.sums[1][0][r];
       const float inv = 1.f / (m.sums[0][1][r] + m.sums[1][1][r]);
-      uint4* orow = reinterpret_cast<uint4*>(p.out + row * D + grp * (D / 2));
+      // This group's half of the O row goes into the Q tile's shared memory
+      // (free: every S product has completed), in the 128-byte-swizzled layout
+      // a TMA store reads; one thread then stores the whole tile, so the
+      // writes to global memory are whole 128-byte rows.
+      uint8_t* so = base + L::OFF_Q;
 #pragma unroll 1
-      for (int c0 = 0; c0 < D / 2; c0 += 32) {
+      for (int c0 = grp * (D / 2); c0 < (grp + 1) * (D / 2); c0 += 32) {
         uint32_t a[32];
-        tmem_ld32(tO + grp * (D / 2) + c0, a);
+        tmem_ld32(tO + c0, a);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 y;
-          y.x = pack_bf16x2(__uint_as_float(a[q4 * 8 + 0]) * inv, __uint_as_float(a[q4 * 8 + 1]) * inv);
-          y.y = pack_bf16x2(__uint_as_float(a[q4 * 8 + 2]) * inv, __uint_as_float(a[q4 * 8 + 3]) * inv);
-          y.z = pack_bf16x2(__uint_as_float(a[q4 * 8 + 4]) * inv, __uint_as_float(a[q4 * 8 + 5]) * inv);
-          y.w = pack_bf16x2(__uint_as_float(a[q4 * 8 + 6]) * inv, __uint_as_float(a[q4 * 8 + 7]) * inv);
-          orow[(c0 >> 3) + q4] = y;
+          const int col = c0 + 8 * q4;  // first of the 8 columns in this 16-byte unit
+          const uint32_t off = (col >> 6) * L::CHUNK + r * 128 + ((((col & 63) >> 3) ^ (r & 7)) << 4);
+          st_shared_v4(smem_u32(so + off),
+                       pack_bf16x2(__uint_as_float(a[q4 * 8 + 0]) * inv, __uint_as_float(a[q4 * 8 + 1]) * inv),
+                       pack_bf16x2(__uint_as_float(a[q4 * 8 + 2]) * inv, __uint_as_float(a[q4 * 8 + 3]) * inv),
+                       pack_bf16x2(__uint_as_float(a[q4 * 8 + 4]) * inv, __uint_as_float(a[q4 * 8 + 5]) * inv),
+                       pack_bf16x2(__uint_as_float(a[q4 * 8 + 6]) * inv, __uint_as_float(a[q4 * 8 + 7]) * inv));
         }
+      }
+      fence_async_smem();  // these writes are read by the TMA store
+      mbar_arrive(&m.o_staged);
+      if (warp == 3 && lane == 0 && g.wait(&m.o_staged, 0, 15)) {
+        const int qrow = (b * p.Hq + h) * p.N + tq * kTile;
+        for (int c = 0; c < D / 64; ++c) tma_store_2d(&tmO, so + c * L::CHUNK, c * 64, qrow);
+        bulk_commit();
+        bulk_wait_all();  // the store has read shared memory (and completed) before the CTA exits
       }
       if (grp == 0) p.lse[row] = m_fin * 0.6931471805599453f + logf(lt);
     }
@@ -460,15 +489,15 @@ __global__ void __launch_bounds__(352, 1)
 template <int D>
 cudaError_t launch_fwd_d(const AttnParams& p, const void* q, const void* k, const void* v, cudaStream_t st) {
   using L = FwdLayout<D>;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const uint64_t qrows = (uint64_t)p.B * p.Hq * p.N, krows = (uint64_t)p.B * p.Hkv * p.N;
   if (!tmap_bf16_2d_sw128(&tq, q, D, qrows, 128) || !tmap_bf16_2d_sw128(&tk, k, D, krows, 128) ||
-      !tmap_bf16_2d_sw128(&tv, v, D, krows, 128))
+      !tmap_bf16_2d_sw128(&tv, v, D, krows, 128) || !tmap_bf16_2d_sw128(&to, p.out, D, qrows, 128))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.T * p.Hq * p.B);
-  fwd_kernel<D><<<grid, 352, L::SMEM, st>>>(tq, tk, tv, p);
+  fwd_kernel<D><<<grid, 352, L::SMEM, st>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 

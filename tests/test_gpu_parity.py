@@ -61,6 +61,17 @@ def test_non_contiguous_ids_full_parity(cuda_dev):
     print(assert_full_parity(c.run(), c.oracle_full(), "noncontig"))
 
 
+def test_skipped_key_tiles_full_parity(cuda_dev):
+    """Ids alternate between two values in blocks, so a query tile's walk
+    skips every other key tile: row 0 in tile-aligned blocks of 128 (skipped
+    tiles only), row 1 in blocks of 96 (skips plus tiles that span two ids)."""
+    w = synth.custom(2, 4, 2, 1024, 128, [[1024], [1024]], seed=28)
+    w.seg[0] = np.array([(i // 128) % 2 for i in range(1024)], np.int32)
+    w.seg[1] = np.array([7 + (i // 96) % 2 for i in range(1024)], np.int32)
+    c = Case(w, cuda_dev)
+    print(assert_full_parity(c.run(), c.oracle_full(), "skipped"))
+
+
 def test_causal_2k_gqa(cuda_dev):
     w = synth.workload("causal_2k_gqa")
     c = Case(w, cuda_dev)
