@@ -54,6 +54,7 @@ struct DqLayout {
 struct DqMisc {
   uint64_t q_full, k_full[3], k_empty[3], v_full[2], v_empty[2];
   uint64_t s_full, s_free, ds_full[2], dq_done[2], mma_final[2];
+  uint64_t o_staged;  // dQ rows written to shared memory by all softmax threads
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) int32_t segkv[3][128];
@@ -63,7 +64,7 @@ template <int D>
 __global__ void __launch_bounds__(352, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-              const AttnParams p) {
+              const __grid_constant__ CUtensorMap tmDQ, const AttnParams p) {
   using L = DqLayout<D>;
   constexpr int NSK = L::NSK, NSV = L::NSV;
   static_assert(sizeof(DqMisc) <= L::MISC_BYTES, "misc region");
@@ -102,6 +103,7 @@ __global__ void __launch_bounds__(352, 1)
     }
     mbar_init(&m.mma_final[0], 1);
     mbar_init(&m.mma_final[1], 1);
+    mbar_init(&m.o_staged, 256);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -312,7 +314,11 @@ __global__ void __launch_bounds__(352, 1)
     }
     if (ok && j > 0) {
       tc_fence_after();
-      uint4* drow = reinterpret_cast<uint4*>(p.dq + row * D);
+      // This thread's half of the dQ row goes into the Q tile's shared memory
+      // (free: every MMA has completed), in the 128-byte-swizzled layout a TMA
+      // store reads; one thread then stores the whole tile, so the writes to
+      // global memory are whole 128-byte rows.
+      uint8_t* so = base + L::OFF_Q;
       const float sc = p.scale;
 #pragma unroll
       for (int c0 = hsel * (D / 2); c0 < (hsel + 1) * (D / 2); c0 += 32) {
@@ -320,13 +326,22 @@ __global__ void __launch_bounds__(352, 1)
         tmem_ld32(tmem + lane_base + L::TM_DQ + c0, v);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(v[q4 * 8 + 0]) * sc, __uint_as_float(v[q4 * 8 + 1]) * sc);
-          w.y = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2]) * sc, __uint_as_float(v[q4 * 8 + 3]) * sc);
-          w.z = pack_bf16x2(__uint_as_float(v[q4 * 8 + 4]) * sc, __uint_as_float(v[q4 * 8 + 5]) * sc);
-          w.w = pack_bf16x2(__uint_as_float(v[q4 * 8 + 6]) * sc, __uint_as_float(v[q4 * 8 + 7]) * sc);
-          drow[(c0 >> 3) + q4] = w;
+          const int col = c0 + 8 * q4;  // first of the 8 columns in this 16-byte unit
+          const uint32_t off = (col >> 6) * L::CHUNK + r * 128 + ((((col & 63) >> 3) ^ (r & 7)) << 4);
+          st_shared_v4(smem_u32(so + off),
+                       pack_bf16x2(__uint_as_float(v[q4 * 8 + 0]) * sc, __uint_as_float(v[q4 * 8 + 1]) * sc),
+                       pack_bf16x2(__uint_as_float(v[q4 * 8 + 2]) * sc, __uint_as_float(v[q4 * 8 + 3]) * sc),
+                       pack_bf16x2(__uint_as_float(v[q4 * 8 + 4]) * sc, __uint_as_float(v[q4 * 8 + 5]) * sc),
+                       pack_bf16x2(__uint_as_float(v[q4 * 8 + 6]) * sc, __uint_as_float(v[q4 * 8 + 7]) * sc));
         }
+      }
+      fence_async_smem();  // these writes are read by the TMA store
+      mbar_arrive(&m.o_staged);
+      if (warp == 3 && lane == 0 && g.wait(&m.o_staged, 0, 12)) {
+        const int qrow = (b * p.Hq + h) * p.N + tq * kTile;
+        for (int c = 0; c < D / 64; ++c) tma_store_2d(&tmDQ, so + c * L::CHUNK, c * 64, qrow);
+        bulk_commit();
+        bulk_wait_all();  // the store has read shared memory (and completed) before the CTA exits
       }
     }
   }
@@ -342,15 +357,16 @@ template <int D>
 cudaError_t launch_dq_d(const AttnParams& p, const void* q, const void* k, const void* v, const void* dout,
                         cudaStream_t st) {
   using L = DqLayout<D>;
-  CUtensorMap tq, tdo, tk, tv;
+  CUtensorMap tq, tdo, tk, tv, tdq;
   const uint64_t qrows = (uint64_t)p.B * p.Hq * p.N, krows = (uint64_t)p.B * p.Hkv * p.N;
   if (!tmap_bf16_2d_sw128(&tq, q, D, qrows, 128) || !tmap_bf16_2d_sw128(&tdo, dout, D, qrows, 128) ||
-      !tmap_bf16_2d_sw128(&tk, k, D, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, D, krows, 128))
+      !tmap_bf16_2d_sw128(&tk, k, D, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, D, krows, 128) ||
+      !tmap_bf16_2d_sw128(&tdq, p.dq, D, qrows, 128))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.T * p.Hq * p.B);
-  dq_kernel<D><<<grid, 352, L::SMEM, st>>>(tq, tdo, tk, tv, p);
+  dq_kernel<D><<<grid, 352, L::SMEM, st>>>(tq, tdo, tk, tv, tdq, p);
   return cudaGetLastError();
 }
 
