@@ -52,6 +52,7 @@ struct DkvMisc {
   uint64_t do_full[kDoStages], do_empty[kDoStages];
   uint64_t s_full[2], dp_full[2], p_full[2], dp_free[2], ds_full[2], grad_done[2];
   uint64_t final_sd, final_grad;
+  uint64_t o_staged;  // dK and dV rows written to shared memory by all softmax threads
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) float lse[kQStages][128];
@@ -79,6 +80,7 @@ template <int D>
 __global__ void __launch_bounds__(kDkvThreads, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                const AttnParams p) {
   using L = DkvLayout<D>;
   static_assert(L::SMEM <= 232448, "shared memory");
@@ -125,6 +127,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
     }
     mbar_init(&m.final_sd, 1);
     mbar_init(&m.final_grad, 1);
+    mbar_init(&m.o_staged, 256);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -395,9 +398,12 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
     }
     if (ok && i > 0) {
       tc_fence_after();
-      const size_t row = (size_t)(b * p.Hkv + hk) * p.N + kvidx;
-      uint4* vrow = reinterpret_cast<uint4*>(p.dv + row * D);
-      uint4* krow = reinterpret_cast<uint4*>(p.dk + row * D);
+      // This thread's halves of the dV and dK rows go into the V and K tiles'
+      // shared memory (free: every MMA has completed), in the
+      // 128-byte-swizzled layout a TMA store reads; one thread then stores
+      // both tiles, so the writes to global memory are whole 128-byte rows.
+      uint8_t* sv = base + L::OFF_V;
+      uint8_t* sk = base + L::OFF_K;
       const float sc = p.scale;
 #pragma unroll
       for (int c0 = hsel * (D / 2); c0 < (hsel + 1) * (D / 2); c0 += 32) {
@@ -405,18 +411,29 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
         tmem_ld32x2(tmem + lane_base + L::TM_DV + c0, tmem + lane_base + L::TM_DK + c0, v, k);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 wv, wk;
-          wv.x = pack_bf16x2(__uint_as_float(v[q4 * 8 + 0]), __uint_as_float(v[q4 * 8 + 1]));
-          wv.y = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2]), __uint_as_float(v[q4 * 8 + 3]));
-          wv.z = pack_bf16x2(__uint_as_float(v[q4 * 8 + 4]), __uint_as_float(v[q4 * 8 + 5]));
-          wv.w = pack_bf16x2(__uint_as_float(v[q4 * 8 + 6]), __uint_as_float(v[q4 * 8 + 7]));
-          wk.x = pack_bf16x2(__uint_as_float(k[q4 * 8 + 0]) * sc, __uint_as_float(k[q4 * 8 + 1]) * sc);
-          wk.y = pack_bf16x2(__uint_as_float(k[q4 * 8 + 2]) * sc, __uint_as_float(k[q4 * 8 + 3]) * sc);
-          wk.z = pack_bf16x2(__uint_as_float(k[q4 * 8 + 4]) * sc, __uint_as_float(k[q4 * 8 + 5]) * sc);
-          wk.w = pack_bf16x2(__uint_as_float(k[q4 * 8 + 6]) * sc, __uint_as_float(k[q4 * 8 + 7]) * sc);
-          vrow[(c0 >> 3) + q4] = wv;
-          krow[(c0 >> 3) + q4] = wk;
+          const int col = c0 + 8 * q4;  // first of the 8 columns in this 16-byte unit
+          const uint32_t off = (col >> 6) * L::CHUNK + r * 128 + ((((col & 63) >> 3) ^ (r & 7)) << 4);
+          st_shared_v4(smem_u32(sv + off), pack_bf16x2(__uint_as_float(v[q4 * 8 + 0]), __uint_as_float(v[q4 * 8 + 1])),
+                       pack_bf16x2(__uint_as_float(v[q4 * 8 + 2]), __uint_as_float(v[q4 * 8 + 3])),
+                       pack_bf16x2(__uint_as_float(v[q4 * 8 + 4]), __uint_as_float(v[q4 * 8 + 5])),
+                       pack_bf16x2(__uint_as_float(v[q4 * 8 + 6]), __uint_as_float(v[q4 * 8 + 7])));
+          st_shared_v4(smem_u32(sk + off),
+                       pack_bf16x2(__uint_as_float(k[q4 * 8 + 0]) * sc, __uint_as_float(k[q4 * 8 + 1]) * sc),
+                       pack_bf16x2(__uint_as_float(k[q4 * 8 + 2]) * sc, __uint_as_float(k[q4 * 8 + 3]) * sc),
+                       pack_bf16x2(__uint_as_float(k[q4 * 8 + 4]) * sc, __uint_as_float(k[q4 * 8 + 5]) * sc),
+                       pack_bf16x2(__uint_as_float(k[q4 * 8 + 6]) * sc, __uint_as_float(k[q4 * 8 + 7]) * sc));
         }
+      }
+      fence_async_smem();  // these writes are read by the TMA stores
+      mbar_arrive(&m.o_staged);
+      if (warp == 3 && lane == 0 && g.wait(&m.o_staged, 0, 17)) {
+        const int krow = (b * p.Hkv + hk) * p.N + tk * kTile;
+        for (int c = 0; c < D / 64; ++c) {
+          tma_store_2d(&tmDV, sv + c * L::CHUNK, c * 64, krow);
+          tma_store_2d(&tmDK, sk + c * L::CHUNK, c * 64, krow);
+        }
+        bulk_commit();
+        bulk_wait_all();  // the stores have read shared memory (and completed) before the CTA exits
       }
     }
   }
@@ -432,15 +449,16 @@ template <int D>
 cudaError_t launch_dkv_d(const AttnParams& p, const void* q, const void* k, const void* v, const void* dout,
                          cudaStream_t st) {
   using L = DkvLayout<D>;
-  CUtensorMap tq, tdo, tk, tv;
+  CUtensorMap tq, tdo, tk, tv, tdk, tdv;
   const uint64_t qrows = (uint64_t)p.B * p.Hq * p.N, krows = (uint64_t)p.B * p.Hkv * p.N;
   if (!tmap_bf16_2d_sw128(&tq, q, D, qrows, 128) || !tmap_bf16_2d_sw128(&tdo, dout, D, qrows, 128) ||
-      !tmap_bf16_2d_sw128(&tk, k, D, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, D, krows, 128))
+      !tmap_bf16_2d_sw128(&tk, k, D, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, D, krows, 128) ||
+      !tmap_bf16_2d_sw128(&tdk, p.dk, D, krows, 128) || !tmap_bf16_2d_sw128(&tdv, p.dv, D, krows, 128))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(dkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.T * p.Hkv * p.B);
-  dkv_kernel<D><<<grid, kDkvThreads, L::SMEM, st>>>(tq, tdo, tk, tv, p);
+  dkv_kernel<D><<<grid, kDkvThreads, L::SMEM, st>>>(tq, tdo, tk, tv, tdk, tdv, p);
   return cudaGetLastError();
 }
 
