@@ -8,16 +8,17 @@
 // (mlx-train-perf 0.5.1 README, "Flash-attention training path").
 //
 // Per visited key tile j: S_j = Q K_j^T (128 x 128, Q and K in shared memory)
-// into one of three TMEM S buffers, P_j = 2^(S_j log2e scale - m) written back
-// as bf16 over S_j, and O += P_j V_j with P_j fed straight from TMEM into one
-// O accumulator. With three S buffers, S_{j+3} waits only for PV_j, which
-// finishes while the softmax is still on later tiles. The softmax runs in two
-// warpgroups, one thread per query row holding the row's 128 scores: group 0
-// takes the even visited tiles and group 1 the odd ones, so two tiles'
-// exponentials are in flight at once. The only step that passes from tile to
-// tile is the row maximum in use, which each group hands to the other through
-// shared memory as soon as it has its tile's maximum. One warp issues the S
-// products, another the PV products, each waiting only on its own
+// into TMEM S buffer j mod 2, P_j = 2^(S_j log2e scale - m) as bf16 into P
+// buffer j mod 2, and O += P_j V_j with P_j fed straight from TMEM into one O
+// accumulator. The softmax runs in two warpgroups, one thread per query row
+// holding the row's 128 scores: group 0 takes the even visited tiles and
+// group 1 the odd ones, so two tiles' exponentials are in flight at once, and
+// each group owns the S and P buffer of its tiles. A group releases its S
+// buffer as soon as it has loaded the scores, so S_{j+2} runs while P_j is
+// being formed; P_{j+2} waits only for PV_j. The only step that passes from
+// tile to tile is the row maximum in use, which each group hands to the other
+// through shared memory as soon as it has its tile's maximum. One warp issues
+// the S products, another the PV products, each waiting only on its own
 // dependencies.
 //
 // Online softmax works in log2 units of the scaled score and rescales O only
@@ -47,7 +48,7 @@ namespace {
 
 template <int D>
 struct FwdLayout {
-  static constexpr int NSK = 3, NSV = 2, NSB = 3;  // K stages, V stages, TMEM S buffers
+  static constexpr int NSK = 3, NSV = 2;  // K stages, V stages
   static constexpr uint32_t TB = 128 * D * 2;   // one 128-row tile of Q, K or V
   static constexpr uint32_t CHUNK = 128 * 128;  // one 64-column chunk of a 128-row tile
   static constexpr uint32_t OFF_Q = 0;
@@ -56,13 +57,15 @@ struct FwdLayout {
   static constexpr uint32_t TILE_BYTES = OFF_V + NSV * TB;
   static constexpr uint32_t MISC_BYTES = 8192;
   static constexpr uint32_t SMEM = TILE_BYTES + MISC_BYTES + 1024;
-  // TMEM: O (D columns) at 0, S buffers of 128 columns at 128, 256, 384
-  static constexpr uint32_t TM_O = 0, TM_S = 128, TMEM_COLS = 512;
+  // TMEM: O (D columns) at 0; S buffers of 128 columns at 128 and 256; P
+  // buffers of 64 columns (bf16 pairs) at 384 and 448. Tile j uses S and P
+  // buffer j mod 2, the buffers of the softmax group that owns it.
+  static constexpr uint32_t TM_O = 0, TM_S = 128, TM_P = 384, TMEM_COLS = 512;
 };
 
 struct FwdMisc {
   uint64_t q_full, k_full[3], k_empty[3], v_full[2], v_empty[2];
-  uint64_t s_full[3], p_full[3], pv_done[3], mh_full[2][4], sums_full, fin_s, fin_pv;
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], mh_full[2][4], sums_full, fin_s, fin_pv;
   uint64_t seg_full[4], seg_empty[4];  // per-key segment ids of the tiles that need them (see seg_stage)
   uint64_t o_staged;                   // O rows written to shared memory by all softmax threads
   uint32_t tmem_base;
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(352, 1)
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                const AttnParams p) {
   using L = FwdLayout<D>;
-  constexpr int NSK = L::NSK, NSV = L::NSV, NSB = L::NSB;
+  constexpr int NSK = L::NSK, NSV = L::NSV;
   static_assert(sizeof(FwdMisc) <= L::MISC_BYTES, "misc region");
   static_assert(L::SMEM <= 232448, "shared memory");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -166,9 +169,10 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(&m.v_full[s], 1);
       mbar_init(&m.v_empty[s], 1);
     }
-    for (int s = 0; s < L::NSB; ++s) {
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&m.s_full[s], 1);
-      mbar_init(&m.p_full[s], 128);  // the softmax group that owns the tile
+      mbar_init(&m.s_free[s], 128);  // the softmax group that owns the tile
+      mbar_init(&m.p_full[s], 128);
       mbar_init(&m.pv_done[s], 1);
     }
     for (int s = 0; s < 2; ++s)
@@ -255,9 +259,9 @@ __global__ void __launch_bounds__(352, 1)
     int4 te, te_next;  // table entries of this and the next visited key tile
     for (int tk = walk.first(te), tk_next; ok && tk <= tq; tk = tk_next, te = te_next, ++j) {
       tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
-      const int sb = j % NSB, sk = j % NSK;
-      // S_j into buffer sb once PV_{j-3} has read the P that was there
-      if (j >= NSB && !g.wait_warp(&m.pv_done[sb], ((j - NSB) / NSB) & 1, 4)) { ok = false; break; }
+      const int sb = j & 1, sk = j % NSK;
+      // S_j into buffer sb once the softmax has loaded S_{j-2} from it
+      if (j >= 2 && !g.wait_warp(&m.s_free[sb], ((j - 2) >> 1) & 1, 4)) { ok = false; break; }
       if (!g.wait_warp(&m.k_full[sk], (j / NSK) & 1, 5)) { ok = false; break; }
       tc_fence_after();
       const uint64_t kd = sdesc_sw128(sK + sk * L::TB, 16, 1024);
@@ -288,15 +292,15 @@ __global__ void __launch_bounds__(352, 1)
     int4 te, te_next;  // table entries of this and the next visited key tile
     for (int tk = walk.first(te), tk_next; ok && tk <= tq; tk = tk_next, te = te_next, ++j) {
       tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
-      const int sb = j % NSB, sv = j % NSV;
+      const int sb = j & 1, sv = j % NSV;
       if (!g.wait_warp(&m.v_full[sv], (j / NSV) & 1, 6)) { ok = false; break; }
-      if (!g.wait_warp(&m.p_full[sb], (j / NSB) & 1, 7)) { ok = false; break; }
+      if (!g.wait_warp(&m.p_full[sb], (j >> 1) & 1, 7)) { ok = false; break; }
       tc_fence_after();
       const uint64_t vd = sdesc_sw128(sV + sv * L::TB, L::CHUNK, 1024);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         if (leader)
-          umma_bf16_ta(tmem + L::TM_O, tmem + L::TM_S + sb * 128 + kk * 8, sdesc_add(vd, kk * 2048), idO,
+          umma_bf16_ta(tmem + L::TM_O, tmem + L::TM_P + sb * 64 + kk * 8, sdesc_add(vd, kk * 2048), idO,
                        (j > 0 || kk > 0) ? 1u : 0u);
       if (leader) {
         umma_commit(&m.pv_done[sb]);
@@ -331,14 +335,16 @@ __global__ void __launch_bounds__(352, 1)
     for (int tk = walk.first(te), tk_next; tk <= tq; tk = tk_next, te = te_next, ++jj) {
       tk_next = walk.next(tk, te_next);  // loaded now, used after this tile's work
       if ((jj & 1) != grp) continue;
-      const int sb = jj % NSB;
       const bool masked = !tile_pair_full(tq, walk.qt, tk, te);
-      ok = g.wait(&m.s_full[sb], (jj / NSB) & 1, 9);
+      // this group's S buffer, released as soon as the scores are loaded
+      ok = g.wait(&m.s_full[grp], (jj >> 1) & 1, 9);
       if (!__all_sync(~0u, ok)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t tS = tmem + lane_base + L::TM_S + sb * 128;
       uint32_t x0[32], x1[32], x2[32], x3[32];
-      tmem_ld128(tS, x0, x1, x2, x3);
+      tmem_ld128(tmem + lane_base + L::TM_S + grp * 128, x0, x1, x2, x3);
+      tc_fence_before();
+      mbar_arrive(&m.s_free[grp]);
+      const uint32_t tP = tmem + lane_base + L::TM_P + grp * 64;
       const bool ids = needs_ids(p, te);  // then the tile is masked too
       const int ss = seg_stage(grp, n_ids);
       if (ids) {  // per-key segment ids, released once the mask is applied
@@ -381,30 +387,37 @@ __global__ void __launch_bounds__(352, 1)
       }
       const float moff = (m_new == -INFINITY) ? 0.f : m_new;
       const uint64_t sc = f2(sl2, sl2), off = f2(-moff, -moff);
-      // P for keys 32c .. 32c+31 -> packed columns 16c .. 16c+15 of the S
-      // buffer, all of whose scores this thread already holds
+      // P for keys 32c .. 32c+31 -> packed columns 16c .. 16c+15 of this
+      // group's P buffer, once PV_{jj-2} has read the P that was there
       // The normaliser of O sums the bf16-rounded weights the PV product
       // uses on masked tiles, where a row with few keys has all of them; on
       // entirely visible tiles it takes the exact weights, whose rounding
       // errors average out over the 128 keys of the tile.
+      if (jj >= 2) {
+        ok = g.wait(&m.pv_done[grp], ((jj - 2) >> 1) & 1, 16);
+        if (!__all_sync(~0u, ok)) { ok = false; break; }
+        tc_fence_after();
+      }
       uint64_t t2 = 0ull, tr2 = 0ull;
       if (masked) {
-        exp_store32<true>(x0, sc, off, tS, t2, tr2);
-        exp_store32<true>(x1, sc, off, tS + 16, t2, tr2);
-        exp_store32<true>(x2, sc, off, tS + 32, t2, tr2);
-        exp_store32<true>(x3, sc, off, tS + 48, t2, tr2);
+        exp_store32<true>(x0, sc, off, tP, t2, tr2);
+        exp_store32<true>(x1, sc, off, tP + 16, t2, tr2);
+        exp_store32<true>(x2, sc, off, tP + 32, t2, tr2);
+        exp_store32<true>(x3, sc, off, tP + 48, t2, tr2);
       } else {
-        exp_store32<false>(x0, sc, off, tS, t2, tr2);
-        exp_store32<false>(x1, sc, off, tS + 16, t2, tr2);
-        exp_store32<false>(x2, sc, off, tS + 32, t2, tr2);
-        exp_store32<false>(x3, sc, off, tS + 48, t2, tr2);
+        exp_store32<false>(x0, sc, off, tP, t2, tr2);
+        exp_store32<false>(x1, sc, off, tP + 16, t2, tr2);
+        exp_store32<false>(x2, sc, off, tP + 32, t2, tr2);
+        exp_store32<false>(x3, sc, off, tP + 48, t2, tr2);
         tr2 = t2;
       }
       l2 = add2(l2, t2);
       lr2 = add2(lr2, tr2);
       if (rescale && jj > 0) {  // O holds earlier tiles: rescale it once their PV is done
+        // (PV_{jj-2} has completed, and with it PV_{jj-3}: this parity wait on
+        // the other group's barrier cannot match an older phase)
         const float alpha = (m_prev == -INFINITY) ? 0.f : ex2(m_prev - m_new);
-        ok = g.wait(&m.pv_done[(jj - 1) % NSB], ((jj - 1) / NSB) & 1, 11);
+        ok = g.wait(&m.pv_done[grp ^ 1], ((jj - 1) >> 1) & 1, 11);
         if (!__all_sync(~0u, ok)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll 1
@@ -418,7 +431,7 @@ __global__ void __launch_bounds__(352, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&m.p_full[sb]);
+      mbar_arrive(&m.p_full[grp]);
     }
     // ------------------------------------------------------------ epilogue
     // The final maximum is the one the last tile's group handed on; both
@@ -439,7 +452,7 @@ __global__ void __launch_bounds__(352, 1)
       ok = __all_sync(~0u, ok);
     }
     if (ok && jj > 0) {  // the last PV has accumulated into O
-      ok = g.wait(&m.pv_done[(jj - 1) % NSB], ((jj - 1) / NSB) & 1, 14);
+      ok = g.wait(&m.fin_pv, 0, 14);  // the PV issuer's final commit covers every PV
       ok = __all_sync(~0u, ok);
     }
     if (ok && jj > 0) {
