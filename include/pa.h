@@ -171,6 +171,19 @@ pa_status pa_bwd_noalloc(const pa_dims* dims, const void* q, const void* k, cons
  */
 uint32_t pa_device_status(const void* ws, pa_stream_t stream);
 
+/*
+ * Self-test of the kernels' bounded waits (failure detection without a GPU
+ * fault): clears the workspace status word, then launches on `stream` one
+ * warp that waits, through the same wait path the kernels use, on an
+ * mbarrier that nothing arrives on. After the wait limit (2 s) it gives up,
+ * sets PA_DEVERR_TIMEOUT with site 99 in bits 8.. of the status word (the
+ * first 4 bytes of `ws`) and exits; the context stays usable. Read the result
+ * with pa_device_status.
+ * Errors: PA_ERR_NULL (ws), PA_ERR_ALIGN, PA_ERR_WORKSPACE (ws_bytes < 4),
+ * PA_ERR_ARCH, PA_ERR_CUDA (launch failed).
+ */
+pa_status pa_selftest_wait_timeout(void* ws, size_t ws_bytes, pa_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* pa_status_string(pa_status s);
 

@@ -27,7 +27,7 @@ STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_NULL", 2: "PA_ERR_HEAD_DIM", 3: "PA_ERR_G
                 5: "PA_ERR_ALIGN", 6: "PA_ERR_WORKSPACE", 7: "PA_ERR_ARCH", 8: "PA_ERR_CUDA"}
 EXPORTS = ["pa_workspace_bytes", "pa_fwd", "pa_bwd", "pa_fwd_causal", "pa_bwd_causal", "pa_build_tile_table",
            "pa_fwd_tiles", "pa_bwd_delta", "pa_bwd_dq", "pa_bwd_dkv", "pa_bwd_noalloc", "pa_device_status",
-           "pa_status_string"]
+           "pa_selftest_wait_timeout", "pa_status_string"]
 
 
 class LibraryMissing(RuntimeError):
@@ -75,6 +75,8 @@ def lib():
                 getattr(L, f).restype = ctypes.c_int
             L.pa_bwd_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P, P, ctypes.POINTER(ctypes.c_uint32), P]
             L.pa_bwd_noalloc.restype = ctypes.c_int
+            L.pa_selftest_wait_timeout.argtypes = [P, S, P]
+            L.pa_selftest_wait_timeout.restype = ctypes.c_int
             L.pa_device_status.argtypes = [P, P]
             L.pa_device_status.restype = ctypes.c_uint32
             L.pa_status_string.argtypes = [ctypes.c_int]
@@ -227,6 +229,12 @@ def pa_bwd_noalloc(q, k, v, out, dout, lse, seg, dq, dk, dv, scale=0.0, stream=N
                                 _ptr(seg, torch.int32, "seg"), _ptr(dq, bf, "dq"), _ptr(dk, bf, "dk"),
                                 _ptr(dv, bf, "dv"), ctypes.byref(st) if wait_status else None, _stream(stream)))
     return int(st.value) if wait_status else None
+
+
+def pa_selftest_wait_timeout(ws, stream=None):
+    """Launch the bounded-wait self-test into the workspace status word (see
+    include/pa.h); read the result with pa_device_status."""
+    _check(lib().pa_selftest_wait_timeout(_ptr(ws, None, "ws"), ws.numel(), _stream(stream)))
 
 
 def pa_device_status(ws, stream=None) -> int:

@@ -239,6 +239,19 @@ pa_status pa_bwd_dkv(const pa_dims* dims, const void* q, const void* k, const vo
   return step_dkv(dims, q, k, v, dout, lse, seg, dk, dv, ws, ws_bytes, stream);
 }
 
+pa_status pa_selftest_wait_timeout(void* ws, size_t ws_bytes, pa_stream_t stream) {
+  if (!ws) return PA_ERR_NULL;
+  if (!aligned16(ws)) return PA_ERR_ALIGN;
+  if (ws_bytes < sizeof(uint32_t)) return PA_ERR_WORKSPACE;
+  pa_status why = device_ok();
+  if (why != PA_OK) return why;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), st) != cudaSuccess ||
+      pa::launch_wait_timeout_selftest(static_cast<uint32_t*>(ws), st) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
 uint32_t pa_device_status(const void* ws, pa_stream_t stream) {
   if (!ws) return 0xFFFFFFFFu;
   uint32_t h = 0;

@@ -19,6 +19,9 @@
 namespace pa {
 
 constexpr int kTile = 128;
+// Status-word site number of the bounded-wait self-test (the kernels use
+// smaller ones).
+constexpr uint32_t kSelftestWaitSite = 99;
 
 struct AttnParams {
   int B, Hq, Hkv, N, T, G;

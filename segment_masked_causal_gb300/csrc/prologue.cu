@@ -15,6 +15,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "sm103.cuh"
 
 namespace pa {
 
@@ -84,6 +85,24 @@ __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restr
   }
 }
 
+// Self-test of the bounded waits: a warp waits, through the kernels' own
+// wait path, on an mbarrier that nothing ever arrives on. Each wait gives up
+// after its limit, records PA_DEVERR_TIMEOUT with the site in the status word
+// and returns false, and the kernel exits normally: no trap, and the context
+// stays usable.
+__global__ void __launch_bounds__(32) wait_timeout_kernel(uint32_t* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  const Guard g{&abort_flag, status};
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  (void)g.wait(&bar, 0, kSelftestWaitSite);
+}
+
 }  // namespace
 
 cudaError_t launch_tile_table(const AttnParams& p, int4* tiles, cudaStream_t st) {
@@ -93,6 +112,11 @@ cudaError_t launch_tile_table(const AttnParams& p, int4* tiles, cudaStream_t st)
     if (e != cudaSuccess) return e;
   }
   tile_table_kernel<<<p.B, 256, smem, st>>>(p.seg, p.N, p.T, tiles, p.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout_selftest(uint32_t* status, cudaStream_t st) {
+  wait_timeout_kernel<<<1, 32, 0, st>>>(status);
   return cudaGetLastError();
 }
 

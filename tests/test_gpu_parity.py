@@ -10,10 +10,13 @@ entry adding the PACKED kernels). Dropping the segment mask must fail the
 tolerance (mlx-train-perf 0.5.1 README, "Sequence packing": contamination
 test).
 """
+import time
+
 import numpy as np
 import pytest
 import torch
 
+import segment_masked_causal_gb300 as pa
 import synth
 from _gpu_common import (Case, assert_full_parity, assert_group_parity, assert_sampled_parity,
                          assert_segment_sums, f64, O_MAXABS)
@@ -133,6 +136,22 @@ def test_single_segment_bit_identical_to_causal(name, cuda_dev):
     for n in ("o", "lse", "dq", "dk", "dv"):
         assert torch.equal(packed[n].view(torch.int16) if packed[n].dtype == torch.bfloat16 else packed[n].view(torch.int32),
                            causal[n].view(torch.int16) if causal[n].dtype == torch.bfloat16 else causal[n].view(torch.int32)), n
+
+
+def test_bounded_wait_gives_up_and_context_survives(cuda_dev):
+    """A wait that nothing completes runs out after its limit, reports
+    PA_DEVERR_TIMEOUT with its site in the status word, and the next calls
+    on the same context still compute correct results."""
+    w = synth.workload("tiny_3seg")
+    c = Case(w, cuda_dev)
+    t0 = time.time()
+    pa.pa_selftest_wait_timeout(c.ws)
+    st = pa.pa_device_status(c.ws)
+    took = time.time() - t0
+    assert st == (0x1 | (99 << 8)), hex(st)  # PA_DEVERR_TIMEOUT, site 99
+    assert 1.0 < took < 30.0, took
+    assert pa.pa_device_status(c.ws) == 0  # reading cleared it
+    print(assert_full_parity(c.run(), c.oracle_full(), "after-timeout"))
 
 
 def test_runs_are_deterministic(cuda_dev):
