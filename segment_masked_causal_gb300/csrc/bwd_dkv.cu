@@ -115,7 +115,9 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
     }
     for (int s = 0; s < kDoStages; ++s) {
       mbar_init(&m.do_full[s], 1);
-      mbar_init(&m.do_empty[s], 2);  // released by the dP^T and by the dV MMAs
+      // released by the dP^T and dV MMAs and by the softmax threads once
+      // phase B has read the stage's delta vector
+      mbar_init(&m.do_empty[s], 2 + 256);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&m.s_full[s], 1);
@@ -390,6 +392,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&m.ds_full[i & 1]);
+        mbar_arrive(&m.do_empty[ds]);  // this step's delta vector has been read
       }
     }
     if (ok && i > 0) {
