@@ -83,11 +83,19 @@ def test_null_and_alignment_refusals(L):
                            1 << 40, None) == 5
 
 
+def test_selftest_refusals(L):
+    """The bounded-wait self-test checks its workspace before any device call."""
+    assert L.pa_selftest_wait_timeout(None, 1 << 20, None) == 1
+    assert L.pa_selftest_wait_timeout(FAKE + 4, 1 << 20, None) == 5
+    assert L.pa_selftest_wait_timeout(FAKE, 3, None) == 6
+
+
 def test_valid_call_without_a_gpu_is_refused_not_run(L):
     import torch
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert fwd(L, d()) in (7, 8)  # no device: arch / CUDA error, nothing launched
+    assert L.pa_selftest_wait_timeout(FAKE, 1 << 20, None) in (7, 8)
 
 
 def test_status_strings(L):
