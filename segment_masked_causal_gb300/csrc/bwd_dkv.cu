@@ -25,13 +25,16 @@
 // other dV_i as soon as P^T_i is ready and dK_i once dS^T_i is. The
 // softmax warps run each step in two phases: phase A turns S^T_i into P^T_i,
 // phase B reads dP^T_i (releasing its region) and forms dS^T_i. Q rides a
-// 3-stage ring because each Q tile is read twice a step apart (by S^T_i and
-// by dK_i); dO rides a 2-stage ring.
+// 3-stage ring (with the step's lse) because each Q tile is read twice a step
+// apart (by S^T_i and by dK_i); dO rides a 2-stage ring with the step's
+// delta vector, and a dO stage is released by the dP^T and dV products and by
+// the softmax once phase B has read delta. dK and dV leave through the K and
+// V tiles' shared memory and TMA stores.
 //
 // Warp roles: warp 0 TMA producer (lane 0 the Q ring, lane 1 the dO ring),
-// warp 1 issues S^T/dP^T and owns TMEM,
-// warp 2 issues dV/dK, warps 3..10 softmax: two threads per key row (TMEM
-// lane quarter = warp index mod 4), 64 query columns each.
+// warp 1 issues S^T/dP^T and owns TMEM, warp 2 issues dV/dK, warps 3..10
+// softmax: two threads per key row (TMEM lane quarter = warp index mod 4),
+// 64 query columns each.
 #include <cuda_runtime.h>
 
 #include "common.cuh"

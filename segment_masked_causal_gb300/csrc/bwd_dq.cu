@@ -16,7 +16,10 @@
 // dP regions used by alternate key tiles; dS is written over its tile's dP.
 // The softmax warps release the S region as soon as they have loaded it, and
 // a dP region is needed again only two tiles later, so the next tile's S and
-// dP run on the tensor core while this tile's dS is being formed.
+// dP run on the tensor core while this tile's dS is being formed. The key
+// tiles' segment ids ride the K ring; a K stage is released only after dQ,
+// which follows the softmax's use of them. dQ leaves through the Q tile's
+// shared memory and a TMA store.
 //
 // Warp roles: warp 0 TMA producer (Q and dO once; K through a 3-stage ring,
 // V through a 2-stage ring), warp 1 dP/S issuer and TMEM owner, warp 2 dQ

@@ -26,15 +26,16 @@
 // computed against the maximum in use, so O and l stay consistent and O / l
 // is exact in real arithmetic. Each group keeps its own partial sums against
 // the maximum it last used; the epilogue brings both to the final maximum and
-// adds them. O is divided by the sum of the bf16-rounded weights the PV
-// product used; lse uses the exact fp32 sum.
+// adds them. O is divided by a sum that takes the bf16-rounded weights the PV
+// product used on masked tiles and the exact weights on entirely visible
+// ones; lse uses the exact fp32 sum. O leaves through the Q tile's shared
+// memory and a TMA store.
 //
 // Warp roles: warp 0 TMA producer (Q once; K through a 3-stage ring, V
 // through a 2-stage ring, the per-key segment ids of key tiles that span
 // several segments through a ring of their own), warp 1 S issuer and TMEM
-// owner, warp 2 PV issuer, warps 3..6
-// softmax group 0 and warps 7..10 softmax group 1 (TMEM lane quarter = warp
-// index mod 4).
+// owner, warp 2 PV issuer, warps 3..6 softmax group 0 and warps 7..10
+// softmax group 1 (TMEM lane quarter = warp index mod 4).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
