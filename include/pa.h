@@ -184,6 +184,55 @@ uint32_t pa_device_status(const void* ws, pa_stream_t stream);
  */
 pa_status pa_selftest_wait_timeout(void* ws, size_t ws_bytes, pa_stream_t stream);
 
+/*
+ * Host packer (mlx-train-perf changelog, "Added": the packed batch iterator
+ * fills fixed rows with (tokens, offset) sequences after a seeded per-epoch
+ * shuffle, by first-fit, and emits per-token segment buffers; the packed loss
+ * masks segment by segment, so the supervised tokens are those of an
+ * unpacked run, per the 0.5.1 README, "Sequence packing"). Host memory only;
+ * no CUDA call is made and no GPU is needed.
+ *
+ * Inputs (host, caller-owned, read only):
+ *   lengths[count]  tokens per sequence, each >= 1. count >= 0.
+ *   offsets[count]  prompt length per sequence, each >= 0 (>= length means
+ *                   nothing of it is supervised); NULL = all 0.
+ *   tokens          the sequences' tokens concatenated in input order
+ *                   (sum(lengths) values); needed only when row_tokens is set.
+ *   rows, N         the output holds `rows` rows of N tokens (rows, N >= 1).
+ *   seed, epoch     the shuffle. Draw n of (seed, epoch) is
+ *                   m(k + (n + 1) * 0x9E3779B97F4A7C15), k = m(seed * 1000003
+ *                   + epoch), m the splitmix64 output function, all mod 2^64;
+ *                   for i = count-1 down to 1, position i swaps with position
+ *                   draw(i) mod (i + 1).
+ * Placement: in shuffled order, each sequence goes whole into the lowest-
+ *   numbered row with room for it, behind that row's earlier sequences; one
+ *   that fits no row is left out (placement -1). So the rows in use are a
+ *   prefix; to pack a whole epoch, pass rows >= count and cut the result into
+ *   batches of B rows.
+ * Outputs (host, caller-owned, fully overwritten; all but seg may be NULL):
+ *   seg[rows*N]         int32, row-major (rows, N): the sequences of a row are
+ *                       segments 0, 1, ... in placement order; the unfilled
+ *                       tail of a row (an unused row: all of it) is one more
+ *                       segment. This is the attention calls' seg.
+ *   loss_mask[rows*N]   1 where the token at that position is trained to
+ *                       predict the next token of its own sequence and that
+ *                       token is past the prompt: position p (0-based within
+ *                       its sequence) with offset <= p + 1 <= length - 1.
+ *                       0 elsewhere, padding included.
+ *   row_tokens[rows*N]  the packed tokens; pad_token in the padding.
+ *   placement[count]    int64 flat index row*N + start of each input
+ *                       sequence (input order), or -1 when it was left out.
+ *   rows_used           1 + the highest row holding a sequence (0 if none).
+ *   placed_tokens       tokens placed in all rows.
+ * Errors: PA_ERR_NULL (seg; lengths when count > 0; tokens when row_tokens
+ * is set and count > 0), PA_ERR_SHAPE (count < 0, rows or N < 1, a length
+ * < 1 or an offset < 0). Nothing is written on error.
+ */
+pa_status pa_pack_first_fit(const int32_t* lengths, const int32_t* offsets, int32_t count, const int32_t* tokens,
+                            int32_t pad_token, int32_t rows, int32_t N, uint64_t seed, uint64_t epoch,
+                            int32_t* seg, uint8_t* loss_mask, int32_t* row_tokens, int64_t* placement,
+                            int32_t* rows_used, int64_t* placed_tokens);
+
 /* Static, human-readable name of a status code. */
 const char* pa_status_string(pa_status s);
 

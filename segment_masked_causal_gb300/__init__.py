@@ -27,7 +27,7 @@ STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_NULL", 2: "PA_ERR_HEAD_DIM", 3: "PA_ERR_G
                 5: "PA_ERR_ALIGN", 6: "PA_ERR_WORKSPACE", 7: "PA_ERR_ARCH", 8: "PA_ERR_CUDA"}
 EXPORTS = ["pa_workspace_bytes", "pa_fwd", "pa_bwd", "pa_fwd_causal", "pa_bwd_causal", "pa_build_tile_table",
            "pa_fwd_tiles", "pa_bwd_delta", "pa_bwd_dq", "pa_bwd_dkv", "pa_bwd_noalloc", "pa_device_status",
-           "pa_selftest_wait_timeout", "pa_status_string"]
+           "pa_selftest_wait_timeout", "pa_pack_first_fit", "pa_status_string"]
 
 
 class LibraryMissing(RuntimeError):
@@ -79,6 +79,9 @@ def lib():
             L.pa_selftest_wait_timeout.restype = ctypes.c_int
             L.pa_device_status.argtypes = [P, P]
             L.pa_device_status.restype = ctypes.c_uint32
+            I32, U64 = ctypes.c_int32, ctypes.c_uint64
+            L.pa_pack_first_fit.argtypes = [P, P, I32, P, I32, I32, I32, U64, U64, P, P, P, P, P, P]
+            L.pa_pack_first_fit.restype = ctypes.c_int
             L.pa_status_string.argtypes = [ctypes.c_int]
             L.pa_status_string.restype = ctypes.c_char_p
             _lib = L
@@ -239,6 +242,58 @@ def pa_selftest_wait_timeout(ws, stream=None):
 
 def pa_device_status(ws, stream=None) -> int:
     return int(lib().pa_device_status(_ptr(ws, None, "ws"), _stream(stream)))
+
+
+def pa_pack_first_fit(lengths, rows, N, seed=0, epoch=0, offsets=None, tokens=None, pad_token=0):
+    """Pack sequences into `rows` rows of N tokens (host call; see include/pa.h).
+
+    lengths/offsets: per-sequence token counts and prompt lengths (offsets
+    None = all 0); tokens: the sequences' tokens concatenated in input order,
+    or None to skip the token rows. Returns a dict of numpy arrays: seg and
+    loss_mask (rows, N), row_tokens (rows, N) or None, placement (count,)
+    int64 flat start index or -1, and the ints rows_used and placed_tokens."""
+    import numpy as np
+    lengths = np.ascontiguousarray(lengths, dtype=np.int32).reshape(-1)
+    count = lengths.size
+    off = None if offsets is None else np.ascontiguousarray(offsets, dtype=np.int32).reshape(-1)
+    if off is not None and off.size != count:
+        raise ValueError("offsets must have one entry per sequence")
+    tok = None if tokens is None else np.ascontiguousarray(tokens, dtype=np.int32).reshape(-1)
+    if tok is not None and tok.size != int(lengths.astype(np.int64).sum()):
+        raise ValueError("tokens must hold sum(lengths) values")
+    rows, N = int(rows), int(N)
+    cells = max(rows, 0) * max(N, 0)
+    seg = np.empty(cells, np.int32)
+    mask = np.empty(cells, np.uint8)
+    row_tokens = np.empty(cells, np.int32) if tok is not None else None
+    placement = np.empty(count, np.int64)
+    used, placed = ctypes.c_int32(0), ctypes.c_int64(0)
+
+    def p(a):
+        return None if a is None or a.size == 0 else a.ctypes.data
+
+    _check(lib().pa_pack_first_fit(p(lengths), p(off), count, p(tok), int(pad_token), rows, N,
+                                   int(seed) & 0xFFFFFFFFFFFFFFFF, int(epoch) & 0xFFFFFFFFFFFFFFFF,
+                                   seg.ctypes.data if cells else None, p(mask), p(row_tokens), p(placement),
+                                   ctypes.byref(used), ctypes.byref(placed)))
+    return {"seg": seg.reshape(rows, N), "loss_mask": mask.reshape(rows, N),
+            "row_tokens": None if row_tokens is None else row_tokens.reshape(rows, N),
+            "placement": placement, "rows_used": int(used.value), "placed_tokens": int(placed.value)}
+
+
+def packed_batches(lengths, B, N, seed, epoch, offsets=None, tokens=None, pad_token=0):
+    """One epoch of fixed-shape packed batches: pack every sequence with
+    pa_pack_first_fit into as many rows as it needs, then yield consecutive
+    groups of B rows as dicts of seg, loss_mask and row_tokens, each (B, N).
+    Rows of the last batch that hold no sequence are one padding segment with
+    no supervised token. Sequences longer than N are left out."""
+    B = int(B)
+    count = len(lengths)
+    rows = max(-(-count // B), 1) * B
+    r = pa_pack_first_fit(lengths, rows, N, seed, epoch, offsets, tokens, pad_token)
+    for b in range(-(-r["rows_used"] // B)):
+        sl = slice(b * B, (b + 1) * B)
+        yield {k: (None if r[k] is None else r[k][sl]) for k in ("seg", "loss_mask", "row_tokens")}
 
 
 def pa_status_string(code: int) -> str:

@@ -19,7 +19,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa.so")
-SOURCES = ["api.cu", "prologue.cu", "fwd.cu", "bwd_dq.cu", "bwd_dkv.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "prologue.cu", "fwd.cu", "bwd_dq.cu", "bwd_dkv.cu", "noalloc.cu", "pack.cpp"]
 HEADERS = ["sm103.cuh", "common.cuh", "kernels.h", "tmap.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -48,7 +48,7 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         objs.append(o)
         if force or _stale(o, [s] + hdrs):
             cmd = [nvcc, *ARCH, *FLAGS, *(extra or []), "-c", s, "-o", o]
