@@ -408,6 +408,7 @@ def run_ours(args):
     }
     if not args.no_extras and w.name == "8k_one_segment":
         line["packed"] = packed_extras(dev, rank, args)
+        line["head_dim_96"] = head_dim_96_extra(dev, rank, args)
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
@@ -443,6 +444,19 @@ def packed_extras(dev, rank, args):
                   "skip_speedup_vs_causal": round(t_causal[k] / t_multi[k], 3),
                   "one_segment_overhead_vs_causal": round(t_packed1[k] / t_causal[k] - 1.0, 4)}
     return out
+
+
+def head_dim_96_extra(dev, rank, args):
+    """The same 8k one-segment step at head dim 96 (the 128-wide kernels on
+    tiles whose columns 96..127 are zero-filled): useful TFLOP/s counted at
+    D = 96, and per-kernel times."""
+    steps = max(3, min(args.steps, 10))
+    w = synth.workload("8k_one_segment_d96")
+    r = Runner(w, dev, replica_seed(w.seed, rank))
+    t, _ = r.timed(steps, 2)
+    del r
+    return {"workload": w.name, "useful_tflops": round(useful_flops(w) / (t["step"] * 1e-3) / 1e12, 3),
+            "ms_per_step": round(t["step"], 4), **{k + "_ms": round(t[k], 4) for k in ("fwd", "dq", "dkv")}}
 
 
 # ------------------------------------------------------------------ the reference arm

@@ -24,6 +24,10 @@
  *                      compared for equality only: any values are valid.
  *                      Tile skipping is fastest when each id forms one
  *                      contiguous run, which is what packing produces.
+ * Head dim 96 (README, "If you maintain a trainer": head_dim in {64, 96,
+ * 128}) runs the 128-wide kernels; the tensors stay 96 wide, the tile loads
+ * fill columns 96..127 with zeros and the stores leave them out, so a D = 96
+ * call takes about as long as a D = 128 one.
  *
  * Ownership: every pointer is device memory owned by the caller. The library
  * allocates no device memory and keeps no pointer after a call returns. The
@@ -58,14 +62,14 @@ typedef struct {
   int32_t Hq;   /* query heads                                       */
   int32_t Hkv;  /* key/value heads; Hq % Hkv == 0                    */
   int32_t N;    /* tokens per row; multiple of 128                   */
-  int32_t D;    /* head dim: 64 or 128                               */
+  int32_t D;    /* head dim: 64, 96 or 128                           */
   float scale;  /* softmax scale; <= 0 selects 1/sqrt(D)             */
 } pa_dims;
 
 typedef enum {
   PA_OK = 0,
   PA_ERR_NULL = 1,      /* a required pointer is NULL                          */
-  PA_ERR_HEAD_DIM = 2,  /* D not in {64, 128}                                  */
+  PA_ERR_HEAD_DIM = 2,  /* D not in {64, 96, 128}                              */
   PA_ERR_GQA = 3,       /* Hq % Hkv != 0                                       */
   PA_ERR_SHAPE = 4,     /* B, H, N <= 0, N % 128 != 0, or sizes overflow int32 */
   PA_ERR_ALIGN = 5,     /* a pointer is not 16-byte aligned                    */

@@ -11,7 +11,7 @@ call raises ``LibraryMissing``.
 Semantics (mlx-train-perf changelog, PACKED kernels; 0.5.1 README,
 "Sequence packing"): token i attends token j iff j <= i and seg[i] == seg[j].
 q/out/dout/dq are (B, Hq, N, D) bf16; k/v/dk/dv are (B, Hkv, N, D) bf16; lse
-is (B, Hq, N) fp32; seg is (B, N) int32; D in {64, 128}; N % 128 == 0.
+is (B, Hq, N) fp32; seg is (B, N) int32; D in {64, 96, 128}; N % 128 == 0.
 """
 from __future__ import annotations
 

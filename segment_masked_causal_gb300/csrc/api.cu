@@ -29,7 +29,7 @@ bool dims_ok(const pa_dims* d, pa_status* why) {
     *why = PA_ERR_SHAPE;
     return false;
   }
-  if (d->D != 64 && d->D != 128) { *why = PA_ERR_HEAD_DIM; return false; }
+  if (d->D != 64 && d->D != 96 && d->D != 128) { *why = PA_ERR_HEAD_DIM; return false; }
   if (d->Hq % d->Hkv != 0) { *why = PA_ERR_GQA; return false; }
   // tensor-map row coordinates and tile counts are 32-bit
   const int64_t rows = (int64_t)d->B * d->Hq * d->N;
@@ -268,7 +268,7 @@ const char* pa_status_string(pa_status s) {
   switch (s) {
     case PA_OK: return "ok";
     case PA_ERR_NULL: return "a required pointer is NULL";
-    case PA_ERR_HEAD_DIM: return "head dim must be 64 or 128";
+    case PA_ERR_HEAD_DIM: return "head dim must be 64, 96 or 128";
     case PA_ERR_GQA: return "Hq must be a multiple of Hkv";
     case PA_ERR_SHAPE: return "bad shape (B, H, N > 0; N % 128 == 0; B*Hq*N < 2^31; finite scale)";
     case PA_ERR_ALIGN: return "a pointer is not 16-byte aligned";

@@ -357,14 +357,14 @@ __global__ void __launch_bounds__(352, 1)
 }
 
 template <int D>
-cudaError_t launch_dq_d(const AttnParams& p, const void* q, const void* k, const void* v, const void* dout,
+cudaError_t launch_dq_d(const AttnParams& p, int Dio, const void* q, const void* k, const void* v, const void* dout,
                         cudaStream_t st) {
   using L = DqLayout<D>;
   CUtensorMap tq, tdo, tk, tv, tdq;
   const uint64_t qrows = (uint64_t)p.B * p.Hq * p.N, krows = (uint64_t)p.B * p.Hkv * p.N;
-  if (!tmap_bf16_2d_sw128(&tq, q, D, qrows, 128) || !tmap_bf16_2d_sw128(&tdo, dout, D, qrows, 128) ||
-      !tmap_bf16_2d_sw128(&tk, k, D, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, D, krows, 128) ||
-      !tmap_bf16_2d_sw128(&tdq, p.dq, D, qrows, 128))
+  if (!tmap_bf16_2d_sw128(&tq, q, Dio, qrows, 128) || !tmap_bf16_2d_sw128(&tdo, dout, Dio, qrows, 128) ||
+      !tmap_bf16_2d_sw128(&tk, k, Dio, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, Dio, krows, 128) ||
+      !tmap_bf16_2d_sw128(&tdq, p.dq, Dio, qrows, 128))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
@@ -377,7 +377,10 @@ cudaError_t launch_dq_d(const AttnParams& p, const void* q, const void* k, const
 
 cudaError_t launch_bwd_dq(const AttnParams& p, int D, const void* q, const void* k, const void* v,
                           const void* dout, cudaStream_t st) {
-  return D == 128 ? launch_dq_d<128>(p, q, k, v, dout, st) : launch_dq_d<64>(p, q, k, v, dout, st);
+  // head dim 96 runs the 128-wide kernel: its tensor maps are 96 elements
+  // wide, so TMA fills columns 96..127 of every loaded tile with zeros
+  // (which add nothing to any product) and drops them from every store.
+  return D == 64 ? launch_dq_d<64>(p, 64, q, k, v, dout, st) : launch_dq_d<128>(p, D, q, k, v, dout, st);
 }
 
 }  // namespace pa

@@ -501,12 +501,12 @@ __global__ void __launch_bounds__(352, 1)
 }
 
 template <int D>
-cudaError_t launch_fwd_d(const AttnParams& p, const void* q, const void* k, const void* v, cudaStream_t st) {
+cudaError_t launch_fwd_d(const AttnParams& p, int Dio, const void* q, const void* k, const void* v, cudaStream_t st) {
   using L = FwdLayout<D>;
   CUtensorMap tq, tk, tv, to;
   const uint64_t qrows = (uint64_t)p.B * p.Hq * p.N, krows = (uint64_t)p.B * p.Hkv * p.N;
-  if (!tmap_bf16_2d_sw128(&tq, q, D, qrows, 128) || !tmap_bf16_2d_sw128(&tk, k, D, krows, 128) ||
-      !tmap_bf16_2d_sw128(&tv, v, D, krows, 128) || !tmap_bf16_2d_sw128(&to, p.out, D, qrows, 128))
+  if (!tmap_bf16_2d_sw128(&tq, q, Dio, qrows, 128) || !tmap_bf16_2d_sw128(&tk, k, Dio, krows, 128) ||
+      !tmap_bf16_2d_sw128(&tv, v, Dio, krows, 128) || !tmap_bf16_2d_sw128(&to, p.out, Dio, qrows, 128))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
@@ -519,7 +519,10 @@ cudaError_t launch_fwd_d(const AttnParams& p, const void* q, const void* k, cons
 
 cudaError_t launch_fwd(const AttnParams& p, int D, const void* q, const void* k, const void* v,
                        cudaStream_t st) {
-  return D == 128 ? launch_fwd_d<128>(p, q, k, v, st) : launch_fwd_d<64>(p, q, k, v, st);
+  // head dim 96 runs the 128-wide kernel: its tensor maps are 96 elements
+  // wide, so TMA fills columns 96..127 of every loaded tile with zeros
+  // (which add nothing to any product) and drops them from every store.
+  return D == 64 ? launch_fwd_d<64>(p, 64, q, k, v, st) : launch_fwd_d<128>(p, D, q, k, v, st);
 }
 
 }  // namespace pa

@@ -55,27 +55,38 @@ __global__ void __launch_bounds__(256) tile_table_kernel(const int32_t* __restri
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Lanes that share one row of the delta kernel: a power of two dividing the
+// row's D/8 16-byte vectors, so a row's lanes sit in one warp.
+constexpr int delta_lanes(int D) { return (D / 8) % 16 == 0 ? 16 : (D / 8) % 8 == 0 ? 8 : 4; }
+
 template <int D>
 __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restrict__ o,
                                                     const __nv_bfloat16* __restrict__ dout,
                                                     const float* __restrict__ lse, float* __restrict__ delta,
                                                     float* __restrict__ lse2, size_t rows) {
-  constexpr int LPR = D / 8;  // lanes per row
+  // each of the row's LPR lanes takes every LPR-th 16-byte vector
+  constexpr int VEC = D / 8;
+  constexpr int LPR = delta_lanes(D);
+  static_assert(VEC % LPR == 0, "head dim must be a multiple of 32");
   const size_t gtid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   const int sub = threadIdx.x % LPR;
   for (size_t t = gtid; t < rows * LPR; t += stride) {
     const size_t row = t / LPR;
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + row * D) + sub);
-    const uint4 c = __ldg(reinterpret_cast<const uint4*>(dout + row * D) + sub);
-    float acc = bf16lo(a.x) * bf16lo(c.x);
-    acc = fmaf(bf16hi(a.x), bf16hi(c.x), acc);
-    acc = fmaf(bf16lo(a.y), bf16lo(c.y), acc);
-    acc = fmaf(bf16hi(a.y), bf16hi(c.y), acc);
-    acc = fmaf(bf16lo(a.z), bf16lo(c.z), acc);
-    acc = fmaf(bf16hi(a.z), bf16hi(c.z), acc);
-    acc = fmaf(bf16lo(a.w), bf16lo(c.w), acc);
-    acc = fmaf(bf16hi(a.w), bf16hi(c.w), acc);
+    float acc = 0.f;
+#pragma unroll
+    for (int v = sub; v < VEC; v += LPR) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + row * D) + v);
+      const uint4 c = __ldg(reinterpret_cast<const uint4*>(dout + row * D) + v);
+      acc = fmaf(bf16lo(a.x), bf16lo(c.x), acc);
+      acc = fmaf(bf16hi(a.x), bf16hi(c.x), acc);
+      acc = fmaf(bf16lo(a.y), bf16lo(c.y), acc);
+      acc = fmaf(bf16hi(a.y), bf16hi(c.y), acc);
+      acc = fmaf(bf16lo(a.z), bf16lo(c.z), acc);
+      acc = fmaf(bf16hi(a.z), bf16hi(c.z), acc);
+      acc = fmaf(bf16lo(a.w), bf16lo(c.w), acc);
+      acc = fmaf(bf16hi(a.w), bf16hi(c.w), acc);
+    }
 #pragma unroll
     for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(~0u, acc, off);
     if (sub == 0) {
@@ -122,7 +133,7 @@ cudaError_t launch_wait_timeout_selftest(uint32_t* status, cudaStream_t st) {
 
 cudaError_t launch_delta(const AttnParams& p, int D, cudaStream_t st) {
   const size_t rows = (size_t)p.B * p.Hq * p.N;
-  const size_t threads = rows * (size_t)(D / 8);
+  const size_t threads = rows * (size_t)delta_lanes(D);
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -131,6 +142,8 @@ cudaError_t launch_delta(const AttnParams& p, int D, cudaStream_t st) {
   if (blocks > cap) blocks = cap;
   if (D == 128)
     delta_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, rows);
+  else if (D == 96)
+    delta_kernel<96><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, rows);
   else
     delta_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, rows);
   return cudaGetLastError();

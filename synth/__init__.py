@@ -256,6 +256,11 @@ def workload(name: str) -> Workload:
     if name == "8k_packed":
         lens = uniform_lengths(1004, 8192, 256, 2048)
         return Workload(name, 1, 32, 8, 8192, 128, 1004, lengths_to_ids(lens)[None, :], [lens])
+    if name == "8k_one_segment_d96":
+        return Workload(name, 1, 32, 8, 8192, 96, 1006, one_segment(1, 8192), [[8192]])
+    if name == "packed_2x4096_short_d96":
+        ids, lens, pad = packed_rows(1007, 2, 4096)
+        return Workload(name, 2, 16, 4, 4096, 96, 1007, ids, lens, pad)
     for n in (32768, 65536):
         if name == f"long_{n // 1024}k_one_segment":
             return Workload(name, 1, 8, 8, n, 64, 1005, one_segment(1, n), [[n]])
@@ -269,6 +274,7 @@ WORKLOADS = [
     "tiny_3seg", "tiny_fixed_1_100_155", "causal_2k_gqa", "packed_4x4096_short",
     "8k_one_segment", "8k_packed",
     "long_32k_one_segment", "long_32k_packed", "long_64k_one_segment", "long_64k_packed",
+    "8k_one_segment_d96", "packed_2x4096_short_d96",
 ]
 
 

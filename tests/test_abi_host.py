@@ -47,7 +47,8 @@ def fwd(L, dims, q=FAKE, k=FAKE, v=FAKE, seg=FAKE, out=FAKE, lse=FAKE, ws=FAKE, 
 
 
 def test_workspace_bytes(L):
-    assert L.pa_workspace_bytes(ctypes.byref(d(D=96))) == 0
+    assert L.pa_workspace_bytes(ctypes.byref(d(D=80))) == 0
+    assert L.pa_workspace_bytes(ctypes.byref(d(D=96))) == L.pa_workspace_bytes(ctypes.byref(d(D=128)))
     assert L.pa_workspace_bytes(None) == 0
     n1 = L.pa_workspace_bytes(ctypes.byref(d(N=256)))
     n2 = L.pa_workspace_bytes(ctypes.byref(d(N=512)))
@@ -57,7 +58,7 @@ def test_workspace_bytes(L):
 
 
 @pytest.mark.parametrize("dims,code", [
-    (dict(D=96), 2), (dict(D=32), 2), (dict(D=256), 2),
+    (dict(D=80), 2), (dict(D=32), 2), (dict(D=256), 2),
     (dict(Hq=6, Hkv=4), 3),
     (dict(N=200), 4), (dict(N=0), 4), (dict(B=0), 4), (dict(Hq=0), 4), (dict(Hkv=0), 4),
     (dict(B=1024, Hq=64, N=65536), 4),  # row coordinates overflow int32

@@ -40,6 +40,10 @@ SMALL = [
     # odd group size and odd tile count: the forward pairs consecutive query
     # tiles and the last pair has one tile only
     ("g3_odd_tiles_d64", synth.custom(2, 3, 1, 384, 64, [[200, 184], [384]], seed=27)),
+    # head dim 96: the 128-wide kernels with tiles whose columns 96..127 the
+    # loads fill with zeros and the stores leave out
+    ("ragged_gqa_d96", synth.custom(2, 4, 2, 512, 96, [[1, 130, 5, 120, 256], [512]], seed=29)),
+    ("len1_runs_g3_d96", synth.custom(1, 3, 1, 384, 96, [[1] * 30 + [3] * 20 + [294]], seed=30)),
 ]
 
 
@@ -127,7 +131,22 @@ def test_long_context(name, cuda_dev):
     assert_segment_sums(c, g)
 
 
-@pytest.mark.parametrize("name", ["causal_2k_gqa", "8k_one_segment", "long_32k_one_segment"])
+@pytest.mark.parametrize("name", ["8k_one_segment_d96", "packed_2x4096_short_d96"])
+def test_head_dim_96(name, cuda_dev):
+    w = synth.workload(name)
+    c = Case(w, cuda_dev)
+    g = c.run()
+    print(assert_sampled_parity(c, g, tag=name))
+    assert_segment_sums(c, g)
+
+
+def test_head_dim_96_full_group(cuda_dev):
+    w = synth.workload("packed_2x4096_short_d96")
+    c = Case(w, cuda_dev)
+    print(assert_group_parity(c, c.run(), 1, tag="packed_2x4096_short_d96 group 1"))
+
+
+@pytest.mark.parametrize("name", ["causal_2k_gqa", "8k_one_segment", "long_32k_one_segment", "8k_one_segment_d96"])
 def test_single_segment_bit_identical_to_causal(name, cuda_dev):
     w = synth.workload(name)
     c = Case(w, cuda_dev)
