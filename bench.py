@@ -409,6 +409,7 @@ def run_ours(args):
     if not args.no_extras and w.name == "8k_one_segment":
         line["packed"] = packed_extras(dev, rank, args)
         line["head_dim_96"] = head_dim_96_extra(dev, rank, args)
+        line["staged_layouts"] = staged_layout_extras(dev, rank, args)
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
@@ -457,6 +458,64 @@ def head_dim_96_extra(dev, rank, args):
     del r
     return {"workload": w.name, "useful_tflops": round(useful_flops(w) / (t["step"] * 1e-3) / 1e12, 3),
             "ms_per_step": round(t["step"], 4), **{k + "_ms": round(t[k], 4) for k in ("fwd", "dq", "dkv")}}
+
+
+def staged_layout_extras(dev, rank, args):
+    """The full public calls (pa_fwd + pa_bwd) on the 8k one-segment row with
+    contiguous tensors, on the same values held as (B, N, H, D) memory (the
+    strided calls, which copy in and out of the workspace), and on a row of
+    8,000 tokens (N not a multiple of 128, same copies)."""
+    import torch
+    import segment_masked_causal_gb300 as pa
+    steps = max(3, min(args.steps, 10))
+    bf = torch.bfloat16
+
+    def timed(q, k, v, do, seg, strided):
+        B, Hq, N, D = q.shape
+        mk = (lambda t: torch.empty_strided(t.shape, t.stride(), dtype=bf, device=dev))
+        out, dq, dk, dv = mk(q), mk(q), mk(k), mk(k)
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+        ws = pa.workspace(q, k, strided=strided)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+        def one():
+            if strided:
+                pa.pa_fwd_strided(q, k, v, seg, out, lse, ws)
+                pa.pa_bwd_strided(q, k, v, out, do, lse, seg, dq, dk, dv, ws)
+            else:
+                pa.pa_fwd(q, k, v, seg, out, lse, ws)
+                pa.pa_bwd(q, k, v, out, do, lse, seg, dq, dk, dv, ws)
+        for _ in range(2):
+            one()
+            flush.zero_()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            one()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        if pa.pa_device_status(ws) != 0:
+            raise RuntimeError("device status after staged-layout run")
+        return statistics.mean(ts)
+
+    one_seg = synth.workload("8k_one_segment")
+    r = Runner(one_seg, dev, replica_seed(one_seg.seed, rank))
+    t_plain = timed(r.q, r.k, r.v, r.do, r.seg, False)
+    bnhd = lambda t: t.transpose(1, 2).contiguous().transpose(1, 2)
+    t_bnhd = timed(bnhd(r.q), bnhd(r.k), bnhd(r.v), bnhd(r.do), r.seg, True)
+    del r
+    w8000 = synth.custom(1, 32, 8, 8000, 128, [[8000]], seed=one_seg.seed)
+    r = Runner(w8000, dev, replica_seed(one_seg.seed, rank))
+    t_8000 = timed(r.q, r.k, r.v, r.do, r.seg, False)
+    del r
+    return {"workload": one_seg.name, "ms_contiguous": round(t_plain, 4),
+            "bnhd_strided": {"ms": round(t_bnhd, 4), "overhead_vs_contiguous": round(t_bnhd / t_plain - 1, 4)},
+            "n8000": {"ms": round(t_8000, 4),
+                      "useful_tflops": round(useful_flops(w8000) / (t_8000 * 1e-3) / 1e12, 3)}}
 
 
 # ------------------------------------------------------------------ the reference arm

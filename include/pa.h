@@ -61,7 +61,7 @@ typedef struct {
   int32_t B;    /* rows (independent packed rows)                    */
   int32_t Hq;   /* query heads                                       */
   int32_t Hkv;  /* key/value heads; Hq % Hkv == 0                    */
-  int32_t N;    /* tokens per row; multiple of 128                   */
+  int32_t N;    /* tokens per row (single-step calls: multiple of 128) */
   int32_t D;    /* head dim: 64, 96 or 128                           */
   float scale;  /* softmax scale; <= 0 selects 1/sqrt(D)             */
 } pa_dims;
@@ -71,7 +71,8 @@ typedef enum {
   PA_ERR_NULL = 1,      /* a required pointer is NULL                          */
   PA_ERR_HEAD_DIM = 2,  /* D not in {64, 96, 128}                              */
   PA_ERR_GQA = 3,       /* Hq % Hkv != 0                                       */
-  PA_ERR_SHAPE = 4,     /* B, H, N <= 0, N % 128 != 0, or sizes overflow int32 */
+  PA_ERR_SHAPE = 4,     /* B, H, N <= 0, sizes overflow int32, a stride < D,
+                           or N % 128 != 0 in a single-step call             */
   PA_ERR_ALIGN = 5,     /* a pointer is not 16-byte aligned                    */
   PA_ERR_WORKSPACE = 6, /* ws_bytes < pa_workspace_bytes(dims)                 */
   PA_ERR_ARCH = 7,      /* current device is not compute capability 10.3       */
@@ -84,7 +85,11 @@ typedef enum {
 #define PA_DEVERR_SMEM 0x4u    /* a kernel's shared memory was not 1 KiB aligned;
                                   the kernel did no work                          */
 
-/* Workspace size in bytes for `dims` (0 if dims are invalid). */
+/*
+ * Workspace size in bytes for `dims` (0 if dims are invalid), for the calls
+ * on contiguous tensors. When N is not a multiple of 128 it includes room for
+ * the staging copies described at pa_fwd_strided.
+ */
 size_t pa_workspace_bytes(const pa_dims* dims);
 
 /*
@@ -117,6 +122,43 @@ pa_status pa_bwd_causal(const pa_dims* dims, const void* q, const void* k, const
                         size_t ws_bytes, pa_stream_t stream);
 
 /*
+ * Strided tensors and any N (README, "If you maintain a trainer": q/k/v are
+ * (B, H, N, D); a model that holds them as (B, N, H, D) passes that memory
+ * with its strides instead of transposing it).
+ *
+ * Same operation and results as pa_fwd / pa_bwd (seg may be NULL for plain
+ * causal), for tensors whose element (b, h, n, c) sits at element offset
+ * b*x_b + h*x_h + n*x_n + c: q, out, dout and dq use the q_* strides; k, v,
+ * dk and dv the k_* strides. lse stays contiguous (B, Hq, N) fp32 and seg
+ * (B, N) int32. Every stride must be >= D and a multiple of 8 elements;
+ * distinct (b, h, n) rows of an output must not overlap.
+ *
+ * How: when the strides are the contiguous ones and N % 128 == 0 the kernels
+ * run on the tensors directly (workspace: pa_workspace_bytes). Otherwise the
+ * call copies its inputs into (B, H, Np, D) buffers inside the workspace,
+ * with Np = N rounded up to 128 and zero rows after N, runs the kernels there
+ * and copies the results out (workspace: pa_workspace_bytes_strided). The
+ * extra tokens lie after every real query, so causality hides them; their
+ * zero dO keeps them out of dK and dV, and their outputs are dropped. The
+ * copies are memory-bound kernels on the same stream; pa_fwd / pa_bwd and
+ * the causal variants take the same path when N % 128 != 0.
+ * Errors: as pa_fwd / pa_bwd, plus PA_ERR_NULL (strides), PA_ERR_SHAPE (a
+ * stride < D), PA_ERR_ALIGN (a stride not a multiple of 8).
+ */
+typedef struct {
+  int64_t q_b, q_h, q_n; /* element strides of q, out, dout, dq */
+  int64_t k_b, k_h, k_n; /* element strides of k, v, dk, dv     */
+} pa_strides;
+
+size_t pa_workspace_bytes_strided(const pa_dims* dims);
+pa_status pa_fwd_strided(const pa_dims* dims, const pa_strides* strides, const void* q, const void* k,
+                         const void* v, const int32_t* seg, void* out, float* lse, void* ws, size_t ws_bytes,
+                         pa_stream_t stream);
+pa_status pa_bwd_strided(const pa_dims* dims, const pa_strides* strides, const void* q, const void* k,
+                         const void* v, const void* out, const void* dout, const float* lse, const int32_t* seg,
+                         void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, pa_stream_t stream);
+
+/*
  * The steps of the path, one kernel each, for callers that schedule or time
  * them individually. pa_fwd is pa_build_tile_table + pa_fwd_tiles; pa_bwd is
  * pa_build_tile_table + pa_bwd_delta + pa_bwd_dq + pa_bwd_dkv, all on one
@@ -126,7 +168,8 @@ pa_status pa_bwd_causal(const pa_dims* dims, const void* q, const void* k, const
  * plain causal throughout). pa_build_tile_table also clears the workspace
  * status word. pa_bwd_delta takes the forward's out and lse and stores, per
  * query row, delta = rowsum(dO * O) and lse * log2(e) (the dK/dV step reads
- * that copy; pa_bwd_dkv still validates its lse argument).
+ * that copy; pa_bwd_dkv still validates its lse argument). These calls take
+ * contiguous tensors with N % 128 == 0 only (else PA_ERR_SHAPE).
  */
 pa_status pa_build_tile_table(const pa_dims* dims, const int32_t* seg, void* ws, size_t ws_bytes,
                               pa_stream_t stream);

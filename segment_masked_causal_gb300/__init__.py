@@ -11,7 +11,9 @@ call raises ``LibraryMissing``.
 Semantics (mlx-train-perf changelog, PACKED kernels; 0.5.1 README,
 "Sequence packing"): token i attends token j iff j <= i and seg[i] == seg[j].
 q/out/dout/dq are (B, Hq, N, D) bf16; k/v/dk/dv are (B, Hkv, N, D) bf16; lse
-is (B, Hq, N) fp32; seg is (B, N) int32; D in {64, 96, 128}; N % 128 == 0.
+is (B, Hq, N) fp32; seg is (B, N) int32; D in {64, 96, 128}. The *_strided
+calls take (B, H, N, D) views with any strides (last dim contiguous); N need
+not be a multiple of 128 except in the single-step calls.
 """
 from __future__ import annotations
 
@@ -27,7 +29,8 @@ STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_NULL", 2: "PA_ERR_HEAD_DIM", 3: "PA_ERR_G
                 5: "PA_ERR_ALIGN", 6: "PA_ERR_WORKSPACE", 7: "PA_ERR_ARCH", 8: "PA_ERR_CUDA"}
 EXPORTS = ["pa_workspace_bytes", "pa_fwd", "pa_bwd", "pa_fwd_causal", "pa_bwd_causal", "pa_build_tile_table",
            "pa_fwd_tiles", "pa_bwd_delta", "pa_bwd_dq", "pa_bwd_dkv", "pa_bwd_noalloc", "pa_device_status",
-           "pa_selftest_wait_timeout", "pa_pack_first_fit", "pa_status_string"]
+           "pa_selftest_wait_timeout", "pa_pack_first_fit", "pa_workspace_bytes_strided", "pa_fwd_strided",
+           "pa_bwd_strided", "pa_status_string"]
 
 
 class LibraryMissing(RuntimeError):
@@ -43,6 +46,11 @@ class PAError(RuntimeError):
 class pa_dims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
                 ("N", ctypes.c_int32), ("D", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+class pa_strides(ctypes.Structure):
+    _fields_ = [("q_b", ctypes.c_int64), ("q_h", ctypes.c_int64), ("q_n", ctypes.c_int64),
+                ("k_b", ctypes.c_int64), ("k_h", ctypes.c_int64), ("k_n", ctypes.c_int64)]
 
 
 _lib = None
@@ -79,6 +87,13 @@ def lib():
             L.pa_selftest_wait_timeout.restype = ctypes.c_int
             L.pa_device_status.argtypes = [P, P]
             L.pa_device_status.restype = ctypes.c_uint32
+            ST = ctypes.POINTER(pa_strides)
+            L.pa_workspace_bytes_strided.argtypes = [D]
+            L.pa_workspace_bytes_strided.restype = S
+            L.pa_fwd_strided.argtypes = [D, ST, P, P, P, P, P, P, P, S, P]
+            L.pa_fwd_strided.restype = ctypes.c_int
+            L.pa_bwd_strided.argtypes = [D, ST, P, P, P, P, P, P, P, P, P, P, P, S, P]
+            L.pa_bwd_strided.restype = ctypes.c_int
             I32, U64 = ctypes.c_int32, ctypes.c_uint64
             L.pa_pack_first_fit.argtypes = [P, P, I32, P, I32, I32, I32, U64, U64, P, P, P, P, P, P]
             L.pa_pack_first_fit.restype = ctypes.c_int
@@ -127,14 +142,64 @@ def pa_workspace_bytes(B, Hq, Hkv, N, D) -> int:
     return int(lib().pa_workspace_bytes(ctypes.byref(d)))
 
 
-def workspace(q, k, device=None):
-    """A device workspace sized for q/k (caller-owned torch uint8 tensor)."""
+def pa_workspace_bytes_strided(B, Hq, Hkv, N, D) -> int:
+    d = make_dims(B, Hq, Hkv, N, D)
+    return int(lib().pa_workspace_bytes_strided(ctypes.byref(d)))
+
+
+def workspace(q, k, device=None, strided=False):
+    """A device workspace sized for q/k (caller-owned torch uint8 tensor);
+    strided=True sizes it for pa_fwd_strided / pa_bwd_strided."""
     import torch
     B, Hq, N, D = q.shape
-    n = pa_workspace_bytes(B, Hq, k.shape[1], N, D)
+    f = pa_workspace_bytes_strided if strided else pa_workspace_bytes
+    n = f(B, Hq, k.shape[1], N, D)
     if n == 0:
         raise PAError(4, "invalid dims")
     return torch.empty(n, dtype=torch.uint8, device=device or q.device)
+
+
+def _ptr_rows(t, dtype, name, like=None):
+    """Device pointer of a (B, H, N, D) CUDA tensor whose last dim is
+    contiguous; `like` (if given) must have the same strides."""
+    if not t.is_cuda or t.dim() != 4 or t.stride(3) != 1:
+        raise ValueError(f"{name} must be a 4-d CUDA tensor with a contiguous last dim")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if like is not None and tuple(t.stride()) != tuple(like.stride()):
+        raise ValueError(f"{name} must have the strides of its group's first tensor")
+    return t.data_ptr()
+
+
+def _strides_of(q, k):
+    return pa_strides(q.stride(0), q.stride(1), q.stride(2), k.stride(0), k.stride(1), k.stride(2))
+
+
+def pa_fwd_strided(q, k, v, seg, out, lse, ws, scale=0.0, stream=None):
+    """pa_fwd on (B, H, N, D) views with any strides (e.g. (B, N, H, D) memory
+    transposed); seg None = plain causal. out must share q's strides."""
+    import torch
+    bf = torch.bfloat16
+    d = _dims_of(q, k, scale)
+    st = _strides_of(q, k)
+    _check(lib().pa_fwd_strided(ctypes.byref(d), ctypes.byref(st), _ptr_rows(q, bf, "q"), _ptr_rows(k, bf, "k"),
+                                _ptr_rows(v, bf, "v", k), _ptr(seg, torch.int32, "seg"),
+                                _ptr_rows(out, bf, "out", q), _ptr(lse, torch.float32, "lse"),
+                                _ptr(ws, None, "ws"), ws.numel(), _stream(stream)))
+
+
+def pa_bwd_strided(q, k, v, out, dout, lse, seg, dq, dk, dv, ws, scale=0.0, stream=None):
+    """pa_bwd on strided (B, H, N, D) views: out, dout and dq share q's
+    strides; v, dk and dv share k's. seg None = plain causal."""
+    import torch
+    bf = torch.bfloat16
+    d = _dims_of(q, k, scale)
+    st = _strides_of(q, k)
+    _check(lib().pa_bwd_strided(ctypes.byref(d), ctypes.byref(st), _ptr_rows(q, bf, "q"), _ptr_rows(k, bf, "k"),
+                                _ptr_rows(v, bf, "v", k), _ptr_rows(out, bf, "out", q),
+                                _ptr_rows(dout, bf, "dout", q), _ptr(lse, torch.float32, "lse"),
+                                _ptr(seg, torch.int32, "seg"), _ptr_rows(dq, bf, "dq", q), _ptr_rows(dk, bf, "dk", k),
+                                _ptr_rows(dv, bf, "dv", k), _ptr(ws, None, "ws"), ws.numel(), _stream(stream)))
 
 
 def pa_fwd(q, k, v, seg, out, lse, ws, scale=0.0, stream=None):
@@ -301,12 +366,22 @@ def pa_status_string(code: int) -> str:
 
 
 # ---------------------------------------------------------------- conveniences
+def _all_contiguous(*ts):
+    return all(t.is_contiguous() for t in ts)
+
+
 def forward(q, k, v, seg=None, scale=0.0, ws=None):
-    """Allocate out/lse and run pa_fwd (seg given) or pa_fwd_causal (seg None)."""
+    """Allocate out/lse and run pa_fwd (seg given) or pa_fwd_causal (seg None);
+    strided q/k/v go through pa_fwd_strided (out then takes q's strides)."""
     import torch
     B, Hq, N, D = q.shape
-    out = torch.empty_like(q)
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    if not _all_contiguous(q, k, v):
+        out = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
+        ws = workspace(q, k, strided=True) if ws is None else ws
+        pa_fwd_strided(q, k, v, seg, out, lse, ws, scale)
+        return out, lse
+    out = torch.empty_like(q)
     ws = workspace(q, k) if ws is None else ws
     if seg is None:
         pa_fwd_causal(q, k, v, out, lse, ws, scale)
@@ -316,8 +391,16 @@ def forward(q, k, v, seg=None, scale=0.0, ws=None):
 
 
 def backward(q, k, v, out, dout, lse, seg=None, scale=0.0, ws=None):
-    """Allocate dq/dk/dv and run pa_bwd (seg given) or pa_bwd_causal (seg None)."""
+    """Allocate dq/dk/dv and run pa_bwd (seg given) or pa_bwd_causal (seg None);
+    strided tensors go through pa_bwd_strided (dq takes q's strides, dk/dv k's)."""
     import torch
+    if not _all_contiguous(q, k, v, out, dout):
+        dq = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
+        dk = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device)
+        dv = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device)
+        ws = workspace(q, k, strided=True) if ws is None else ws
+        pa_bwd_strided(q, k, v, out, dout, lse, seg, dq, dk, dv, ws, scale)
+        return dq, dk, dv
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = workspace(q, k) if ws is None else ws
     if seg is None:

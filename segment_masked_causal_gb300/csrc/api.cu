@@ -19,33 +19,54 @@ namespace {
 constexpr size_t kAlign = 256;
 inline size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+// Tokens per row as the kernels see them: N rounded up to whole tiles.
+inline int padded_n(const pa_dims* d) { return (d->N + pa::kTile - 1) / pa::kTile * pa::kTile; }
+inline bool tiled(const pa_dims* d) { return d->N % pa::kTile == 0; }
+
+// The kernels' part (status word, tile table, delta, lse * log2 e) sized for
+// padded_n, then the staging copies used when the caller's tensors are not in
+// the kernels' layout (N not a multiple of 128, or strided tensors).
 struct WsLayout {
-  size_t status, tiles, delta, lse2, total;
+  size_t status, tiles, delta, lse2, base;
+  size_t sq, sk, sv, so, sdo, sdq, sdk, sdv, slse, sseg, staged;
 };
 
 bool dims_ok(const pa_dims* d, pa_status* why) {
   if (!d) { *why = PA_ERR_NULL; return false; }
-  if (d->B <= 0 || d->Hq <= 0 || d->Hkv <= 0 || d->N <= 0 || (d->N % pa::kTile) != 0) {
-    *why = PA_ERR_SHAPE;
-    return false;
-  }
+  if (d->B <= 0 || d->Hq <= 0 || d->Hkv <= 0 || d->N <= 0) { *why = PA_ERR_SHAPE; return false; }
   if (d->D != 64 && d->D != 96 && d->D != 128) { *why = PA_ERR_HEAD_DIM; return false; }
   if (d->Hq % d->Hkv != 0) { *why = PA_ERR_GQA; return false; }
   // tensor-map row coordinates and tile counts are 32-bit
-  const int64_t rows = (int64_t)d->B * d->Hq * d->N;
-  if (rows >= (int64_t(1) << 31) || (int64_t)d->N / pa::kTile > 65535 * 2) { *why = PA_ERR_SHAPE; return false; }
+  const int64_t rows = (int64_t)d->B * d->Hq * padded_n(d);
+  if (d->N > (1 << 30) || rows >= (int64_t(1) << 31) || (int64_t)padded_n(d) / pa::kTile > 65535 * 2) {
+    *why = PA_ERR_SHAPE;
+    return false;
+  }
   if (!(std::isfinite(d->scale))) { *why = PA_ERR_SHAPE; return false; }
   return true;
 }
 
 WsLayout ws_layout(const pa_dims* d) {
   WsLayout w;
-  const size_t T = (size_t)d->N / pa::kTile;
+  const size_t Np = (size_t)padded_n(d), T = Np / pa::kTile;
+  const size_t qrows = (size_t)d->B * d->Hq * Np, krows = (size_t)d->B * d->Hkv * Np;
+  const size_t qb = round_up(qrows * d->D * 2), kb = round_up(krows * d->D * 2);
   w.status = 0;
   w.tiles = kAlign;
   w.delta = w.tiles + round_up((size_t)d->B * T * sizeof(int4));
-  w.lse2 = w.delta + round_up((size_t)d->B * d->Hq * d->N * sizeof(float));
-  w.total = w.lse2 + round_up((size_t)d->B * d->Hq * d->N * sizeof(float));
+  w.lse2 = w.delta + round_up(qrows * sizeof(float));
+  w.base = w.lse2 + round_up(qrows * sizeof(float));
+  w.sq = w.base;
+  w.so = w.sq + qb;
+  w.sdo = w.so + qb;
+  w.sdq = w.sdo + qb;
+  w.sk = w.sdq + qb;
+  w.sv = w.sk + kb;
+  w.sdk = w.sv + kb;
+  w.sdv = w.sdk + kb;
+  w.slse = w.sdv + kb;
+  w.sseg = w.slse + round_up(qrows * sizeof(float));
+  w.staged = w.sseg + round_up((size_t)d->B * Np * sizeof(int32_t));
   return w;
 }
 
@@ -85,12 +106,15 @@ pa::AttnParams make_params(const pa_dims* d, const int32_t* seg, void* ws) {
   return p;
 }
 
+// The kernels run on the caller's tensors directly only when N is a whole
+// number of tiles; the single-step calls require that.
 pa_status common_checks(const pa_dims* d, void* ws, size_t ws_bytes) {
   pa_status why = PA_OK;
   if (!dims_ok(d, &why)) return why;
+  if (!tiled(d)) return PA_ERR_SHAPE;
   if (!ws) return PA_ERR_NULL;
   if (!aligned16(ws)) return PA_ERR_ALIGN;
-  if (ws_bytes < ws_layout(d).total) return PA_ERR_WORKSPACE;
+  if (ws_bytes < ws_layout(d).base) return PA_ERR_WORKSPACE;
   return PA_OK;
 }
 
@@ -179,6 +203,138 @@ pa_status bwd_impl(const pa_dims* d, const void* q, const void* k, const void* v
   return step_dkv(d, q, k, v, dout, lse, seg, dk, dv, ws, ws_bytes, stream);
 }
 
+// ------------------------------------------------------------ staged calls
+// Element strides of the q group (q, out, dout, dq) and the k group (k, v,
+// dk, dv); D is contiguous.
+pa_strides contiguous_strides(const pa_dims* d) {
+  pa_strides s;
+  s.q_n = s.k_n = d->D;
+  s.q_h = s.k_h = (int64_t)d->N * d->D;
+  s.q_b = (int64_t)d->Hq * d->N * d->D;
+  s.k_b = (int64_t)d->Hkv * d->N * d->D;
+  return s;
+}
+
+bool same_strides(const pa_strides& a, const pa_strides& b) {
+  return a.q_b == b.q_b && a.q_h == b.q_h && a.q_n == b.q_n && a.k_b == b.k_b && a.k_h == b.k_h && a.k_n == b.k_n;
+}
+
+pa_status strides_ok(const pa_dims* d, const pa_strides* s) {
+  if (!s) return PA_ERR_NULL;
+  for (int64_t x : {s->q_b, s->q_h, s->q_n, s->k_b, s->k_h, s->k_n})
+    if (x < d->D) return PA_ERR_SHAPE;
+  for (int64_t x : {s->q_b, s->q_h, s->q_n, s->k_b, s->k_h, s->k_n})
+    if (x % 8 != 0) return PA_ERR_ALIGN;
+  return PA_OK;
+}
+
+// Validation of a staged call: dims (any N), strides, the staged workspace,
+// the pointers, the device.
+pa_status check_staged(const pa_dims* d, const pa_strides* s, void* ws, size_t ws_bytes,
+                       std::initializer_list<const void*> required, const int32_t* seg) {
+  pa_status why = PA_OK;
+  if (!dims_ok(d, &why)) return why;
+  if ((why = strides_ok(d, s)) != PA_OK) return why;
+  if (!ws) return PA_ERR_NULL;
+  if (!aligned16(ws)) return PA_ERR_ALIGN;
+  if (ws_bytes < ws_layout(d).staged) return PA_ERR_WORKSPACE;
+  for (const void* x : required)
+    if (!x) return PA_ERR_NULL;
+  for (const void* x : required)
+    if (!aligned16(x)) return PA_ERR_ALIGN;
+  if (seg && !aligned16(seg)) return PA_ERR_ALIGN;
+  return device_ok();
+}
+
+struct Staging {
+  pa_dims dp;  // the kernels' dims: N padded to whole tiles
+  pa::RowsView vq, vk;
+  uint8_t* w;
+  WsLayout L;
+  Staging(const pa_dims* d, const pa_strides* s, void* ws) : dp(*d), w(static_cast<uint8_t*>(ws)), L(ws_layout(d)) {
+    dp.N = padded_n(d);
+    vq = pa::RowsView{d->B, d->Hq, d->N, dp.N, d->D / 8, s->q_b, s->q_h, s->q_n};
+    vk = pa::RowsView{d->B, d->Hkv, d->N, dp.N, d->D / 8, s->k_b, s->k_h, s->k_n};
+  }
+  void* at(size_t off) const { return w + off; }
+};
+
+pa_status fwd_staged(const pa_dims* d, const pa_strides* s, const void* q, const void* k, const void* v,
+                     const int32_t* seg, void* out, float* lse, void* ws, size_t ws_bytes, pa_stream_t stream) {
+  pa_status st = check_staged(d, s, ws, ws_bytes, {q, k, v, out, lse}, seg);
+  if (st != PA_OK) return st;
+  const Staging g(d, s, ws);
+  const cudaStream_t cs = cu(stream);
+  const uint64_t qr = (uint64_t)d->B * d->Hq;
+  if (pa::launch_stage_rows_in(g.at(g.L.sq), q, g.vq, cs) != cudaSuccess ||
+      pa::launch_stage_rows_in(g.at(g.L.sk), k, g.vk, cs) != cudaSuccess ||
+      pa::launch_stage_rows_in(g.at(g.L.sv), v, g.vk, cs) != cudaSuccess ||
+      (seg && pa::launch_stage_words_in(g.at(g.L.sseg), seg, (uint64_t)d->B, d->N, g.dp.N, true, cs) != cudaSuccess))
+    return PA_ERR_CUDA;
+  const int32_t* sseg = seg ? static_cast<const int32_t*>(g.at(g.L.sseg)) : nullptr;
+  st = fwd_impl(&g.dp, g.at(g.L.sq), g.at(g.L.sk), g.at(g.L.sv), sseg, g.at(g.L.so),
+                static_cast<float*>(g.at(g.L.slse)), ws, ws_bytes, stream);
+  if (st != PA_OK) return st;
+  if (pa::launch_stage_rows_out(out, g.at(g.L.so), g.vq, cs) != cudaSuccess ||
+      pa::launch_stage_words_out(lse, g.at(g.L.slse), qr, d->N, g.dp.N, cs) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+pa_status bwd_staged(const pa_dims* d, const pa_strides* s, const void* q, const void* k, const void* v,
+                     const void* out, const void* dout, const float* lse, const int32_t* seg, void* dq, void* dk,
+                     void* dv, void* ws, size_t ws_bytes, pa_stream_t stream) {
+  pa_status st = check_staged(d, s, ws, ws_bytes, {q, k, v, out, dout, lse, dq, dk, dv}, seg);
+  if (st != PA_OK) return st;
+  const Staging g(d, s, ws);
+  const cudaStream_t cs = cu(stream);
+  const uint64_t qr = (uint64_t)d->B * d->Hq;
+  if (pa::launch_stage_rows_in(g.at(g.L.sq), q, g.vq, cs) != cudaSuccess ||
+      pa::launch_stage_rows_in(g.at(g.L.sk), k, g.vk, cs) != cudaSuccess ||
+      pa::launch_stage_rows_in(g.at(g.L.sv), v, g.vk, cs) != cudaSuccess ||
+      pa::launch_stage_rows_in(g.at(g.L.so), out, g.vq, cs) != cudaSuccess ||
+      pa::launch_stage_rows_in(g.at(g.L.sdo), dout, g.vq, cs) != cudaSuccess ||
+      pa::launch_stage_words_in(g.at(g.L.slse), lse, qr, d->N, g.dp.N, false, cs) != cudaSuccess ||
+      (seg && pa::launch_stage_words_in(g.at(g.L.sseg), seg, (uint64_t)d->B, d->N, g.dp.N, true, cs) != cudaSuccess))
+    return PA_ERR_CUDA;
+  const int32_t* sseg = seg ? static_cast<const int32_t*>(g.at(g.L.sseg)) : nullptr;
+  st = bwd_impl(&g.dp, g.at(g.L.sq), g.at(g.L.sk), g.at(g.L.sv), g.at(g.L.so), g.at(g.L.sdo),
+                static_cast<const float*>(g.at(g.L.slse)), sseg, g.at(g.L.sdq), g.at(g.L.sdk), g.at(g.L.sdv), ws,
+                ws_bytes, stream);
+  if (st != PA_OK) return st;
+  if (pa::launch_stage_rows_out(dq, g.at(g.L.sdq), g.vq, cs) != cudaSuccess ||
+      pa::launch_stage_rows_out(dk, g.at(g.L.sdk), g.vk, cs) != cudaSuccess ||
+      pa::launch_stage_rows_out(dv, g.at(g.L.sdv), g.vk, cs) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+// The public forward and backward: the kernels run on the caller's tensors
+// when they are contiguous and N is whole tiles, else through the staging
+// copies.
+pa_status fwd_any(const pa_dims* d, const pa_strides* s, const void* q, const void* k, const void* v,
+                  const int32_t* seg, void* out, float* lse, void* ws, size_t ws_bytes, pa_stream_t stream) {
+  pa_status why = PA_OK;
+  if (!dims_ok(d, &why)) return why;
+  if (s && (why = strides_ok(d, s)) != PA_OK) return why;
+  if (tiled(d) && (!s || same_strides(*s, contiguous_strides(d))))
+    return fwd_impl(d, q, k, v, seg, out, lse, ws, ws_bytes, stream);
+  const pa_strides c = contiguous_strides(d);
+  return fwd_staged(d, s ? s : &c, q, k, v, seg, out, lse, ws, ws_bytes, stream);
+}
+
+pa_status bwd_any(const pa_dims* d, const pa_strides* s, const void* q, const void* k, const void* v,
+                  const void* out, const void* dout, const float* lse, const int32_t* seg, void* dq, void* dk,
+                  void* dv, void* ws, size_t ws_bytes, pa_stream_t stream) {
+  pa_status why = PA_OK;
+  if (!dims_ok(d, &why)) return why;
+  if (s && (why = strides_ok(d, s)) != PA_OK) return why;
+  if (tiled(d) && (!s || same_strides(*s, contiguous_strides(d))))
+    return bwd_impl(d, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream);
+  const pa_strides c = contiguous_strides(d);
+  return bwd_staged(d, s ? s : &c, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -186,31 +342,52 @@ extern "C" {
 size_t pa_workspace_bytes(const pa_dims* dims) {
   pa_status why;
   if (!dims_ok(dims, &why)) return 0;
-  return ws_layout(dims).total;
+  const WsLayout w = ws_layout(dims);
+  return tiled(dims) ? w.base : w.staged;
+}
+
+size_t pa_workspace_bytes_strided(const pa_dims* dims) {
+  pa_status why;
+  if (!dims_ok(dims, &why)) return 0;
+  return ws_layout(dims).staged;
+}
+
+pa_status pa_fwd_strided(const pa_dims* dims, const pa_strides* strides, const void* q, const void* k,
+                         const void* v, const int32_t* seg, void* out, float* lse, void* ws, size_t ws_bytes,
+                         pa_stream_t stream) {
+  if (!strides) return PA_ERR_NULL;
+  return fwd_any(dims, strides, q, k, v, seg, out, lse, ws, ws_bytes, stream);
+}
+
+pa_status pa_bwd_strided(const pa_dims* dims, const pa_strides* strides, const void* q, const void* k,
+                         const void* v, const void* out, const void* dout, const float* lse, const int32_t* seg,
+                         void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, pa_stream_t stream) {
+  if (!strides) return PA_ERR_NULL;
+  return bwd_any(dims, strides, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream);
 }
 
 pa_status pa_fwd(const pa_dims* dims, const void* q, const void* k, const void* v, const int32_t* seg, void* out,
                  float* lse, void* ws, size_t ws_bytes, pa_stream_t stream) {
   if (!seg) return PA_ERR_NULL;
-  return fwd_impl(dims, q, k, v, seg, out, lse, ws, ws_bytes, stream);
+  return fwd_any(dims, nullptr, q, k, v, seg, out, lse, ws, ws_bytes, stream);
 }
 
 pa_status pa_fwd_causal(const pa_dims* dims, const void* q, const void* k, const void* v, void* out, float* lse,
                         void* ws, size_t ws_bytes, pa_stream_t stream) {
-  return fwd_impl(dims, q, k, v, nullptr, out, lse, ws, ws_bytes, stream);
+  return fwd_any(dims, nullptr, q, k, v, nullptr, out, lse, ws, ws_bytes, stream);
 }
 
 pa_status pa_bwd(const pa_dims* dims, const void* q, const void* k, const void* v, const void* out,
                  const void* dout, const float* lse, const int32_t* seg, void* dq, void* dk, void* dv, void* ws,
                  size_t ws_bytes, pa_stream_t stream) {
   if (!seg) return PA_ERR_NULL;
-  return bwd_impl(dims, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream);
+  return bwd_any(dims, nullptr, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream);
 }
 
 pa_status pa_bwd_causal(const pa_dims* dims, const void* q, const void* k, const void* v, const void* out,
                         const void* dout, const float* lse, void* dq, void* dk, void* dv, void* ws,
                         size_t ws_bytes, pa_stream_t stream) {
-  return bwd_impl(dims, q, k, v, out, dout, lse, nullptr, dq, dk, dv, ws, ws_bytes, stream);
+  return bwd_any(dims, nullptr, q, k, v, out, dout, lse, nullptr, dq, dk, dv, ws, ws_bytes, stream);
 }
 
 pa_status pa_build_tile_table(const pa_dims* dims, const int32_t* seg, void* ws, size_t ws_bytes,
@@ -270,7 +447,9 @@ const char* pa_status_string(pa_status s) {
     case PA_ERR_NULL: return "a required pointer is NULL";
     case PA_ERR_HEAD_DIM: return "head dim must be 64, 96 or 128";
     case PA_ERR_GQA: return "Hq must be a multiple of Hkv";
-    case PA_ERR_SHAPE: return "bad shape (B, H, N > 0; N % 128 == 0; B*Hq*N < 2^31; finite scale)";
+    case PA_ERR_SHAPE:
+      return "bad shape (B, H, N > 0; B*Hq*N < 2^31; finite scale; N % 128 == 0 for the single-step calls; "
+             "strides >= D)";
     case PA_ERR_ALIGN: return "a pointer is not 16-byte aligned";
     case PA_ERR_WORKSPACE: return "workspace too small (see pa_workspace_bytes)";
     case PA_ERR_ARCH: return "device is not compute capability 10.3 (GB300)";

@@ -60,7 +60,7 @@ def test_workspace_bytes(L):
 @pytest.mark.parametrize("dims,code", [
     (dict(D=80), 2), (dict(D=32), 2), (dict(D=256), 2),
     (dict(Hq=6, Hkv=4), 3),
-    (dict(N=200), 4), (dict(N=0), 4), (dict(B=0), 4), (dict(Hq=0), 4), (dict(Hkv=0), 4),
+    (dict(N=0), 4), (dict(B=0), 4), (dict(Hq=0), 4), (dict(Hkv=0), 4),
     (dict(B=1024, Hq=64, N=65536), 4),  # row coordinates overflow int32
 ])
 def test_shape_refusals(L, dims, code):
@@ -84,6 +84,62 @@ def test_null_and_alignment_refusals(L):
                            1 << 40, None) == 5
 
 
+def strides(q_b, q_h, q_n, k_b, k_h, k_n):
+    return pa.pa_strides(q_b, q_h, q_n, k_b, k_h, k_n)
+
+
+def test_ragged_n_and_strided_workspace(L):
+    """N not a multiple of 128 needs the staging copies: the workspace then
+    holds (B, H, Np, D) buffers for q, out, dout, dq (Hq heads) and k, v, dk,
+    dv (Hkv heads), plus lse and seg, with Np = N rounded up to 128."""
+    base = L.pa_workspace_bytes(ctypes.byref(d(N=256)))
+    ragged = L.pa_workspace_bytes(ctypes.byref(d(N=200)))
+    assert ragged == L.pa_workspace_bytes_strided(ctypes.byref(d(N=200)))
+    assert ragged == L.pa_workspace_bytes_strided(ctypes.byref(d(N=256)))
+    B, Hq, Hkv, Np, D = 1, 4, 2, 256, 128
+    assert ragged >= base + 4 * B * Hq * Np * D * 2 + 4 * B * Hkv * Np * D * 2 + 4 * B * Hq * Np + 4 * B * Np
+    assert L.pa_workspace_bytes(ctypes.byref(d(N=1))) > 0
+
+
+def test_ragged_n_refusals(L):
+    """The single-step calls need whole tiles; the full calls take any N and
+    then need the staged workspace."""
+    dims = d(N=200)
+    assert L.pa_fwd_tiles(ctypes.byref(dims), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == 4
+    assert L.pa_build_tile_table(ctypes.byref(dims), FAKE, FAKE, 1 << 40, None) == 4
+    assert L.pa_bwd_delta(ctypes.byref(dims), FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == 4
+    assert L.pa_bwd_dq(ctypes.byref(dims), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == 4
+    assert L.pa_bwd_dkv(ctypes.byref(dims), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40,
+                        None) == 4
+    base = L.pa_workspace_bytes(ctypes.byref(d(N=256)))
+    assert fwd(L, dims, ws_bytes=base) == 6
+    assert fwd(L, dims, q=None) == 1
+
+
+def test_strided_refusals(L):
+    dims = d()
+    good = strides(2 * 256 * 128 * 4, 128, 4 * 128, 256 * 2 * 128, 128, 2 * 128)  # (B, N, H, D) memory
+    big = L.pa_workspace_bytes_strided(ctypes.byref(dims))
+
+    def f(st, ws_bytes=big, seg=FAKE, q=FAKE):
+        return L.pa_fwd_strided(ctypes.byref(dims), None if st is None else ctypes.byref(st), q, FAKE, FAKE, seg,
+                                FAKE, FAKE, FAKE, ws_bytes, None)
+    assert f(None) == 1
+    assert f(strides(1 << 20, 128, 64, 1 << 20, 128, 256)) == 4  # q_n < D
+    assert f(strides(1 << 20, 128, 132, 1 << 20, 128, 256)) == 5  # not a multiple of 8
+    assert f(good, ws_bytes=big - 1) == 6
+    assert f(good, q=None) == 1
+    assert f(good, seg=FAKE + 4) == 5
+    # contiguous strides with whole tiles need only the plain workspace
+    cont = strides(4 * 256 * 128, 256 * 128, 128, 2 * 256 * 128, 256 * 128, 128)
+    plain = L.pa_workspace_bytes(ctypes.byref(dims))
+    assert f(cont, ws_bytes=plain - 1) == 6
+    assert L.pa_bwd_strided(ctypes.byref(dims), None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                            FAKE, big, None) == 1
+    assert L.pa_bwd_strided(ctypes.byref(dims), ctypes.byref(good), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                            FAKE + 8, FAKE, FAKE, FAKE, big, None) == 5
+
+
 def test_selftest_refusals(L):
     """The bounded-wait self-test checks its workspace before any device call."""
     assert L.pa_selftest_wait_timeout(None, 1 << 20, None) == 1
@@ -96,6 +152,7 @@ def test_valid_call_without_a_gpu_is_refused_not_run(L):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert fwd(L, d()) in (7, 8)  # no device: arch / CUDA error, nothing launched
+    assert fwd(L, d(N=200)) in (7, 8)  # ragged N passes the host checks, then the same
     assert L.pa_selftest_wait_timeout(FAKE, 1 << 20, None) in (7, 8)
 
 

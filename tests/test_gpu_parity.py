@@ -44,6 +44,12 @@ SMALL = [
     # loads fill with zeros and the stores leave out
     ("ragged_gqa_d96", synth.custom(2, 4, 2, 512, 96, [[1, 130, 5, 120, 256], [512]], seed=29)),
     ("len1_runs_g3_d96", synth.custom(1, 3, 1, 384, 96, [[1] * 30 + [3] * 20 + [294]], seed=30)),
+    # N not a multiple of 128: staged through whole tiles inside the workspace
+    ("ragged_n200_d64", synth.custom(1, 2, 2, 200, 64, [[1, 100, 99]], seed=31)),
+    ("ragged_n300_gqa_d128", synth.custom(2, 4, 2, 300, 128, [[150, 150], [1, 298, 1]], seed=32)),
+    ("ragged_n129_d96", synth.custom(1, 3, 1, 129, 96, [[129]], seed=33)),
+    ("ragged_n1_d64", synth.custom(1, 2, 1, 1, 64, [[1]], seed=34)),
+    ("ragged_n127_d128", synth.custom(1, 2, 1, 127, 128, [[60, 67]], seed=35)),
 ]
 
 
@@ -57,6 +63,45 @@ def test_causal_entry_points_full_parity(cuda_dev):
     w = synth.custom(1, 4, 1, 384, 128, [[384]], seed=25)
     c = Case(w, cuda_dev)
     print(assert_full_parity(c.run(causal=True), c.oracle_full(causal=True), "causal"))
+
+
+def test_causal_ragged_n_full_parity(cuda_dev):
+    w = synth.custom(1, 4, 2, 333, 64, [[333]], seed=36)
+    c = Case(w, cuda_dev)
+    print(assert_full_parity(c.run(causal=True), c.oracle_full(causal=True), "causal ragged"))
+
+
+STRIDED = [
+    ("bnhd_gqa_d128", synth.custom(2, 4, 2, 512, 128, [[1, 130, 5, 120, 256], [512]], seed=37)),
+    ("bnhd_ragged_n300_d64", synth.custom(1, 4, 1, 300, 64, [[100, 200]], seed=38)),
+    ("bnhd_ragged_n200_d96", synth.custom(2, 2, 2, 200, 96, [[200], [7, 193]], seed=39)),
+]
+
+
+@pytest.mark.parametrize("name,w", STRIDED, ids=[n for n, _ in STRIDED])
+def test_strided_bnhd_full_parity(name, w, cuda_dev):
+    """(B, N, H, D) memory through the strided entry points: oracle parity,
+    and bit-identical to the contiguous call on the same values."""
+    c = Case(w, cuda_dev)
+    g = c.run_strided()
+    print(assert_full_parity(g, c.oracle_full(), name))
+    ref = c.run()
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        assert torch.equal(g[n], ref[n]), n
+
+
+def test_strided_bnhd_causal(cuda_dev):
+    w = synth.custom(1, 4, 2, 256, 128, [[256]], seed=40)
+    c = Case(w, cuda_dev)
+    print(assert_full_parity(c.run_strided(causal=True), c.oracle_full(causal=True), "bnhd causal"))
+
+
+def test_ragged_n_5000_sampled(cuda_dev):
+    w = synth.custom(1, 16, 4, 5000, 128, [[1000, 2999, 1, 1000]], seed=41)
+    c = Case(w, cuda_dev)
+    g = c.run()
+    print(assert_sampled_parity(c, g, tag="ragged_5000"))
+    assert_segment_sums(c, g)
 
 
 def test_non_contiguous_ids_full_parity(cuda_dev):

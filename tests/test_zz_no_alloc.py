@@ -39,9 +39,14 @@ def _rel(a, b):
     return float((a - b).norm() / b.norm())
 
 
-@pytest.mark.parametrize("name,causal", [("packed_4x4096_short", False), ("causal_2k_gqa", True)])
+RAGGED = synth.custom(2, 4, 2, 300, 128, [[150, 150], [1, 298, 1]], seed=32)
+
+
+@pytest.mark.parametrize("name,causal", [("packed_4x4096_short", False), ("causal_2k_gqa", True),
+                                         ("ragged_n300", False)])
 def test_noalloc_matches_workspace_backward_twice(name, causal, cuda_dev):
-    w = synth.workload(name)
+    """N = 300 goes through the staging copies, which fit in the scratch."""
+    w = RAGGED if name == "ragged_n300" else synth.workload(name)
     q, k, v, do, seg = _inputs(w, cuda_dev)
     seg_arg = None if causal else seg
     out, lse = pa.forward(q, k, v, seg_arg)
@@ -70,6 +75,6 @@ def test_noalloc_refuses_dims_beyond_its_scratch(cuda_dev):
     fake = 0x100000
     rc = L.pa_bwd_noalloc(ctypes.byref(big), fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, None, None)
     assert rc == 6  # PA_ERR_WORKSPACE, refused before anything touches the device
-    bad = pa.make_dims(1, 4, 2, 200, 128)
+    bad = pa.make_dims(1, 4, 2, 256, 80)
     assert L.pa_bwd_noalloc(ctypes.byref(bad), fake, fake, fake, fake, fake, fake, fake, fake, fake, fake,
-                            None, None) == 4  # PA_ERR_SHAPE, from the same checks as pa_bwd
+                            None, None) == 2  # PA_ERR_HEAD_DIM, from the same checks as pa_bwd
