@@ -76,7 +76,8 @@ typedef enum {
   PA_ERR_ALIGN = 5,     /* a pointer is not 16-byte aligned                    */
   PA_ERR_WORKSPACE = 6, /* ws_bytes < pa_workspace_bytes(dims)                 */
   PA_ERR_ARCH = 7,      /* current device is not compute capability 10.3       */
-  PA_ERR_CUDA = 8       /* a CUDA runtime / driver call or launch failed       */
+  PA_ERR_CUDA = 8,      /* a CUDA runtime / driver call or launch failed       */
+  PA_ERR_DTYPE = 9      /* io_dtype is not a pa_io_dtype                       */
 } pa_status;
 
 /* Device status bits (pa_device_status). */
@@ -130,11 +131,18 @@ pa_status pa_bwd_causal(const pa_dims* dims, const void* q, const void* k, const
  * causal), for tensors whose element (b, h, n, c) sits at element offset
  * b*x_b + h*x_h + n*x_n + c: q, out, dout and dq use the q_* strides; k, v,
  * dk and dv the k_* strides. lse stays contiguous (B, Hq, N) fp32 and seg
- * (B, N) int32. Every stride must be >= D and a multiple of 8 elements;
- * distinct (b, h, n) rows of an output must not overlap.
+ * (B, N) int32. Every stride must be >= D and a multiple of 16 bytes (8 bf16
+ * or 4 fp32 elements); distinct (b, h, n) rows of an output must not overlap.
+ *
+ * io_dtype is the element type of q, k, v, out, dout, dq, dk and dv
+ * (README, "If you maintain a trainer": the kernels take bf16 or fp32).
+ * PA_IO_F32 tensors are rounded to bf16 (nearest even) on the way in and the
+ * bf16 results widened exactly on the way out, so an fp32 call returns what
+ * the bf16 call returns on the rounded inputs: fp32 is an I/O format here,
+ * not a compute precision.
  *
  * How: when the strides are the contiguous ones and N % 128 == 0 the kernels
- * run on the tensors directly (workspace: pa_workspace_bytes). Otherwise the
+ * run on bf16 tensors directly (workspace: pa_workspace_bytes). Otherwise the
  * call copies its inputs into (B, H, Np, D) buffers inside the workspace,
  * with Np = N rounded up to 128 and zero rows after N, runs the kernels there
  * and copies the results out (workspace: pa_workspace_bytes_strided). The
@@ -143,20 +151,22 @@ pa_status pa_bwd_causal(const pa_dims* dims, const void* q, const void* k, const
  * copies are memory-bound kernels on the same stream; pa_fwd / pa_bwd and
  * the causal variants take the same path when N % 128 != 0.
  * Errors: as pa_fwd / pa_bwd, plus PA_ERR_NULL (strides), PA_ERR_SHAPE (a
- * stride < D), PA_ERR_ALIGN (a stride not a multiple of 8).
+ * stride < D), PA_ERR_ALIGN (a stride not a 16-byte multiple), PA_ERR_DTYPE.
  */
+typedef enum { PA_IO_BF16 = 0, PA_IO_F32 = 1 } pa_io_dtype;
 typedef struct {
   int64_t q_b, q_h, q_n; /* element strides of q, out, dout, dq */
   int64_t k_b, k_h, k_n; /* element strides of k, v, dk, dv     */
 } pa_strides;
 
 size_t pa_workspace_bytes_strided(const pa_dims* dims);
-pa_status pa_fwd_strided(const pa_dims* dims, const pa_strides* strides, const void* q, const void* k,
-                         const void* v, const int32_t* seg, void* out, float* lse, void* ws, size_t ws_bytes,
+pa_status pa_fwd_strided(const pa_dims* dims, const pa_strides* strides, int32_t io_dtype, const void* q,
+                         const void* k, const void* v, const int32_t* seg, void* out, float* lse, void* ws,
+                         size_t ws_bytes, pa_stream_t stream);
+pa_status pa_bwd_strided(const pa_dims* dims, const pa_strides* strides, int32_t io_dtype, const void* q,
+                         const void* k, const void* v, const void* out, const void* dout, const float* lse,
+                         const int32_t* seg, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
                          pa_stream_t stream);
-pa_status pa_bwd_strided(const pa_dims* dims, const pa_strides* strides, const void* q, const void* k,
-                         const void* v, const void* out, const void* dout, const float* lse, const int32_t* seg,
-                         void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, pa_stream_t stream);
 
 /*
  * The steps of the path, one kernel each, for callers that schedule or time

@@ -26,7 +26,8 @@ LIB_PATH = os.path.join(HERE, "libpa.so")
 
 PA_OK = 0
 STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_NULL", 2: "PA_ERR_HEAD_DIM", 3: "PA_ERR_GQA", 4: "PA_ERR_SHAPE",
-                5: "PA_ERR_ALIGN", 6: "PA_ERR_WORKSPACE", 7: "PA_ERR_ARCH", 8: "PA_ERR_CUDA"}
+                5: "PA_ERR_ALIGN", 6: "PA_ERR_WORKSPACE", 7: "PA_ERR_ARCH", 8: "PA_ERR_CUDA", 9: "PA_ERR_DTYPE"}
+PA_IO_BF16, PA_IO_F32 = 0, 1
 EXPORTS = ["pa_workspace_bytes", "pa_fwd", "pa_bwd", "pa_fwd_causal", "pa_bwd_causal", "pa_build_tile_table",
            "pa_fwd_tiles", "pa_bwd_delta", "pa_bwd_dq", "pa_bwd_dkv", "pa_bwd_noalloc", "pa_device_status",
            "pa_selftest_wait_timeout", "pa_pack_first_fit", "pa_workspace_bytes_strided", "pa_fwd_strided",
@@ -90,9 +91,9 @@ def lib():
             ST = ctypes.POINTER(pa_strides)
             L.pa_workspace_bytes_strided.argtypes = [D]
             L.pa_workspace_bytes_strided.restype = S
-            L.pa_fwd_strided.argtypes = [D, ST, P, P, P, P, P, P, P, S, P]
+            L.pa_fwd_strided.argtypes = [D, ST, ctypes.c_int32, P, P, P, P, P, P, P, S, P]
             L.pa_fwd_strided.restype = ctypes.c_int
-            L.pa_bwd_strided.argtypes = [D, ST, P, P, P, P, P, P, P, P, P, P, P, S, P]
+            L.pa_bwd_strided.argtypes = [D, ST, ctypes.c_int32, P, P, P, P, P, P, P, P, P, P, P, S, P]
             L.pa_bwd_strided.restype = ctypes.c_int
             I32, U64 = ctypes.c_int32, ctypes.c_uint64
             L.pa_pack_first_fit.argtypes = [P, P, I32, P, I32, I32, I32, U64, U64, P, P, P, P, P, P]
@@ -175,27 +176,38 @@ def _strides_of(q, k):
     return pa_strides(q.stride(0), q.stride(1), q.stride(2), k.stride(0), k.stride(1), k.stride(2))
 
 
+def _io_dtype(q):
+    import torch
+    if q.dtype == torch.bfloat16:
+        return q.dtype, PA_IO_BF16
+    if q.dtype == torch.float32:
+        return q.dtype, PA_IO_F32
+    raise ValueError(f"q must be bfloat16 or float32, got {q.dtype}")
+
+
 def pa_fwd_strided(q, k, v, seg, out, lse, ws, scale=0.0, stream=None):
     """pa_fwd on (B, H, N, D) views with any strides (e.g. (B, N, H, D) memory
-    transposed); seg None = plain causal. out must share q's strides."""
+    transposed), bf16 or fp32 (all tensors alike; fp32 is rounded to bf16 on
+    the way in); seg None = plain causal. out must share q's strides."""
     import torch
-    bf = torch.bfloat16
+    bf, io = _io_dtype(q)
     d = _dims_of(q, k, scale)
     st = _strides_of(q, k)
-    _check(lib().pa_fwd_strided(ctypes.byref(d), ctypes.byref(st), _ptr_rows(q, bf, "q"), _ptr_rows(k, bf, "k"),
+    _check(lib().pa_fwd_strided(ctypes.byref(d), ctypes.byref(st), io, _ptr_rows(q, bf, "q"), _ptr_rows(k, bf, "k"),
                                 _ptr_rows(v, bf, "v", k), _ptr(seg, torch.int32, "seg"),
                                 _ptr_rows(out, bf, "out", q), _ptr(lse, torch.float32, "lse"),
                                 _ptr(ws, None, "ws"), ws.numel(), _stream(stream)))
 
 
 def pa_bwd_strided(q, k, v, out, dout, lse, seg, dq, dk, dv, ws, scale=0.0, stream=None):
-    """pa_bwd on strided (B, H, N, D) views: out, dout and dq share q's
-    strides; v, dk and dv share k's. seg None = plain causal."""
+    """pa_bwd on strided (B, H, N, D) views, bf16 or fp32 (all alike): out,
+    dout and dq share q's strides; v, dk and dv share k's. seg None = plain
+    causal."""
     import torch
-    bf = torch.bfloat16
+    bf, io = _io_dtype(q)
     d = _dims_of(q, k, scale)
     st = _strides_of(q, k)
-    _check(lib().pa_bwd_strided(ctypes.byref(d), ctypes.byref(st), _ptr_rows(q, bf, "q"), _ptr_rows(k, bf, "k"),
+    _check(lib().pa_bwd_strided(ctypes.byref(d), ctypes.byref(st), io, _ptr_rows(q, bf, "q"), _ptr_rows(k, bf, "k"),
                                 _ptr_rows(v, bf, "v", k), _ptr_rows(out, bf, "out", q),
                                 _ptr_rows(dout, bf, "dout", q), _ptr(lse, torch.float32, "lse"),
                                 _ptr(seg, torch.int32, "seg"), _ptr_rows(dq, bf, "dq", q), _ptr_rows(dk, bf, "dk", k),
@@ -376,7 +388,7 @@ def forward(q, k, v, seg=None, scale=0.0, ws=None):
     import torch
     B, Hq, N, D = q.shape
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
-    if not _all_contiguous(q, k, v):
+    if not _all_contiguous(q, k, v) or q.dtype == torch.float32:
         out = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
         ws = workspace(q, k, strided=True) if ws is None else ws
         pa_fwd_strided(q, k, v, seg, out, lse, ws, scale)
@@ -394,7 +406,7 @@ def backward(q, k, v, out, dout, lse, seg=None, scale=0.0, ws=None):
     """Allocate dq/dk/dv and run pa_bwd (seg given) or pa_bwd_causal (seg None);
     strided tensors go through pa_bwd_strided (dq takes q's strides, dk/dv k's)."""
     import torch
-    if not _all_contiguous(q, k, v, out, dout):
+    if not _all_contiguous(q, k, v, out, dout) or q.dtype == torch.float32:
         dq = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
         dk = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device)
         dv = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device)

@@ -219,22 +219,23 @@ bool same_strides(const pa_strides& a, const pa_strides& b) {
   return a.q_b == b.q_b && a.q_h == b.q_h && a.q_n == b.q_n && a.k_b == b.k_b && a.k_h == b.k_h && a.k_n == b.k_n;
 }
 
-pa_status strides_ok(const pa_dims* d, const pa_strides* s) {
+// Strides of at least D elements that keep every row 16-byte aligned.
+pa_status strides_ok(const pa_dims* d, const pa_strides* s, bool f32) {
   if (!s) return PA_ERR_NULL;
   for (int64_t x : {s->q_b, s->q_h, s->q_n, s->k_b, s->k_h, s->k_n})
     if (x < d->D) return PA_ERR_SHAPE;
   for (int64_t x : {s->q_b, s->q_h, s->q_n, s->k_b, s->k_h, s->k_n})
-    if (x % 8 != 0) return PA_ERR_ALIGN;
+    if (x % (f32 ? 4 : 8) != 0) return PA_ERR_ALIGN;
   return PA_OK;
 }
 
 // Validation of a staged call: dims (any N), strides, the staged workspace,
 // the pointers, the device.
-pa_status check_staged(const pa_dims* d, const pa_strides* s, void* ws, size_t ws_bytes,
+pa_status check_staged(const pa_dims* d, const pa_strides* s, bool f32, void* ws, size_t ws_bytes,
                        std::initializer_list<const void*> required, const int32_t* seg) {
   pa_status why = PA_OK;
   if (!dims_ok(d, &why)) return why;
-  if ((why = strides_ok(d, s)) != PA_OK) return why;
+  if ((why = strides_ok(d, s, f32)) != PA_OK) return why;
   if (!ws) return PA_ERR_NULL;
   if (!aligned16(ws)) return PA_ERR_ALIGN;
   if (ws_bytes < ws_layout(d).staged) return PA_ERR_WORKSPACE;
@@ -259,41 +260,41 @@ struct Staging {
   void* at(size_t off) const { return w + off; }
 };
 
-pa_status fwd_staged(const pa_dims* d, const pa_strides* s, const void* q, const void* k, const void* v,
+pa_status fwd_staged(const pa_dims* d, const pa_strides* s, bool f32, const void* q, const void* k, const void* v,
                      const int32_t* seg, void* out, float* lse, void* ws, size_t ws_bytes, pa_stream_t stream) {
-  pa_status st = check_staged(d, s, ws, ws_bytes, {q, k, v, out, lse}, seg);
+  pa_status st = check_staged(d, s, f32, ws, ws_bytes, {q, k, v, out, lse}, seg);
   if (st != PA_OK) return st;
   const Staging g(d, s, ws);
   const cudaStream_t cs = cu(stream);
   const uint64_t qr = (uint64_t)d->B * d->Hq;
-  if (pa::launch_stage_rows_in(g.at(g.L.sq), q, g.vq, cs) != cudaSuccess ||
-      pa::launch_stage_rows_in(g.at(g.L.sk), k, g.vk, cs) != cudaSuccess ||
-      pa::launch_stage_rows_in(g.at(g.L.sv), v, g.vk, cs) != cudaSuccess ||
+  if (pa::launch_stage_rows_in(g.at(g.L.sq), q, g.vq, f32, cs) != cudaSuccess ||
+      pa::launch_stage_rows_in(g.at(g.L.sk), k, g.vk, f32, cs) != cudaSuccess ||
+      pa::launch_stage_rows_in(g.at(g.L.sv), v, g.vk, f32, cs) != cudaSuccess ||
       (seg && pa::launch_stage_words_in(g.at(g.L.sseg), seg, (uint64_t)d->B, d->N, g.dp.N, true, cs) != cudaSuccess))
     return PA_ERR_CUDA;
   const int32_t* sseg = seg ? static_cast<const int32_t*>(g.at(g.L.sseg)) : nullptr;
   st = fwd_impl(&g.dp, g.at(g.L.sq), g.at(g.L.sk), g.at(g.L.sv), sseg, g.at(g.L.so),
                 static_cast<float*>(g.at(g.L.slse)), ws, ws_bytes, stream);
   if (st != PA_OK) return st;
-  if (pa::launch_stage_rows_out(out, g.at(g.L.so), g.vq, cs) != cudaSuccess ||
+  if (pa::launch_stage_rows_out(out, g.at(g.L.so), g.vq, f32, cs) != cudaSuccess ||
       pa::launch_stage_words_out(lse, g.at(g.L.slse), qr, d->N, g.dp.N, cs) != cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
 }
 
-pa_status bwd_staged(const pa_dims* d, const pa_strides* s, const void* q, const void* k, const void* v,
+pa_status bwd_staged(const pa_dims* d, const pa_strides* s, bool f32, const void* q, const void* k, const void* v,
                      const void* out, const void* dout, const float* lse, const int32_t* seg, void* dq, void* dk,
                      void* dv, void* ws, size_t ws_bytes, pa_stream_t stream) {
-  pa_status st = check_staged(d, s, ws, ws_bytes, {q, k, v, out, dout, lse, dq, dk, dv}, seg);
+  pa_status st = check_staged(d, s, f32, ws, ws_bytes, {q, k, v, out, dout, lse, dq, dk, dv}, seg);
   if (st != PA_OK) return st;
   const Staging g(d, s, ws);
   const cudaStream_t cs = cu(stream);
   const uint64_t qr = (uint64_t)d->B * d->Hq;
-  if (pa::launch_stage_rows_in(g.at(g.L.sq), q, g.vq, cs) != cudaSuccess ||
-      pa::launch_stage_rows_in(g.at(g.L.sk), k, g.vk, cs) != cudaSuccess ||
-      pa::launch_stage_rows_in(g.at(g.L.sv), v, g.vk, cs) != cudaSuccess ||
-      pa::launch_stage_rows_in(g.at(g.L.so), out, g.vq, cs) != cudaSuccess ||
-      pa::launch_stage_rows_in(g.at(g.L.sdo), dout, g.vq, cs) != cudaSuccess ||
+  if (pa::launch_stage_rows_in(g.at(g.L.sq), q, g.vq, f32, cs) != cudaSuccess ||
+      pa::launch_stage_rows_in(g.at(g.L.sk), k, g.vk, f32, cs) != cudaSuccess ||
+      pa::launch_stage_rows_in(g.at(g.L.sv), v, g.vk, f32, cs) != cudaSuccess ||
+      pa::launch_stage_rows_in(g.at(g.L.so), out, g.vq, f32, cs) != cudaSuccess ||
+      pa::launch_stage_rows_in(g.at(g.L.sdo), dout, g.vq, f32, cs) != cudaSuccess ||
       pa::launch_stage_words_in(g.at(g.L.slse), lse, qr, d->N, g.dp.N, false, cs) != cudaSuccess ||
       (seg && pa::launch_stage_words_in(g.at(g.L.sseg), seg, (uint64_t)d->B, d->N, g.dp.N, true, cs) != cudaSuccess))
     return PA_ERR_CUDA;
@@ -302,37 +303,45 @@ pa_status bwd_staged(const pa_dims* d, const pa_strides* s, const void* q, const
                 static_cast<const float*>(g.at(g.L.slse)), sseg, g.at(g.L.sdq), g.at(g.L.sdk), g.at(g.L.sdv), ws,
                 ws_bytes, stream);
   if (st != PA_OK) return st;
-  if (pa::launch_stage_rows_out(dq, g.at(g.L.sdq), g.vq, cs) != cudaSuccess ||
-      pa::launch_stage_rows_out(dk, g.at(g.L.sdk), g.vk, cs) != cudaSuccess ||
-      pa::launch_stage_rows_out(dv, g.at(g.L.sdv), g.vk, cs) != cudaSuccess)
+  if (pa::launch_stage_rows_out(dq, g.at(g.L.sdq), g.vq, f32, cs) != cudaSuccess ||
+      pa::launch_stage_rows_out(dk, g.at(g.L.sdk), g.vk, f32, cs) != cudaSuccess ||
+      pa::launch_stage_rows_out(dv, g.at(g.L.sdv), g.vk, f32, cs) != cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
 }
 
 // The public forward and backward: the kernels run on the caller's tensors
-// when they are contiguous and N is whole tiles, else through the staging
-// copies.
-pa_status fwd_any(const pa_dims* d, const pa_strides* s, const void* q, const void* k, const void* v,
+// when they are contiguous bf16 and N is whole tiles, else through the
+// staging copies.
+pa_status io_ok(int32_t io_dtype) {
+  return (io_dtype == PA_IO_BF16 || io_dtype == PA_IO_F32) ? PA_OK : PA_ERR_DTYPE;
+}
+
+pa_status fwd_any(const pa_dims* d, const pa_strides* s, int32_t io, const void* q, const void* k, const void* v,
                   const int32_t* seg, void* out, float* lse, void* ws, size_t ws_bytes, pa_stream_t stream) {
   pa_status why = PA_OK;
   if (!dims_ok(d, &why)) return why;
-  if (s && (why = strides_ok(d, s)) != PA_OK) return why;
-  if (tiled(d) && (!s || same_strides(*s, contiguous_strides(d))))
+  if ((why = io_ok(io)) != PA_OK) return why;
+  const bool f32 = io == PA_IO_F32;
+  if (s && (why = strides_ok(d, s, f32)) != PA_OK) return why;
+  if (!f32 && tiled(d) && (!s || same_strides(*s, contiguous_strides(d))))
     return fwd_impl(d, q, k, v, seg, out, lse, ws, ws_bytes, stream);
   const pa_strides c = contiguous_strides(d);
-  return fwd_staged(d, s ? s : &c, q, k, v, seg, out, lse, ws, ws_bytes, stream);
+  return fwd_staged(d, s ? s : &c, f32, q, k, v, seg, out, lse, ws, ws_bytes, stream);
 }
 
-pa_status bwd_any(const pa_dims* d, const pa_strides* s, const void* q, const void* k, const void* v,
+pa_status bwd_any(const pa_dims* d, const pa_strides* s, int32_t io, const void* q, const void* k, const void* v,
                   const void* out, const void* dout, const float* lse, const int32_t* seg, void* dq, void* dk,
                   void* dv, void* ws, size_t ws_bytes, pa_stream_t stream) {
   pa_status why = PA_OK;
   if (!dims_ok(d, &why)) return why;
-  if (s && (why = strides_ok(d, s)) != PA_OK) return why;
-  if (tiled(d) && (!s || same_strides(*s, contiguous_strides(d))))
+  if ((why = io_ok(io)) != PA_OK) return why;
+  const bool f32 = io == PA_IO_F32;
+  if (s && (why = strides_ok(d, s, f32)) != PA_OK) return why;
+  if (!f32 && tiled(d) && (!s || same_strides(*s, contiguous_strides(d))))
     return bwd_impl(d, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream);
   const pa_strides c = contiguous_strides(d);
-  return bwd_staged(d, s ? s : &c, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream);
+  return bwd_staged(d, s ? s : &c, f32, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream);
 }
 
 }  // namespace
@@ -352,42 +361,43 @@ size_t pa_workspace_bytes_strided(const pa_dims* dims) {
   return ws_layout(dims).staged;
 }
 
-pa_status pa_fwd_strided(const pa_dims* dims, const pa_strides* strides, const void* q, const void* k,
-                         const void* v, const int32_t* seg, void* out, float* lse, void* ws, size_t ws_bytes,
-                         pa_stream_t stream) {
+pa_status pa_fwd_strided(const pa_dims* dims, const pa_strides* strides, int32_t io_dtype, const void* q,
+                         const void* k, const void* v, const int32_t* seg, void* out, float* lse, void* ws,
+                         size_t ws_bytes, pa_stream_t stream) {
   if (!strides) return PA_ERR_NULL;
-  return fwd_any(dims, strides, q, k, v, seg, out, lse, ws, ws_bytes, stream);
+  return fwd_any(dims, strides, io_dtype, q, k, v, seg, out, lse, ws, ws_bytes, stream);
 }
 
-pa_status pa_bwd_strided(const pa_dims* dims, const pa_strides* strides, const void* q, const void* k,
-                         const void* v, const void* out, const void* dout, const float* lse, const int32_t* seg,
-                         void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, pa_stream_t stream) {
+pa_status pa_bwd_strided(const pa_dims* dims, const pa_strides* strides, int32_t io_dtype, const void* q,
+                         const void* k, const void* v, const void* out, const void* dout, const float* lse,
+                         const int32_t* seg, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                         pa_stream_t stream) {
   if (!strides) return PA_ERR_NULL;
-  return bwd_any(dims, strides, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream);
+  return bwd_any(dims, strides, io_dtype, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream);
 }
 
 pa_status pa_fwd(const pa_dims* dims, const void* q, const void* k, const void* v, const int32_t* seg, void* out,
                  float* lse, void* ws, size_t ws_bytes, pa_stream_t stream) {
   if (!seg) return PA_ERR_NULL;
-  return fwd_any(dims, nullptr, q, k, v, seg, out, lse, ws, ws_bytes, stream);
+  return fwd_any(dims, nullptr, PA_IO_BF16, q, k, v, seg, out, lse, ws, ws_bytes, stream);
 }
 
 pa_status pa_fwd_causal(const pa_dims* dims, const void* q, const void* k, const void* v, void* out, float* lse,
                         void* ws, size_t ws_bytes, pa_stream_t stream) {
-  return fwd_any(dims, nullptr, q, k, v, nullptr, out, lse, ws, ws_bytes, stream);
+  return fwd_any(dims, nullptr, PA_IO_BF16, q, k, v, nullptr, out, lse, ws, ws_bytes, stream);
 }
 
 pa_status pa_bwd(const pa_dims* dims, const void* q, const void* k, const void* v, const void* out,
                  const void* dout, const float* lse, const int32_t* seg, void* dq, void* dk, void* dv, void* ws,
                  size_t ws_bytes, pa_stream_t stream) {
   if (!seg) return PA_ERR_NULL;
-  return bwd_any(dims, nullptr, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream);
+  return bwd_any(dims, nullptr, PA_IO_BF16, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream);
 }
 
 pa_status pa_bwd_causal(const pa_dims* dims, const void* q, const void* k, const void* v, const void* out,
                         const void* dout, const float* lse, void* dq, void* dk, void* dv, void* ws,
                         size_t ws_bytes, pa_stream_t stream) {
-  return bwd_any(dims, nullptr, q, k, v, out, dout, lse, nullptr, dq, dk, dv, ws, ws_bytes, stream);
+  return bwd_any(dims, nullptr, PA_IO_BF16, q, k, v, out, dout, lse, nullptr, dq, dk, dv, ws, ws_bytes, stream);
 }
 
 pa_status pa_build_tile_table(const pa_dims* dims, const int32_t* seg, void* ws, size_t ws_bytes,
@@ -454,6 +464,7 @@ const char* pa_status_string(pa_status s) {
     case PA_ERR_WORKSPACE: return "workspace too small (see pa_workspace_bytes)";
     case PA_ERR_ARCH: return "device is not compute capability 10.3 (GB300)";
     case PA_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case PA_ERR_DTYPE: return "io dtype must be PA_IO_BF16 or PA_IO_F32";
   }
   return "unknown status";
 }

@@ -18,16 +18,17 @@ cudaError_t launch_bwd_dq(const AttnParams& p, int D, const void* q, const void*
 cudaError_t launch_bwd_dkv(const AttnParams& p, int D, const void* q, const void* k, const void* v,
                            const void* dout, cudaStream_t st);
 
-// A (B, H, N, D) bf16 tensor with element strides sb, sh, sn (each a multiple
-// of 8) and contiguous D, against the kernels' contiguous (B, H, Np, D) copy;
-// vec = D / 8 16-byte vectors per token row.
+// A (B, H, N, D) bf16 or fp32 tensor with element strides sb, sh, sn (16-byte
+// multiples) and contiguous D, against the kernels' contiguous bf16
+// (B, H, Np, D) copy; vec = D / 8 bf16 16-byte vectors per token row.
 struct RowsView {
   int B, H, N, Np, vec;
   int64_t sb, sh, sn;
 };
-// Copies in (tail rows n >= N zero) and out (real rows only).
-cudaError_t launch_stage_rows_in(void* dst, const void* src, const RowsView& v, cudaStream_t st);
-cudaError_t launch_stage_rows_out(void* dst, const void* src, const RowsView& v, cudaStream_t st);
+// Copies in (tail rows n >= N zero) and out (real rows only); f32: the
+// caller's tensor is fp32 (rounded to bf16 in, widened out).
+cudaError_t launch_stage_rows_in(void* dst, const void* src, const RowsView& v, bool f32, cudaStream_t st);
+cudaError_t launch_stage_rows_out(void* dst, const void* src, const RowsView& v, bool f32, cudaStream_t st);
 // (R, N) 32-bit words to (R, Np) with a tail of 0 or of the row's last word, and back.
 cudaError_t launch_stage_words_in(void* dst, const void* src, uint64_t R, int N, int Np, bool repeat_last,
                                   cudaStream_t st);

@@ -5,13 +5,16 @@
 // a caller's N is not a multiple of 128, or its tensors are strided (for
 // instance (B, N, H, D) memory viewed as (B, H, N, D)), the public calls copy
 // the inputs into that layout inside the workspace, run the kernels there and
-// copy the results back. These are plain memory-bound copies: 16-byte vectors,
+// copy the results back. The same copies take fp32 tensors: inputs are rounded
+// to bf16 (nearest even) on the way in and bf16 results widened exactly on the
+// way out. These are plain memory-bound copies: 16-byte bf16 vectors in
 // grid-stride loops over the destination (inputs) or the source (outputs).
 //
 // Tail tokens n in [N, Np) are zero rows (q, k, v, o, dO), lse 0, and the
 // last real segment id: a tail query then has dO = 0 and delta = 0, so it adds
 // nothing to any key's dK or dV, and a tail key lies after every real query,
 // so causality hides it from all of them. The tail's own outputs are dropped.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -21,8 +24,36 @@
 namespace pa {
 namespace {
 
-// dst (R, Np, VEC) uint4 <- src strided rows; zeros for n >= N.
-__global__ void __launch_bounds__(256) stage_rows_in_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src,
+// One 16-byte vector of 8 bf16 from element offset e (a multiple of 8) of
+// a bf16 tensor, or of 8 fp32 values (rounded to nearest even) from a float
+// tensor (e a multiple of 4).
+__device__ __forceinline__ uint4 load8(const uint16_t* src, uint64_t e) {
+  return __ldg(reinterpret_cast<const uint4*>(src + e));
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint4 load8(const float* src, uint64_t e) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(src + e));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(src + e) + 1);
+  return make_uint4(pack2(a.x, a.y), pack2(a.z, a.w), pack2(b.x, b.y), pack2(b.z, b.w));
+}
+__device__ __forceinline__ void store8(uint16_t* dst, uint64_t e, uint4 x) {
+  *reinterpret_cast<uint4*>(dst + e) = x;
+}
+__device__ __forceinline__ void store8(float* dst, uint64_t e, uint4 x) {
+  // bf16 -> fp32 is exact: the bf16 bits are the float's top half
+  float4* d = reinterpret_cast<float4*>(dst + e);
+  d[0] = make_float4(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xFFFF0000u), __uint_as_float(x.y << 16),
+                     __uint_as_float(x.y & 0xFFFF0000u));
+  d[1] = make_float4(__uint_as_float(x.z << 16), __uint_as_float(x.z & 0xFFFF0000u), __uint_as_float(x.w << 16),
+                     __uint_as_float(x.w & 0xFFFF0000u));
+}
+
+// dst (R, Np, VEC) bf16 vectors <- src strided rows of T; zeros for n >= N.
+template <typename T>
+__global__ void __launch_bounds__(256) stage_rows_in_kernel(uint4* __restrict__ dst, const T* __restrict__ src,
                                                             RowsView v) {
   const uint64_t total = (uint64_t)v.B * v.H * v.Np * v.vec;
   const uint64_t step = (uint64_t)gridDim.x * blockDim.x;
@@ -34,14 +65,15 @@ __global__ void __launch_bounds__(256) stage_rows_in_kernel(uint4* __restrict__ 
     uint4 x = make_uint4(0u, 0u, 0u, 0u);
     if (n < v.N) {
       const uint64_t b = r / v.H, h = r - b * v.H;
-      x = __ldg(src + (b * v.sb + h * v.sh + (uint64_t)n * v.sn) / 8 + c);
+      x = load8(src, b * v.sb + h * v.sh + (uint64_t)n * v.sn + (uint64_t)c * 8);
     }
     dst[u] = x;
   }
 }
 
-// dst strided rows <- src (R, Np, VEC) uint4, real tokens only.
-__global__ void __launch_bounds__(256) stage_rows_out_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src,
+// dst strided rows of T <- src (R, Np, VEC) bf16 vectors, real tokens only.
+template <typename T>
+__global__ void __launch_bounds__(256) stage_rows_out_kernel(T* __restrict__ dst, const uint4* __restrict__ src,
                                                              RowsView v) {
   const uint64_t total = (uint64_t)v.B * v.H * v.N * v.vec;
   const uint64_t step = (uint64_t)gridDim.x * blockDim.x;
@@ -51,7 +83,7 @@ __global__ void __launch_bounds__(256) stage_rows_out_kernel(uint4* __restrict__
     const uint64_t r = row / v.N;
     const int n = (int)(row - r * v.N);
     const uint64_t b = r / v.H, h = r - b * v.H;
-    dst[(b * v.sb + h * v.sh + (uint64_t)n * v.sn) / 8 + c] = __ldg(src + (r * v.Np + n) * v.vec + c);
+    store8(dst, b * v.sb + h * v.sh + (uint64_t)n * v.sn + (uint64_t)c * 8, __ldg(src + (r * v.Np + n) * v.vec + c));
   }
 }
 
@@ -93,18 +125,27 @@ unsigned grid_for(uint64_t units) {
 
 }  // namespace
 
-cudaError_t launch_stage_rows_in(void* dst, const void* src, const RowsView& v, cudaStream_t st) {
+cudaError_t launch_stage_rows_in(void* dst, const void* src, const RowsView& v, bool f32, cudaStream_t st) {
   const uint64_t units = (uint64_t)v.B * v.H * v.Np * v.vec;
   if (units == 0) return cudaSuccess;
-  stage_rows_in_kernel<<<grid_for(units), 256, 0, st>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src), v);
+  if (f32)
+    stage_rows_in_kernel<float><<<grid_for(units), 256, 0, st>>>(static_cast<uint4*>(dst),
+                                                                 static_cast<const float*>(src), v);
+  else
+    stage_rows_in_kernel<uint16_t><<<grid_for(units), 256, 0, st>>>(static_cast<uint4*>(dst),
+                                                                    static_cast<const uint16_t*>(src), v);
   return cudaGetLastError();
 }
 
-cudaError_t launch_stage_rows_out(void* dst, const void* src, const RowsView& v, cudaStream_t st) {
+cudaError_t launch_stage_rows_out(void* dst, const void* src, const RowsView& v, bool f32, cudaStream_t st) {
   const uint64_t units = (uint64_t)v.B * v.H * v.N * v.vec;
   if (units == 0) return cudaSuccess;
-  stage_rows_out_kernel<<<grid_for(units), 256, 0, st>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src),
-                                                         v);
+  if (f32)
+    stage_rows_out_kernel<float><<<grid_for(units), 256, 0, st>>>(static_cast<float*>(dst),
+                                                                  static_cast<const uint4*>(src), v);
+  else
+    stage_rows_out_kernel<uint16_t><<<grid_for(units), 256, 0, st>>>(static_cast<uint16_t*>(dst),
+                                                                     static_cast<const uint4*>(src), v);
   return cudaGetLastError();
 }
 

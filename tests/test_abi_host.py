@@ -121,12 +121,15 @@ def test_strided_refusals(L):
     good = strides(2 * 256 * 128 * 4, 128, 4 * 128, 256 * 2 * 128, 128, 2 * 128)  # (B, N, H, D) memory
     big = L.pa_workspace_bytes_strided(ctypes.byref(dims))
 
-    def f(st, ws_bytes=big, seg=FAKE, q=FAKE):
-        return L.pa_fwd_strided(ctypes.byref(dims), None if st is None else ctypes.byref(st), q, FAKE, FAKE, seg,
-                                FAKE, FAKE, FAKE, ws_bytes, None)
+    def f(st, ws_bytes=big, seg=FAKE, q=FAKE, io=0):
+        return L.pa_fwd_strided(ctypes.byref(dims), None if st is None else ctypes.byref(st), io, q, FAKE, FAKE,
+                                seg, FAKE, FAKE, FAKE, ws_bytes, None)
     assert f(None) == 1
     assert f(strides(1 << 20, 128, 64, 1 << 20, 128, 256)) == 4  # q_n < D
-    assert f(strides(1 << 20, 128, 132, 1 << 20, 128, 256)) == 5  # not a multiple of 8
+    assert f(strides(1 << 20, 128, 132, 1 << 20, 128, 256)) == 5  # not a multiple of 8 bf16
+    assert f(strides(1 << 20, 128, 130, 1 << 20, 128, 256), io=1) == 5  # not a multiple of 4 fp32
+    assert f(good, io=2) == 9
+    assert f(good, io=-1) == 9
     assert f(good, ws_bytes=big - 1) == 6
     assert f(good, q=None) == 1
     assert f(good, seg=FAKE + 4) == 5
@@ -134,10 +137,15 @@ def test_strided_refusals(L):
     cont = strides(4 * 256 * 128, 256 * 128, 128, 2 * 256 * 128, 256 * 128, 128)
     plain = L.pa_workspace_bytes(ctypes.byref(dims))
     assert f(cont, ws_bytes=plain - 1) == 6
-    assert L.pa_bwd_strided(ctypes.byref(dims), None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
-                            FAKE, big, None) == 1
-    assert L.pa_bwd_strided(ctypes.byref(dims), ctypes.byref(good), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+    assert L.pa_bwd_strided(ctypes.byref(dims), None, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                            FAKE, FAKE, big, None) == 1
+    assert L.pa_bwd_strided(ctypes.byref(dims), ctypes.byref(good), 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                             FAKE + 8, FAKE, FAKE, FAKE, big, None) == 5
+    assert L.pa_bwd_strided(ctypes.byref(dims), ctypes.byref(good), 3, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                            FAKE, FAKE, FAKE, FAKE, big, None) == 9
+    # fp32 I/O always stages, so the contiguous layout then needs the staged workspace too
+    cont = strides(4 * 256 * 128, 256 * 128, 128, 2 * 256 * 128, 256 * 128, 128)
+    assert f(cont, ws_bytes=L.pa_workspace_bytes(ctypes.byref(dims)), io=1) == 6
 
 
 def test_selftest_refusals(L):
@@ -157,6 +165,7 @@ def test_valid_call_without_a_gpu_is_refused_not_run(L):
 
 
 def test_status_strings(L):
-    for c in range(9):
+    for c in range(10):
         assert L.pa_status_string(c)
+    assert pa.pa_status_string(9).startswith("io dtype")
     assert pa.pa_status_string(2).startswith("head dim")

@@ -96,6 +96,52 @@ def test_strided_bnhd_causal(cuda_dev):
     print(assert_full_parity(c.run_strided(causal=True), c.oracle_full(causal=True), "bnhd causal"))
 
 
+def _run_f32(c, q, k, v, do, causal=False):
+    seg = None if causal else c.seg
+    ws = pa.workspace(q, k, strided=True)
+    out, lse = pa.forward(q, k, v, seg, ws=ws)
+    dq, dk, dv = pa.backward(q, k, v, out, do, lse, seg, ws=ws)
+    torch.cuda.synchronize()
+    assert pa.pa_device_status(ws) == 0
+    assert out.dtype == dq.dtype == dk.dtype == torch.float32
+    return {"o": out, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+
+
+FP32 = [
+    ("f32_gqa_d128", synth.custom(2, 4, 2, 512, 128, [[1, 130, 5, 120, 256], [512]], seed=42), False),
+    ("f32_ragged_n300_d96_bnhd", synth.custom(1, 4, 2, 300, 96, [[100, 200]], seed=43), True),
+]
+
+
+@pytest.mark.parametrize("name,w,bnhd", FP32, ids=[n for n, _, _ in FP32])
+def test_fp32_io(name, w, bnhd, cuda_dev):
+    """fp32 tensors are rounded to bf16 on the way in and results widened on
+    the way out: on bf16-representable inputs the fp32 call returns the bf16
+    call's results exactly, and it meets the oracle's bars."""
+    c = Case(w, cuda_dev)
+    lay = (lambda t: t.transpose(1, 2).contiguous().transpose(1, 2)) if bnhd else (lambda t: t)
+    g32 = _run_f32(c, *(lay(t.float()) for t in (c.q, c.k, c.v, c.do)))
+    print(assert_full_parity(g32, c.oracle_full(), name))
+    ref = c.run()
+    for n in ("o", "dq", "dk", "dv"):
+        assert torch.equal(g32[n], ref[n].float()), n
+    assert torch.equal(g32["lse"], ref["lse"])
+
+
+def test_fp32_io_rounds_to_nearest_even(cuda_dev):
+    """Inputs that bf16 cannot hold: the fp32 call equals the bf16 call on
+    the inputs rounded by torch (round to nearest even)."""
+    w = synth.custom(1, 2, 2, 256, 64, [[100, 156]], seed=44)
+    c = Case(w, cuda_dev)
+    gen = torch.Generator(device="cpu").manual_seed(44)
+    q, k, v, do = (torch.randn(t.shape, generator=gen).to(cuda_dev) for t in (c.q, c.k, c.v, c.do))
+    g32 = _run_f32(c, q, k, v, do)
+    out, lse = pa.forward(q.bfloat16(), k.bfloat16(), v.bfloat16(), c.seg)
+    dq, dk, dv = pa.backward(q.bfloat16(), k.bfloat16(), v.bfloat16(), out, do.bfloat16(), lse, c.seg)
+    for n, ref in (("o", out), ("dq", dq), ("dk", dk), ("dv", dv)):
+        assert torch.equal(g32[n], ref.float()), n
+
+
 def test_ragged_n_5000_sampled(cuda_dev):
     w = synth.custom(1, 16, 4, 5000, 128, [[1000, 2999, 1, 1000]], seed=41)
     c = Case(w, cuda_dev)
