@@ -290,6 +290,31 @@ pa_status pa_pack_first_fit(const int32_t* lengths, const int32_t* offsets, int3
                             int32_t* seg, uint8_t* loss_mask, int32_t* row_tokens, int64_t* placement,
                             int32_t* rows_used, int64_t* placed_tokens);
 
+/*
+ * Fused linear cross-entropy, forward (mlx-train-perf 0.5.1 README, "The
+ * fused cross-entropy loss" and "If you maintain a trainer":
+ * linear_cross_entropy(hidden, head, targets)). With logits z = H W^T it
+ * writes, per token i,
+ *   lse[i]          = log sum_v exp(z[i, v])
+ *   target_logit[i] = z[i, targets[i]]
+ *   nll[i]          = lse[i] - target_logit[i]
+ * without storing z: the tensor cores form 128 x 128 logit tiles in TMEM
+ * and the epilogue folds each into a running maximum and sum.
+ *   hidden       : (N, D) bf16, row-major      head : (V, D) bf16, row-major
+ *   targets      : (N) int32; a target outside [0, V) is ignored: its nll
+ *                  and target_logit are 0 (lse is still written)
+ *   nll, lse, target_logit : (N) fp32
+ * N, V >= 1; D a multiple of 64 in [64, 16384]. Device pointers, caller-owned,
+ * 16-byte aligned; ws >= pa_lce_workspace_bytes(N, V, D) bytes (its first 4
+ * bytes are the device status word read by pa_device_status). Asynchronous
+ * on `stream`, like the attention calls.
+ * Errors: PA_ERR_SHAPE, PA_ERR_NULL, PA_ERR_ALIGN, PA_ERR_WORKSPACE,
+ * PA_ERR_ARCH, PA_ERR_CUDA.
+ */
+size_t pa_lce_workspace_bytes(int32_t N, int32_t V, int32_t D);
+pa_status pa_lce_fwd(int32_t N, int32_t V, int32_t D, const void* hidden, const void* head, const int32_t* targets,
+                     float* nll, float* lse, float* target_logit, void* ws, size_t ws_bytes, pa_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* pa_status_string(pa_status s);
 

@@ -31,7 +31,7 @@ PA_IO_BF16, PA_IO_F32 = 0, 1
 EXPORTS = ["pa_workspace_bytes", "pa_fwd", "pa_bwd", "pa_fwd_causal", "pa_bwd_causal", "pa_build_tile_table",
            "pa_fwd_tiles", "pa_bwd_delta", "pa_bwd_dq", "pa_bwd_dkv", "pa_bwd_noalloc", "pa_device_status",
            "pa_selftest_wait_timeout", "pa_pack_first_fit", "pa_workspace_bytes_strided", "pa_fwd_strided",
-           "pa_bwd_strided", "pa_status_string"]
+           "pa_bwd_strided", "pa_lce_workspace_bytes", "pa_lce_fwd", "pa_status_string"]
 
 
 class LibraryMissing(RuntimeError):
@@ -96,6 +96,10 @@ def lib():
             L.pa_bwd_strided.argtypes = [D, ST, ctypes.c_int32, P, P, P, P, P, P, P, P, P, P, P, S, P]
             L.pa_bwd_strided.restype = ctypes.c_int
             I32, U64 = ctypes.c_int32, ctypes.c_uint64
+            L.pa_lce_workspace_bytes.argtypes = [I32, I32, I32]
+            L.pa_lce_workspace_bytes.restype = S
+            L.pa_lce_fwd.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, S, P]
+            L.pa_lce_fwd.restype = ctypes.c_int
             L.pa_pack_first_fit.argtypes = [P, P, I32, P, I32, I32, I32, U64, U64, P, P, P, P, P, P]
             L.pa_pack_first_fit.restype = ctypes.c_int
             L.pa_status_string.argtypes = [ctypes.c_int]
@@ -371,6 +375,41 @@ def packed_batches(lengths, B, N, seed, epoch, offsets=None, tokens=None, pad_to
     for b in range(-(-r["rows_used"] // B)):
         sl = slice(b * B, (b + 1) * B)
         yield {k: (None if r[k] is None else r[k][sl]) for k in ("seg", "loss_mask", "row_tokens")}
+
+
+def pa_lce_workspace_bytes(N, V, D) -> int:
+    return int(lib().pa_lce_workspace_bytes(int(N), int(V), int(D)))
+
+
+def pa_lce_fwd(hidden, head, targets, nll, lse, target_logit, ws, stream=None):
+    """Fused linear cross-entropy forward (see include/pa.h): hidden (N, D)
+    and head (V, D) bf16, targets (N) int32; writes nll, lse and
+    target_logit, (N) fp32 each."""
+    import torch
+    N, D = hidden.shape
+    V = head.shape[0]
+    if head.shape[1] != D:
+        raise ValueError("head must be (V, D) with the hidden states' D")
+    f = torch.float32
+    _check(lib().pa_lce_fwd(N, V, D, _ptr(hidden, torch.bfloat16, "hidden"), _ptr(head, torch.bfloat16, "head"),
+                            _ptr(targets, torch.int32, "targets"), _ptr(nll, f, "nll"), _ptr(lse, f, "lse"),
+                            _ptr(target_logit, f, "target_logit"), _ptr(ws, None, "ws"), ws.numel(),
+                            _stream(stream)))
+
+
+def linear_cross_entropy_forward(hidden, head, targets, ws=None):
+    """Allocate the outputs (and a workspace) and run pa_lce_fwd; returns
+    (nll, lse, target_logit)."""
+    import torch
+    N, D = hidden.shape
+    out = [torch.empty(N, dtype=torch.float32, device=hidden.device) for _ in range(3)]
+    if ws is None:
+        n = pa_lce_workspace_bytes(N, head.shape[0], D)
+        if n == 0:
+            raise PAError(4, "invalid linear cross-entropy dims")
+        ws = torch.empty(n, dtype=torch.uint8, device=hidden.device)
+    pa_lce_fwd(hidden, head, targets, *out, ws)
+    return tuple(out)
 
 
 def pa_status_string(code: int) -> str:

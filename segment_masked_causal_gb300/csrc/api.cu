@@ -426,6 +426,38 @@ pa_status pa_bwd_dkv(const pa_dims* dims, const void* q, const void* k, const vo
   return step_dkv(dims, q, k, v, dout, lse, seg, dk, dv, ws, ws_bytes, stream);
 }
 
+// ------------------------------------------------------ linear cross-entropy
+static bool lce_dims_ok(int32_t N, int32_t V, int32_t D) {
+  return N > 0 && V > 0 && D >= 64 && D <= 16384 && D % 64 == 0;
+}
+
+size_t pa_lce_workspace_bytes(int32_t N, int32_t V, int32_t D) {
+  if (!lce_dims_ok(N, V, D)) return 0;
+  const pa::LceSplit sp = pa::lce_split(N, V);
+  return kAlign + round_up((size_t)3 * sp.splits * N * sizeof(float));
+}
+
+pa_status pa_lce_fwd(int32_t N, int32_t V, int32_t D, const void* hidden, const void* head, const int32_t* targets,
+                     float* nll, float* lse, float* target_logit, void* ws, size_t ws_bytes, pa_stream_t stream) {
+  if (!lce_dims_ok(N, V, D)) return PA_ERR_SHAPE;
+  for (const void* x : {hidden, head, (const void*)targets, (const void*)nll, (const void*)lse,
+                        (const void*)target_logit, (const void*)ws})
+    if (!x) return PA_ERR_NULL;
+  for (const void* x : {hidden, head, (const void*)targets, (const void*)nll, (const void*)lse,
+                        (const void*)target_logit, (const void*)ws})
+    if (!aligned16(x)) return PA_ERR_ALIGN;
+  if (ws_bytes < pa_lce_workspace_bytes(N, V, D)) return PA_ERR_WORKSPACE;
+  pa_status why = device_ok();
+  if (why != PA_OK) return why;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), st) != cudaSuccess) return PA_ERR_CUDA;
+  return pa::launch_lce_fwd(N, V, D, hidden, head, targets, nll, lse, target_logit,
+                            reinterpret_cast<float*>(w + kAlign), reinterpret_cast<uint32_t*>(w), st) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
 pa_status pa_selftest_wait_timeout(void* ws, size_t ws_bytes, pa_stream_t stream) {
   if (!ws) return PA_ERR_NULL;
   if (!aligned16(ws)) return PA_ERR_ALIGN;

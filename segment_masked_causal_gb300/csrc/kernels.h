@@ -34,4 +34,15 @@ cudaError_t launch_stage_words_in(void* dst, const void* src, uint64_t R, int N,
                                   cudaStream_t st);
 cudaError_t launch_stage_words_out(void* dst, const void* src, uint64_t R, int N, int Np, cudaStream_t st);
 
+// Fused linear cross-entropy forward. The vocabulary's 128-row tiles are cut
+// into `splits` runs of `per` tiles, one CTA column each; `part` holds
+// 3 * splits * N floats of per-split partial results.
+struct LceSplit {
+  int splits, per;
+};
+LceSplit lce_split(int N, int V);
+cudaError_t launch_lce_fwd(int N, int V, int D, const void* hidden, const void* head, const int32_t* targets,
+                           float* nll, float* lse, float* target_logit, float* part, uint32_t* status,
+                           cudaStream_t st);
+
 }  // namespace pa

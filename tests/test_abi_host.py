@@ -169,3 +169,24 @@ def test_status_strings(L):
         assert L.pa_status_string(c)
     assert pa.pa_status_string(9).startswith("io dtype")
     assert pa.pa_status_string(2).startswith("head dim")
+
+
+def test_lce_refusals(L):
+    """The linear cross-entropy forward checks dims, pointers and workspace on
+    the host before any device call."""
+    assert L.pa_lce_workspace_bytes(256, 1000, 128) > 0
+    assert L.pa_lce_workspace_bytes(0, 1000, 128) == 0
+    assert L.pa_lce_workspace_bytes(256, 1000, 96) == 0  # D must be a multiple of 64
+    big = 1 << 30
+
+    def f(N=256, V=1000, D=128, h=FAKE, w=FAKE, t=FAKE, ws=FAKE, ws_bytes=big):
+        return L.pa_lce_fwd(N, V, D, h, w, t, FAKE, FAKE, FAKE, ws, ws_bytes, None)
+    assert f(N=0) == 4
+    assert f(V=0) == 4
+    assert f(D=96) == 4
+    assert f(D=32) == 4
+    assert f(h=None) == 1
+    assert f(ws=None) == 1
+    assert f(w=FAKE + 8) == 5
+    assert f(t=FAKE + 4) == 5
+    assert f(ws_bytes=L.pa_lce_workspace_bytes(256, 1000, 128) - 1) == 6

@@ -1,0 +1,78 @@
+"""Fused linear cross-entropy forward on the GPU against the fp64 oracle
+(mlx-train-perf 0.5.1 README, "The fused cross-entropy loss": the per-token
+NLL, log-sum-exp and target logit of H W^T, with no (N, V) logits stored).
+
+Inputs are bf16 normals from the seeded generator; the oracle takes the same
+bf16 values in fp64. The kernel accumulates the D products of each logit in
+fp32, so the bar is max |err| <= 1e-3 + 1e-5 |exact| on each output."""
+import numpy as np
+import pytest
+import torch
+
+import segment_masked_causal_gb300 as pa
+import synth
+from oracle import linear_ce as lce
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 1e-3, 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from segment_masked_causal_gb300 import build
+    build.build()
+
+
+def _inputs(N, V, D, seed, dev, ignored=()):
+    hb = synth.bf16_normal(seed, 50, (N, D))
+    wb = synth.bf16_normal(seed, 51, (V, D))
+    t = (synth.uint64s(seed, 52, N) % np.uint64(V)).astype(np.int32)
+    for i, val in ignored:
+        t[i] = val
+    to = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(dev)
+    return hb, wb, t, to(hb), to(wb), torch.from_numpy(t).to(dev)
+
+
+def _run(H, W, T):
+    N, D = H.shape
+    ws = torch.empty(pa.pa_lce_workspace_bytes(N, W.shape[0], D), dtype=torch.uint8, device=H.device)
+    nll, lse, tgt = pa.linear_cross_entropy_forward(H, W, T, ws=ws)
+    torch.cuda.synchronize()
+    assert pa.pa_device_status(ws) == 0
+    return nll, lse, tgt
+
+
+CASES = [
+    # name, N, V, D: ragged vocabulary; ragged tokens over many splits; a
+    # 4-stage ring that wraps (8 K slices) with 3 vocabulary tiles per CTA
+    ("ragged_v", 256, 1000, 128),
+    ("ragged_n", 300, 4096, 256),
+    ("ring_wraps", 2048, 5000, 512),
+    ("d64_small_v", 128, 130, 64),
+]
+
+
+@pytest.mark.parametrize("name,N,V,D", CASES, ids=[c[0] for c in CASES])
+def test_lce_forward_matches_oracle(name, N, V, D, cuda_dev):
+    hb, wb, t, H, W, T = _inputs(N, V, D, 60 + len(name), cuda_dev, ignored=[(3, -1), (N - 1, V)])
+    nll, lse, tgt = _run(H, W, T)
+    h64, w64 = synth.bf16_bits_to_f64(hb), synth.bf16_bits_to_f64(wb)
+    valid = (t >= 0) & (t < V)
+    t_safe = np.where(valid, t, 0)
+    e_nll, e_lse, e_tgt = lce.forward(h64, w64, t_safe)
+    e_nll, e_tgt = np.where(valid, e_nll, 0.0), np.where(valid, e_tgt, 0.0)
+    for got, exp, n in ((lse, e_lse, "lse"), (tgt, e_tgt, "target_logit"), (nll, e_nll, "nll")):
+        g = got.cpu().numpy().astype(np.float64)
+        err = np.abs(g - exp)
+        bar = ATOL + RTOL * np.abs(exp)
+        print(f"{name} {n}: max err {err.max():.3e} (|exact| up to {np.abs(exp).max():.1f})")
+        assert (err <= bar).all(), (n, float(err.max()), int(err.argmax()))
+    assert float(nll[3]) == 0.0 and float(tgt[N - 1]) == 0.0  # ignored targets
+
+
+def test_lce_forward_is_deterministic(cuda_dev):
+    _, _, _, H, W, T = _inputs(512, 3000, 256, 70, cuda_dev)
+    a, b = _run(H, W, T), _run(H, W, T)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
