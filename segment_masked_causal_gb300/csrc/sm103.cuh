@@ -64,8 +64,8 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // Polling loop of a bounded wait, kept out of line: every wait site inlines
 // only its first test, so the hot loops of the kernels stay small enough for
 // the instruction cache.
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint32_t site, volatile int* abort_flag,
-                                            uint32_t* status) {
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint32_t site,
+                                                   volatile int* abort_flag, uint32_t* status) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_test(bar, parity)) return true;

@@ -243,9 +243,9 @@ def test_single_segment_bit_identical_to_causal(name, cuda_dev):
     c = Case(w, cuda_dev)
     packed = c.run()
     causal = c.run(causal=True)
+    bits = lambda t: t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
     for n in ("o", "lse", "dq", "dk", "dv"):
-        assert torch.equal(packed[n].view(torch.int16) if packed[n].dtype == torch.bfloat16 else packed[n].view(torch.int32),
-                           causal[n].view(torch.int16) if causal[n].dtype == torch.bfloat16 else causal[n].view(torch.int32)), n
+        assert torch.equal(bits(packed[n]), bits(causal[n])), n
 
 
 def test_bounded_wait_gives_up_and_context_survives(cuda_dev):
