@@ -77,7 +77,8 @@ typedef enum {
   PA_ERR_WORKSPACE = 6, /* ws_bytes < pa_workspace_bytes(dims)                 */
   PA_ERR_ARCH = 7,      /* current device is not compute capability 10.3       */
   PA_ERR_CUDA = 8,      /* a CUDA runtime / driver call or launch failed       */
-  PA_ERR_DTYPE = 9      /* io_dtype is not a pa_io_dtype                       */
+  PA_ERR_DTYPE = 9,     /* io_dtype is not a pa_io_dtype                       */
+  PA_ERR_HOST_MEMORY = 10 /* a host-side call could not allocate its scratch    */
 } pa_status;
 
 /* Device status bits (pa_device_status). */
@@ -283,7 +284,8 @@ pa_status pa_selftest_wait_timeout(void* ws, size_t ws_bytes, pa_stream_t stream
  *   placed_tokens       tokens placed in all rows.
  * Errors: PA_ERR_NULL (seg; lengths when count > 0; tokens when row_tokens
  * is set and count > 0), PA_ERR_SHAPE (count < 0, rows or N < 1, a length
- * < 1 or an offset < 0). Nothing is written on error.
+ * < 1 or an offset < 0), PA_ERR_HOST_MEMORY (its O(count + rows) scratch
+ * could not be allocated). Nothing is written on error.
  */
 pa_status pa_pack_first_fit(const int32_t* lengths, const int32_t* offsets, int32_t count, const int32_t* tokens,
                             int32_t pad_token, int32_t rows, int32_t N, uint64_t seed, uint64_t epoch,

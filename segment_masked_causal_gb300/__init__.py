@@ -26,7 +26,8 @@ LIB_PATH = os.path.join(HERE, "libpa.so")
 
 PA_OK = 0
 STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_NULL", 2: "PA_ERR_HEAD_DIM", 3: "PA_ERR_GQA", 4: "PA_ERR_SHAPE",
-                5: "PA_ERR_ALIGN", 6: "PA_ERR_WORKSPACE", 7: "PA_ERR_ARCH", 8: "PA_ERR_CUDA", 9: "PA_ERR_DTYPE"}
+                5: "PA_ERR_ALIGN", 6: "PA_ERR_WORKSPACE", 7: "PA_ERR_ARCH", 8: "PA_ERR_CUDA", 9: "PA_ERR_DTYPE",
+                10: "PA_ERR_HOST_MEMORY"}
 PA_IO_BF16, PA_IO_F32 = 0, 1
 EXPORTS = ["pa_workspace_bytes", "pa_fwd", "pa_bwd", "pa_fwd_causal", "pa_bwd_causal", "pa_build_tile_table",
            "pa_fwd_tiles", "pa_bwd_delta", "pa_bwd_dq", "pa_bwd_dkv", "pa_bwd_noalloc", "pa_device_status",

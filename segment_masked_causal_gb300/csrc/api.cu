@@ -497,6 +497,7 @@ const char* pa_status_string(pa_status s) {
     case PA_ERR_ARCH: return "device is not compute capability 10.3 (GB300)";
     case PA_ERR_CUDA: return "a CUDA call or kernel launch failed";
     case PA_ERR_DTYPE: return "io dtype must be PA_IO_BF16 or PA_IO_F32";
+    case PA_ERR_HOST_MEMORY: return "host memory for the call's scratch could not be allocated";
   }
   return "unknown status";
 }

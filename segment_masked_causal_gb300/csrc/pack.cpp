@@ -11,6 +11,7 @@
 // Host code only; no CUDA call is made.
 #include <cstdint>
 #include <cstring>
+#include <new>
 #include <vector>
 
 #include "pa.h"
@@ -63,18 +64,12 @@ class FreeTree {
   std::vector<int64_t> t_;
 };
 
-}  // namespace
-
-extern "C" pa_status pa_pack_first_fit(const int32_t* lengths, const int32_t* offsets, int32_t count,
-                                       const int32_t* tokens, int32_t pad_token, int32_t rows, int32_t N,
-                                       uint64_t seed, uint64_t epoch, int32_t* seg, uint8_t* loss_mask,
-                                       int32_t* row_tokens, int64_t* placement, int32_t* rows_used,
-                                       int64_t* placed_tokens) {
-  if (!seg || (count > 0 && !lengths) || (row_tokens && count > 0 && !tokens)) return PA_ERR_NULL;
-  if (count < 0 || rows <= 0 || N <= 0) return PA_ERR_SHAPE;
-  for (int32_t i = 0; i < count; ++i)
-    if (lengths[i] <= 0 || (offsets && offsets[i] < 0)) return PA_ERR_SHAPE;
-
+// Everything that allocates runs before the first write to an output, so an
+// allocation failure leaves the outputs untouched.
+pa_status pack(const int32_t* lengths, const int32_t* offsets, int32_t count, const int32_t* tokens,
+               int32_t pad_token, int32_t rows, int32_t N, uint64_t seed, uint64_t epoch, int32_t* seg,
+               uint8_t* loss_mask, int32_t* row_tokens, int64_t* placement, int32_t* rows_used,
+               int64_t* placed_tokens) {
   // where each sequence's tokens start in the concatenated `tokens`
   std::vector<int64_t> src(count);
   int64_t total = 0;
@@ -94,16 +89,16 @@ extern "C" pa_status pa_pack_first_fit(const int32_t* lengths, const int32_t* of
     order[j] = t;
   }
 
+  FreeTree tree(rows, N);
+  std::vector<int64_t> used(rows, 0);
+  std::vector<int32_t> nseg(rows, 0);
+
   const int64_t cells = (int64_t)rows * N;
   if (loss_mask) std::memset(loss_mask, 0, (size_t)cells);
   if (row_tokens)
     for (int64_t k = 0; k < cells; ++k) row_tokens[k] = pad_token;
   if (placement)
     for (int32_t i = 0; i < count; ++i) placement[i] = -1;
-
-  FreeTree tree(rows, N);
-  std::vector<int64_t> used(rows, 0);
-  std::vector<int32_t> nseg(rows, 0);
   int64_t placed = 0;
   int32_t last_row = -1;
   for (const int32_t s : order) {
@@ -132,4 +127,25 @@ extern "C" pa_status pa_pack_first_fit(const int32_t* lengths, const int32_t* of
   if (rows_used) *rows_used = last_row + 1;
   if (placed_tokens) *placed_tokens = placed;
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status pa_pack_first_fit(const int32_t* lengths, const int32_t* offsets, int32_t count,
+                                       const int32_t* tokens, int32_t pad_token, int32_t rows, int32_t N,
+                                       uint64_t seed, uint64_t epoch, int32_t* seg, uint8_t* loss_mask,
+                                       int32_t* row_tokens, int64_t* placement, int32_t* rows_used,
+                                       int64_t* placed_tokens) {
+  if (!seg || (count > 0 && !lengths) || (row_tokens && count > 0 && !tokens)) return PA_ERR_NULL;
+  if (count < 0 || rows <= 0 || N <= 0) return PA_ERR_SHAPE;
+  for (int32_t i = 0; i < count; ++i)
+    if (lengths[i] <= 0 || (offsets && offsets[i] < 0)) return PA_ERR_SHAPE;
+  // no C++ exception may cross the C boundary: the scratch vectors' allocation
+  // is the only thing here that can throw
+  try {
+    return pack(lengths, offsets, count, tokens, pad_token, rows, N, seed, epoch, seg, loss_mask, row_tokens,
+                placement, rows_used, placed_tokens);
+  } catch (const std::bad_alloc&) {
+    return PA_ERR_HOST_MEMORY;
+  }
 }
