@@ -315,3 +315,36 @@ def test_refusals_write_nothing(kw, code, L):
     got, seg_buf, tok_buf = _raw(L, **kw)
     assert got == code
     assert (seg_buf == 12345).all() and (tok_buf == 12345).all()
+
+
+def test_library_matches_oracle_on_generated_inputs(L):
+    """Property-based sweep (small shapes): element-by-element equality with
+    the oracle, and the first-fit properties, for generated datasets."""
+    hyp = pytest.importorskip("hypothesis")
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=150, deadline=None, derandomize=True)
+    @hyp.given(lengths=st.lists(st.integers(1, 40), min_size=0, max_size=40),
+               rows=st.integers(1, 6), N=st.integers(1, 64), seed=st.integers(0, 2**64 - 1),
+               epoch=st.integers(0, 2**64 - 1), data=st.data())
+    def check(lengths, rows, N, seed, epoch, data):
+        offsets = [data.draw(st.integers(0, x + 1)) for x in lengths]
+        tokens = list(range(100, 100 + sum(lengths)))
+        a = _lib_pack(lengths, rows, N, seed, epoch, offsets, tokens, pad_token=-1)
+        b = opk.pack(lengths, rows, N, seed, epoch, offsets, tokens, pad_token=-1)
+        _assert_same(a, b)
+        _check_pack_properties(a, lengths, offsets, rows, N)
+
+    check()
+
+
+def test_packed_rows_are_sorted_runs(L):
+    """Segment ids come out as nondecreasing runs per row (0, 1, ..., then the
+    padding id), the layout the attention kernels' tile skipping is fastest on."""
+    rng = np.random.default_rng(3)
+    lengths, offsets = _random_dataset(rng, 90, 2, 300, 1024)
+    res = _lib_pack(lengths, 8, 1024, 5, 2, offsets)
+    seg = res["seg"]
+    assert (np.diff(seg, axis=1) >= 0).all()
+    assert (np.diff(seg, axis=1) <= 1).all()
+    assert (seg[:, 0] == 0).all()
