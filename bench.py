@@ -413,6 +413,8 @@ def run_ours(args):
         line["packed"] = packed_extras(dev, rank, args)
         line["head_dim_96"] = head_dim_96_extra(dev, rank, args)
         line["staged_layouts"] = staged_layout_extras(dev, rank, args)
+    if not args.no_extras and w.name == "8k_one_segment" and rank == 0 and world == 1:
+        line["linear_cross_entropy"] = lce_extra()
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
@@ -521,6 +523,61 @@ def staged_layout_extras(dev, rank, args):
                       "useful_tflops": round(useful_flops(w8000) / (t_8000 * 1e-3) / 1e12, 3)}}
 
 
+LCE_SHAPE = (8192, 151936, 4096)  # tokens, vocabulary, hidden: the README's isolated loss-layer shape
+
+
+def lce_measure(steps: int = 5, warmup: int = 2) -> dict:
+    """The fused linear cross-entropy forward (pa_lce_fwd) at N = 8192,
+    V = 151,936, D = 4096 in bf16 (mlx-train-perf 0.5.1 README, "The fused
+    cross-entropy loss", its isolated measurement). Seeded device-side
+    normals (head scaled by 2/sqrt(D)); the 1.2 GB head is larger than L2.
+    Tensor-bound: 2 N V D flops per call."""
+    import torch
+    import segment_masked_causal_gb300 as pa
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    N, V, D = LCE_SHAPE
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1008)
+    H = torch.randn((N, D), generator=gen, device=dev).to(torch.bfloat16)
+    W = (torch.randn((V, D), generator=gen, device=dev) * (2.0 / math.sqrt(D))).to(torch.bfloat16)
+    T = torch.randint(0, V, (N,), generator=gen, device=dev, dtype=torch.int32)
+    nll, lse, tgt = (torch.empty(N, dtype=torch.float32, device=dev) for _ in range(3))
+    ws = torch.empty(pa.pa_lce_workspace_bytes(N, V, D), dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        pa.pa_lce_fwd(H, W, T, nll, lse, tgt, ws)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        a.record()
+        pa.pa_lce_fwd(H, W, T, nll, lse, tgt, ws)
+        b.record()
+    torch.cuda.synchronize()
+    status = pa.pa_device_status(ws)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    tflops = 2.0 * N * V * D / (ms * 1e-3) / 1e12
+    pk = peaks()
+    return {"workload": f"N{N} V{V} D{D} bf16", "ms": round(ms, 4), "tflops": round(tflops, 2),
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(tflops / pk["bf16_tflops"], 4)},
+            "launches_per_call": 2, "device_status": status,
+            "finite": bool(torch.isfinite(nll).all().item() and torch.isfinite(lse).all().item())}
+
+
+def lce_extra() -> dict:
+    """lce_measure in a child process, so that whatever happens there cannot
+    take the main measurement down with it."""
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--lce-only"], capture_output=True,
+                           text=True, timeout=300)
+        lines = [x for x in r.stdout.strip().splitlines() if x.startswith("{")]
+        if r.returncode == 0 and lines:
+            return json.loads(lines[-1])
+        return {"error": f"exit {r.returncode}: " + (r.stderr.strip().splitlines() or ["no output"])[-1][:300]}
+    except Exception as e:  # a timeout or a launch failure is reported, not raised
+        return {"error": repr(e)[:300]}
+
+
 # ------------------------------------------------------------------ the reference arm
 def run_reference(args):
     world, rank, _ = dist_env()
@@ -570,7 +627,11 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip the packed / causal comparison runs")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--lce-only", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
+    if args.lce_only:
+        print(json.dumps(lce_measure()), flush=True)
+        return
     args.warmup = max(3, args.warmup)  # at least 3 warm-up steps, whatever was asked
     if args.impl == "reference":
         run_reference(args)

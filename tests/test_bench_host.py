@@ -93,3 +93,14 @@ def test_multi_rank_reduction_gloo():
         assert p.exitcode == 0
     assert [m for _, m, _ in res] == [2.5, 2.5]           # max over ranks, seen by every rank
     assert res[0][2] != res[1][2]                         # independent replica inputs per rank
+
+
+def test_lce_extra_reports_failure_instead_of_raising():
+    """The cross-entropy measurement runs in a child process; without a GPU
+    the child fails and the extra reports it as an error entry."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    import bench
+    r = bench.lce_extra()
+    assert set(r) == {"error"} and r["error"].startswith("exit ")
