@@ -255,7 +255,8 @@ pa_status pa_selftest_wait_timeout(void* ws, size_t ws_bytes, pa_stream_t stream
  *   offsets[count]  prompt length per sequence, each >= 0 (>= length means
  *                   nothing of it is supervised); NULL = all 0.
  *   tokens          the sequences' tokens concatenated in input order
- *                   (sum(lengths) values); needed only when row_tokens is set.
+ *                   (sum(lengths) values); needed when row_tokens or
+ *                   row_targets is set.
  *   rows, N         the output holds `rows` rows of N tokens (rows, N >= 1).
  *   seed, epoch     the shuffle. Draw n of (seed, epoch) is
  *                   m(k + (n + 1) * 0x9E3779B97F4A7C15), k = m(seed * 1000003
@@ -278,19 +279,22 @@ pa_status pa_selftest_wait_timeout(void* ws, size_t ws_bytes, pa_stream_t stream
  *                       its sequence) with offset <= p + 1 <= length - 1.
  *                       0 elsewhere, padding included.
  *   row_tokens[rows*N]  the packed tokens; pad_token in the padding.
+ *   row_targets[rows*N] where loss_mask is 1, the token that position is
+ *                       trained to predict (the next token of its own
+ *                       sequence); -1 elsewhere, which pa_lce_fwd ignores.
  *   placement[count]    int64 flat index row*N + start of each input
  *                       sequence (input order), or -1 when it was left out.
  *   rows_used           1 + the highest row holding a sequence (0 if none).
  *   placed_tokens       tokens placed in all rows.
  * Errors: PA_ERR_NULL (seg; lengths when count > 0; tokens when row_tokens
- * is set and count > 0), PA_ERR_SHAPE (count < 0, rows or N < 1, a length
+ * or row_targets is set and count > 0), PA_ERR_SHAPE (count < 0, rows or N < 1, a length
  * < 1 or an offset < 0), PA_ERR_HOST_MEMORY (its O(count + rows) scratch
  * could not be allocated). Nothing is written on error.
  */
 pa_status pa_pack_first_fit(const int32_t* lengths, const int32_t* offsets, int32_t count, const int32_t* tokens,
                             int32_t pad_token, int32_t rows, int32_t N, uint64_t seed, uint64_t epoch,
-                            int32_t* seg, uint8_t* loss_mask, int32_t* row_tokens, int64_t* placement,
-                            int32_t* rows_used, int64_t* placed_tokens);
+                            int32_t* seg, uint8_t* loss_mask, int32_t* row_tokens, int32_t* row_targets,
+                            int64_t* placement, int32_t* rows_used, int64_t* placed_tokens);
 
 /*
  * Fused linear cross-entropy, forward (mlx-train-perf 0.5.1 README, "The

@@ -18,7 +18,8 @@ Readings where the pages leave a step open:
   * a row's unfilled tail is one extra segment (padding), never supervised;
   * supervision (the unpacked rule applied per sequence): the token at
     position p of a sequence of length L with prompt length `offset` is
-    trained to predict token p + 1, and counts iff offset <= p + 1 <= L - 1.
+    trained to predict token p + 1, and counts iff offset <= p + 1 <= L - 1;
+    the target of a supervised position is that next token, -1 elsewhere.
 
 Pins: tests/test_packer_host.py (published splitmix64 outputs, uniformity of
 the shuffle over all permutations of three items, a hand-worked first-fit
@@ -75,6 +76,7 @@ def pack(lengths, rows, N, seed, epoch, offsets=None, tokens=None, pad_token=0) 
     seg = [[None] * N for _ in range(rows)]
     mask = [[0] * N for _ in range(rows)]
     toks = [[pad_token] * N for _ in range(rows)]
+    tgts = [[-1] * N for _ in range(rows)]
     placement = [-1] * count
     next_id = [0] * rows
     placed = 0
@@ -90,6 +92,8 @@ def pack(lengths, rows, N, seed, epoch, offsets=None, tokens=None, pad_token=0) 
             mask[r][start + p] = 1 if sup[p] else 0
             if tokens is not None:
                 toks[r][start + p] = int(tokens[starts[s] + p])
+                if sup[p]:
+                    tgts[r][start + p] = int(tokens[starts[s] + p + 1])
         placement[s] = r * N + start
         placed += lengths[s]
     for r in range(rows):
@@ -98,5 +102,6 @@ def pack(lengths, rows, N, seed, epoch, offsets=None, tokens=None, pad_token=0) 
                 seg[r][t] = next_id[r]
     used_rows = [r for r in range(rows) if next_id[r] > 0]
     return {"seg": seg, "loss_mask": mask, "row_tokens": toks if tokens is not None else None,
+            "row_targets": tgts if tokens is not None else None,
             "placement": placement, "rows_used": (max(used_rows) + 1) if used_rows else 0,
             "placed_tokens": placed}

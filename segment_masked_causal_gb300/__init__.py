@@ -101,7 +101,7 @@ def lib():
             L.pa_lce_workspace_bytes.restype = S
             L.pa_lce_fwd.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, S, P]
             L.pa_lce_fwd.restype = ctypes.c_int
-            L.pa_pack_first_fit.argtypes = [P, P, I32, P, I32, I32, I32, U64, U64, P, P, P, P, P, P]
+            L.pa_pack_first_fit.argtypes = [P, P, I32, P, I32, I32, I32, U64, U64, P, P, P, P, P, P, P]
             L.pa_pack_first_fit.restype = ctypes.c_int
             L.pa_status_string.argtypes = [ctypes.c_int]
             L.pa_status_string.restype = ctypes.c_char_p
@@ -332,8 +332,11 @@ def pa_pack_first_fit(lengths, rows, N, seed=0, epoch=0, offsets=None, tokens=No
     lengths/offsets: per-sequence token counts and prompt lengths (offsets
     None = all 0); tokens: the sequences' tokens concatenated in input order,
     or None to skip the token rows. Returns a dict of numpy arrays: seg and
-    loss_mask (rows, N), row_tokens (rows, N) or None, placement (count,)
-    int64 flat start index or -1, and the ints rows_used and placed_tokens."""
+    loss_mask (rows, N), row_tokens and row_targets (rows, N) or None,
+    placement (count,) int64 flat start index or -1, and the ints rows_used
+    and placed_tokens. row_targets holds, where loss_mask is 1, the next token
+    of the same sequence, and -1 elsewhere (an ignored target for
+    pa_lce_fwd)."""
     import numpy as np
     lengths = np.ascontiguousarray(lengths, dtype=np.int32).reshape(-1)
     count = lengths.size
@@ -348,6 +351,7 @@ def pa_pack_first_fit(lengths, rows, N, seed=0, epoch=0, offsets=None, tokens=No
     seg = np.empty(cells, np.int32)
     mask = np.empty(cells, np.uint8)
     row_tokens = np.empty(cells, np.int32) if tok is not None else None
+    row_targets = np.empty(cells, np.int32) if tok is not None else None
     placement = np.empty(count, np.int64)
     used, placed = ctypes.c_int32(0), ctypes.c_int64(0)
 
@@ -356,17 +360,20 @@ def pa_pack_first_fit(lengths, rows, N, seed=0, epoch=0, offsets=None, tokens=No
 
     _check(lib().pa_pack_first_fit(p(lengths), p(off), count, p(tok), int(pad_token), rows, N,
                                    int(seed) & 0xFFFFFFFFFFFFFFFF, int(epoch) & 0xFFFFFFFFFFFFFFFF,
-                                   seg.ctypes.data if cells else None, p(mask), p(row_tokens), p(placement),
+                                   seg.ctypes.data if cells else None, p(mask), p(row_tokens), p(row_targets),
+                                   p(placement),
                                    ctypes.byref(used), ctypes.byref(placed)))
     return {"seg": seg.reshape(rows, N), "loss_mask": mask.reshape(rows, N),
             "row_tokens": None if row_tokens is None else row_tokens.reshape(rows, N),
+            "row_targets": None if row_targets is None else row_targets.reshape(rows, N),
             "placement": placement, "rows_used": int(used.value), "placed_tokens": int(placed.value)}
 
 
 def packed_batches(lengths, B, N, seed, epoch, offsets=None, tokens=None, pad_token=0):
     """One epoch of fixed-shape packed batches: pack every sequence with
     pa_pack_first_fit into as many rows as it needs, then yield consecutive
-    groups of B rows as dicts of seg, loss_mask and row_tokens, each (B, N).
+    groups of B rows as dicts of seg, loss_mask, row_tokens and row_targets,
+    each (B, N).
     Rows of the last batch that hold no sequence are one padding segment with
     no supervised token. Sequences longer than N are left out."""
     B = int(B)
@@ -375,7 +382,7 @@ def packed_batches(lengths, B, N, seed, epoch, offsets=None, tokens=None, pad_to
     r = pa_pack_first_fit(lengths, rows, N, seed, epoch, offsets, tokens, pad_token)
     for b in range(-(-r["rows_used"] // B)):
         sl = slice(b * B, (b + 1) * B)
-        yield {k: (None if r[k] is None else r[k][sl]) for k in ("seg", "loss_mask", "row_tokens")}
+        yield {k: (None if r[k] is None else r[k][sl]) for k in ("seg", "loss_mask", "row_tokens", "row_targets")}
 
 
 def pa_lce_workspace_bytes(N, V, D) -> int:

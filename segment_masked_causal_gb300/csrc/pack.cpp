@@ -68,8 +68,8 @@ class FreeTree {
 // allocation failure leaves the outputs untouched.
 pa_status pack(const int32_t* lengths, const int32_t* offsets, int32_t count, const int32_t* tokens,
                int32_t pad_token, int32_t rows, int32_t N, uint64_t seed, uint64_t epoch, int32_t* seg,
-               uint8_t* loss_mask, int32_t* row_tokens, int64_t* placement, int32_t* rows_used,
-               int64_t* placed_tokens) {
+               uint8_t* loss_mask, int32_t* row_tokens, int32_t* row_targets, int64_t* placement,
+               int32_t* rows_used, int64_t* placed_tokens) {
   // where each sequence's tokens start in the concatenated `tokens`
   std::vector<int64_t> src(count);
   int64_t total = 0;
@@ -97,6 +97,8 @@ pa_status pack(const int32_t* lengths, const int32_t* offsets, int32_t count, co
   if (loss_mask) std::memset(loss_mask, 0, (size_t)cells);
   if (row_tokens)
     for (int64_t k = 0; k < cells; ++k) row_tokens[k] = pad_token;
+  if (row_targets)
+    for (int64_t k = 0; k < cells; ++k) row_targets[k] = -1;
   if (placement)
     for (int32_t i = 0; i < count; ++i) placement[i] = -1;
   int64_t placed = 0;
@@ -109,11 +111,12 @@ pa_status pack(const int32_t* lengths, const int32_t* offsets, int32_t count, co
     const int64_t base = (int64_t)r * N + used[r];
     const int32_t id = nseg[r]++;
     for (int32_t p = 0; p < L; ++p) seg[base + p] = id;
-    if (loss_mask) {
-      // Position p predicts token p + 1 of the same sequence; it is supervised
-      // when that token is past the prompt: offset <= p + 1 <= L - 1.
-      const int32_t off = offsets ? offsets[s] : 0;
-      for (int32_t p = (off > 1 ? off - 1 : 0); p + 1 < L; ++p) loss_mask[base + p] = 1;
+    // Position p predicts token p + 1 of the same sequence; it is supervised
+    // when that token is past the prompt: offset <= p + 1 <= L - 1.
+    const int32_t off = offsets ? offsets[s] : 0;
+    for (int32_t p = (off > 1 ? off - 1 : 0); p + 1 < L; ++p) {
+      if (loss_mask) loss_mask[base + p] = 1;
+      if (row_targets) row_targets[base + p] = tokens[src[s] + p + 1];
     }
     if (row_tokens) std::memcpy(row_tokens + base, tokens + src[s], sizeof(int32_t) * (size_t)L);
     if (placement) placement[s] = base;
@@ -134,9 +137,9 @@ pa_status pack(const int32_t* lengths, const int32_t* offsets, int32_t count, co
 extern "C" pa_status pa_pack_first_fit(const int32_t* lengths, const int32_t* offsets, int32_t count,
                                        const int32_t* tokens, int32_t pad_token, int32_t rows, int32_t N,
                                        uint64_t seed, uint64_t epoch, int32_t* seg, uint8_t* loss_mask,
-                                       int32_t* row_tokens, int64_t* placement, int32_t* rows_used,
-                                       int64_t* placed_tokens) {
-  if (!seg || (count > 0 && !lengths) || (row_tokens && count > 0 && !tokens)) return PA_ERR_NULL;
+                                       int32_t* row_tokens, int32_t* row_targets, int64_t* placement,
+                                       int32_t* rows_used, int64_t* placed_tokens) {
+  if (!seg || (count > 0 && !lengths) || ((row_tokens || row_targets) && count > 0 && !tokens)) return PA_ERR_NULL;
   if (count < 0 || rows <= 0 || N <= 0) return PA_ERR_SHAPE;
   for (int32_t i = 0; i < count; ++i)
     if (lengths[i] <= 0 || (offsets && offsets[i] < 0)) return PA_ERR_SHAPE;
@@ -144,7 +147,7 @@ extern "C" pa_status pa_pack_first_fit(const int32_t* lengths, const int32_t* of
   // is the only thing here that can throw
   try {
     return pack(lengths, offsets, count, tokens, pad_token, rows, N, seed, epoch, seg, loss_mask, row_tokens,
-                placement, rows_used, placed_tokens);
+                row_targets, placement, rows_used, placed_tokens);
   } catch (const std::bad_alloc&) {
     return PA_ERR_HOST_MEMORY;
   }

@@ -23,14 +23,17 @@ int main(void) {
   const int32_t lengths[3] = {5, 4, 3};
   const int32_t offsets[3] = {2, 0, 1};
   const int32_t tokens[12] = {10, 11, 12, 13, 14, 20, 21, 22, 23, 30, 31, 32};
-  int32_t seg[16], rows_tok[16], used = -1;
+  int32_t seg[16], rows_tok[16], rows_tgt[16], used = -1;
   uint8_t mask[16];
   int64_t placement[3], placed = -1;
-  CHECK(pa_pack_first_fit(lengths, offsets, 3, tokens, -1, 2, 8, 7, 0, seg, mask, rows_tok, placement, &used,
-                          &placed) == PA_OK);
+  CHECK(pa_pack_first_fit(lengths, offsets, 3, tokens, -1, 2, 8, 7, 0, seg, mask, rows_tok, rows_tgt, placement,
+                          &used, &placed) == PA_OK);
   CHECK(placed == 12 && used == 2);
   int64_t sup = 0;
-  for (int i = 0; i < 16; ++i) sup += mask[i];
+  for (int i = 0; i < 16; ++i) {
+    sup += mask[i];
+    CHECK(mask[i] ? rows_tgt[i] == rows_tok[i + 1] : rows_tgt[i] == -1);
+  }
   CHECK(sup == (5 - 2) + (4 - 1) + (3 - 1)); /* max(0, L - max(offset, 1)) per sequence */
   for (int s = 0; s < 3; ++s) {
     int64_t at = placement[s], start = 0;
@@ -38,8 +41,10 @@ int main(void) {
     CHECK(at >= 0 && at + lengths[s] <= 16);
     CHECK(memcmp(rows_tok + at, tokens + start, sizeof(int32_t) * (size_t)lengths[s]) == 0);
   }
-  CHECK(pa_pack_first_fit(lengths, offsets, 3, NULL, 0, 0, 8, 7, 0, seg, NULL, NULL, NULL, NULL, NULL) ==
+  CHECK(pa_pack_first_fit(lengths, offsets, 3, NULL, 0, 0, 8, 7, 0, seg, NULL, NULL, NULL, NULL, NULL, NULL) ==
         PA_ERR_SHAPE);
+  CHECK(pa_pack_first_fit(lengths, offsets, 3, NULL, 0, 2, 8, 7, 0, seg, NULL, NULL, rows_tgt, NULL, NULL, NULL) ==
+        PA_ERR_NULL);
 
   /* device calls refuse bad arguments on the host, before any device call */
   pa_dims d = {1, 4, 2, 256, 80, 0.0f};

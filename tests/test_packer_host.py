@@ -160,6 +160,10 @@ def test_oracle_pack_supervised_pairs_equal_unpacked():
             if p + 1 >= offsets[s]:
                 alone_pairs.append((seq[p], seq[p + 1]))
     assert sorted(packed_pairs) == sorted(alone_pairs)
+    tg = np.asarray(res["row_targets"])
+    target_pairs = [(int(rt[r, t]), int(tg[r, t])) for r, t in zip(*np.nonzero(tg >= 0))]
+    assert sorted(target_pairs) == sorted(alone_pairs)
+    assert ((tg >= 0) == (m == 1)).all()
 
 
 # ------------------------------------------------------- library vs oracle
@@ -168,7 +172,7 @@ def _lib_pack(lengths, rows, N, seed, epoch, offsets=None, tokens=None, pad_toke
 
 
 def _assert_same(lib_res, orc_res):
-    for k in ("seg", "loss_mask", "row_tokens"):
+    for k in ("seg", "loss_mask", "row_tokens", "row_targets"):
         if orc_res[k] is None:
             assert lib_res[k] is None
             continue
@@ -297,7 +301,7 @@ def _raw(L, lengths, count, rows, N, offsets=None, tokens=None, seg=True, row_to
     code = L.pa_pack_first_fit(None if la is None else la.ctypes.data, None if oa is None else oa.ctypes.data,
                                count, None if ta is None else ta.ctypes.data, 0, rows, N, 0, 0,
                                seg_buf.ctypes.data if seg else None, None,
-                               tok_buf.ctypes.data if row_tokens else None, None, None, None)
+                               tok_buf.ctypes.data if row_tokens else None, None, None, None, None)
     return code, seg_buf, tok_buf
 
 
@@ -348,3 +352,17 @@ def test_packed_rows_are_sorted_runs(L):
     assert (np.diff(seg, axis=1) >= 0).all()
     assert (np.diff(seg, axis=1) <= 1).all()
     assert (seg[:, 0] == 0).all()
+
+
+def test_row_targets_are_the_next_token_where_supervised(L):
+    """row_targets: the next token of the same sequence where the loss mask
+    is 1, else -1 (the ignored target of the fused cross-entropy)."""
+    rng = np.random.default_rng(11)
+    lengths, offsets = _random_dataset(rng, 70, 1, 200, 512)
+    tokens = [int(t) for t in rng.integers(0, 1 << 20, size=sum(lengths))]
+    r = _lib_pack(lengths, 12, 512, 3, 1, offsets, tokens, pad_token=-5)
+    m, rt, tg, seg = r["loss_mask"], r["row_tokens"], r["row_targets"], r["seg"]
+    assert (tg[m == 0] == -1).all()
+    rr, tt = np.nonzero(m)
+    assert (tg[rr, tt] == rt[rr, tt + 1]).all() and (seg[rr, tt] == seg[rr, tt + 1]).all()
+    assert (tg[m == 1] >= 0).all()
