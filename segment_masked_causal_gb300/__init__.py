@@ -369,20 +369,37 @@ def pa_pack_first_fit(lengths, rows, N, seed=0, epoch=0, offsets=None, tokens=No
             "placement": placement, "rows_used": int(used.value), "placed_tokens": int(placed.value)}
 
 
-def packed_batches(lengths, B, N, seed, epoch, offsets=None, tokens=None, pad_token=0):
+def packed_batches(lengths, B, N, seed, epoch, offsets=None, tokens=None, pad_token=0, rank=0, world=1):
     """One epoch of fixed-shape packed batches: pack every sequence with
     pa_pack_first_fit into as many rows as it needs, then yield consecutive
     groups of B rows as dicts of seg, loss_mask, row_tokens and row_targets,
     each (B, N).
     Rows of the last batch that hold no sequence are one padding segment with
-    no supervised token. Sequences longer than N are left out."""
-    B = int(B)
+    no supervised token. Sequences longer than N are left out.
+
+    Data parallel: with world > 1, every rank packs the same epoch (same seed
+    and epoch give the same rows) and takes batches rank, rank + world, ...;
+    every rank gets the same number of batches, the missing ones being all
+    padding (no supervised token), so ranks that step together never wait on
+    one that ran out."""
+    import numpy as np
+    B, world, rank = int(B), int(world), int(rank)
+    if not 0 <= rank < world:
+        raise ValueError("need 0 <= rank < world")
     count = len(lengths)
     rows = max(-(-count // B), 1) * B
     r = pa_pack_first_fit(lengths, rows, N, seed, epoch, offsets, tokens, pad_token)
-    for b in range(-(-r["rows_used"] // B)):
-        sl = slice(b * B, (b + 1) * B)
-        yield {k: (None if r[k] is None else r[k][sl]) for k in ("seg", "loss_mask", "row_tokens", "row_targets")}
+    keys = ("seg", "loss_mask", "row_tokens", "row_targets")
+    fill = {"seg": 0, "loss_mask": 0, "row_tokens": pad_token, "row_targets": -1}
+    n_batches = -(-r["rows_used"] // B)
+    per_rank = -(-n_batches // world)
+    for i in range(per_rank):
+        b = rank + i * world
+        if b < n_batches:
+            sl = slice(b * B, (b + 1) * B)
+            yield {k: (None if r[k] is None else r[k][sl]) for k in keys}
+        else:
+            yield {k: (None if r[k] is None else np.full((B, N), fill[k], dtype=r[k].dtype)) for k in keys}
 
 
 def pa_lce_workspace_bytes(N, V, D) -> int:

@@ -366,3 +366,29 @@ def test_row_targets_are_the_next_token_where_supervised(L):
     rr, tt = np.nonzero(m)
     assert (tg[rr, tt] == rt[rr, tt + 1]).all() and (seg[rr, tt] == seg[rr, tt + 1]).all()
     assert (tg[m == 1] >= 0).all()
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 4])
+def test_packed_batches_shard_across_ranks(world, L):
+    """Every rank gets the same number of (B, N) batches; together they hold
+    each packed batch exactly once, and the extras are all padding."""
+    rng = np.random.default_rng(21)
+    lengths, offsets = _random_dataset(rng, 130, 4, 500, 1024)
+    tokens = list(range(sum(lengths)))
+    whole = list(pa.packed_batches(lengths, 2, 1024, 4, 0, offsets, tokens, pad_token=-1))
+    per = [list(pa.packed_batches(lengths, 2, 1024, 4, 0, offsets, tokens, pad_token=-1, rank=r, world=world))
+           for r in range(world)]
+    assert len({len(p) for p in per}) == 1
+    seen = []
+    for r, batches in enumerate(per):
+        for i, b in enumerate(batches):
+            idx = r + i * world
+            if idx < len(whole):
+                for k in ("seg", "loss_mask", "row_tokens", "row_targets"):
+                    np.testing.assert_array_equal(b[k], whole[idx][k])
+                seen.append(idx)
+            else:
+                assert b["loss_mask"].sum() == 0 and (b["row_targets"] == -1).all() and (b["seg"] == 0).all()
+    assert sorted(seen) == list(range(len(whole)))
+    with pytest.raises(ValueError):
+        next(pa.packed_batches(lengths, 2, 1024, 4, 0, rank=world, world=world))
