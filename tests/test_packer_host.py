@@ -392,3 +392,20 @@ def test_packed_batches_shard_across_ranks(world, L):
     assert sorted(seen) == list(range(len(whole)))
     with pytest.raises(ValueError):
         next(pa.packed_batches(lengths, 2, 1024, 4, 0, rank=world, world=world))
+
+
+def test_packer_is_reentrant_across_threads(L):
+    """Concurrent calls from several threads (ctypes releases the GIL) return
+    the same results as serial calls: the packer keeps no shared state."""
+    import concurrent.futures as cf
+    rng = np.random.default_rng(31)
+    jobs = []
+    for j in range(16):
+        lengths, offsets = _random_dataset(rng, 400, 1, 300, 1024)
+        jobs.append((lengths, offsets, 1000 + j))
+    serial = [_lib_pack(l, 60, 1024, s, 1, o) for l, o, s in jobs]
+    with cf.ThreadPoolExecutor(8) as ex:
+        threaded = list(ex.map(lambda a: _lib_pack(a[0], 60, 1024, a[2], 1, a[1]), jobs))
+    for a, b in zip(serial, threaded):
+        np.testing.assert_array_equal(a["seg"], b["seg"])
+        np.testing.assert_array_equal(a["placement"], b["placement"])
