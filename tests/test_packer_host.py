@@ -409,3 +409,42 @@ def test_packer_is_reentrant_across_threads(L):
     for a, b in zip(serial, threaded):
         np.testing.assert_array_equal(a["seg"], b["seg"])
         np.testing.assert_array_equal(a["placement"], b["placement"])
+
+
+def test_packed_loss_equals_unpacked_loss(L):
+    """The supervised set is that of an unpacked run (0.5.1 README, "Sequence
+    packing"), at the level of the loss: given each token's final hidden
+    state, the masked mean NLL over the packed rows -- targets from
+    row_targets, -1 ignored -- equals the mean over every sequence run alone
+    under the unpacked rule (the fp64 cross-entropy oracle on both sides)."""
+    from oracle import linear_ce as lce
+    rng = np.random.default_rng(41)
+    V, D, N, rows = 97, 12, 256, 6
+    lengths, offsets = _random_dataset(rng, 25, 1, 120, N)
+    tokens = [int(t) for t in rng.integers(0, V, size=sum(lengths))]
+    W = rng.standard_normal((V, D))
+    hid = rng.standard_normal((sum(lengths), D))  # each token's hidden state, unpacked order
+    r = _lib_pack(lengths, rows, N, 8, 0, offsets, tokens, pad_token=0)
+    starts = np.concatenate([[0], np.cumsum(lengths)[:-1]]).astype(np.int64)
+
+    packed_h = rng.standard_normal((rows * N, D))  # padding rows: anything
+    for s, at in enumerate(r["placement"]):
+        if at >= 0:
+            packed_h[at:at + lengths[s]] = hid[starts[s]:starts[s] + lengths[s]]
+    tg = r["row_targets"].reshape(-1)
+    keep = tg >= 0
+    nll_p, _, _ = lce.forward(packed_h[keep], W, tg[keep])
+
+    nll_u = []
+    for s, at in enumerate(r["placement"]):
+        if at < 0:
+            continue
+        L_, o = lengths[s], offsets[s]
+        seq_t = tokens[starts[s]:starts[s] + L_]
+        pos = [p for p in range(L_ - 1) if p + 1 >= o]
+        if pos:
+            nll_u.append(lce.forward(hid[starts[s] + np.array(pos)], W, [seq_t[p + 1] for p in pos])[0])
+    nll_u = np.concatenate(nll_u)
+    assert len(nll_p) == len(nll_u) == int(r["loss_mask"].sum())
+    assert nll_p.mean() == pytest.approx(nll_u.mean(), rel=1e-12)
+    np.testing.assert_allclose(np.sort(nll_p), np.sort(nll_u), rtol=1e-12)
