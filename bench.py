@@ -10,7 +10,7 @@ into packed segments is measured too and reported under "packed".
 
 Timing: W warm-up steps, then K timed steps; every step is bracketed by CUDA
 events on the launching stream, with the L2 flushed (a 256 MiB write) between
-steps outside the events. Useful FLOPs count only visible pairs (j <= i, same
+steps outside the events; reported times are the median over the K steps. Useful FLOPs count only visible pairs (j <= i, same
 segment, padding segments excluded): 4*D per pair forward, 10*D backward.
 Under torchrun each rank runs its own replica of the workload (weak scaling,
 no collective on the data path); the reported time is the max over ranks.
@@ -231,8 +231,26 @@ class Runner:
         pa.pa_bwd_dkv(q, k, v, do, self.lse, seg, self.dk, self.dv, self.ws)
         rec(ev[6])
 
+    def checked_step(self, causal=False):
+        """One untimed step that reads the status word after the forward and
+        after the backward (each tile-table step clears it)."""
+        pa, seg = self.pa, (None if causal else self.seg)
+        pa.pa_build_tile_table(self.q, self.k, seg, self.ws)
+        pa.pa_fwd_tiles(self.q, self.k, self.v, seg, self.out, self.lse, self.ws)
+        st = pa.pa_device_status(self.ws)
+        if st != 0:
+            raise RuntimeError(f"device status after the forward {st:#x}")
+        pa.pa_build_tile_table(self.q, self.k, seg, self.ws)
+        pa.pa_bwd_delta(self.q, self.k, self.out, self.do, self.lse, self.ws)
+        pa.pa_bwd_dq(self.q, self.k, self.v, self.do, self.lse, seg, self.dq, self.ws)
+        pa.pa_bwd_dkv(self.q, self.k, self.v, self.do, self.lse, seg, self.dk, self.dv, self.ws)
+        st = pa.pa_device_status(self.ws)
+        if st != 0:
+            raise RuntimeError(f"device status after the backward {st:#x}")
+
     def timed(self, steps: int, warmup: int, causal=False, sampler=None):
         torch = self.torch
+        self.checked_step(causal)
         for _ in range(warmup):
             self.step(causal=causal)
             self.flush()
@@ -256,7 +274,7 @@ class Runner:
             for n, key in enumerate(keys):
                 per[key].append(e[n].elapsed_time(e[n + 1]))
             per["step"].append(e[0].elapsed_time(e[6]))
-        return {k: statistics.mean(v) for k, v in per.items()}, clocks
+        return {k: statistics.median(v) for k, v in per.items()}, clocks
 
     def e2e(self, steps: int, warmup: int):
         """Public pa_fwd + pa_bwd with pinned host inputs/outputs: every step
@@ -386,7 +404,7 @@ def run_ours(args):
     kernels["delta"]["gbs"] = round(delta_bytes / (kern["delta"] * 1e-3) / 1e9, 1)
     kernels["delta"]["hbm_frac"] = round(kernels["delta"]["gbs"] / pk["hbm_gbs"], 4)
 
-    e2e_ms, h2d, d2h = r.e2e(max(3, min(args.steps, 10)), 2)
+    e2e_ms, h2d, d2h = r.e2e(args.steps, args.warmup)
     e2e_ms = reduce_max(e2e_ms, dev)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -413,6 +431,7 @@ def run_ours(args):
         line["packed"] = packed_extras(dev, rank, args)
         line["head_dim_96"] = head_dim_96_extra(dev, rank, args)
         line["staged_layouts"] = staged_layout_extras(dev, rank, args)
+        line["configs"] = config_extras(dev, rank, args)
     if not args.no_extras and w.name == "8k_one_segment" and rank == 0 and world == 1:
         line["linear_cross_entropy"] = lce_extra()
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -449,6 +468,107 @@ def packed_extras(dev, rank, args):
                   "packed_multi_ms": round(t_multi[k], 4),
                   "skip_speedup_vs_causal": round(t_causal[k] / t_multi[k], 3),
                   "one_segment_overhead_vs_causal": round(t_packed1[k] / t_causal[k] - 1.0, 4)}
+    return out
+
+
+def oracle_estimate(w: synth.Workload, max_rows: int = 2048) -> dict:
+    """The fp64 oracle's time for a whole fwd+bwd step of `w` on this host's
+    cores. The oracle's time does not depend on the values, so one query
+    head's worth of seeded inputs of the workload's shape is drawn. Rows with
+    up to ~4e9 (pairs x D) per head: the complete forward + backward of one
+    query head against its kv head (that head's share of dK/dV), times Hq.
+    Longer rows: forward and dQ of `max_rows` query rows spread evenly over
+    the head, scaled by visible pairs; the oracle's dK/dV visits the same pairs
+    with the same work per pair as its dQ, so the step is forward + 2 x dQ."""
+    import oracle
+    oracle.build()
+    shape = (w.B, 1, w.N, w.D)
+    q, k, v, do = (synth.bf16_bits_to_f64(synth.bf16_normal(w.seed, 11 + i, shape)) for i in range(4))
+    per_head = visible_pairs_per_head(w, exclude_padding=False)
+    if per_head * w.D <= 4e9:
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, w.seg, w.scale, do)
+        sec = (time.perf_counter() - t0) * w.Hq
+        sample = "complete fp64 forward + backward of one query head, times Hq"
+    else:
+        flat = w.B * w.N
+        rows = np.unique(np.linspace(0, flat - 1, min(max_rows, flat)).astype(np.int64))
+        # visible pairs of the sampled rows: the row's position in its segment, plus one
+        pos = np.concatenate([np.concatenate([np.arange(L) for L in lens]) for lens, _ in segment_lengths(w)])
+        pairs = float(np.sum(pos[rows] + 1))
+        t0 = time.perf_counter()
+        o, lse, delta = oracle.forward(q, k, v, w.seg, w.scale, do, rows=rows)
+        t1 = time.perf_counter()
+        lse_f, delta_f = np.zeros((w.B, 1, w.N)), np.zeros((w.B, 1, w.N))
+        lse_f.reshape(-1)[rows], delta_f.reshape(-1)[rows] = lse.reshape(-1), delta.reshape(-1)
+        oracle.dq(q, k, v, w.seg, w.scale, do, lse_f, delta_f, rows=rows)
+        t2 = time.perf_counter()
+        sec = ((t1 - t0) + 2 * (t2 - t1)) / pairs * per_head * w.Hq
+        sample = (f"forward and dQ of {len(rows)} query rows of one head, scaled by visible pairs "
+                  f"(step = forward + 2 x dQ)")
+    return {"seconds_per_step_est": round(sec, 2), "cores": oracle.num_threads(), "sample": sample}
+
+
+def _kernel_ms(t):
+    return {k: round(t[k], 4) for k in ("fwd", "delta", "dq", "dkv")}
+
+
+def config_extras(dev, rank, args):
+    """Every other configuration of the target, each timed as the main line
+    is (the steps of pa_fwd + pa_bwd, L2 flushed between steps): config 2
+    (2k GQA causal), config 3 (short packed rows, the pages' Alpaca
+    analogue) against the causal entry points and the same rows in one
+    segment, and config 5 (32k / 64k rows at head dim 64, one segment and
+    packed). Each reports useful TFLOP/s, its fraction of the measured bf16
+    peak and the oracle's estimated time for the same step."""
+    steps = max(3, min(args.steps, 10))
+    pk = peaks()
+    out = {}
+
+    def entry(w, t):
+        flops = useful_flops(w)
+        return {"B": w.B, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                "segments": sum(len(l) for l in w.lengths), "ms_per_step": round(t["step"], 4),
+                "useful_tflops": round(flops / (t["step"] * 1e-3) / 1e12, 3),
+                "frac_of_peak": round(flops / (t["step"] * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+                "kernels_ms": _kernel_ms(t)}
+
+    def run(w, causal=False):
+        r = Runner(w, dev, replica_seed(w.seed, rank))
+        t, _ = r.timed(steps, 2, causal=causal)
+        del r
+        return t
+
+    w2 = synth.workload("causal_2k_gqa")
+    out["causal_2k_gqa"] = entry(w2, run(w2))
+    # config 3: packed rows vs the causal kernels on the same tokens, and the
+    # packed kernels on the same shape in one segment per row
+    w3 = synth.workload("packed_4x4096_short")
+    t_multi = run(w3)
+    t_causal = run(w3, causal=True)
+    one = synth.custom(w3.B, w3.Hq, w3.Hkv, w3.N, w3.D, [[w3.N]] * w3.B, seed=w3.seed)
+    t_one = run(one)
+    e = entry(w3, t_multi)
+    e["visible_fraction_of_causal"] = round(visible_pairs_per_head(w3) / visible_pairs_per_head(one), 4)
+    e["executed_tile_fraction_of_causal"] = round(executed_tile_pairs(w3) / executed_tile_pairs(one), 4)
+    for k in ("fwd", "dq", "dkv", "step"):
+        e[k] = {"causal_ms": round(t_causal[k], 4), "packed_one_segment_ms": round(t_one[k], 4),
+                "packed_multi_ms": round(t_multi[k], 4),
+                "skip_speedup_vs_causal": round(t_causal[k] / t_multi[k], 3),
+                "one_segment_overhead_vs_causal": round(t_one[k] / t_causal[k] - 1.0, 4)}
+    out["packed_4x4096_short"] = e
+    for n in (32, 64):
+        w1 = synth.workload(f"long_{n}k_one_segment")
+        wp = synth.workload(f"long_{n}k_packed")
+        t1, tp = run(w1), run(wp)
+        out[w1.name] = entry(w1, t1)
+        e = entry(wp, tp)
+        e["executed_tile_fraction_of_one_segment"] = round(executed_tile_pairs(wp) / executed_tile_pairs(w1), 4)
+        e["skip_speedup_vs_one_segment"] = {k: round(t1[k] / tp[k], 3) for k in ("fwd", "dq", "dkv", "step")}
+        out[wp.name] = e
+    if rank == 0 and not args.no_cpu:
+        for name in out:
+            out[name]["oracle"] = oracle_estimate(synth.workload(name))
     return out
 
 
@@ -505,7 +625,7 @@ def staged_layout_extras(dev, rank, args):
             ts.append(a.elapsed_time(b))
         if pa.pa_device_status(ws) != 0:
             raise RuntimeError("device status after staged-layout run")
-        return statistics.mean(ts)
+        return statistics.median(ts)
 
     one_seg = synth.workload("8k_one_segment")
     r = Runner(one_seg, dev, replica_seed(one_seg.seed, rank))
@@ -554,7 +674,7 @@ def lce_measure(steps: int = 5, warmup: int = 2) -> dict:
         b.record()
     torch.cuda.synchronize()
     status = pa.pa_device_status(ws)
-    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
     tflops = 2.0 * N * V * D / (ms * 1e-3) / 1e12
     pk = peaks()
     return {"workload": f"N{N} V{V} D{D} bf16", "ms": round(ms, 4), "tflops": round(tflops, 2),

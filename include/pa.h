@@ -31,9 +31,15 @@
  *
  * Ownership: every pointer is device memory owned by the caller. The library
  * allocates no device memory and keeps no pointer after a call returns. The
- * workspace `ws` (pa_workspace_bytes) holds the per-tile segment-range table,
- * the backward's per-row delta = rowsum(dO * O) and lse * log2(e), and a
- * device status word.
+ * workspace `ws` (pa_workspace_bytes) holds, in this order and each region
+ * starting on a 256-byte boundary: the device status word (uint32 at byte
+ * 0); the per-tile segment-range table, (B, N/128) int4 {smallest id,
+ * largest id, first key tile whose id range overlaps, last query tile whose
+ * id range overlaps} at byte 256; two work lists of B*N/128 int32 entries
+ * b*(N/128) + t each, the query tiles and then the key tiles ordered by
+ * decreasing walk length; then the backward's per-row delta = rowsum(dO * O)
+ * and lse * log2(e). For N % 128 != 0 the table and lists describe the
+ * padded row (N rounded up to 128).
  *
  * Execution: every call validates its arguments synchronously and returns an
  * error before launching anything; otherwise it enqueues its kernels on
@@ -176,8 +182,9 @@ pa_status pa_bwd_strided(const pa_dims* dims, const pa_strides* strides, int32_t
  * stream, in that order. The later steps read the tile table (and the bwd
  * steps the per-row values of pa_bwd_delta) from `ws`, so they must follow
  * the steps that write it with the same dims and the same seg (NULL seg =
- * plain causal throughout). pa_build_tile_table also clears the workspace
- * status word. pa_bwd_delta takes the forward's out and lse and stores, per
+ * plain causal throughout). pa_build_tile_table writes the tile table and
+ * the two work lists (the forward, dQ and dK/dV calls take their tiles in
+ * that order) and clears the workspace status word. pa_bwd_delta takes the forward's out and lse and stores, per
  * query row, delta = rowsum(dO * O) and lse * log2(e) (the dK/dV step reads
  * that copy; pa_bwd_dkv still validates its lse argument). These calls take
  * contiguous tensors with N % 128 == 0 only (else PA_ERR_SHAPE).
@@ -205,8 +212,13 @@ pa_status pa_bwd_dkv(const pa_dims* dims, const void* q, const void* k, const vo
  * device array of PA_NOALLOC_SCRATCH_BYTES (8 MiB) inside the library, held by
  * every GPU that loads the library until the process exits. The call makes no
  * allocation of any kind.
- *   - Limit: dims whose pa_workspace_bytes exceeds PA_NOALLOC_SCRATCH_BYTES
- *     (about B*Hq*N > 1 million query rows) are refused with PA_ERR_WORKSPACE.
+ *   - Limit: the call runs when pa_workspace_bytes(dims) <=
+ *     PA_NOALLOC_SCRATCH_BYTES and is refused with PA_ERR_WORKSPACE
+ *     otherwise; compare the two before calling. With N % 128 == 0 that is
+ *     about 1 million query rows (B*Hq*N: 8 bytes of scratch per row). With
+ *     N % 128 != 0 the workspace also holds the staging copies (about
+ *     8*D*(1 + Hkv/Hq) + 12 bytes per query row), which caps it far lower:
+ *     roughly 4,000 to 6,500 query rows at D = 128.
  *   - The first call on each device looks up the array's device address with
  *     that device current; make that first call before any stream capture.
  *   - Every call on a device shares the one array, which keeps the last call's

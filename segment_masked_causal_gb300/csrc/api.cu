@@ -27,7 +27,7 @@ inline bool tiled(const pa_dims* d) { return d->N % pa::kTile == 0; }
 // padded_n, then the staging copies used when the caller's tensors are not in
 // the kernels' layout (N not a multiple of 128, or strided tensors).
 struct WsLayout {
-  size_t status, tiles, delta, lse2, base;
+  size_t status, tiles, work_q, work_k, delta, lse2, base;
   size_t sq, sk, sv, so, sdo, sdq, sdk, sdv, slse, sseg, staged;
 };
 
@@ -53,7 +53,9 @@ WsLayout ws_layout(const pa_dims* d) {
   const size_t qb = round_up(qrows * d->D * 2), kb = round_up(krows * d->D * 2);
   w.status = 0;
   w.tiles = kAlign;
-  w.delta = w.tiles + round_up((size_t)d->B * T * sizeof(int4));
+  w.work_q = w.tiles + round_up((size_t)d->B * T * sizeof(int4));
+  w.work_k = w.work_q + round_up((size_t)d->B * T * sizeof(int32_t));
+  w.delta = w.work_k + round_up((size_t)d->B * T * sizeof(int32_t));
   w.lse2 = w.delta + round_up(qrows * sizeof(float));
   w.base = w.lse2 + round_up(qrows * sizeof(float));
   w.sq = w.base;
@@ -72,8 +74,12 @@ WsLayout ws_layout(const pa_dims* d) {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+pa_status device_ok() { return pa::device_check(); }
+
+}  // namespace
+
 // Per-device: compute capability 10.3 and enough opt-in shared memory.
-pa_status device_ok() {
+pa_status pa::device_check() {
   static std::mutex mu;
   static int checked[64] = {0};  // 0 unknown, 1 ok, 2 refused
   int dev = 0;
@@ -91,6 +97,8 @@ pa_status device_ok() {
   return checked[dev] == 1 ? PA_OK : PA_ERR_ARCH;
 }
 
+namespace {
+
 pa::AttnParams make_params(const pa_dims* d, const int32_t* seg, void* ws) {
   pa::AttnParams p{};
   p.B = d->B; p.Hq = d->Hq; p.Hkv = d->Hkv; p.N = d->N; p.T = d->N / pa::kTile; p.G = d->Hq / d->Hkv;
@@ -101,6 +109,8 @@ pa::AttnParams make_params(const pa_dims* d, const int32_t* seg, void* ws) {
   uint8_t* base = static_cast<uint8_t*>(ws);
   p.status = reinterpret_cast<uint32_t*>(base + w.status);
   p.tiles = reinterpret_cast<const int4*>(base + w.tiles);
+  p.work_q = reinterpret_cast<const int32_t*>(base + w.work_q);
+  p.work_k = reinterpret_cast<const int32_t*>(base + w.work_k);
   p.delta = reinterpret_cast<float*>(base + w.delta);
   p.lse2 = reinterpret_cast<float*>(base + w.lse2);
   return p;

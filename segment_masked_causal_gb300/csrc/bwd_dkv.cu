@@ -100,10 +100,10 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
   const uint32_t sQ = smem_u32(base + L::OFF_Q), sDO = smem_u32(base + L::OFF_DO);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // heaviest causal walks (smallest key tile index) first, across all heads
-  const int per_tile = p.Hkv * p.B;
-  const int tk = (int)blockIdx.x / per_tile;
-  const int hk = (int)blockIdx.x % p.Hkv, b = ((int)blockIdx.x / p.Hkv) % p.B;
+  // the prologue's work list: longest query walks first, all kv heads of a tile together
+  const int ent = p.work_k[(int)blockIdx.x / p.Hkv];
+  const int tk = ent % p.T, b = ent / p.T;
+  const int hk = (int)blockIdx.x % p.Hkv;
   const int4* trow = p.tiles + (size_t)b * p.T;
   const Guard g{&m.abort_flag, p.status};
   const QWalk walk(trow, tk);

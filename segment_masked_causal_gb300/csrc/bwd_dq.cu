@@ -80,10 +80,10 @@ __global__ void __launch_bounds__(352, 1)
   const uint32_t sK = smem_u32(base + L::OFF_K), sV = smem_u32(base + L::OFF_V);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // longest causal rows first, across all heads and batch rows
-  const int per_tile = p.Hq * p.B;
-  const int tq = p.T - 1 - (int)blockIdx.x / per_tile;
-  const int h = (int)blockIdx.x % p.Hq, b = ((int)blockIdx.x / p.Hq) % p.B, hk = h / p.G;
+  // the prologue's work list: the same order as the forward: longest key walks first, all heads of a tile together
+  const int ent = p.work_q[(int)blockIdx.x / p.Hq];
+  const int tq = ent % p.T, b = ent / p.T;
+  const int h = (int)blockIdx.x % p.Hq, hk = h / p.G;
   const int4* trow = p.tiles + (size_t)b * p.T;
   const Guard g{&m.abort_flag, p.status};
 

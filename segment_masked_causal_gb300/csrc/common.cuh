@@ -29,6 +29,11 @@ struct AttnParams {
   float scale_log2;  // scale * log2(e)
   const int32_t* seg;   // (B, N) or null (every token in one segment)
   const int4* tiles;    // (B, T) table written by the prologue
+  // Work lists written by the prologue: entries b*T + t, longest walks first;
+  // work_q orders the query tiles of the forward and dQ kernels, work_k the
+  // key tiles of the dK/dV kernel.
+  const int32_t* work_q;
+  const int32_t* work_k;
   uint32_t* status;     // device status word
   // forward outputs
   __nv_bfloat16* out;

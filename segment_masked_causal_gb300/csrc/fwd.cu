@@ -1,6 +1,7 @@
 // fwd.cu -- packed (block-diagonal causal) attention forward for sm_103a.
 //
-// One CTA per (query tile of 128 rows, query head, batch row). It visits only
+// One CTA per (query tile of 128 rows, query head, batch row), launched in the
+// order of the prologue's work list (longest key walks first). It visits only
 // key tiles whose segment-id range overlaps the query tile's (the changelog's
 // PACKED forward: cross-segment blocks are skipped, not masked) and applies
 // the element mask (j <= i and seg[i] == seg[j]) only on tile pairs that are
@@ -152,10 +153,10 @@ __global__ void __launch_bounds__(352, 1)
   const uint32_t sQ = smem_u32(base + L::OFF_Q), sK = smem_u32(base + L::OFF_K), sV = smem_u32(base + L::OFF_V);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // longest causal rows first, across all heads and batch rows
-  const int per_tile = p.Hq * p.B;
-  const int tq = p.T - 1 - (int)blockIdx.x / per_tile;
-  const int h = (int)blockIdx.x % p.Hq, b = ((int)blockIdx.x / p.Hq) % p.B, hk = h / p.G;
+  // the prologue's work list: longest key walks first, all heads of a tile together
+  const int ent = p.work_q[(int)blockIdx.x / p.Hq];
+  const int tq = ent % p.T, b = ent / p.T;
+  const int h = (int)blockIdx.x % p.Hq, hk = h / p.G;
   const int4* trow = p.tiles + (size_t)b * p.T;
   const Guard g{&m.abort_flag, p.status};
 

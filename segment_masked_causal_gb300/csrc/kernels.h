@@ -2,11 +2,18 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include "../../include/pa.h"
 #include "common.cuh"
 
 namespace pa {
 
-// Tile table (B, T) x {smin, smax, kv_lo, q_hi}; also clears the status word.
+// PA_OK when the current device is compute capability 10.3 with enough
+// opt-in shared memory for the kernels, else PA_ERR_ARCH (or PA_ERR_CUDA if
+// the query itself fails). Cached per device.
+pa_status device_check();
+
+// Tile table (B, T) x {smin, smax, kv_lo, q_hi} and the two work lists; also
+// clears the status word.
 cudaError_t launch_tile_table(const AttnParams& p, int4* tiles, cudaStream_t st);
 // delta[b, h, i] = sum_c dO[b, h, i, c] * O[b, h, i, c] (fp32), and lse2 = lse * log2(e).
 cudaError_t launch_delta(const AttnParams& p, int D, cudaStream_t st);

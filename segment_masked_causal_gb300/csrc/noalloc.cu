@@ -21,6 +21,7 @@
 #include <mutex>
 
 #include "../../include/pa.h"
+#include "kernels.h"
 
 constexpr size_t kScratchBytes = size_t(8) << 20;
 static_assert(kScratchBytes == PA_NOALLOC_SCRATCH_BYTES, "header and array size disagree");
@@ -54,14 +55,20 @@ extern "C" pa_status pa_bwd_noalloc(const pa_dims* dims, const void* q, const vo
                                     const void* out, const void* dout, const float* lse, const int32_t* seg,
                                     void* dq, void* dk, void* dv, uint32_t* device_status, pa_stream_t stream) {
   const size_t need = pa_workspace_bytes(dims);
-  if (need == 0)  // invalid dims: let the regular entry point name the reason
-    return pa_bwd(dims, q, k, v, out, dout, lse, seg, dq, dk, dv, nullptr, 0, stream);
+  if (need == 0)  // invalid dims: let the regular entry point (causal when seg is NULL) name the reason
+    return seg ? pa_bwd(dims, q, k, v, out, dout, lse, seg, dq, dk, dv, nullptr, 0, stream)
+               : pa_bwd_causal(dims, q, k, v, out, dout, lse, dq, dk, dv, nullptr, 0, stream);
   if (need > kScratchBytes) return PA_ERR_WORKSPACE;
+  // The same device check as every other entry point, before the symbol
+  // lookup: on a device this library has no code for, that lookup would fail
+  // with a generic CUDA error instead of PA_ERR_ARCH.
+  pa_status s = pa::device_check();
+  if (s != PA_OK) return s;
   void* scratch = nullptr;
-  pa_status s = scratch_address(&scratch);
+  s = scratch_address(&scratch);
   if (s != PA_OK) return s;
   // Nothing needs clearing here: the tile-table kernel zeroes the status word
-  // and every later kernel overwrites the table and delta it reads.
+  // and every later kernel overwrites the table, work lists and delta it reads.
   s = seg ? pa_bwd(dims, q, k, v, out, dout, lse, seg, dq, dk, dv, scratch, kScratchBytes, stream)
           : pa_bwd_causal(dims, q, k, v, out, dout, lse, dq, dk, dv, scratch, kScratchBytes, stream);
   if (s != PA_OK || !device_status) return s;

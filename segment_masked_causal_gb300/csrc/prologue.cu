@@ -52,6 +52,101 @@ __global__ void __launch_bounds__(256) tile_table_kernel(const int32_t* __restri
   }
 }
 
+// Work lists: the (row, tile) entries b*T + t in decreasing order of the
+// number of tiles their walk visits at most -- key tiles kv_lo..tq for a
+// query tile of the forward and dQ kernels, query tiles tk..q_hi for a key
+// tile of the dK/dV kernel -- so the kernels start the longest walks first.
+// Ties keep a fixed canonical order (query tiles from the last down, key
+// tiles from the first up, batch rows increasing within one tile index), so a
+// row in one segment gets exactly the longest-causal-walk-first order and
+// the order never depends on timing. A counting sort over the costs 1..T:
+// all threads count, one scan turns the counts into starting positions, and
+// one warp per list places the entries 32 at a time, ranking equal costs
+// within the warp by lane so that the sort is stable.
+constexpr int kMaxSortedTiles = 4095;  // T above this: canonical order, unsorted
+
+__device__ __forceinline__ int canon_q(int e, int B, int T) { return (e % B) * T + (T - 1 - e / B); }
+__device__ __forceinline__ int canon_k(int e, int B, int T) { return (e % B) * T + e / B; }
+__device__ __forceinline__ int cost_q(int4 te, int t) { return t - te.z + 1; }
+__device__ __forceinline__ int cost_k(int4 te, int t) { return te.w - t + 1; }
+
+__global__ void __launch_bounds__(1024) work_list_kernel(const int4* __restrict__ tiles, int B, int T,
+                                                         int32_t* __restrict__ wq, int32_t* __restrict__ wk) {
+  const int n = B * T;
+  if (T > kMaxSortedTiles) {
+    for (int e = threadIdx.x; e < n; e += blockDim.x) {
+      wq[e] = canon_q(e, B, T);
+      wk[e] = canon_k(e, B, T);
+    }
+    return;
+  }
+  __shared__ int cnt[2][kMaxSortedTiles + 1];  // [list][cost]: counts, then next free position
+  __shared__ int part[2][32];
+  for (int c = threadIdx.x; c <= T; c += blockDim.x) cnt[0][c] = cnt[1][c] = 0;
+  __syncthreads();
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const int eq = canon_q(e, B, T), ek = canon_k(e, B, T);
+    atomicAdd(&cnt[0][cost_q(tiles[eq], eq % T)], 1);
+    atomicAdd(&cnt[1][cost_k(tiles[ek], ek % T)], 1);
+  }
+  __syncthreads();
+  // Starting position of cost c = entries of cost > c. Thread i sums a run of
+  // costs (highest first), the warps scan those sums, then each thread writes
+  // its run's starting positions.
+  const int per = (T + blockDim.x) / blockDim.x;  // costs per thread, covering 1..T
+  const int hi = T - threadIdx.x * per;           // this thread's run: costs hi, hi-1, .., hi-per+1 (>= 1)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int l = 0; l < 2; ++l) {
+    int s = 0;
+    for (int c = hi; c > hi - per && c >= 1; --c) s += cnt[l][c];
+    int x = s;  // inclusive scan over the block, in thread order
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(~0u, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) part[l][warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < (int)(blockDim.x >> 5) ? part[l][lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(~0u, w, o);
+        if (lane >= o) w += y;
+      }
+      part[l][lane] = w;
+    }
+    __syncthreads();
+    int pos = x - s + (warp > 0 ? part[l][warp - 1] : 0);  // exclusive start of this run
+    for (int c = hi; c > hi - per && c >= 1; --c) {
+      const int k = cnt[l][c];
+      cnt[l][c] = pos;
+      pos += k;
+    }
+    __syncthreads();
+  }
+  if (warp < 2) {
+    int32_t* out = warp == 0 ? wq : wk;
+    int* next = cnt[warp];
+    for (int e0 = 0; e0 < n; e0 += 32) {
+      const int e = e0 + lane;
+      const bool live = e < n;
+      int ent = 0, key = -1 - lane;  // lanes past the end take keys of their own
+      if (live) {
+        ent = warp == 0 ? canon_q(e, B, T) : canon_k(e, B, T);
+        key = warp == 0 ? cost_q(tiles[ent], ent % T) : cost_k(tiles[ent], ent % T);
+      }
+      const unsigned same = __match_any_sync(~0u, key);
+      const int rank = __popc(same & ((1u << lane) - 1u));
+      const int at = live ? next[key] + rank : 0;
+      __syncwarp();
+      if (live && rank == 0) next[key] += __popc(same);
+      __syncwarp();
+      if (live) out[at] = ent;
+    }
+  }
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -123,6 +218,10 @@ cudaError_t launch_tile_table(const AttnParams& p, int4* tiles, cudaStream_t st)
     if (e != cudaSuccess) return e;
   }
   tile_table_kernel<<<p.B, 256, smem, st>>>(p.seg, p.N, p.T, tiles, p.status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  work_list_kernel<<<1, 1024, 0, st>>>(tiles, p.B, p.T, const_cast<int32_t*>(p.work_q),
+                                       const_cast<int32_t*>(p.work_k));
   return cudaGetLastError();
 }
 

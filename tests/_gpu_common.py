@@ -43,10 +43,13 @@ class Case:
         q, k, v, do = self.q, self.k, self.v, self.do
         seg = None if causal else self.seg
         out, lse = pa.forward(q, k, v, seg, ws=self.ws)
+        # read after each call: the backward's tile-table step clears the word
+        st = pa.pa_device_status(self.ws)
+        assert st == 0, f"device status after the forward {st:#x}"
         dq, dk, dv = pa.backward(q, k, v, out, do, lse, seg, ws=self.ws)
         torch.cuda.synchronize()
         st = pa.pa_device_status(self.ws)
-        assert st == 0, f"device status {st:#x}"
+        assert st == 0, f"device status after the backward {st:#x}"
         return {"o": out, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
 
     def run_strided(self, causal: bool = False):
@@ -58,6 +61,8 @@ class Case:
         seg = None if causal else self.seg
         ws = pa.workspace(q, k, strided=True)
         out, lse = pa.forward(q, k, v, seg, ws=ws)
+        st = pa.pa_device_status(ws)
+        assert st == 0, f"device status after the forward {st:#x}"
         dq, dk, dv = pa.backward(q, k, v, out, do, lse, seg, ws=ws)
         torch.cuda.synchronize()
         st = pa.pa_device_status(ws)

@@ -100,6 +100,7 @@ def _run_f32(c, q, k, v, do, causal=False):
     seg = None if causal else c.seg
     ws = pa.workspace(q, k, strided=True)
     out, lse = pa.forward(q, k, v, seg, ws=ws)
+    assert pa.pa_device_status(ws) == 0  # read before the backward's tile-table step clears it
     dq, dk, dv = pa.backward(q, k, v, out, do, lse, seg, ws=ws)
     torch.cuda.synchronize()
     assert pa.pa_device_status(ws) == 0
@@ -262,6 +263,26 @@ def test_bounded_wait_gives_up_and_context_survives(cuda_dev):
     assert 1.0 < took < 30.0, took
     assert pa.pa_device_status(c.ws) == 0  # reading cleared it
     print(assert_full_parity(c.run(), c.oracle_full(), "after-timeout"))
+
+
+@pytest.mark.parametrize("name", ["tiny_3seg", "long_32k_packed", "8k_packed", "packed_4x4096_short"])
+def test_forward_alone_is_healthy_and_prompt(name, cuda_dev):
+    """The forward on its own leaves a clean status word (every bounded wait
+    completed) and takes well under the 2 s wait limit: a pipeline that
+    waits for work that never comes would show up here even when its
+    outputs are right."""
+    w = synth.workload(name)
+    c = Case(w, cuda_dev, host64=False)
+    pa.forward(c.q, c.k, c.v, c.seg, ws=c.ws)  # warm-up
+    torch.cuda.synchronize()
+    assert pa.pa_device_status(c.ws) == 0
+    t0 = time.time()
+    for _ in range(3):
+        pa.forward(c.q, c.k, c.v, c.seg, ws=c.ws)
+    torch.cuda.synchronize()
+    took = time.time() - t0
+    assert pa.pa_device_status(c.ws) == 0
+    assert took < 0.5, took
 
 
 def test_runs_are_deterministic(cuda_dev):

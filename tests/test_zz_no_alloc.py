@@ -68,6 +68,40 @@ def test_noalloc_matches_workspace_backward_twice(name, causal, cuda_dev):
             assert _rel(got, exp) <= GRAD_RELL2, (call, n, _rel(got, exp))
 
 
+def _noalloc(L, w, q, k, v, out, do, lse, seg):
+    dims = pa.make_dims(w.B, w.Hq, w.Hkv, w.N, w.D)
+    dq, dk, dv = (torch.full_like(x, float("nan")) for x in (q, k, v))
+    status = ctypes.c_uint32(0xFFFFFFFF)
+    rc = L.pa_bwd_noalloc(ctypes.byref(dims), q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          do.data_ptr(), lse.data_ptr(), None if seg is None else seg.data_ptr(), dq.data_ptr(),
+                          dk.data_ptr(), dv.data_ptr(), ctypes.byref(status),
+                          torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, pa.pa_status_string(rc)
+    assert status.value == 0, hex(status.value)
+    torch.cuda.synchronize()
+    return dq, dk, dv
+
+
+def test_noalloc_sequence_of_different_shapes(cuda_dev):
+    """The shared array keeps whatever the previous call left in it: a large
+    packed call, then a small causal one, then a ragged N that goes through
+    the staging copies, then the large packed call again must each match
+    pa_bwd with its own workspace."""
+    L = pa.lib()
+    runs = []
+    for name, causal in (("packed_4x4096_short", False), ("causal_2k_gqa", True), ("ragged_n300", False)):
+        w = RAGGED if name == "ragged_n300" else synth.workload(name)
+        q, k, v, do, seg = _inputs(w, cuda_dev)
+        seg_arg = None if causal else seg
+        out, lse = pa.forward(q, k, v, seg_arg)
+        runs.append((name, w, (q, k, v, out, do, lse, seg_arg), pa.backward(q, k, v, out, do, lse, seg_arg)))
+    for name, w, args, ref in runs + runs[:1]:
+        got = _noalloc(L, w, *args)
+        for g, e, n in zip(got, ref, ("dq", "dk", "dv")):
+            assert torch.isfinite(g.float()).all(), (name, n)
+            assert _rel(g, e) <= GRAD_RELL2, (name, n, _rel(g, e))
+
+
 def test_noalloc_refuses_dims_beyond_its_scratch(cuda_dev):
     L = pa.lib()
     big = pa.make_dims(4, 64, 8, 16384, 128)  # 4M query rows of delta: 16 MiB > 8 MiB
@@ -78,3 +112,6 @@ def test_noalloc_refuses_dims_beyond_its_scratch(cuda_dev):
     bad = pa.make_dims(1, 4, 2, 256, 80)
     assert L.pa_bwd_noalloc(ctypes.byref(bad), fake, fake, fake, fake, fake, fake, fake, fake, fake, fake,
                             None, None) == 2  # PA_ERR_HEAD_DIM, from the same checks as pa_bwd
+    # the same refusal without seg (plain causal): the causal checks name it too
+    assert L.pa_bwd_noalloc(ctypes.byref(bad), fake, fake, fake, fake, fake, fake, None, fake, fake, fake,
+                            None, None) == 2
