@@ -647,11 +647,12 @@ LCE_SHAPE = (8192, 151936, 4096)  # tokens, vocabulary, hidden: the README's iso
 
 
 def lce_measure(steps: int = 5, warmup: int = 2) -> dict:
-    """The fused linear cross-entropy forward (pa_lce_fwd) at N = 8192,
+    """The fused linear cross-entropy forward (pa_lce_fwd) and backward
+    (pa_lce_bwd, with and without the head's gradient) at N = 8192,
     V = 151,936, D = 4096 in bf16 (mlx-train-perf 0.5.1 README, "The fused
     cross-entropy loss", its isolated measurement). Seeded device-side
     normals (head scaled by 2/sqrt(D)); the 1.2 GB head is larger than L2.
-    Tensor-bound: 2 N V D flops per call."""
+    Tensor-bound: 2 N V D flops for the forward."""
     import torch
     import segment_masked_causal_gb300 as pa
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
@@ -677,11 +678,36 @@ def lce_measure(steps: int = 5, warmup: int = 2) -> dict:
     ms = statistics.median(a.elapsed_time(b) for a, b in evs)
     tflops = 2.0 * N * V * D / (ms * 1e-3) / 1e12
     pk = peaks()
-    return {"workload": f"N{N} V{V} D{D} bf16", "ms": round(ms, 4), "tflops": round(tflops, 2),
-            "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": pk["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": round(tflops / pk["bf16_tflops"], 4)},
-            "launches_per_call": 2, "device_status": status,
-            "finite": bool(torch.isfinite(nll).all().item() and torch.isfinite(lse).all().item())}
+    out = {"workload": f"N{N} V{V} D{D} bf16", "ms": round(ms, 4), "tflops": round(tflops, 2),
+           "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": pk["bf16_tflops"],
+                        "unit": "TFLOP/s", "frac": round(tflops / pk["bf16_tflops"], 4)},
+           "launches_per_call": 2, "device_status": status,
+           "finite": bool(torch.isfinite(nll).all().item() and torch.isfinite(lse).all().item())}
+    # the backward for L = mean NLL: dz recomputed per vocabulary chunk, then
+    # dW = dz^T H and dH = dz W (6 N V D flops with the head training, 4 N V D
+    # without)
+    g = torch.full((N,), 1.0 / N, dtype=torch.float32, device=dev)
+    dh, dw = torch.empty_like(H), torch.empty_like(W)
+    wsb = torch.empty(pa.pa_lce_bwd_workspace_bytes(N, V, D), dtype=torch.uint8, device=dev)
+    for train in (True, False):
+        for _ in range(warmup):
+            pa.pa_lce_bwd(H, W, T, lse, g, dh, dw if train else None, wsb)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in evs:
+            a.record()
+            pa.pa_lce_bwd(H, W, T, lse, g, dh, dw if train else None, wsb)
+            b.record()
+        torch.cuda.synchronize()
+        st_b = pa.pa_device_status(wsb)
+        ms_b = statistics.median(a.elapsed_time(b) for a, b in evs)
+        fl = (6.0 if train else 4.0) * N * V * D
+        tf = fl / (ms_b * 1e-3) / 1e12
+        key = "backward" if train else "backward_frozen_head"
+        out[key] = {"ms": round(ms_b, 4), "tflops": round(tf, 2), "frac_of_peak": round(tf / pk["bf16_tflops"], 4),
+                    "device_status": st_b, "finite": bool(torch.isfinite(dh.float()).all().item()),
+                    "workspace_bytes": wsb.numel()}
+    return out
 
 
 def lce_extra() -> dict:

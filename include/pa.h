@@ -333,6 +333,36 @@ size_t pa_lce_workspace_bytes(int32_t N, int32_t V, int32_t D);
 pa_status pa_lce_fwd(int32_t N, int32_t V, int32_t D, const void* hidden, const void* head, const int32_t* targets,
                      float* nll, float* lse, float* target_logit, void* ws, size_t ws_bytes, pa_stream_t stream);
 
+/*
+ * Fused linear cross-entropy, backward (same README section: the backward
+ * recomputes the logit tiles it needs instead of reading a stored matrix).
+ * For L = sum_i g[i] * nll[i] it writes
+ *   dz[i, v]     = g[i] * (exp(z[i, v] - lse[i]) - [v == targets[i]])
+ *   dhidden[i]   = sum_v dz[i, v] head[v]          (N, D) bf16, overwritten
+ *   dhead[v]     = sum_i dz[i, v] hidden[i]        (V, D) bf16, overwritten;
+ *                  pass NULL when the head does not train (then only
+ *                  dhidden is computed)
+ * lse (N) fp32 is the forward's; g (N) fp32 is dL/dnll per token (for a
+ * masked mean, mask[i] / count). A target outside [0, V) contributes
+ * nothing (its row of dz is 0, whatever g[i] is).
+ * How: the vocabulary is taken in chunks of Vc rows (8192 for N <= 16384,
+ * fewer for longer inputs, so that the two dz buffers of a chunk stay within
+ * 512 MiB); per chunk one kernel recomputes the chunk's logits on the tensor
+ * cores and writes dz in bf16 (tokens x Vc and Vc x tokens), and two tcgen05
+ * GEMMs form dhead's rows of the chunk and add the chunk's share of dhidden
+ * to an fp32 accumulator in the workspace. The chunks run in a fixed order,
+ * so results do not depend on timing. Nothing of size N x V is stored.
+ * Arguments as pa_lce_fwd (16-byte aligned device pointers, caller-owned);
+ * ws >= pa_lce_bwd_workspace_bytes(N, V, D), its first 4 bytes the status
+ * word. Asynchronous on `stream`.
+ * Errors: PA_ERR_SHAPE, PA_ERR_NULL, PA_ERR_ALIGN, PA_ERR_WORKSPACE,
+ * PA_ERR_ARCH, PA_ERR_CUDA.
+ */
+size_t pa_lce_bwd_workspace_bytes(int32_t N, int32_t V, int32_t D);
+pa_status pa_lce_bwd(int32_t N, int32_t V, int32_t D, const void* hidden, const void* head, const int32_t* targets,
+                     const float* lse, const float* g, void* dhidden, void* dhead, void* ws, size_t ws_bytes,
+                     pa_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* pa_status_string(pa_status s);
 

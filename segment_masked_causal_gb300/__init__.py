@@ -32,7 +32,8 @@ PA_IO_BF16, PA_IO_F32 = 0, 1
 EXPORTS = ["pa_workspace_bytes", "pa_fwd", "pa_bwd", "pa_fwd_causal", "pa_bwd_causal", "pa_build_tile_table",
            "pa_fwd_tiles", "pa_bwd_delta", "pa_bwd_dq", "pa_bwd_dkv", "pa_bwd_noalloc", "pa_device_status",
            "pa_selftest_wait_timeout", "pa_pack_first_fit", "pa_workspace_bytes_strided", "pa_fwd_strided",
-           "pa_bwd_strided", "pa_lce_workspace_bytes", "pa_lce_fwd", "pa_status_string"]
+           "pa_bwd_strided", "pa_lce_workspace_bytes", "pa_lce_fwd", "pa_lce_bwd_workspace_bytes", "pa_lce_bwd",
+           "pa_status_string"]
 
 
 class LibraryMissing(RuntimeError):
@@ -101,6 +102,10 @@ def lib():
             L.pa_lce_workspace_bytes.restype = S
             L.pa_lce_fwd.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, S, P]
             L.pa_lce_fwd.restype = ctypes.c_int
+            L.pa_lce_bwd_workspace_bytes.argtypes = [I32, I32, I32]
+            L.pa_lce_bwd_workspace_bytes.restype = S
+            L.pa_lce_bwd.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, S, P]
+            L.pa_lce_bwd.restype = ctypes.c_int
             L.pa_pack_first_fit.argtypes = [P, P, I32, P, I32, I32, I32, U64, U64, P, P, P, P, P, P, P]
             L.pa_pack_first_fit.restype = ctypes.c_int
             L.pa_status_string.argtypes = [ctypes.c_int]
@@ -435,6 +440,42 @@ def linear_cross_entropy_forward(hidden, head, targets, ws=None):
         ws = torch.empty(n, dtype=torch.uint8, device=hidden.device)
     pa_lce_fwd(hidden, head, targets, *out, ws)
     return tuple(out)
+
+
+def pa_lce_bwd_workspace_bytes(N, V, D) -> int:
+    return int(lib().pa_lce_bwd_workspace_bytes(int(N), int(V), int(D)))
+
+
+def pa_lce_bwd(hidden, head, targets, lse, g, dhidden, dhead, ws, stream=None):
+    """Fused linear cross-entropy backward (see include/pa.h): writes dhidden
+    (N, D) bf16 and, unless dhead is None, dhead (V, D) bf16, for the loss
+    sum_i g[i] nll[i] with the forward's lse."""
+    import torch
+    N, D = hidden.shape
+    V = head.shape[0]
+    if head.shape[1] != D or tuple(dhidden.shape) != (N, D) or (dhead is not None and tuple(dhead.shape) != (V, D)):
+        raise ValueError("hidden/dhidden must be (N, D) and head/dhead (V, D)")
+    f, bf = torch.float32, torch.bfloat16
+    _check(lib().pa_lce_bwd(N, V, D, _ptr(hidden, bf, "hidden"), _ptr(head, bf, "head"),
+                            _ptr(targets, torch.int32, "targets"), _ptr(lse, f, "lse"), _ptr(g, f, "g"),
+                            _ptr(dhidden, bf, "dhidden"), _ptr(dhead, bf, "dhead"), _ptr(ws, None, "ws"),
+                            ws.numel(), _stream(stream)))
+
+
+def linear_cross_entropy_backward(hidden, head, targets, lse, g, train_head=True, ws=None):
+    """Allocate the outputs (and a workspace) and run pa_lce_bwd; returns
+    (dhidden, dhead), dhead None when the head does not train."""
+    import torch
+    N, D = hidden.shape
+    dh = torch.empty_like(hidden)
+    dw = torch.empty_like(head) if train_head else None
+    if ws is None:
+        n = pa_lce_bwd_workspace_bytes(N, head.shape[0], D)
+        if n == 0:
+            raise PAError(4, "invalid linear cross-entropy dims")
+        ws = torch.empty(n, dtype=torch.uint8, device=hidden.device)
+    pa_lce_bwd(hidden, head, targets, lse, g, dh, dw, ws)
+    return dh, dw
 
 
 def pa_status_string(code: int) -> str:

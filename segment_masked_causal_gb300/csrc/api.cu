@@ -443,8 +443,10 @@ static bool lce_dims_ok(int32_t N, int32_t V, int32_t D) {
 
 size_t pa_lce_workspace_bytes(int32_t N, int32_t V, int32_t D) {
   if (!lce_dims_ok(N, V, D)) return 0;
-  const pa::LceSplit sp = pa::lce_split(N, V);
-  return kAlign + round_up((size_t)3 * sp.splits * N * sizeof(float));
+  // partial sums for the largest split count lce_split may choose
+  const int VT = (V + pa::kTile - 1) / pa::kTile;
+  const size_t splits = VT < pa::kLceMaxSplits ? VT : pa::kLceMaxSplits;
+  return kAlign + round_up((size_t)3 * splits * N * sizeof(float));
 }
 
 pa_status pa_lce_fwd(int32_t N, int32_t V, int32_t D, const void* hidden, const void* head, const int32_t* targets,
@@ -464,6 +466,32 @@ pa_status pa_lce_fwd(int32_t N, int32_t V, int32_t D, const void* hidden, const 
   if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), st) != cudaSuccess) return PA_ERR_CUDA;
   return pa::launch_lce_fwd(N, V, D, hidden, head, targets, nll, lse, target_logit,
                             reinterpret_cast<float*>(w + kAlign), reinterpret_cast<uint32_t*>(w), st) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+size_t pa_lce_bwd_workspace_bytes(int32_t N, int32_t V, int32_t D) {
+  if (!lce_dims_ok(N, V, D)) return 0;
+  return pa::lce_bwd_layout(N, V, D).bytes;
+}
+
+pa_status pa_lce_bwd(int32_t N, int32_t V, int32_t D, const void* hidden, const void* head, const int32_t* targets,
+                     const float* lse, const float* g, void* dhidden, void* dhead, void* ws, size_t ws_bytes,
+                     pa_stream_t stream) {
+  if (!lce_dims_ok(N, V, D)) return PA_ERR_SHAPE;
+  const void* req[] = {hidden, head, targets, lse, g, dhidden, ws};
+  for (const void* x : req)
+    if (!x) return PA_ERR_NULL;
+  for (const void* x : req)
+    if (!aligned16(x)) return PA_ERR_ALIGN;
+  if (dhead && !aligned16(dhead)) return PA_ERR_ALIGN;
+  if (ws_bytes < pa_lce_bwd_workspace_bytes(N, V, D)) return PA_ERR_WORKSPACE;
+  pa_status why = device_ok();
+  if (why != PA_OK) return why;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), st) != cudaSuccess) return PA_ERR_CUDA;
+  return pa::launch_lce_bwd(N, V, D, hidden, head, targets, lse, g, dhidden, dhead, ws,
+                            static_cast<uint32_t*>(ws), st) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
 }

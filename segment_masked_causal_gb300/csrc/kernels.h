@@ -47,7 +47,21 @@ cudaError_t launch_stage_words_out(void* dst, const void* src, uint64_t R, int N
 struct LceSplit {
   int splits, per;
 };
-LceSplit lce_split(int N, int V);
+constexpr int kLceMaxSplits = 64;
+LceSplit lce_split(int N, int V, int slots);
+// CTAs of the cross-entropy kernel resident at once on the current device.
+int lce_slots();
+// Fused linear cross-entropy backward: the vocabulary in chunks of vc rows;
+// workspace after the 256-byte status region: the fp32 dH accumulator (only
+// with more than one chunk), dz (N x vc) and dz^T (vc x ld_dzt), bf16.
+struct LceBwdLayout {
+  int vc, chunks, ld_dzt;
+  size_t acc, dz, dzt, bytes;
+};
+LceBwdLayout lce_bwd_layout(int N, int V, int D);
+cudaError_t launch_lce_bwd(int N, int V, int D, const void* hidden, const void* head, const int32_t* targets,
+                           const float* lse, const float* g, void* dhidden, void* dhead, void* ws, uint32_t* status,
+                           cudaStream_t st);
 cudaError_t launch_lce_fwd(int N, int V, int D, const void* hidden, const void* head, const int32_t* targets,
                            float* nll, float* lse, float* target_logit, float* part, uint32_t* status,
                            cudaStream_t st);

@@ -1,11 +1,14 @@
-// lce.cu -- fused linear cross-entropy forward: per-token NLL, log-sum-exp and
-// target logit of z = H W^T without storing the (N, V) logits
-// (mlx-train-perf 0.5.1 README, "The fused cross-entropy loss").
+// lce.cu -- fused linear cross-entropy: per-token NLL, log-sum-exp and target
+// logit of z = H W^T without storing the (N, V) logits, and the backward into
+// the hidden states and the head (mlx-train-perf 0.5.1 README, "The fused
+// cross-entropy loss": the backward recomputes the tiles it needs instead of
+// reading a stored logit matrix).
 //
+// Forward:
 // Grid: (token tiles of 128) x (vocabulary splits). A CTA walks its split's
 // vocabulary tiles of 128 rows; for each, the tcgen05 tensor cores form the
 // 128 x 128 logit tile in TMEM from 64-wide K slices of H and W that TMA
-// streams through a 4-stage ring, and four epilogue warps (one thread per
+// streams through a 3-stage ring (two CTAs share an SM), and four epilogue warps (one thread per
 // token, reading its TMEM lane) fold the tile into a running maximum and sum
 // of exponentials and pick up the target logit when it falls in the tile.
 // Two TMEM accumulators let the next tile's products run while the epilogue
@@ -16,6 +19,14 @@
 // Roles: warp 0 lane 0 loads (TMA), warp 1 issues the MMAs (lane 0) and owns
 // the TMEM allocation, warps 4..7 are the epilogue (warp % 4 = TMEM lane
 // quarter). Every wait is bounded (sm103.cuh).
+//
+// Backward, over the vocabulary in chunks of Vc rows (so that nothing of size
+// N x V is ever held): the same kernel, with an epilogue that turns each
+// recomputed logit tile into dz = g (exp(z - lse) - [v == target]) in bf16
+// and writes it twice, as dz (tokens x Vc) and dz^T (Vc x tokens); then two
+// tcgen05 GEMMs, dW[chunk] = dz^T H (written once per chunk) and
+// dH += dz W[chunk] (fp32 in the workspace across chunks, in chunk order, so
+// the result does not depend on timing; the last chunk writes bf16 dH).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -30,7 +41,7 @@
 namespace pa {
 namespace {
 
-constexpr int kLceStages = 4;
+constexpr int kLceStages = 3;  // 3 x 32 KB: two CTAs fit on an SM
 constexpr int kLceTile = 128;                  // tokens per CTA and vocabulary rows per tile
 constexpr uint32_t kLceSlice = 128 * 128;      // one 128 x 64 bf16 slice (128-byte rows), 16 KB
 constexpr uint32_t kLceStage = 2 * kLceSlice;  // H slice + W slice
@@ -54,11 +65,22 @@ struct LceParams {
   float* part_s;  // (splits, N): sum of exp(z - max) over the split
   float* part_t;  // (splits, N): the target logit, written by the split holding it
   uint32_t* status;
+  // backward: vocabulary tiles from vt_base on (one chunk), and dz for them
+  int vt_base, vt_end;        // the chunk's vocabulary tiles: vt_base <= vt < vt_end
+  const float* lse;           // (N) from the forward
+  const float* g;             // (N) upstream gradient dL/dnll
+  __nv_bfloat16* dz;          // (N, ld_dz): column v - vt_base * 128
+  int ld_dz;
+  __nv_bfloat16* dzt;         // (Vc, ld_dzt): row v - vt_base * 128, or null (no dW)
+  int ld_dzt;
 };
 
-__global__ void __launch_bounds__(kLceThreads, 1)
-    lce_fwd_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW,
-                   const LceParams p) {
+// BWD = false: the forward's online log-sum-exp epilogue. BWD = true: the
+// backward's dz epilogue (grid.y splits the chunk's vocabulary tiles).
+template <bool BWD>
+__global__ void __launch_bounds__(kLceThreads, 2)
+    lce_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW,
+               const LceParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   LceMisc& m = *reinterpret_cast<LceMisc*>(smem_raw);
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1024 + 1023) &
@@ -66,8 +88,8 @@ __global__ void __launch_bounds__(kLceThreads, 1)
   const uint32_t sRing = smem_u32(ring);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tm = blockIdx.x;
-  const int VT = (p.V + kLceTile - 1) / kLceTile;
-  const int vt0 = blockIdx.y * p.vt_per_split;
+  const int VT = BWD ? p.vt_end : (p.V + kLceTile - 1) / kLceTile;  // end of the tiles this launch covers
+  const int vt0 = (BWD ? p.vt_base : 0) + blockIdx.y * p.vt_per_split;
   const int vt1 = min(vt0 + p.vt_per_split, VT);
   const int nt = vt1 - vt0;  // >= 1 by construction of the grid
   const int KS = p.D / 64;   // K slices per tile
@@ -149,6 +171,69 @@ __global__ void __launch_bounds__(kLceThreads, 1)
       g.drain(&m.fin, 0);
     }
     __syncwarp();
+  } else if (warp >= 4 && BWD) {
+    // ------------------------------------------------------------ dz epilogue
+    // Thread r owns token row r of the tile: dz = g (2^(z log2e - lse log2e)
+    // - [v == target]) for every vocabulary column, zero for an ignored
+    // target (outside [0, V)). dz goes out in the token's row (16-byte
+    // stores) and, when the head trains, in dz^T, where the 32 lanes of a
+    // warp write 32 consecutive tokens of one vocabulary row.
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int token = tm * kLceTile + r;
+    const bool live = token < p.N;
+    const int t = live ? p.targets[token] : -1;
+    const bool use = live && t >= 0 && t < p.V;
+    const float gl = use ? p.g[token] : 0.f;
+    const float l2 = use ? p.lse[token] * 1.4426950408889634f : 0.f;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      const int buf = j & 1;
+      ok = g.wait(&m.acc_full[buf], (j >> 1) & 1, 44);
+      ok = __all_sync(~0u, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int v0 = (vt0 + j) * kLceTile;
+      const int c0v = v0 - p.vt_base * kLceTile;  // column of v0 in the chunk
+#pragma unroll 1
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t a[32];
+        tmem_ld32(tmem + lane_base + buf * 128 + c0, a);
+        const int vc = v0 + c0;
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          // columns past V (the last tile's tail) are exactly zero
+          const float d0 = (use && vc + i < p.V)
+                               ? gl * (ex2(fmaf(__uint_as_float(a[i]), 1.4426950408889634f, -l2)) -
+                                       (vc + i == t ? 1.f : 0.f))
+                               : 0.f;
+          const float d1 = (use && vc + i + 1 < p.V)
+                               ? gl * (ex2(fmaf(__uint_as_float(a[i + 1]), 1.4426950408889634f, -l2)) -
+                                       (vc + i + 1 == t ? 1.f : 0.f))
+                               : 0.f;
+          w[i >> 1] = pack_bf16x2(d0, d1);
+        }
+        if (live) {
+          // the tile's columns past V are not part of the chunk's output
+          __nv_bfloat16* row = p.dz + (size_t)token * p.ld_dz + c0v + c0;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (vc + 8 * u < p.V)
+              *reinterpret_cast<uint4*>(row + 8 * u) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+          if (p.dzt) {
+            __nv_bfloat16* col = p.dzt + (size_t)(c0v + c0) * p.ld_dzt + token;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (vc + i < p.V)
+                col[(size_t)i * p.ld_dzt] = __ushort_as_bfloat16((unsigned short)(i & 1 ? w[i >> 1] >> 16 : w[i >> 1] & 0xFFFFu));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&m.acc_empty[buf]);
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
@@ -234,33 +319,341 @@ __global__ void __launch_bounds__(256) lce_merge_kernel(const LceParams p, int s
   nll[i] = n;
 }
 
+// ------------------------------------------------------------------ GEMM
+// C (M x N) from A (M x K, K contiguous) and B (K x N, N contiguous): one
+// 128 x 128 output tile per CTA, K in steps of 64 through a 3-stage TMA ring
+// (A as one 128-row x 64 box, B as two 64-row x 64 boxes, all 128-byte
+// swizzled; elements past M, N or K read as zero), tcgen05 products into one
+// 128-column fp32 TMEM accumulator. Two CTAs fit on an SM, so one's epilogue
+// runs beside the other's products. The epilogue (one thread per output row)
+// stores bf16, or starts / adds to / finishes an fp32 accumulator in global
+// memory; each output tile belongs to one CTA, so no two threads touch the
+// same element.
+constexpr int kGemmStages = 3;
+constexpr uint32_t kGemmA = 128 * 128;                    // 128 rows x 64 K, 16 KB
+constexpr uint32_t kGemmBHalf = 64 * 128;                 // 64 K rows x 64 N columns, 8 KB
+constexpr uint32_t kGemmStage = kGemmA + 2 * kGemmBHalf;  // 32 KB
+constexpr int kGemmThreads = 192;
+constexpr uint32_t kGemmSmem = 1024 /* misc */ + 1024 /* alignment */ + kGemmStages * kGemmStage;
+
+enum GemmMode : int { kStoreBf16 = 0, kAccInit = 1, kAccAdd = 2, kAccFinal = 3 };
+
+struct GemmParams {
+  int M, N, K;         // N a multiple of 64
+  int mode;            // GemmMode
+  __nv_bfloat16* c;    // bf16 result (kStoreBf16: the product; kAccFinal: accumulator + product)
+  int ldc;
+  float* acc;          // fp32 accumulator (kAccInit: set; kAccAdd: add; kAccFinal: read)
+  int ldacc;
+  uint32_t* status;
+};
+
+struct GemmMisc {
+  uint64_t full[kGemmStages], empty[kGemmStages];
+  uint64_t acc_full, fin;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__global__ void __launch_bounds__(kGemmThreads, 2)
+    lce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const GemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  GemmMisc& m = *reinterpret_cast<GemmMisc*>(smem_raw);
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1024 + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sRing = smem_u32(ring);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * 128, n0 = blockIdx.y * 128;
+  const int KB = (p.K + 63) / 64;
+  const Guard g{&m.abort_flag, p.status};
+
+  if (threadIdx.x == 0) {
+    m.abort_flag = 0;
+    for (int s = 0; s < kGemmStages; ++s) {
+      mbar_init(&m.full[s], 1);
+      mbar_init(&m.empty[s], 1);
+    }
+    mbar_init(&m.acc_full, 1);
+    mbar_init(&m.fin, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&m.tmem_base, 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = m.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      int kb = 0;
+      for (; kb < KB; ++kb) {
+        const int st = kb % kGemmStages;
+        if (!g.wait(&m.empty[st], ((kb / kGemmStages) & 1) ^ 1, 45)) break;
+        uint8_t* sa = ring + st * kGemmStage;
+        mbar_expect_tx(&m.full[st], kGemmStage);
+        tma_load_2d(sa, &tmA, &m.full[st], kb * 64, m0);
+        tma_load_2d(sa + kGemmA, &tmB, &m.full[st], n0, kb * 64);
+        tma_load_2d(sa + kGemmA + kGemmBHalf, &tmB, &m.full[st], n0 + 64, kb * 64);
+      }
+      // no copy may still be landing when the CTA exits
+      for (int i = (kb > kGemmStages ? kb - kGemmStages : 0); i < kb; ++i)
+        g.drain(&m.full[i % kGemmStages], (i / kGemmStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    const bool leader = lane == 0;
+    constexpr uint32_t idC = idesc_bf16_f32(128, 128, false, true);
+    bool ok = true;
+    for (int kb = 0; kb < KB; ++kb) {
+      const int st = kb % kGemmStages;
+      if (!g.wait_warp(&m.full[st], (kb / kGemmStages) & 1, 46)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sa = sRing + st * kGemmStage;
+      const uint64_t ad = sdesc_sw128(sa, 16, 1024);
+      const uint64_t bd = sdesc_sw128(sa + kGemmA, kGemmBHalf, 1024);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        if (leader)
+          umma_bf16(tmem, sdesc_add(ad, kk * 32), sdesc_add(bd, kk * 2048), idC, (kb > 0 || kk > 0) ? 1u : 0u);
+      if (leader) umma_commit(&m.empty[st]);
+      __syncwarp();
+    }
+    if (leader) {
+      if (ok) umma_commit(&m.acc_full);
+      umma_commit(&m.fin);
+      g.drain(&m.fin, 0);
+    }
+    __syncwarp();
+  } else {
+    // warps 2..5: TMEM lane quarter warp % 4, one thread per output row
+    const int quarter = warp & 3;
+    const int row = m0 + quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const bool ok = __all_sync(~0u, g.wait(&m.acc_full, 0, 47));
+    if (ok) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t a[32];
+        tmem_ld32(tmem + lane_base + c0, a);
+        const int col = n0 + c0;
+        if (row >= p.M || col >= p.N) continue;  // N is a multiple of 64: 32 columns are all in or all out
+        if (p.mode == kAccInit || p.mode == kAccAdd || p.mode == kAccFinal) {
+          float4* ac = reinterpret_cast<float4*>(p.acc + (size_t)row * p.ldacc + col);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float4 v = make_float4(__uint_as_float(a[4 * q]), __uint_as_float(a[4 * q + 1]),
+                                   __uint_as_float(a[4 * q + 2]), __uint_as_float(a[4 * q + 3]));
+            if (p.mode != kAccInit) {
+              const float4 o = ac[q];
+              v.x += o.x;
+              v.y += o.y;
+              v.z += o.z;
+              v.w += o.w;
+            }
+            if (p.mode == kAccFinal) {
+              a[4 * q] = __float_as_uint(v.x);
+              a[4 * q + 1] = __float_as_uint(v.y);
+              a[4 * q + 2] = __float_as_uint(v.z);
+              a[4 * q + 3] = __float_as_uint(v.w);
+            } else {
+              ac[q] = v;
+            }
+          }
+        }
+        if (p.mode == kStoreBf16 || p.mode == kAccFinal) {
+          uint4* cr = reinterpret_cast<uint4*>(p.c + (size_t)row * p.ldc + col);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            cr[q] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * q]), __uint_as_float(a[8 * q + 1])),
+                               pack_bf16x2(__uint_as_float(a[8 * q + 2]), __uint_as_float(a[8 * q + 3])),
+                               pack_bf16x2(__uint_as_float(a[8 * q + 4]), __uint_as_float(a[8 * q + 5])),
+                               pack_bf16x2(__uint_as_float(a[8 * q + 6]), __uint_as_float(a[8 * q + 7])));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+cudaError_t launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, const GemmParams& gp, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(lce_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid((gp.M + 127) / 128, (gp.N + 127) / 128);
+  lce_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, st>>>(tA, tB, gp);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
-LceSplit lce_split(int N, int V) {
+// The vocabulary split of the (token tile x split) grid: the one that makes
+// waves x (tiles per CTA + 1) smallest for `slots` resident CTAs, i.e. the
+// shortest run once the last wave's idle SMs and each CTA's pipeline fill (about
+// one tile) are counted. At most kLceMaxSplits splits (the workspace's partial
+// sums are sized for that).
+LceSplit lce_split(int N, int V, int slots) {
   const int TT = (N + kLceTile - 1) / kLceTile, VT = (V + kLceTile - 1) / kLceTile;
-  int splits = (2 * 148 + TT - 1) / TT;
-  if (splits < 1) splits = 1;
-  if (splits > VT) splits = VT;
-  const int per = (VT + splits - 1) / splits;
-  return LceSplit{(VT + per - 1) / per, per};
+  if (slots < 1) slots = 1;
+  LceSplit best{1, VT};
+  long long best_cost = -1;
+  for (int s = 1; s <= VT && s <= kLceMaxSplits; ++s) {
+    const int per = (VT + s - 1) / s, used = (VT + per - 1) / per;
+    const long long ctas = (long long)TT * used, waves = (ctas + slots - 1) / slots;
+    const long long cost = waves * (per + 1);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = LceSplit{used, per};
+    }
+  }
+  return best;
+}
+
+int lce_slots() {
+  // the kernel is built for two resident CTAs per SM: 3 x 32 KB stages (about
+  // 100 KB of shared memory) and at most 128 registers a thread
+  static_assert(kLceSmem + 1024 <= 232448 / 2 + 1024, "two CTAs must fit an SM's shared memory");
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms <= 0)
+    sms = 148;
+  return 2 * sms;
 }
 
 cudaError_t launch_lce_fwd(int N, int V, int D, const void* hidden, const void* head, const int32_t* targets,
                            float* nll, float* lse, float* target_logit, float* part, uint32_t* status,
                            cudaStream_t st) {
-  const LceSplit sp = lce_split(N, V);
+  const LceSplit sp = lce_split(N, V, lce_slots());
   CUtensorMap tH, tW;
   if (!tmap_bf16_2d_sw128(&tH, hidden, D, N, kLceTile) || !tmap_bf16_2d_sw128(&tW, head, D, V, kLceTile))
     return cudaErrorInvalidValue;
-  LceParams p{N, V, D, sp.per, targets, part, part + (size_t)sp.splits * N, part + (size_t)2 * sp.splits * N,
-              status};
-  cudaError_t e = cudaFuncSetAttribute(lce_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLceSmem);
+  LceParams p{};
+  p.N = N;
+  p.V = V;
+  p.D = D;
+  p.vt_per_split = sp.per;
+  p.targets = targets;
+  p.part_m = part;
+  p.part_s = part + (size_t)sp.splits * N;
+  p.part_t = part + (size_t)2 * sp.splits * N;
+  p.status = status;
+  cudaError_t e = cudaFuncSetAttribute(lce_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLceSmem);
   if (e != cudaSuccess) return e;
   dim3 grid((N + kLceTile - 1) / kLceTile, sp.splits);
-  lce_fwd_kernel<<<grid, kLceThreads, kLceSmem, st>>>(tH, tW, p);
+  lce_kernel<false><<<grid, kLceThreads, kLceSmem, st>>>(tH, tW, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   lce_merge_kernel<<<(N + 255) / 256, 256, 0, st>>>(p, sp.splits, nll, lse, target_logit);
   return cudaGetLastError();
+}
+
+}  // namespace pa
+
+namespace pa {
+
+int lce_bwd_chunk(int N, int V) {
+  // dz and dz^T of one chunk together take 4 N Vc bytes: at most 512 MiB
+  long long vc = ((1ll << 27) / (N > 0 ? N : 1)) / kLceTile * kLceTile;
+  const long long vmax = (long long)(V + kLceTile - 1) / kLceTile * kLceTile;
+  if (vc > 8192) vc = 8192;
+  if (vc > vmax) vc = vmax;
+  if (vc < kLceTile) vc = kLceTile;
+  return (int)vc;
+}
+
+LceBwdLayout lce_bwd_layout(int N, int V, int D) {
+  LceBwdLayout L;
+  L.vc = lce_bwd_chunk(N, V);
+  L.chunks = (V + L.vc - 1) / L.vc;
+  L.ld_dzt = (N + 63) / 64 * 64;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  L.acc = 256;
+  L.dz = L.acc + (L.chunks > 1 ? up((size_t)N * D * 4) : 0);
+  L.dzt = L.dz + up((size_t)N * L.vc * 2);
+  L.bytes = L.dzt + up((size_t)L.vc * L.ld_dzt * 2);
+  return L;
+}
+
+cudaError_t launch_lce_bwd(int N, int V, int D, const void* hidden, const void* head, const int32_t* targets,
+                           const float* lse, const float* g, void* dhidden, void* dhead, void* ws, uint32_t* status,
+                           cudaStream_t st) {
+  const LceBwdLayout L = lce_bwd_layout(N, V, D);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(w + L.dz);
+  __nv_bfloat16* dzt = reinterpret_cast<__nv_bfloat16*>(w + L.dzt);
+  float* acc = reinterpret_cast<float*>(w + L.acc);
+  CUtensorMap tH, tW, tHb;
+  if (!tmap_bf16_2d_sw128(&tH, hidden, D, N, kLceTile) || !tmap_bf16_2d_sw128(&tW, head, D, V, kLceTile) ||
+      !tmap_bf16_2d_sw128(&tHb, hidden, D, N, 64))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(lce_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLceSmem);
+  if (e != cudaSuccess) return e;
+  for (int c = 0; c < L.chunks; ++c) {
+    const int cv0 = c * L.vc, kc = (V - cv0 < L.vc) ? V - cv0 : L.vc;  // the chunk's vocabulary rows
+    // dz (and dz^T) of the chunk
+    const LceSplit sp = lce_split(N, kc, lce_slots());
+    LceParams p{};
+    p.N = N;
+    p.V = V;
+    p.D = D;
+    p.vt_per_split = sp.per;
+    p.targets = targets;
+    p.status = status;
+    p.vt_base = cv0 / kLceTile;
+    p.vt_end = (cv0 + kc + kLceTile - 1) / kLceTile;
+    p.lse = lse;
+    p.g = g;
+    p.dz = dz;
+    p.ld_dz = L.vc;
+    p.dzt = dhead ? dzt : nullptr;
+    p.ld_dzt = L.ld_dzt;
+    lce_kernel<true><<<dim3((N + kLceTile - 1) / kLceTile, sp.splits), kLceThreads, kLceSmem, st>>>(tH, tW, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // dW rows of the chunk = dz^T H (tokens are the contraction)
+    if (dhead) {
+      CUtensorMap tA;
+      if (!tmap_bf16_2d_sw128_pitch(&tA, dzt, N, kc, L.ld_dzt, 128)) return cudaErrorInvalidValue;
+      GemmParams gp{};
+      gp.M = kc;
+      gp.N = D;
+      gp.K = N;
+      gp.mode = kStoreBf16;
+      gp.c = static_cast<__nv_bfloat16*>(dhead) + (size_t)cv0 * D;
+      gp.ldc = D;
+      gp.status = status;
+      if ((e = launch_gemm(tA, tHb, gp, st)) != cudaSuccess) return e;
+    }
+    // dH += dz W[chunk] (the chunk's vocabulary rows are the contraction)
+    CUtensorMap tA, tB;
+    if (!tmap_bf16_2d_sw128_pitch(&tA, dz, kc, N, L.vc, 128) ||
+        !tmap_bf16_2d_sw128(&tB, static_cast<const __nv_bfloat16*>(head) + (size_t)cv0 * D, D, kc, 64))
+      return cudaErrorInvalidValue;
+    GemmParams gp{};
+    gp.M = N;
+    gp.N = D;
+    gp.K = kc;
+    gp.mode = L.chunks == 1 ? kStoreBf16 : c == 0 ? kAccInit : c == L.chunks - 1 ? kAccFinal : kAccAdd;
+    gp.c = static_cast<__nv_bfloat16*>(dhidden);
+    gp.ldc = D;
+    gp.acc = acc;
+    gp.ldacc = D;
+    gp.status = status;
+    if ((e = launch_gemm(tA, tB, gp, st)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace pa

@@ -24,6 +24,24 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   return fn;
 }
 
+// A 2-D bf16 tensor of `rows` rows x `inner` elements, rows `pitch` elements
+// apart (pitch >= inner, pitch * 2 a multiple of 16), read in boxes of
+// box_rows x 64 elements (128 bytes) with the 128-byte swizzle. Elements past
+// `inner` or `rows` read as zero.
+inline bool tmap_bf16_2d_sw128_pitch(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                                     uint64_t pitch, uint32_t box_rows) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {pitch * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // A 2-D bf16 tensor of `rows` rows x `inner` contiguous elements, read in
 // boxes of box_rows x 64 elements (128 bytes) with the 128-byte swizzle.
 inline bool tmap_bf16_2d_sw128(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
