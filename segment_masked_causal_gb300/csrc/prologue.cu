@@ -67,27 +67,21 @@ constexpr int kMaxSortedTiles = 4095;  // T above this: canonical order, unsorte
 
 __device__ __forceinline__ int canon_q(int e, int B, int T) { return (e % B) * T + (T - 1 - e / B); }
 __device__ __forceinline__ int canon_k(int e, int B, int T) { return (e % B) * T + e / B; }
-__device__ __forceinline__ int cost_q(int4 te, int t) { return t - te.z + 1; }
-__device__ __forceinline__ int cost_k(int4 te, int t) { return te.w - t + 1; }
 
-__global__ void __launch_bounds__(1024) work_list_kernel(const int4* __restrict__ tiles, int B, int T,
-                                                         int32_t* __restrict__ wq, int32_t* __restrict__ wk) {
-  const int n = B * T;
-  if (T > kMaxSortedTiles) {
-    for (int e = threadIdx.x; e < n; e += blockDim.x) {
-      wq[e] = canon_q(e, B, T);
-      wk[e] = canon_k(e, B, T);
-    }
-    return;
-  }
-  __shared__ int cnt[2][kMaxSortedTiles + 1];  // [list][cost]: counts, then next free position
+// The counting sort itself, for a block of 1024 threads. range(ent) gives
+// {kv_lo, q_hi} of table entry ent; cnt0 and cnt1 hold T + 1 ints each.
+template <class Range>
+__device__ __forceinline__ void build_work_lists(int B, int T, Range range, int* cnt0, int* cnt1,
+                                                 int32_t* __restrict__ wq, int32_t* __restrict__ wk) {
   __shared__ int part[2][32];
-  for (int c = threadIdx.x; c <= T; c += blockDim.x) cnt[0][c] = cnt[1][c] = 0;
+  int* cnt[2] = {cnt0, cnt1};
+  const int n = B * T;
+  for (int c = threadIdx.x; c <= T; c += blockDim.x) cnt0[c] = cnt1[c] = 0;
   __syncthreads();
   for (int e = threadIdx.x; e < n; e += blockDim.x) {
     const int eq = canon_q(e, B, T), ek = canon_k(e, B, T);
-    atomicAdd(&cnt[0][cost_q(tiles[eq], eq % T)], 1);
-    atomicAdd(&cnt[1][cost_k(tiles[ek], ek % T)], 1);
+    atomicAdd(&cnt0[eq % T - range(eq).x + 1], 1);
+    atomicAdd(&cnt1[range(ek).y - ek % T + 1], 1);
   }
   __syncthreads();
   // Starting position of cost c = entries of cost > c. Thread i sums a run of
@@ -134,7 +128,7 @@ __global__ void __launch_bounds__(1024) work_list_kernel(const int4* __restrict_
       int ent = 0, key = -1 - lane;  // lanes past the end take keys of their own
       if (live) {
         ent = warp == 0 ? canon_q(e, B, T) : canon_k(e, B, T);
-        key = warp == 0 ? cost_q(tiles[ent], ent % T) : cost_k(tiles[ent], ent % T);
+        key = warp == 0 ? ent % T - range(ent).x + 1 : range(ent).y - ent % T + 1;
       }
       const unsigned same = __match_any_sync(~0u, key);
       const int rank = __popc(same & ((1u << lane) - 1u));
@@ -145,6 +139,74 @@ __global__ void __launch_bounds__(1024) work_list_kernel(const int4* __restrict_
       if (live) out[at] = ent;
     }
   }
+}
+
+__global__ void __launch_bounds__(1024) work_list_kernel(const int4* __restrict__ tiles, int B, int T,
+                                                         int32_t* __restrict__ wq, int32_t* __restrict__ wk) {
+  const int n = B * T;
+  if (T > kMaxSortedTiles) {
+    for (int e = threadIdx.x; e < n; e += blockDim.x) {
+      wq[e] = canon_q(e, B, T);
+      wk[e] = canon_k(e, B, T);
+    }
+    return;
+  }
+  __shared__ int cnt[2][kMaxSortedTiles + 1];  // [list][cost]: counts, then next free position
+  build_work_lists(B, T, [&](int ent) { const int4 v = tiles[ent]; return make_int2(v.z, v.w); }, cnt[0], cnt[1],
+                   wq, wk);
+}
+
+// Rows with few tiles in all (B * T <= kSmallPrologue): the table and both
+// lists in one CTA, with the per-tile id ranges kept in shared memory. Each
+// warp takes four tiles at a time, so four loads of segment ids are in flight.
+constexpr int kSmallPrologue = 4096;
+constexpr size_t small_prologue_smem(int n, int T) { return (size_t)n * 16 + (size_t)2 * (T + 1) * 4; }
+
+__global__ void __launch_bounds__(1024) prologue_small_kernel(const int32_t* __restrict__ seg, int B, int N, int T,
+                                                              int4* __restrict__ tiles, int32_t* __restrict__ wq,
+                                                              int32_t* __restrict__ wk, uint32_t* status) {
+  extern __shared__ int2 sm2[];
+  const int n = B * T;
+  int2* mm = sm2;                                  // {min, max} per tile
+  int2* range = sm2 + n;                           // {kv_lo, q_hi} per tile
+  int* cnt = reinterpret_cast<int*>(sm2 + 2 * n);  // 2 (T + 1)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, warps = blockDim.x >> 5;
+  if (threadIdx.x == 0 && status) *status = 0u;
+  for (int e0 = 4 * warp; e0 < n; e0 += 4 * warps) {
+    int4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = e0 + u;
+      v[u] = make_int4(0, 0, 0, 0);
+      if (seg && e < n) v[u] = reinterpret_cast<const int4*>(seg + (size_t)(e / T) * N + (size_t)(e % T) * kTile)[lane];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      int lo = min(min(v[u].x, v[u].y), min(v[u].z, v[u].w));
+      int hi = max(max(v[u].x, v[u].y), max(v[u].z, v[u].w));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(~0u, lo, o));
+        hi = max(hi, __shfl_xor_sync(~0u, hi, o));
+      }
+      if (lane == 0 && e0 + u < n) mm[e0 + u] = make_int2(lo, hi);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const int2* row = mm + (e / T) * T;
+    const int t = e % T;
+    const int2 me = row[t];
+    int lo = t, hi = t;
+    for (int u = 0; u < t; ++u)
+      if (row[u].x <= me.y && me.x <= row[u].y) { lo = u; break; }
+    for (int u = T - 1; u > t; --u)
+      if (row[u].x <= me.y && me.x <= row[u].y) { hi = u; break; }
+    range[e] = make_int2(lo, hi);
+    tiles[e] = make_int4(me.x, me.y, lo, hi);
+  }
+  __syncthreads();
+  build_work_lists(B, T, [&](int ent) { return range[ent]; }, cnt, cnt + T + 1, wq, wk);
 }
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -212,6 +274,17 @@ __global__ void __launch_bounds__(32) wait_timeout_kernel(uint32_t* status) {
 }  // namespace
 
 cudaError_t launch_tile_table(const AttnParams& p, int4* tiles, cudaStream_t st) {
+  const int n = p.B * p.T;
+  if (n <= kSmallPrologue && p.T <= kMaxSortedTiles) {
+    const size_t smem = small_prologue_smem(n, p.T);
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(prologue_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    prologue_small_kernel<<<1, 1024, smem, st>>>(p.seg, p.B, p.N, p.T, tiles, const_cast<int32_t*>(p.work_q),
+                                                  const_cast<int32_t*>(p.work_k), p.status);
+    return cudaGetLastError();
+  }
   const size_t smem = (size_t)p.T * sizeof(int2);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(tile_table_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -91,6 +91,25 @@ def _noncontig():
     return w
 
 
+def _many_rows():
+    """40 rows of 16,384 tokens (5,120 tiles): more tiles than one CTA of the
+    prologue takes, so the table and the lists come from the multi-CTA path."""
+    lengths = []
+    for b in range(40):
+        u = synth.uniforms(31 + b, 1, 64)
+        row, left = [], 16384
+        for x in u:
+            L = min(left, 100 + int(x * 3000))
+            row.append(L)
+            left -= L
+            if left == 0:
+                break
+        if left:
+            row.append(left)
+        lengths.append(row)
+    return synth.custom(40, 1, 1, 16384, 64, lengths, seed=33)
+
+
 CASES = {
     "packed_4x4096_short": lambda: synth.workload("packed_4x4096_short"),
     "8k_packed": lambda: synth.workload("8k_packed"),
@@ -98,6 +117,7 @@ CASES = {
     "long_64k_packed": lambda: synth.workload("long_64k_packed"),
     "noncontiguous_ids": _noncontig,
     "alternating_blocks": _alternating,
+    "many_rows_multi_cta": _many_rows,
 }
 
 
