@@ -646,7 +646,7 @@ def staged_layout_extras(dev, rank, args):
 LCE_SHAPE = (8192, 151936, 4096)  # tokens, vocabulary, hidden: the README's isolated loss-layer shape
 
 
-def lce_measure(steps: int = 5, warmup: int = 2) -> dict:
+def lce_measure(steps: int = 5, warmup: int = 2, shape=None) -> dict:
     """The fused linear cross-entropy forward (pa_lce_fwd) and backward
     (pa_lce_bwd, with and without the head's gradient) at N = 8192,
     V = 151,936, D = 4096 in bf16 (mlx-train-perf 0.5.1 README, "The fused
@@ -657,7 +657,7 @@ def lce_measure(steps: int = 5, warmup: int = 2) -> dict:
     import segment_masked_causal_gb300 as pa
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    N, V, D = LCE_SHAPE
+    N, V, D = shape or LCE_SHAPE
     gen = torch.Generator(device=dev)
     gen.manual_seed(1008)
     H = torch.randn((N, D), generator=gen, device=dev).to(torch.bfloat16)
@@ -773,10 +773,14 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip the packed / causal comparison runs")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--lce-only", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--lce-only", action="store_true",
+                    help="only the fused linear cross-entropy forward and backward, printed as one JSON line")
+    ap.add_argument("--lce-shape", default=None,
+                    help="N,V,D for --lce-only (default 8192,151936,4096, the README's isolated-loss shape)")
     args = ap.parse_args(argv)
     if args.lce_only:
-        print(json.dumps(lce_measure()), flush=True)
+        shape = tuple(int(x) for x in args.lce_shape.split(",")) if args.lce_shape else None
+        print(json.dumps(lce_measure(shape=shape)), flush=True)
         return
     args.warmup = max(3, args.warmup)  # at least 3 warm-up steps, whatever was asked
     if args.impl == "reference":

@@ -61,21 +61,36 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test with a suspend-time hint: a thread whose phase has not
+// completed sleeps until it completes or `ns` nanoseconds pass, instead of
+// returning at once, so a waiting warp takes no issue slots from the warps
+// that share its SM sub-partition.
+__device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kWaitSleepNs = 10000;  // 10 us: the abort flag and the limit are checked at least this often
+
 // Polling loop of a bounded wait, kept out of line: every wait site inlines
 // only its first test, so the hot loops of the kernels stay small enough for
 // the instruction cache.
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint32_t site,
                                                    volatile int* abort_flag, uint32_t* status) {
   const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_test(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        if (status) atomicOr(status, PA_DEVERR_TIMEOUT | (site << 8));
-        return false;
-      }
+  for (;;) {
+    if (mbar_test_sleep(bar, parity, kWaitSleepNs)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      if (status) atomicOr(status, PA_DEVERR_TIMEOUT | (site << 8));
+      return false;
     }
   }
 }

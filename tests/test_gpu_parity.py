@@ -204,6 +204,14 @@ def test_8k_packed_group_full(cuda_dev):
     print(assert_group_parity(c, c.run(), 3, tag="8k_packed group 3"))
 
 
+def test_8k_one_segment_group_full(cuda_dev):
+    """The headline row: every element of one kv group (4 query heads x 8192
+    rows of O, lse and dQ; the kv head's dK and dV) against the oracle."""
+    w = synth.workload("8k_one_segment")
+    c = Case(w, cuda_dev)
+    print(assert_group_parity(c, c.run(), 5, tag="8k_one_segment group 5"))
+
+
 @pytest.mark.parametrize("name", ["8k_one_segment", "8k_packed"])
 def test_8k(name, cuda_dev):
     w = synth.workload(name)
