@@ -341,6 +341,7 @@ enum GemmMode : int { kStoreBf16 = 0, kAccInit = 1, kAccAdd = 2, kAccFinal = 3 }
 struct GemmParams {
   int M, N, K;         // N a multiple of 64
   int mode;            // GemmMode
+  int n_fastest;       // grid.x walks the N tiles (else the M tiles)
   __nv_bfloat16* c;    // bf16 result (kStoreBf16: the product; kAccFinal: accumulator + product)
   int ldc;
   float* acc;          // fp32 accumulator (kAccInit: set; kAccAdd: add; kAccFinal: read)
@@ -364,7 +365,11 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                                              ~uintptr_t(1023));
   const uint32_t sRing = smem_u32(ring);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * 128, n0 = blockIdx.y * 128;
+  // N tiles run fastest: the CTAs that share an A row block run together and
+  // keep it in L2 (with M tiles fastest, a launch read A about five times);
+  // past 65535 M tiles (grid.y's limit) the launch puts M in grid.x instead
+  const int m0 = (p.n_fastest ? blockIdx.y : blockIdx.x) * 128;
+  const int n0 = (p.n_fastest ? blockIdx.x : blockIdx.y) * 128;
   const int KB = (p.K + 63) / 64;
   const Guard g{&m.abort_flag, p.status};
 
@@ -494,8 +499,11 @@ cudaError_t launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, const Gemm
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid((gp.M + 127) / 128, (gp.N + 127) / 128);
-  lce_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, st>>>(tA, tB, gp);
+  GemmParams q = gp;
+  const unsigned mt = (unsigned)((gp.M + 127) / 128), nt = (unsigned)((gp.N + 127) / 128);
+  q.n_fastest = mt <= 65535;
+  const dim3 grid = q.n_fastest ? dim3(nt, mt) : dim3(mt, nt);
+  lce_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, st>>>(tA, tB, q);
   return cudaGetLastError();
 }
 
