@@ -368,6 +368,11 @@ def run_ours(args):
     import torch
     import torch.distributed as dist
     world, rank, local = dist_env()
+    if args.gpus != world:
+        # one rank per GPU: N GPUs come from a launcher's N processes (torchrun);
+        # a single process times one GPU whatever --gpus says
+        print(f"bench.py: --gpus {args.gpus} with {world} process(es): timing {world} GPU(s), one per process",
+              file=sys.stderr, flush=True)
     if world > 1 and not dist.is_initialized():
         dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
     dev = torch.device(f"cuda:{local}")
@@ -749,7 +754,7 @@ def run_reference(args):
         t0 = time.perf_counter()
         one(args.warmup + i)
         times.append(time.perf_counter() - t0)
-    ms = 1e3 * statistics.mean(times)
+    ms = 1e3 * statistics.median(times)
     value = 14.0 * w.D * pairs / (ms * 1e-3) / 1e12
     sample = f"one query head (rotating) of {w.Hq} of {w.name} per step, complete fp64 forward+backward"
     line = {"metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": args.steps,
