@@ -202,6 +202,28 @@ pa_status pa_bwd_dkv(const pa_dims* dims, const void* q, const void* k, const vo
                      pa_stream_t stream);
 
 /*
+ * Single-pass backward (no counterpart on the pages; built to compare with
+ * the split dQ / dK-dV design of pa_bwd). One kernel walks the key tiles as
+ * pa_bwd_dkv does and also forms each key tile's share of dQ (dS K), which
+ * it adds into an fp32 accumulator in the workspace with vector reductions;
+ * a last kernel rounds the accumulator to bf16 into dq. Same arguments and
+ * operation as pa_bwd; seg may be NULL (plain causal).
+ *   - Results: dk and dv are bitwise those of pa_bwd / pa_bwd_causal. dq
+ *     matches them within rounding but is not bitwise reproducible from run
+ *     to run: the shares of one query row are added in whatever order the
+ *     key tiles finish.
+ *   - Workspace: pa_bwd_fused_workspace_bytes(dims) = pa_workspace_bytes(dims)
+ *     plus B*Hq*N*D*4 bytes for the accumulator (0 if dims are invalid or
+ *     N % 128 != 0).
+ *   - Errors: as pa_bwd, and PA_ERR_SHAPE when N % 128 != 0 (no staging
+ *     copies on this path).
+ */
+size_t pa_bwd_fused_workspace_bytes(const pa_dims* dims);
+pa_status pa_bwd_fused(const pa_dims* dims, const void* q, const void* k, const void* v, const void* out,
+                       const void* dout, const float* lse, const int32_t* seg, void* dq, void* dk, void* dv,
+                       void* ws, size_t ws_bytes, pa_stream_t stream);
+
+/*
  * Backward without a caller workspace, for callers that cannot allocate device
  * memory when they run it: code inside a region where its allocator or memory
  * pool forbids new allocations, or a host runtime that only hands out its own

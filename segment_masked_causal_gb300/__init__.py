@@ -33,7 +33,7 @@ EXPORTS = ["pa_workspace_bytes", "pa_fwd", "pa_bwd", "pa_fwd_causal", "pa_bwd_ca
            "pa_fwd_tiles", "pa_bwd_delta", "pa_bwd_dq", "pa_bwd_dkv", "pa_bwd_noalloc", "pa_device_status",
            "pa_selftest_wait_timeout", "pa_pack_first_fit", "pa_workspace_bytes_strided", "pa_fwd_strided",
            "pa_bwd_strided", "pa_lce_workspace_bytes", "pa_lce_fwd", "pa_lce_bwd_workspace_bytes", "pa_lce_bwd",
-           "pa_status_string"]
+           "pa_bwd_fused_workspace_bytes", "pa_bwd_fused", "pa_status_string"]
 
 
 class LibraryMissing(RuntimeError):
@@ -84,6 +84,10 @@ def lib():
             for f in ("pa_fwd", "pa_fwd_causal", "pa_bwd", "pa_bwd_causal", "pa_build_tile_table", "pa_fwd_tiles",
                       "pa_bwd_delta", "pa_bwd_dq", "pa_bwd_dkv"):
                 getattr(L, f).restype = ctypes.c_int
+            L.pa_bwd_fused_workspace_bytes.argtypes = [D]
+            L.pa_bwd_fused_workspace_bytes.restype = S
+            L.pa_bwd_fused.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P, S, P]
+            L.pa_bwd_fused.restype = ctypes.c_int
             L.pa_bwd_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P, P, ctypes.POINTER(ctypes.c_uint32), P]
             L.pa_bwd_noalloc.restype = ctypes.c_int
             L.pa_selftest_wait_timeout.argtypes = [P, S, P]
@@ -250,6 +254,38 @@ def pa_bwd(q, k, v, out, dout, lse, seg, dq, dk, dv, ws, scale=0.0, stream=None)
                         _ptr(out, bf, "out"), _ptr(dout, bf, "dout"), _ptr(lse, torch.float32, "lse"),
                         _ptr(seg, torch.int32, "seg"), _ptr(dq, bf, "dq"), _ptr(dk, bf, "dk"), _ptr(dv, bf, "dv"),
                         _ptr(ws, None, "ws"), ws.numel(), _stream(stream)))
+
+
+def pa_bwd_fused_workspace_bytes(B, Hq, Hkv, N, D) -> int:
+    d = make_dims(B, Hq, Hkv, N, D)
+    return int(lib().pa_bwd_fused_workspace_bytes(ctypes.byref(d)))
+
+
+def pa_bwd_fused(q, k, v, out, dout, lse, seg, dq, dk, dv, ws, scale=0.0, stream=None):
+    """The single-pass backward (seg None = plain causal); ws sized by
+    pa_bwd_fused_workspace_bytes."""
+    import torch
+    bf = torch.bfloat16
+    d = _dims_of(q, k, scale)
+    _check(lib().pa_bwd_fused(ctypes.byref(d), _ptr(q, bf, "q"), _ptr(k, bf, "k"), _ptr(v, bf, "v"),
+                              _ptr(out, bf, "out"), _ptr(dout, bf, "dout"), _ptr(lse, torch.float32, "lse"),
+                              _ptr(seg, torch.int32, "seg"), _ptr(dq, bf, "dq"), _ptr(dk, bf, "dk"),
+                              _ptr(dv, bf, "dv"), _ptr(ws, None, "ws"), ws.numel(), _stream(stream)))
+
+
+def backward_fused(q, k, v, out, dout, lse, seg=None, scale=0.0, ws=None):
+    """Allocate dq/dk/dv and run the single-pass backward (contiguous bf16,
+    N % 128 == 0); dq is not bitwise reproducible from run to run."""
+    import torch
+    B, Hq, N, D = q.shape
+    if ws is None:
+        n = pa_bwd_fused_workspace_bytes(B, Hq, k.shape[1], N, D)
+        if n == 0:
+            raise PAError(4, "invalid dims for the single-pass backward")
+        ws = torch.empty(n, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    pa_bwd_fused(q, k, v, out, dout, lse, seg, dq, dk, dv, ws, scale)
+    return dq, dk, dv
 
 
 def pa_bwd_causal(q, k, v, out, dout, lse, dq, dk, dv, ws, scale=0.0, stream=None):

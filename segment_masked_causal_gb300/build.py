@@ -19,8 +19,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa.so")
-SOURCES = ["api.cu", "prologue.cu", "stage.cu", "fwd.cu", "bwd_dq.cu", "bwd_dkv.cu", "noalloc.cu", "lce.cu",
-           "pack.cpp"]
+SOURCES = ["api.cu", "prologue.cu", "stage.cu", "fwd.cu", "bwd_dq.cu", "bwd_dkv.cu", "bwd_fused.cu", "noalloc.cu",
+           "lce.cu", "pack.cpp"]
 HEADERS = ["sm103.cuh", "common.cuh", "kernels.h", "tmap.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

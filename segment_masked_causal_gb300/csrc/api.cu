@@ -213,6 +213,36 @@ pa_status bwd_impl(const pa_dims* d, const void* q, const void* k, const void* v
   return step_dkv(d, q, k, v, dout, lse, seg, dk, dv, ws, ws_bytes, stream);
 }
 
+// Single-pass backward: the fp32 dQ accumulator sits after the kernels'
+// part of the workspace.
+size_t fused_acc_offset(const pa_dims* d) { return round_up(ws_layout(d).base); }
+size_t fused_ws_bytes(const pa_dims* d) {
+  return fused_acc_offset(d) + round_up((size_t)d->B * d->Hq * d->N * d->D * sizeof(float));
+}
+
+pa_status bwd_fused_impl(const pa_dims* d, const void* q, const void* k, const void* v, const void* out,
+                         const void* dout, const float* lse, const int32_t* seg, void* dq, void* dk, void* dv,
+                         void* ws, size_t ws_bytes, pa_stream_t stream) {
+  pa_status s = check_call(d, ws, ws_bytes, {q, k, v, out, dout, lse, dq, dk, dv}, seg);
+  if (s != PA_OK) return s;
+  if (ws_bytes < fused_ws_bytes(d)) return PA_ERR_WORKSPACE;
+  if ((s = step_tile_table(d, seg, ws, ws_bytes, stream)) != PA_OK) return s;
+  pa::AttnParams p = make_params(d, seg, ws);
+  p.lse_in = lse;
+  p.o = static_cast<const __nv_bfloat16*>(out);
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + fused_acc_offset(d));
+  p.dq_ld = d->D;
+  const cudaStream_t st = cu(stream);
+  if (pa::launch_delta(p, d->D, st) != cudaSuccess || pa::launch_bwd_fused(p, d->D, q, k, v, dout, st) != cudaSuccess ||
+      pa::launch_dq_round(p, d->D, st) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
 // ------------------------------------------------------------ staged calls
 // Element strides of the q group (q, out, dout, dq) and the k group (k, v,
 // dk, dv); D is contiguous.
@@ -408,6 +438,18 @@ pa_status pa_bwd_causal(const pa_dims* dims, const void* q, const void* k, const
                         const void* dout, const float* lse, void* dq, void* dk, void* dv, void* ws,
                         size_t ws_bytes, pa_stream_t stream) {
   return bwd_any(dims, nullptr, PA_IO_BF16, q, k, v, out, dout, lse, nullptr, dq, dk, dv, ws, ws_bytes, stream);
+}
+
+size_t pa_bwd_fused_workspace_bytes(const pa_dims* dims) {
+  pa_status why;
+  if (!dims_ok(dims, &why) || !tiled(dims)) return 0;
+  return fused_ws_bytes(dims);
+}
+
+pa_status pa_bwd_fused(const pa_dims* dims, const void* q, const void* k, const void* v, const void* out,
+                       const void* dout, const float* lse, const int32_t* seg, void* dq, void* dk, void* dv,
+                       void* ws, size_t ws_bytes, pa_stream_t stream) {
+  return bwd_fused_impl(dims, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream);
 }
 
 pa_status pa_build_tile_table(const pa_dims* dims, const int32_t* seg, void* ws, size_t ws_bytes,

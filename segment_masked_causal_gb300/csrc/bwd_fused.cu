@@ -1,0 +1,545 @@
+// bwd_fused.cu -- packed attention backward in one pass over the key tiles,
+// for sm_103a: dK, dV and dQ from the same recomputed tiles.
+//
+// The CTA layout and walk are the dK/dV kernel's: one CTA per (key tile of
+// 128 rows, kv head, batch row), every query head of the group in turn, and
+// for each the query tiles from the diagonal to the key tile's segment end.
+// Per visited (query head, query tile) step i, with K and V resident:
+//   S^T_i  = K Q_i^T   (TMEM A)   P^T_i  = exp2(scale*log2e * S^T_i - lse*log2e)  (bf16, over S^T_i)
+//   dP^T_i = V dO_i^T  (TMEM B)   dS^T_i = P^T_i * (dP^T_i - delta)  (bf16, shared memory)
+//   dV += P^T_i dO_i   dK += dS^T_i Q_i   dQ_i = dS_i K  (TMEM B, once dP^T_i is read)
+// dQ_i is this key tile's share of the query tile's gradient; it is scaled and
+// added into an fp32 accumulator in global memory with vector reductions, and
+// a last kernel rounds the accumulator to bf16. The shares of one query row
+// arrive from every key tile it sees, in no fixed order, so dQ is not
+// bitwise reproducible from run to run (dK and dV are: their sums stay in one
+// CTA, in a fixed order). This is the single-pass backward with fp32 dQ
+// accumulation that the split dQ / dK-dV design is compared against.
+//
+// dS^T_i lives in one 128 x 128 bf16 shared-memory tile, rows = keys: read
+// K-major it is the A operand of dK (keys x queries), read MN-major it is the
+// A operand of dQ (queries x keys). The same tile is the softmax warps'
+// transpose buffer when they move dQ_{i-1} out: each warp only ever touches
+// the 32 rows x 64 columns of the tile that it writes dS^T into itself.
+//
+// TMEM: dV and dK accumulators, region A (S^T_i, then P^T_i) and region B
+// (dP^T_i, then dQ_i). The softmax warps run each step as phase A (S^T_i to
+// P^T_i), then move dQ_{i-1} out of region B (which lets dP^T_i in), then
+// phase B (dS^T_i). Warp roles are the dK/dV kernel's: warp 0 TMA producer,
+// warp 1 issues S^T/dP^T and owns TMEM, warp 2 issues dV/dQ/dK, warps 3..10
+// softmax, two threads per key row, 64 query columns each.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "sm103.cuh"
+#include "tmap.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kFusedThreads = 352;
+constexpr int kFQStages = 2, kFDoStages = 2;
+
+struct FusedMisc {
+  uint64_t kv_full;
+  uint64_t q_full[kFQStages], q_empty[kFQStages];
+  uint64_t do_full[kFDoStages], do_empty[kFDoStages];
+  // one barrier per event; every waiter sees each phase before the next can
+  // complete (each event of step i+1 depends on the waiter having passed step i)
+  uint64_t s_full, dp_full, p_full, a_free, dv_done, ds_full, dq_full, dq_free, dk_done;
+  uint64_t final_sd, final_grad;
+  uint64_t o_staged;
+  uint32_t tmem_base;
+  int abort_flag;
+  alignas(16) float lse[kFQStages][128];
+  alignas(16) float dl[kFDoStages][128];
+};
+
+template <int D>
+struct FusedLayout {
+  static constexpr uint32_t TB = 128 * D * 2;    // one 128-row tile of K, V, Q or dO
+  static constexpr uint32_t CHUNK = 128 * 128;   // one 64-column chunk of a 128-row tile
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = OFF_K + TB;
+  static constexpr uint32_t OFF_Q = OFF_V + TB;
+  static constexpr uint32_t OFF_DO = OFF_Q + kFQStages * TB;
+  static constexpr uint32_t OFF_DS = OFF_DO + kFDoStages * TB;  // 128 keys x 128 queries bf16
+  static constexpr uint32_t OFF_MISC = OFF_DS + 2 * CHUNK;
+  static constexpr uint32_t SMEM = OFF_MISC + (uint32_t)((sizeof(FusedMisc) + 127) & ~size_t(127));
+  static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_A = 256, TM_B = 384, TMEM_COLS = 512;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    fused_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
+                     const AttnParams p) {
+  using L = FusedLayout<D>;
+  static_assert(L::SMEM <= 232448, "shared memory");
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32_runtime(smem_raw) & 1023u) {
+    if (threadIdx.x == 0 && p.status) atomicOr(p.status, PA_DEVERR_SMEM);
+    return;
+  }
+  uint8_t* base = smem_raw;
+  FusedMisc& m = *reinterpret_cast<FusedMisc*>(base + L::OFF_MISC);
+  const uint32_t sK = smem_u32(base + L::OFF_K), sV = smem_u32(base + L::OFF_V);
+  const uint32_t sQ = smem_u32(base + L::OFF_Q), sDO = smem_u32(base + L::OFF_DO);
+  const uint32_t sDS = smem_u32(base + L::OFF_DS);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ent = p.work_k[(int)blockIdx.x / p.Hkv];
+  const int tk = ent % p.T, b = ent / p.T;
+  const int hk = (int)blockIdx.x % p.Hkv;
+  const int4* trow = p.tiles + (size_t)b * p.T;
+  const Guard g{&m.abort_flag, p.status};
+  const QWalk walk(trow, tk);
+  const int h0 = hk * p.G, h1 = h0 + p.G;
+
+  if (threadIdx.x == 0) {
+    m.abort_flag = 0;
+    mbar_init(&m.kv_full, 1);
+    for (int s = 0; s < kFQStages; ++s) {
+      mbar_init(&m.q_full[s], 1);
+      mbar_init(&m.q_empty[s], 1);
+    }
+    for (int s = 0; s < kFDoStages; ++s) {
+      mbar_init(&m.do_full[s], 1);
+      mbar_init(&m.do_empty[s], 2 + 256);  // dP^T and dV MMAs, softmax after reading delta
+    }
+    mbar_init(&m.s_full, 1);
+    mbar_init(&m.dp_full, 1);
+    mbar_init(&m.p_full, 256);
+    mbar_init(&m.a_free, 256);
+    mbar_init(&m.dv_done, 1);
+    mbar_init(&m.ds_full, 256);
+    mbar_init(&m.dq_full, 1);
+    mbar_init(&m.dq_free, 256);
+    mbar_init(&m.dk_done, 1);
+    mbar_init(&m.final_sd, 1);
+    mbar_init(&m.final_grad, 1);
+    mbar_init(&m.o_staged, 256);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&m.tmem_base, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = m.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      const int krow = (b * p.Hkv + hk) * p.N + tk * kTile;
+      mbar_expect_tx(&m.kv_full, 2 * L::TB);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_2d(base + L::OFF_K + c * L::CHUNK, &tmK, &m.kv_full, c * 64, krow);
+        tma_load_2d(base + L::OFF_V + c * L::CHUNK, &tmV, &m.kv_full, c * 64, krow);
+      }
+      int i = 0;
+      bool ok = true;
+      for (int hq = h0; ok && hq < h1; ++hq) {
+        int4 te = walk.kt, te_next;
+        for (int tq = walk.first(), tq_next; tq < walk.end(); tq = tq_next, te = te_next, ++i) {
+          tq_next = walk.next(tq, te_next);
+          const int qs = i % kFQStages;
+          const int qrow = (b * p.Hq + hq) * p.N + tq * kTile;
+          if (!g.wait(&m.q_empty[qs], ((i / kFQStages) & 1) ^ 1, 41)) { ok = false; break; }
+          mbar_expect_tx(&m.q_full[qs], L::TB + 512);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(base + L::OFF_Q + qs * L::TB + c * L::CHUNK, &tmQ, &m.q_full[qs], c * 64, qrow);
+          bulk_load(m.lse[qs], p.lse2 + qrow, 512, &m.q_full[qs]);
+        }
+      }
+      g.drain(&m.kv_full, 0);
+      for (int k = (i > kFQStages ? i - kFQStages : 0); k < i; ++k)
+        g.drain(&m.q_full[k % kFQStages], (k / kFQStages) & 1);
+    } else if (lane == 1) {
+      prefetch_tmap(&tmDO);
+      int i = 0;
+      bool ok = true;
+      for (int hq = h0; ok && hq < h1; ++hq) {
+        int4 te = walk.kt, te_next;
+        for (int tq = walk.first(), tq_next; tq < walk.end(); tq = tq_next, te = te_next, ++i) {
+          tq_next = walk.next(tq, te_next);
+          const int ds = i % kFDoStages;
+          const int qrow = (b * p.Hq + hq) * p.N + tq * kTile;
+          if (!g.wait(&m.do_empty[ds], ((i / kFDoStages) & 1) ^ 1, 42)) { ok = false; break; }
+          mbar_expect_tx(&m.do_full[ds], L::TB + 512);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(base + L::OFF_DO + ds * L::TB + c * L::CHUNK, &tmDO, &m.do_full[ds], c * 64, qrow);
+          bulk_load(m.dl[ds], p.delta + qrow, 512, &m.do_full[ds]);
+        }
+      }
+      for (int k = (i > kFDoStages ? i - kFDoStages : 0); k < i; ++k)
+        g.drain(&m.do_full[k % kFDoStages], (k / kFDoStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ S^T / dP^T issuer
+    const bool leader = lane == 0;
+    constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+    const uint64_t kd = sdesc_sw128(sK, 16, 1024), vd = sdesc_sw128(sV, 16, 1024);
+    bool ok = g.wait_warp(&m.kv_full, 0, 43);
+    int i = 0;
+    for (int hq = h0; ok && hq < h1; ++hq) {
+      int4 te = walk.kt, te_next;
+      for (int tq = walk.first(), tq_next; tq < walk.end(); tq = tq_next, te = te_next, ++i) {
+        tq_next = walk.next(tq, te_next);
+        const int qs = i % kFQStages, ds = i % kFDoStages;
+        if (!g.wait_warp(&m.q_full[qs], (i / kFQStages) & 1, 44)) { ok = false; break; }
+        // region A: P^T_{i-1} read by phase B and by the dV product
+        if (i >= 1 && !(g.wait_warp(&m.a_free, (i - 1) & 1, 45) && g.wait_warp(&m.dv_done, (i - 1) & 1, 46))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t qd = sdesc_sw128(sQ + qs * L::TB, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
+          if (leader) umma_bf16(tmem + L::TM_A, sdesc_add(kd, ko), sdesc_add(qd, ko), idS, kk > 0 ? 1u : 0u);
+        }
+        if (leader) umma_commit(&m.s_full);
+        __syncwarp();
+        // region B: dQ_{i-1} moved out by the softmax warps
+        if (!g.wait_warp(&m.do_full[ds], (i / kFDoStages) & 1, 47)) { ok = false; break; }
+        if (i >= 1 && !g.wait_warp(&m.dq_free, (i - 1) & 1, 48)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t dod = sdesc_sw128(sDO + ds * L::TB, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
+          if (leader) umma_bf16(tmem + L::TM_B, sdesc_add(vd, ko), sdesc_add(dod, ko), idS, kk > 0 ? 1u : 0u);
+        }
+        if (leader) {
+          umma_commit(&m.dp_full);
+          umma_commit(&m.do_empty[ds]);
+        }
+        __syncwarp();
+      }
+    }
+    if (leader) {
+      umma_commit(&m.final_sd);
+      g.drain(&m.final_sd, 0);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ dV / dQ / dK issuer
+    const bool leader = lane == 0;
+    constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);  // A K-major (TMEM or smem), B MN-major
+    constexpr uint32_t idQ = idesc_bf16_f32(128, D, true, true);   // dS MN-major from the dS^T tile
+    const uint64_t dsk = sdesc_sw128(sDS, 16, 1024);               // dS^T, keys x queries, K-major
+    const uint64_t dsm = sdesc_sw128(sDS, L::CHUNK, 1024);         // the same bytes as dS, queries x keys
+    const uint64_t kdm = sdesc_sw128(sK, L::CHUNK, 1024);          // K as keys x D, MN-major
+    bool ok = true;
+    int j = 0;
+    for (int hq = h0; ok && hq < h1; ++hq) {
+      int4 te = walk.kt, te_next;
+      for (int tq = walk.first(), tq_next; tq < walk.end(); tq = tq_next, te = te_next, ++j) {
+        tq_next = walk.next(tq, te_next);
+        const int qs = j % kFQStages, ds = j % kFDoStages;
+        const uint32_t areg = tmem + L::TM_A;
+        if (!g.wait_warp(&m.do_full[ds], (j / kFDoStages) & 1, 49)) { ok = false; break; }
+        if (!g.wait_warp(&m.p_full, j & 1, 50)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t gd = sdesc_sw128(sDO + ds * L::TB, L::CHUNK, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          if (leader)
+            umma_bf16_ta(tmem + L::TM_DV, areg + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(gd, kk * 2048), idG,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+        if (leader) {
+          umma_commit(&m.dv_done);
+          umma_commit(&m.do_empty[ds]);
+        }
+        __syncwarp();
+        // dQ_j first (the softmax warps wait for it), then dK_j
+        if (!g.wait_warp(&m.q_full[qs], (j / kFQStages) & 1, 51)) { ok = false; break; }
+        if (!g.wait_warp(&m.ds_full, j & 1, 52)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          if (leader) umma_bf16(tmem + L::TM_B, sdesc_add(dsm, kk * 2048), sdesc_add(kdm, kk * 2048), idQ, kk > 0 ? 1u : 0u);
+        if (leader) umma_commit(&m.dq_full);
+        __syncwarp();
+        const uint64_t gq = sdesc_sw128(sQ + qs * L::TB, L::CHUNK, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          if (leader)
+            umma_bf16(tmem + L::TM_DK, sdesc_add(dsk, (kk >> 2) * L::CHUNK + (kk & 3) * 32), sdesc_add(gq, kk * 2048),
+                      idG, (j > 0 || kk > 0) ? 1u : 0u);
+        if (leader) {
+          umma_commit(&m.dk_done);
+          umma_commit(&m.q_empty[qs]);
+        }
+        __syncwarp();
+      }
+    }
+    if (leader) {
+      umma_commit(&m.final_grad);
+      g.drain(&m.final_grad, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quarter = warp & 3;
+    const int hsel = (warp - 3) >> 2;  // which 64 query columns of every step
+    const int r = quarter * 32 + lane;
+    const int kvidx = tk * kTile + r;
+    const int32_t segk = p.seg ? p.seg[(size_t)b * p.N + kvidx] : 0;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const int4 kt = trow[tk];
+    // this warp's 32 rows x 64 columns of the dS^T tile: its own dS^T rows,
+    // and its transpose buffer when dQ leaves
+    const uint32_t my_ds = sDS + hsel * L::CHUNK + quarter * 32 * 128;
+    bool ok = true;
+    int i = 0;
+    int prev_row = 0;  // first accumulator row of the previous step's query tile
+
+    // Move dQ of the previous step out of region B: this thread's TMEM lane is
+    // query row `lane` of the warp's quarter, and it holds D/2 columns.
+    auto drain_dq = [&](int step, int row0) -> bool {
+      bool w = g.wait(&m.dq_full, step & 1, 53);
+      if (!__all_sync(~0u, w)) return false;
+      tc_fence_after();
+      constexpr int NP = D / 64;  // 32-column passes per thread
+      uint32_t v[NP][32];
+      if constexpr (NP == 2)
+        tmem_ld32x2(tmem + lane_base + L::TM_B + hsel * 64, tmem + lane_base + L::TM_B + hsel * 64 + 32, v[0], v[1]);
+      else
+        tmem_ld32(tmem + lane_base + L::TM_B + hsel * 32, v[0]);
+      tc_fence_before();
+      mbar_arrive(&m.dq_free);  // region B may take dP^T of this step
+      // the dS^T tile is free once dK of the previous step has read it
+      w = g.wait(&m.dk_done, step & 1, 54);
+      if (!__all_sync(~0u, w)) return false;
+      const float sc = p.scale;
+#pragma unroll
+      for (int ps = 0; ps < NP; ++ps) {
+        // row `lane` of the buffer, 16-byte units rotated by the row
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(my_ds + lane * 128 + ((u ^ (lane & 7)) << 4)),
+                       "f"(__uint_as_float(v[ps][4 * u]) * sc), "f"(__uint_as_float(v[ps][4 * u + 1]) * sc),
+                       "f"(__uint_as_float(v[ps][4 * u + 2]) * sc), "f"(__uint_as_float(v[ps][4 * u + 3]) * sc)
+                       : "memory");
+        __syncwarp();
+        // read back 4 rows x 128 bytes per instruction and add them into the
+        // accumulator: whole 128-byte lines per reduction
+        const int col = hsel * (D / 2) + ps * 32 + (lane & 7) * 4;
+#pragma unroll
+        for (int jr = 0; jr < 8; ++jr) {
+          const int rr = jr * 4 + (lane >> 3);
+          float4 x;
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                       : "r"(my_ds + rr * 128 + (((lane & 7) ^ (rr & 7)) << 4))
+                       : "memory");
+          if (col < p.dq_ld)
+            atomicAdd(reinterpret_cast<float4*>(p.dq_acc + (size_t)(row0 + quarter * 32 + rr) * p.dq_ld + col), x);
+        }
+        __syncwarp();
+      }
+      return true;
+    };
+
+    for (int hq = h0; ok && hq < h1; ++hq) {
+      int4 te = walk.kt, te_next;
+      for (int tq = walk.first(), tq_next; tq < walk.end(); tq = tq_next, te = te_next, ++i) {
+        tq_next = walk.next(tq, te_next);
+        const int qs = i % kFQStages, ds = i % kFDoStages;
+        ok = g.wait(&m.q_full[qs], (i / kFQStages) & 1, 55) && g.wait(&m.do_full[ds], (i / kFDoStages) & 1, 56);
+        if (!__all_sync(~0u, ok)) { ok = false; break; }
+        ok = g.wait(&m.s_full, i & 1, 57);
+        if (!__all_sync(~0u, ok)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t areg = tmem + lane_base + L::TM_A + hsel * 64;
+        const uint32_t breg = tmem + lane_base + L::TM_B + hsel * 64;
+        const bool masked = !tile_pair_full(tq, te, tk, kt);
+        const int c0 = hsel * 64;
+        const int q0 = tq * kTile + c0;
+        // ---- phase A: P^T = exp2(S^T * scale*log2e - lse*log2e), bf16 over S^T
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          uint32_t sv[32];
+          tmem_ld32(areg + 32 * c, sv);
+          const float4* l4 = reinterpret_cast<const float4*>(&m.lse[qs][c0 + 32 * c]);
+          const int qc = q0 + 32 * c;
+          uint32_t pw[16];
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 lv = l4[e4];
+            const float lz[4] = {lv.x, lv.y, lv.z, lv.w};
+            float sz[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sz[e] = __uint_as_float(sv[e4 * 4 + e]);
+            if (masked) {
+              const int4 gv = p.seg ? __ldg(reinterpret_cast<const int4*>(p.seg + (size_t)b * p.N + qc) + e4)
+                                    : make_int4(0, 0, 0, 0);
+              const int32_t gz[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                sz[e] = (qc + e4 * 4 + e >= kvidx && gz[e] == segk) ? sz[e] : -INFINITY;
+            }
+            float pz[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pz[e] = ex2(fmaf(sz[e], sl2, -lz[e]));
+            pw[e4 * 2] = pack_bf16x2(pz[0], pz[1]);
+            pw[e4 * 2 + 1] = pack_bf16x2(pz[2], pz[3]);
+          }
+          tmem_st16_nowait(areg + 16 * c, pw);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&m.p_full);
+        // ---- dQ of the previous step leaves region B
+        if (i >= 1 && !drain_dq(i - 1, prev_row)) { ok = false; break; }
+        prev_row = (b * p.Hq + hq) * p.N + tq * kTile;
+        // ---- phase B: dS^T = P^T * (dP^T - delta), bf16 into the dS^T tile
+        ok = g.wait(&m.dp_full, i & 1, 58);
+        if (!__all_sync(~0u, ok)) { ok = false; break; }
+        tc_fence_after();
+        const float4* d4 = reinterpret_cast<const float4*>(&m.dl[ds][c0]);
+        uint32_t dpa[32], dpb[32], pb[32];
+        tmem_ld32x3(breg, breg + 32, areg, dpa, dpb, pb);
+        tc_fence_before();
+        mbar_arrive(&m.a_free);  // region A may take S^T of the next step once dV has run
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t dw[16];
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 dv = d4[c * 8 + e4];
+            const uint32_t w0 = pb[c * 16 + e4 * 2], w1 = pb[c * 16 + e4 * 2 + 1];
+            const float pp[4] = {__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u),
+                                 __uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u)};
+            const uint32_t* dp = c ? dpb : dpa;
+            dw[e4 * 2] = pack_bf16x2(pp[0] * (__uint_as_float(dp[e4 * 4]) - dv.x),
+                                     pp[1] * (__uint_as_float(dp[e4 * 4 + 1]) - dv.y));
+            dw[e4 * 2 + 1] = pack_bf16x2(pp[2] * (__uint_as_float(dp[e4 * 4 + 2]) - dv.z),
+                                         pp[3] * (__uint_as_float(dp[e4 * 4 + 3]) - dv.w));
+          }
+          // row r of chunk hsel, 16-byte units 4c..4c+3 in the 128-byte swizzle
+#pragma unroll
+          for (int u4 = 0; u4 < 4; ++u4)
+            st_shared_v4(my_ds + lane * 128 + (((4 * c + u4) ^ (lane & 7)) << 4), dw[4 * u4], dw[4 * u4 + 1],
+                         dw[4 * u4 + 2], dw[4 * u4 + 3]);
+        }
+        fence_async_smem();  // read by the dK and dQ products
+        mbar_arrive(&m.ds_full);
+        mbar_arrive(&m.do_empty[ds]);  // this step's delta vector has been read
+      }
+    }
+    if (ok && i > 0 && !drain_dq(i - 1, prev_row)) ok = false;
+    if (ok && i > 0) {
+      ok = g.wait(&m.final_grad, 0, 59);
+      ok = __all_sync(~0u, ok);
+    }
+    if (ok && i > 0) {
+      tc_fence_after();
+      // dV and dK rows leave through the V and K tiles' shared memory (every
+      // MMA has completed) and TMA stores of whole 128-byte rows.
+      uint8_t* sv = base + L::OFF_V;
+      uint8_t* sk = base + L::OFF_K;
+      const float sc = p.scale;
+#pragma unroll
+      for (int cc = hsel * (D / 2); cc < (hsel + 1) * (D / 2); cc += 32) {
+        uint32_t v[32], k[32];
+        tmem_ld32x2(tmem + lane_base + L::TM_DV + cc, tmem + lane_base + L::TM_DK + cc, v, k);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int col = cc + 8 * q4;
+          const uint32_t off = (col >> 6) * L::CHUNK + r * 128 + ((((col & 63) >> 3) ^ (r & 7)) << 4);
+          st_shared_v4(smem_u32(sv + off), pack_bf16x2(__uint_as_float(v[q4 * 8 + 0]), __uint_as_float(v[q4 * 8 + 1])),
+                       pack_bf16x2(__uint_as_float(v[q4 * 8 + 2]), __uint_as_float(v[q4 * 8 + 3])),
+                       pack_bf16x2(__uint_as_float(v[q4 * 8 + 4]), __uint_as_float(v[q4 * 8 + 5])),
+                       pack_bf16x2(__uint_as_float(v[q4 * 8 + 6]), __uint_as_float(v[q4 * 8 + 7])));
+          st_shared_v4(smem_u32(sk + off),
+                       pack_bf16x2(__uint_as_float(k[q4 * 8 + 0]) * sc, __uint_as_float(k[q4 * 8 + 1]) * sc),
+                       pack_bf16x2(__uint_as_float(k[q4 * 8 + 2]) * sc, __uint_as_float(k[q4 * 8 + 3]) * sc),
+                       pack_bf16x2(__uint_as_float(k[q4 * 8 + 4]) * sc, __uint_as_float(k[q4 * 8 + 5]) * sc),
+                       pack_bf16x2(__uint_as_float(k[q4 * 8 + 6]) * sc, __uint_as_float(k[q4 * 8 + 7]) * sc));
+        }
+      }
+      fence_async_smem();
+      mbar_arrive(&m.o_staged);
+      if (warp == 3 && lane == 0 && g.wait(&m.o_staged, 0, 60)) {
+        const int krow = (b * p.Hkv + hk) * p.N + tk * kTile;
+        for (int c = 0; c < D / 64; ++c) {
+          tma_store_2d(&tmDV, sv + c * L::CHUNK, c * 64, krow);
+          tma_store_2d(&tmDK, sk + c * L::CHUNK, c * 64, krow);
+        }
+        bulk_commit();
+        bulk_wait_all();
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+template <int D>
+cudaError_t launch_fused_d(const AttnParams& p, int Dio, const void* q, const void* k, const void* v,
+                           const void* dout, cudaStream_t st) {
+  using L = FusedLayout<D>;
+  CUtensorMap tq, tdo, tk, tv, tdk, tdv;
+  const uint64_t qrows = (uint64_t)p.B * p.Hq * p.N, krows = (uint64_t)p.B * p.Hkv * p.N;
+  if (!tmap_bf16_2d_sw128(&tq, q, Dio, qrows, 128) || !tmap_bf16_2d_sw128(&tdo, dout, Dio, qrows, 128) ||
+      !tmap_bf16_2d_sw128(&tk, k, Dio, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, Dio, krows, 128) ||
+      !tmap_bf16_2d_sw128(&tdk, p.dk, Dio, krows, 128) || !tmap_bf16_2d_sw128(&tdv, p.dv, Dio, krows, 128))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(fused_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.T * p.Hkv * p.B);
+  fused_bwd_kernel<D><<<grid, kFusedThreads, L::SMEM, st>>>(tq, tdo, tk, tv, tdk, tdv, p);
+  return cudaGetLastError();
+}
+
+// dq (bf16) = the fp32 accumulator rounded to nearest even, 8 elements a thread.
+__global__ void __launch_bounds__(256) dq_round_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq,
+                                                       size_t n8) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x; t < n8; t += stride) {
+    const float4 a = acc[2 * t], c = acc[2 * t + 1];
+    dq[t] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(c.x, c.y), pack_bf16x2(c.z, c.w));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_fused(const AttnParams& p, int D, const void* q, const void* k, const void* v,
+                             const void* dout, cudaStream_t st) {
+  // head dim 96 runs the 128-wide kernel, as the dK/dV kernel does; the dQ
+  // reductions skip the zero columns 96..127
+  return D == 64 ? launch_fused_d<64>(p, 64, q, k, v, dout, st) : launch_fused_d<128>(p, D, q, k, v, dout, st);
+}
+
+cudaError_t launch_dq_round(const AttnParams& p, int D, cudaStream_t st) {
+  const size_t n8 = (size_t)p.B * p.Hq * p.N * D / 8;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  size_t blocks = (n8 + 255) / 256;
+  if (blocks > (size_t)sms * 8) blocks = (size_t)sms * 8;
+  if (blocks == 0) return cudaSuccess;
+  dq_round_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(p.dq_acc),
+                                                   reinterpret_cast<uint4*>(p.dq), n8);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -47,6 +47,10 @@ struct AttnParams {
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
+  // single-pass backward only: fp32 dQ accumulator (B, Hq, N, dq_ld), zeroed
+  // by the delta kernel when non-null
+  float* dq_acc;
+  int dq_ld;
 };
 
 __device__ __forceinline__ bool tiles_overlap(int4 a, int4 b) { return a.x <= b.y && b.x <= a.y; }

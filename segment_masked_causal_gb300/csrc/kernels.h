@@ -15,7 +15,8 @@ pa_status device_check();
 // Tile table (B, T) x {smin, smax, kv_lo, q_hi} and the two work lists; also
 // clears the status word.
 cudaError_t launch_tile_table(const AttnParams& p, int4* tiles, cudaStream_t st);
-// delta[b, h, i] = sum_c dO[b, h, i, c] * O[b, h, i, c] (fp32), and lse2 = lse * log2(e).
+// delta[b, h, i] = sum_c dO[b, h, i, c] * O[b, h, i, c] (fp32), and lse2 = lse * log2(e);
+// also zeroes the rows of p.dq_acc when it is non-null.
 cudaError_t launch_delta(const AttnParams& p, int D, cudaStream_t st);
 // Self-test of the bounded waits: one warp waits on an mbarrier nothing arrives on.
 cudaError_t launch_wait_timeout_selftest(uint32_t* status, cudaStream_t st);
@@ -24,6 +25,11 @@ cudaError_t launch_bwd_dq(const AttnParams& p, int D, const void* q, const void*
                           const void* dout, cudaStream_t st);
 cudaError_t launch_bwd_dkv(const AttnParams& p, int D, const void* q, const void* k, const void* v,
                            const void* dout, cudaStream_t st);
+// Single-pass backward: dK, dV and the fp32 dQ accumulator p.dq_acc (zeroed
+// beforehand), then p.dq = the accumulator rounded to bf16.
+cudaError_t launch_bwd_fused(const AttnParams& p, int D, const void* q, const void* k, const void* v,
+                             const void* dout, cudaStream_t st);
+cudaError_t launch_dq_round(const AttnParams& p, int D, cudaStream_t st);
 
 // A (B, H, N, D) bf16 or fp32 tensor with element strides sb, sh, sn (16-byte
 // multiples) and contiguous D, against the kernels' contiguous bf16

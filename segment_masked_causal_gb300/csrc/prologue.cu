@@ -220,7 +220,8 @@ template <int D>
 __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restrict__ o,
                                                     const __nv_bfloat16* __restrict__ dout,
                                                     const float* __restrict__ lse, float* __restrict__ delta,
-                                                    float* __restrict__ lse2, size_t rows) {
+                                                    float* __restrict__ lse2, float* __restrict__ zero_acc,
+                                                    size_t rows) {
   // each of the row's LPR lanes takes every LPR-th 16-byte vector
   constexpr int VEC = D / 8;
   constexpr int LPR = delta_lanes(D);
@@ -243,6 +244,11 @@ __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restr
       acc = fmaf(bf16hi(a.z), bf16hi(c.z), acc);
       acc = fmaf(bf16lo(a.w), bf16lo(c.w), acc);
       acc = fmaf(bf16hi(a.w), bf16hi(c.w), acc);
+      if (zero_acc) {
+        float4* z = reinterpret_cast<float4*>(zero_acc + row * D) + 2 * v;
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
 #pragma unroll
     for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(~0u, acc, off);
@@ -313,11 +319,11 @@ cudaError_t launch_delta(const AttnParams& p, int D, cudaStream_t st) {
   const size_t cap = (size_t)sms * 8;
   if (blocks > cap) blocks = cap;
   if (D == 128)
-    delta_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, rows);
+    delta_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, p.dq_acc, rows);
   else if (D == 96)
-    delta_kernel<96><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, rows);
+    delta_kernel<96><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, p.dq_acc, rows);
   else
-    delta_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, rows);
+    delta_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, p.dq_acc, rows);
   return cudaGetLastError();
 }
 
