@@ -437,6 +437,7 @@ def run_ours(args):
         line["head_dim_96"] = head_dim_96_extra(dev, rank, args)
         line["staged_layouts"] = staged_layout_extras(dev, rank, args)
         line["configs"] = config_extras(dev, rank, args)
+        line["single_pass_backward"] = single_pass_extra(dev, rank, args)
     if not args.no_extras and w.name == "8k_one_segment" and rank == 0 and world == 1:
         line["linear_cross_entropy"] = lce_extra()
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -574,6 +575,62 @@ def config_extras(dev, rank, args):
     if rank == 0 and not args.no_cpu:
         for name in out:
             out[name]["oracle"] = oracle_estimate(synth.workload(name))
+    return out
+
+
+def single_pass_extra(dev, rank, args, names=("8k_one_segment", "8k_packed", "packed_4x4096_short", "causal_2k_gqa",
+                                               "long_32k_one_segment", "long_32k_packed", "long_64k_one_segment",
+                                               "long_64k_packed")):
+    """The split backward (tile table + delta + dQ + dK/dV kernels) against
+    the single-pass backward (pa_bwd_fused: tile table + delta with the
+    accumulator zeroed + one kernel + the bf16 rounding), each timed as a
+    whole with CUDA events, L2 flushed before every call, median of the
+    steps, on configs 2-5."""
+    import torch
+    import segment_masked_causal_gb300 as pa
+    steps = max(3, min(args.steps, 10))
+    out = {}
+    for name in names:
+        w = synth.workload(name)
+        r = Runner(w, dev, replica_seed(w.seed, rank))
+        r.checked_step()
+        fws = torch.empty(pa.pa_bwd_fused_workspace_bytes(w.B, w.Hq, w.Hkv, w.N, w.D), dtype=torch.uint8,
+                          device=dev)
+        fdq, fdk, fdv = torch.empty_like(r.dq), torch.empty_like(r.dk), torch.empty_like(r.dv)
+        q, k, v, do, seg = r.q, r.k, r.v, r.do, r.seg
+
+        def split():
+            pa.pa_build_tile_table(q, k, seg, r.ws)
+            pa.pa_bwd_delta(q, k, r.out, do, r.lse, r.ws)
+            pa.pa_bwd_dq(q, k, v, do, r.lse, seg, r.dq, r.ws)
+            pa.pa_bwd_dkv(q, k, v, do, r.lse, seg, r.dk, r.dv, r.ws)
+
+        def fused():
+            pa.pa_bwd_fused(q, k, v, r.out, do, r.lse, seg, fdq, fdk, fdv, fws)
+
+        res = {}
+        for key, fn, ws in (("split_ms", split, r.ws), ("single_pass_ms", fused, fws)):
+            for _ in range(2):
+                fn()
+                r.flush()
+            evs = []
+            for _ in range(steps):
+                r.flush()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                evs.append((a, b))
+            torch.cuda.synchronize()
+            st = pa.pa_device_status(ws)
+            if st != 0:
+                raise RuntimeError(f"device status {st:#x} after the {key[:-3]} backward")
+            res[key] = round(statistics.median(a.elapsed_time(b) for a, b in evs), 4)
+        res["single_pass_speedup"] = round(res["split_ms"] / res["single_pass_ms"], 3)
+        res["dk_dv_bitwise_equal"] = bool(torch.equal(fdk, r.dk) and torch.equal(fdv, r.dv))
+        out[name] = res
+        del r, fws, fdq, fdk, fdv
+        torch.cuda.empty_cache()
     return out
 
 
@@ -782,10 +839,17 @@ def main(argv=None):
                     help="only the fused linear cross-entropy forward and backward, printed as one JSON line")
     ap.add_argument("--lce-shape", default=None,
                     help="N,V,D for --lce-only (default 8192,151936,4096, the README's isolated-loss shape)")
+    ap.add_argument("--single-pass-only", action="store_true",
+                    help="only the split vs single-pass backward comparison on --workload, one JSON line")
     args = ap.parse_args(argv)
     if args.lce_only:
         shape = tuple(int(x) for x in args.lce_shape.split(",")) if args.lce_shape else None
         print(json.dumps(lce_measure(shape=shape)), flush=True)
+        return
+    if args.single_pass_only:
+        import torch
+        dev = torch.device("cuda:0")
+        print(json.dumps(single_pass_extra(dev, 0, args, names=(args.workload,))), flush=True)
         return
     args.warmup = max(3, args.warmup)  # at least 3 warm-up steps, whatever was asked
     if args.impl == "reference":
