@@ -15,6 +15,9 @@
 // summed inside the CTA in a fixed order, so dK/dV need no atomics and are
 // deterministic.
 //
+// Thread slice h of a key row keeps P^T of its 32 query columns in packed
+// columns 32h..32h+15 of step i's S region and dS^T in 32h+16..32h+31.
+//
 // TMEM holds the dV and dK accumulators and two 128-column regions whose roles
 // swap every step: S^T_{i+1} goes where dP^T_i was as soon as the softmax
 // warps have read dP^T_i, and dP^T_{i+1} goes where P^T_i/dS^T_i were once
@@ -32,9 +35,11 @@
 // V tiles' shared memory and TMA stores.
 //
 // Warp roles: warp 0 TMA producer (lane 0 the Q ring, lane 1 the dO ring),
-// warp 1 issues S^T/dP^T and owns TMEM, warp 2 issues dV/dK, warps 3..10
-// softmax: two threads per key row (TMEM lane quarter = warp index mod 4),
-// 64 query columns each.
+// warp 1 issues S^T/dP^T and owns TMEM, warp 2 issues dV/dK, warps 3..18
+// softmax: four threads per key row (TMEM lane quarter = warp index mod 4),
+// 32 query columns each. Nothing in a step reduces along a row, so the
+// columns split freely; sixteen warps hide the TMEM-load, exponential and
+// barrier latencies of the two phases better than eight did.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -46,7 +51,7 @@ namespace pa {
 
 namespace {
 
-constexpr int kDkvThreads = 352;
+constexpr int kDkvThreads = 608;  // warps 3..18 softmax: four threads per key row
 constexpr int kQStages = 3, kDoStages = 2;
 
 struct DkvMisc {
@@ -120,19 +125,19 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
       mbar_init(&m.do_full[s], 1);
       // released by the dP^T and dV MMAs and by the softmax threads once
       // phase B has read the stage's delta vector
-      mbar_init(&m.do_empty[s], 2 + 256);
+      mbar_init(&m.do_empty[s], 2 + 512);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&m.s_full[s], 1);
       mbar_init(&m.dp_full[s], 1);
-      mbar_init(&m.p_full[s], 256);
-      mbar_init(&m.dp_free[s], 256);
-      mbar_init(&m.ds_full[s], 256);
+      mbar_init(&m.p_full[s], 512);
+      mbar_init(&m.dp_free[s], 512);
+      mbar_init(&m.ds_full[s], 512);
       mbar_init(&m.grad_done[s], 1);
     }
     mbar_init(&m.final_sd, 1);
     mbar_init(&m.final_grad, 1);
-    mbar_init(&m.o_staged, 256);
+    mbar_init(&m.o_staged, 512);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -247,8 +252,8 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
     __syncwarp();
   } else if (warp == 2) {
     // ------------------------------------------------------------ dV / dK issuer
-    // thread-half h keeps P^T of its 64 query columns in columns 64h..64h+31
-    // of step j's S region and dS^T in columns 64h+32..64h+63
+    // thread slice h keeps P^T of its 32 query columns in columns 32h..32h+15
+    // of step j's S region and dS^T in columns 32h+16..32h+31
     const bool leader = lane == 0;
     constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);
     bool ok = true;
@@ -269,7 +274,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           if (leader)
-            umma_bf16_ta(tmem + L::TM_DV, sreg + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(gd, kk * 2048), idG,
+            umma_bf16_ta(tmem + L::TM_DV, sreg + (kk >> 1) * 32 + (kk & 1) * 8, sdesc_add(gd, kk * 2048), idG,
                          (j > 0 || kk > 0) ? 1u : 0u);
         if (leader) umma_commit(&m.do_empty[ds]);
         __syncwarp();
@@ -280,7 +285,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           if (leader)
-            umma_bf16_ta(tmem + L::TM_DK, sreg + (kk >> 2) * 64 + 32 + (kk & 3) * 8, sdesc_add(gq, kk * 2048), idG,
+            umma_bf16_ta(tmem + L::TM_DK, sreg + (kk >> 1) * 32 + 16 + (kk & 1) * 8, sdesc_add(gq, kk * 2048), idG,
                          (j > 0 || kk > 0) ? 1u : 0u);
         if (leader) {
           umma_commit(&m.grad_done[j & 1]);
@@ -297,7 +302,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
   } else {
     // ------------------------------------------------------------ softmax
     const int quarter = warp & 3;
-    const int hsel = (warp - 3) >> 2;  // which 64 query columns of every step
+    const int hsel = (warp - 3) >> 2;  // which 32 query columns of every step
     const int r = quarter * 32 + lane;
     const int kvidx = tk * kTile + r;
     const int32_t segk = p.seg ? p.seg[(size_t)b * p.N + kvidx] : 0;
@@ -311,28 +316,21 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
       for (int tq = walk.first(), tq_next; tq < walk.end(); tq = tq_next, te = te_next, ++i) {
         tq_next = walk.next(tq, te_next);  // loaded now, used after this tile's work
         const int qs = i % kQStages, ds = i % kDoStages;
-        // this step's lse and delta vectors (waited here, before this thread
-        // releases anything of the step, so neither ring can run ahead)
         ok = g.wait(&m.q_full[qs], (i / kQStages) & 1, 12) && g.wait(&m.do_full[ds], (i / kDoStages) & 1, 13);
         if (!__all_sync(~0u, ok)) { ok = false; break; }
         ok = g.wait(&m.s_full[i & 1], (i >> 1) & 1, 14);
         if (!__all_sync(~0u, ok)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sreg = tmem + lane_base + L::reg_s(i) + hsel * 64;
-        const uint32_t dreg = tmem + lane_base + L::reg_dp(i) + hsel * 64;
+        const uint32_t sreg = tmem + lane_base + L::reg_s(i) + hsel * 32;
+        const uint32_t dreg = tmem + lane_base + L::reg_dp(i) + hsel * 32;
         const bool masked = !tile_pair_full(tq, te, tk, kt);
-        const int c0 = hsel * 64;        // first query column of this thread within the tile
+        const int c0 = hsel * 32;        // first query column of this thread within the tile
         const int q0 = tq * kTile + c0;  // its token index
         // ---- phase A: P^T = exp2(S^T * scale*log2e - lse*log2e), bf16 over S^T
-        // (the delta step stored lse*log2e).
-        // Two 32-column chunks in a rolled loop (the softmax code must stay
-        // small: instruction fetch, not arithmetic, limits these warps).
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
+        {
           uint32_t sv[32];
-          tmem_ld32(sreg + 32 * c, sv);
-          const float4* l4 = reinterpret_cast<const float4*>(&m.lse[qs][c0 + 32 * c]);
-          const int qc = q0 + 32 * c;
+          tmem_ld32(sreg, sv);
+          const float4* l4 = reinterpret_cast<const float4*>(&m.lse[qs][c0]);
           uint32_t pw[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
@@ -342,12 +340,12 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) sz[e] = __uint_as_float(sv[e4 * 4 + e]);
             if (masked) {
-              const int4 gv = p.seg ? __ldg(reinterpret_cast<const int4*>(p.seg + (size_t)b * p.N + qc) + e4)
+              const int4 gv = p.seg ? __ldg(reinterpret_cast<const int4*>(p.seg + (size_t)b * p.N + q0) + e4)
                                     : make_int4(0, 0, 0, 0);
               const int32_t gz[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                sz[e] = (qc + e4 * 4 + e >= kvidx && gz[e] == segk) ? sz[e] : -INFINITY;
+                sz[e] = (q0 + e4 * 4 + e >= kvidx && gz[e] == segk) ? sz[e] : -INFINITY;
             }
             float pz[4];
 #pragma unroll
@@ -355,42 +353,36 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
             pw[e4 * 2] = pack_bf16x2(pz[0], pz[1]);
             pw[e4 * 2 + 1] = pack_bf16x2(pz[2], pz[3]);
           }
-          // packed columns 16c..16c+15: S^T columns this thread has already read
-          tmem_st16_nowait(sreg + 16 * c, pw);
+          // packed columns 0..15 of this thread's slice: S^T columns it has already read
+          tmem_st16_nowait(sreg, pw);
         }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&m.p_full[i & 1]);
-        // ---- phase B: dS^T = P^T * (dP^T - delta), bf16 next to P^T. P^T is read
-        // back as the bf16 values the dV product uses, so dS^T is formed from
-        // the same rounded probabilities
+        // ---- phase B: dS^T = P^T * (dP^T - delta), bf16 next to P^T
         ok = g.wait(&m.dp_full[i & 1], (i >> 1) & 1, 15);
         if (!__all_sync(~0u, ok)) { ok = false; break; }
         tc_fence_after();
         const float4* d4 = reinterpret_cast<const float4*>(&m.dl[ds][c0]);
-        // all of dP^T (64 columns) and P^T (32 packed columns) first, so the
-        // dP^T region is released before any arithmetic
-        uint32_t dpa[32], dpb[32], pb[32];
-        tmem_ld32x3(dreg, dreg + 32, sreg, dpa, dpb, pb);
+        uint32_t dpa[32], pb[16];
+        tmem_ld32_ld16(dreg, sreg, dpa, pb);
         tc_fence_before();
         mbar_arrive(&m.dp_free[i & 1]);
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        {
           uint32_t dw[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 dv = d4[c * 8 + e4];
-            const uint32_t w0 = pb[c * 16 + e4 * 2], w1 = pb[c * 16 + e4 * 2 + 1];
+            const float4 dv = d4[e4];
+            const uint32_t w0 = pb[e4 * 2], w1 = pb[e4 * 2 + 1];
             const float pp[4] = {__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u),
                                  __uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u)};
-            const uint32_t* dp = c ? dpb : dpa;
-            dw[e4 * 2] = pack_bf16x2(pp[0] * (__uint_as_float(dp[e4 * 4]) - dv.x),
-                                     pp[1] * (__uint_as_float(dp[e4 * 4 + 1]) - dv.y));
-            dw[e4 * 2 + 1] = pack_bf16x2(pp[2] * (__uint_as_float(dp[e4 * 4 + 2]) - dv.z),
-                                         pp[3] * (__uint_as_float(dp[e4 * 4 + 3]) - dv.w));
+            dw[e4 * 2] = pack_bf16x2(pp[0] * (__uint_as_float(dpa[e4 * 4]) - dv.x),
+                                     pp[1] * (__uint_as_float(dpa[e4 * 4 + 1]) - dv.y));
+            dw[e4 * 2 + 1] = pack_bf16x2(pp[2] * (__uint_as_float(dpa[e4 * 4 + 2]) - dv.z),
+                                         pp[3] * (__uint_as_float(dpa[e4 * 4 + 3]) - dv.w));
           }
-          // over this thread's own S^T columns 32..63 (read in phase A)
-          tmem_st16_nowait(sreg + 32 + 16 * c, dw);
+          // packed columns 16..31 of this thread's slice (read in phase A)
+          tmem_st16_nowait(sreg + 16, dw);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -412,7 +404,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
       uint8_t* sk = base + L::OFF_K;
       const float sc = p.scale;
 #pragma unroll
-      for (int c0 = hsel * (D / 2); c0 < (hsel + 1) * (D / 2); c0 += 32) {
+      for (int c0 = hsel * 32; c0 < D && c0 < (hsel + 1) * 32; c0 += 32) {
         uint32_t v[32], k[32];
         tmem_ld32x2(tmem + lane_base + L::TM_DV + c0, tmem + lane_base + L::TM_DK + c0, v, k);
 #pragma unroll
