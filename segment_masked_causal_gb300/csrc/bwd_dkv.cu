@@ -84,7 +84,7 @@ struct DkvLayout {
   static __device__ __forceinline__ uint32_t reg_dp(int i) { return (i & 1) ? TM_X : TM_Y; }
 };
 
-template <int D>
+template <int D, int DM>
 __global__ void __launch_bounds__(kDkvThreads, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
         tc_fence_after();
         const uint64_t qd = sdesc_sw128(sQ + qs * L::TB, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < DM / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
           if (leader) umma_bf16(tmem + L::reg_s(i), sdesc_add(kd, ko), sdesc_add(qd, ko), idS, kk > 0 ? 1u : 0u);
         }
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
         tc_fence_after();
         const uint64_t dod = sdesc_sw128(sDO + ds * L::TB, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < DM / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
           if (leader) umma_bf16(tmem + L::reg_dp(i), sdesc_add(vd, ko), sdesc_add(dod, ko), idS, kk > 0 ? 1u : 0u);
         }
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
     // thread slice h keeps P^T of its 32 query columns in columns 32h..32h+15
     // of step j's S region and dS^T in columns 32h+16..32h+31
     const bool leader = lane == 0;
-    constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);
+    constexpr uint32_t idG = idesc_bf16_f32(128, DM, false, true);
     bool ok = true;
     int j = 0;
     for (int hq = h0; ok && hq < h1; ++hq) {
@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
   }
 }
 
-template <int D>
+template <int D, int DM = D>
 cudaError_t launch_dkv_d(const AttnParams& p, int Dio, const void* q, const void* k, const void* v, const void* dout,
                          cudaStream_t st) {
   using L = DkvLayout<D>;
@@ -453,10 +453,10 @@ cudaError_t launch_dkv_d(const AttnParams& p, int Dio, const void* q, const void
       !tmap_bf16_2d_sw128(&tk, k, Dio, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, Dio, krows, 128) ||
       !tmap_bf16_2d_sw128(&tdk, p.dk, Dio, krows, 128) || !tmap_bf16_2d_sw128(&tdv, p.dv, Dio, krows, 128))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(dkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(dkv_kernel<D, DM>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.T * p.Hkv * p.B);
-  dkv_kernel<D><<<grid, kDkvThreads, L::SMEM, st>>>(tq, tdo, tk, tv, tdk, tdv, p);
+  dkv_kernel<D, DM><<<grid, kDkvThreads, L::SMEM, st>>>(tq, tdo, tk, tv, tdk, tdv, p);
   return cudaGetLastError();
 }
 
@@ -464,10 +464,13 @@ cudaError_t launch_dkv_d(const AttnParams& p, int Dio, const void* q, const void
 
 cudaError_t launch_bwd_dkv(const AttnParams& p, int D, const void* q, const void* k, const void* v,
                            const void* dout, cudaStream_t st) {
-  // head dim 96 runs the 128-wide kernel: its tensor maps are 96 elements
-  // wide, so TMA fills columns 96..127 of every loaded tile with zeros
-  // (which add nothing to any product) and drops them from every store.
-  return D == 64 ? launch_dkv_d<64>(p, 64, q, k, v, dout, st) : launch_dkv_d<128>(p, D, q, k, v, dout, st);
+  // head dim 96 runs the 128-wide tile layout: its tensor maps are 96
+  // elements wide, so TMA fills columns 96..127 of every loaded tile with
+  // zeros and drops them from every store; the MMAs contract over 96 (six
+  // K-steps) and produce 96 columns (N = 96), so no work is spent on them.
+  if (D == 64) return launch_dkv_d<64>(p, 64, q, k, v, dout, st);
+  if (D == 96) return launch_dkv_d<128, 96>(p, 96, q, k, v, dout, st);
+  return launch_dkv_d<128>(p, 128, q, k, v, dout, st);
 }
 
 }  // namespace pa

@@ -63,7 +63,7 @@ struct DqMisc {
   alignas(16) int32_t segkv[3][128];
 };
 
-template <int D>
+template <int D, int DM>
 __global__ void __launch_bounds__(352, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(352, 1)
       tc_fence_after();
       const uint64_t vd = sdesc_sw128(sV + sv * L::TB, 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
+      for (int kk = 0; kk < DM / 16; ++kk) {
         const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
         if (leader) umma_bf16(tmem + L::reg_p(j), sdesc_add(dod, ko), sdesc_add(vd, ko), idS, kk > 0 ? 1u : 0u);
       }
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(352, 1)
       tc_fence_after();
       const uint64_t kd = sdesc_sw128(sK + sk * L::TB, 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
+      for (int kk = 0; kk < DM / 16; ++kk) {
         const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
         if (leader) umma_bf16(tmem + L::TM_S, sdesc_add(qd, ko), sdesc_add(kd, ko), idS, kk > 0 ? 1u : 0u);
       }
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(352, 1)
     // its 64 key columns in columns 64h..64h+31 of the tile's dP region; K is
     // the MN-major B operand.
     const bool leader = lane == 0;
-    constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, true);
+    constexpr uint32_t idQ = idesc_bf16_f32(128, DM, false, true);
     bool ok = true;
     int j = 0;
     int4 te, te_next;  // table entries of this and the next visited key tile
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(352, 1)
   }
 }
 
-template <int D>
+template <int D, int DM = D>
 cudaError_t launch_dq_d(const AttnParams& p, int Dio, const void* q, const void* k, const void* v, const void* dout,
                         cudaStream_t st) {
   using L = DqLayout<D>;
@@ -366,10 +366,10 @@ cudaError_t launch_dq_d(const AttnParams& p, int Dio, const void* q, const void*
       !tmap_bf16_2d_sw128(&tk, k, Dio, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, Dio, krows, 128) ||
       !tmap_bf16_2d_sw128(&tdq, p.dq, Dio, qrows, 128))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(dq_kernel<D, DM>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.T * p.Hq * p.B);
-  dq_kernel<D><<<grid, 352, L::SMEM, st>>>(tq, tdo, tk, tv, tdq, p);
+  dq_kernel<D, DM><<<grid, 352, L::SMEM, st>>>(tq, tdo, tk, tv, tdq, p);
   return cudaGetLastError();
 }
 
@@ -377,10 +377,13 @@ cudaError_t launch_dq_d(const AttnParams& p, int Dio, const void* q, const void*
 
 cudaError_t launch_bwd_dq(const AttnParams& p, int D, const void* q, const void* k, const void* v,
                           const void* dout, cudaStream_t st) {
-  // head dim 96 runs the 128-wide kernel: its tensor maps are 96 elements
-  // wide, so TMA fills columns 96..127 of every loaded tile with zeros
-  // (which add nothing to any product) and drops them from every store.
-  return D == 64 ? launch_dq_d<64>(p, 64, q, k, v, dout, st) : launch_dq_d<128>(p, D, q, k, v, dout, st);
+  // head dim 96 runs the 128-wide tile layout: its tensor maps are 96
+  // elements wide, so TMA fills columns 96..127 of every loaded tile with
+  // zeros and drops them from every store; the MMAs contract over 96 (six
+  // K-steps) and produce 96 columns (N = 96), so no work is spent on them.
+  if (D == 64) return launch_dq_d<64>(p, 64, q, k, v, dout, st);
+  if (D == 96) return launch_dq_d<128, 96>(p, 96, q, k, v, dout, st);
+  return launch_dq_d<128>(p, 128, q, k, v, dout, st);
 }
 
 }  // namespace pa

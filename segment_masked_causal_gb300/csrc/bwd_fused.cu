@@ -71,7 +71,7 @@ struct FusedLayout {
   static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_A = 256, TM_B = 384, TMEM_COLS = 512;
 };
 
-template <int D>
+template <int D, int DM>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     fused_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         tc_fence_after();
         const uint64_t qd = sdesc_sw128(sQ + qs * L::TB, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < DM / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
           if (leader) umma_bf16(tmem + L::TM_A, sdesc_add(kd, ko), sdesc_add(qd, ko), idS, kk > 0 ? 1u : 0u);
         }
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         tc_fence_after();
         const uint64_t dod = sdesc_sw128(sDO + ds * L::TB, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < DM / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
           if (leader) umma_bf16(tmem + L::TM_B, sdesc_add(vd, ko), sdesc_add(dod, ko), idS, kk > 0 ? 1u : 0u);
         }
@@ -236,8 +236,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   } else if (warp == 2) {
     // ------------------------------------------------------------ dV / dQ / dK issuer
     const bool leader = lane == 0;
-    constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);  // A K-major (TMEM or smem), B MN-major
-    constexpr uint32_t idQ = idesc_bf16_f32(128, D, true, true);   // dS MN-major from the dS^T tile
+    constexpr uint32_t idG = idesc_bf16_f32(128, DM, false, true);  // A K-major (TMEM or smem), B MN-major
+    constexpr uint32_t idQ = idesc_bf16_f32(128, DM, true, true);   // dS MN-major from the dS^T tile
     const uint64_t dsk = sdesc_sw128(sDS, 16, 1024);               // dS^T, keys x queries, K-major
     const uint64_t dsm = sdesc_sw128(sDS, L::CHUNK, 1024);         // the same bytes as dS, queries x keys
     const uint64_t kdm = sdesc_sw128(sK, L::CHUNK, 1024);          // K as keys x D, MN-major
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   }
 }
 
-template <int D>
+template <int D, int DM = D>
 cudaError_t launch_fused_d(const AttnParams& p, int Dio, const void* q, const void* k, const void* v,
                            const void* dout, cudaStream_t st) {
   using L = FusedLayout<D>;
@@ -503,10 +503,10 @@ cudaError_t launch_fused_d(const AttnParams& p, int Dio, const void* q, const vo
       !tmap_bf16_2d_sw128(&tk, k, Dio, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, Dio, krows, 128) ||
       !tmap_bf16_2d_sw128(&tdk, p.dk, Dio, krows, 128) || !tmap_bf16_2d_sw128(&tdv, p.dv, Dio, krows, 128))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fused_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(fused_bwd_kernel<D, DM>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.T * p.Hkv * p.B);
-  fused_bwd_kernel<D><<<grid, kFusedThreads, L::SMEM, st>>>(tq, tdo, tk, tv, tdk, tdv, p);
+  fused_bwd_kernel<D, DM><<<grid, kFusedThreads, L::SMEM, st>>>(tq, tdo, tk, tv, tdk, tdv, p);
   return cudaGetLastError();
 }
 
@@ -524,9 +524,11 @@ __global__ void __launch_bounds__(256) dq_round_kernel(const float4* __restrict_
 
 cudaError_t launch_bwd_fused(const AttnParams& p, int D, const void* q, const void* k, const void* v,
                              const void* dout, cudaStream_t st) {
-  // head dim 96 runs the 128-wide kernel, as the dK/dV kernel does; the dQ
-  // reductions skip the zero columns 96..127
-  return D == 64 ? launch_fused_d<64>(p, 64, q, k, v, dout, st) : launch_fused_d<128>(p, D, q, k, v, dout, st);
+  // head dim 96 runs the 128-wide tile layout with 96-wide MMAs, as the dK/dV
+  // kernel does; the dQ reductions skip columns 96..127
+  if (D == 64) return launch_fused_d<64>(p, 64, q, k, v, dout, st);
+  if (D == 96) return launch_fused_d<128, 96>(p, 96, q, k, v, dout, st);
+  return launch_fused_d<128>(p, 128, q, k, v, dout, st);
 }
 
 cudaError_t launch_dq_round(const AttnParams& p, int D, cudaStream_t st) {

@@ -137,7 +137,7 @@ __device__ __forceinline__ void exp_store32(const uint32_t (&x)[32], uint64_t sc
 __device__ __forceinline__ bool needs_ids(const AttnParams& p, int4 te) { return p.seg && te.x != te.y; }
 __device__ __forceinline__ int seg_stage(int g, int n) { return g + 2 * (n & 1); }
 
-template <int D>
+template <int D, int DM>
 __global__ void __launch_bounds__(352, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(352, 1)
       tc_fence_after();
       const uint64_t kd = sdesc_sw128(sK + sk * L::TB, 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
+      for (int kk = 0; kk < DM / 16; ++kk) {
         const uint32_t ko = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
         if (leader) umma_bf16(tmem + L::TM_S + sb * 128, sdesc_add(qd, ko), sdesc_add(kd, ko), idS, kk > 0 ? 1u : 0u);
       }
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(352, 1)
     // O += P_j V_j with P_j (bf16, packed in the first 64 columns of its S
     // buffer) as the A operand straight from TMEM and V MN-major.
     const bool leader = lane == 0;
-    constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
+    constexpr uint32_t idO = idesc_bf16_f32(128, DM, false, true);
     bool ok = true;
     int j = 0;
     int4 te, te_next;  // table entries of this and the next visited key tile
@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(352, 1)
   }
 }
 
-template <int D>
+template <int D, int DM = D>
 cudaError_t launch_fwd_d(const AttnParams& p, int Dio, const void* q, const void* k, const void* v, cudaStream_t st) {
   using L = FwdLayout<D>;
   CUtensorMap tq, tk, tv, to;
@@ -509,10 +509,10 @@ cudaError_t launch_fwd_d(const AttnParams& p, int Dio, const void* q, const void
   if (!tmap_bf16_2d_sw128(&tq, q, Dio, qrows, 128) || !tmap_bf16_2d_sw128(&tk, k, Dio, krows, 128) ||
       !tmap_bf16_2d_sw128(&tv, v, Dio, krows, 128) || !tmap_bf16_2d_sw128(&to, p.out, Dio, qrows, 128))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, DM>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.T * p.Hq * p.B);
-  fwd_kernel<D><<<grid, 352, L::SMEM, st>>>(tq, tk, tv, to, p);
+  fwd_kernel<D, DM><<<grid, 352, L::SMEM, st>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
@@ -520,10 +520,13 @@ cudaError_t launch_fwd_d(const AttnParams& p, int Dio, const void* q, const void
 
 cudaError_t launch_fwd(const AttnParams& p, int D, const void* q, const void* k, const void* v,
                        cudaStream_t st) {
-  // head dim 96 runs the 128-wide kernel: its tensor maps are 96 elements
-  // wide, so TMA fills columns 96..127 of every loaded tile with zeros
-  // (which add nothing to any product) and drops them from every store.
-  return D == 64 ? launch_fwd_d<64>(p, 64, q, k, v, st) : launch_fwd_d<128>(p, D, q, k, v, st);
+  // head dim 96 runs the 128-wide tile layout: its tensor maps are 96
+  // elements wide, so TMA fills columns 96..127 of every loaded tile with
+  // zeros and drops them from every store; the MMAs contract over 96 (six
+  // K-steps) and produce 96 columns (N = 96), so no work is spent on them.
+  if (D == 64) return launch_fwd_d<64>(p, 64, q, k, v, st);
+  if (D == 96) return launch_fwd_d<128, 96>(p, 96, q, k, v, st);
+  return launch_fwd_d<128>(p, 128, q, k, v, st);
 }
 
 }  // namespace pa
