@@ -148,8 +148,10 @@ pa_status pa_bwd_causal(const pa_dims* dims, const void* q, const void* k, const
  * the bf16 call returns on the rounded inputs: fp32 is an I/O format here,
  * not a compute precision.
  *
- * How: when the strides are the contiguous ones and N % 128 == 0 the kernels
- * run on bf16 tensors directly (workspace: pa_workspace_bytes). Otherwise the
+ * How: with bf16 tensors and N % 128 == 0 the kernels read and write the
+ * caller's tensors in place, whatever their strides (their TMA tensor maps
+ * are 4-D, {D, N, H, B} with the given strides; workspace:
+ * pa_workspace_bytes). Otherwise (fp32, or N % 128 != 0) the
  * call copies its inputs into (B, H, Np, D) buffers inside the workspace,
  * with Np = N rounded up to 128 and zero rows after N, runs the kernels there
  * and copies the results out (workspace: pa_workspace_bytes_strided). The

@@ -144,6 +144,13 @@ pa_status check_call(const pa_dims* d, void* ws, size_t ws_bytes, std::initializ
 
 inline cudaStream_t cu(pa_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// The kernels' view of the caller's (B, H, N, D) tensors: the given strides,
+// or contiguous ones.
+pa::RowStrides rows_of(const pa_dims* d, const pa_strides* s) {
+  if (!s) return pa::contiguous_rows(d->Hq, d->Hkv, d->N, d->D);
+  return pa::RowStrides{s->q_n, s->q_h, s->q_b, s->k_n, s->k_h, s->k_b};
+}
+
 pa_status step_tile_table(const pa_dims* d, const int32_t* seg, void* ws, size_t ws_bytes, pa_stream_t stream) {
   pa_status s = check_call(d, ws, ws_bytes, {}, seg);
   if (s != PA_OK) return s;
@@ -152,65 +159,68 @@ pa_status step_tile_table(const pa_dims* d, const int32_t* seg, void* ws, size_t
 }
 
 pa_status step_fwd(const pa_dims* d, const void* q, const void* k, const void* v, const int32_t* seg, void* out,
-                   float* lse, void* ws, size_t ws_bytes, pa_stream_t stream) {
+                   float* lse, void* ws, size_t ws_bytes, pa_stream_t stream, const pa_strides* strides = nullptr) {
   pa_status s = check_call(d, ws, ws_bytes, {q, k, v, out, lse}, seg);
   if (s != PA_OK) return s;
   pa::AttnParams p = make_params(d, seg, ws);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
-  return pa::launch_fwd(p, d->D, q, k, v, cu(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return pa::launch_fwd(p, d->D, rows_of(d, strides), q, k, v, cu(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status step_delta(const pa_dims* d, const void* out, const void* dout, const float* lse, void* ws,
-                     size_t ws_bytes, pa_stream_t stream) {
+                     size_t ws_bytes, pa_stream_t stream, const pa_strides* strides = nullptr) {
   pa_status s = check_call(d, ws, ws_bytes, {out, dout, lse}, nullptr);
   if (s != PA_OK) return s;
   pa::AttnParams p = make_params(d, nullptr, ws);
   p.lse_in = lse;
   p.o = static_cast<const __nv_bfloat16*>(out);
   p.dout = static_cast<const __nv_bfloat16*>(dout);
-  return pa::launch_delta(p, d->D, cu(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return pa::launch_delta(p, d->D, rows_of(d, strides), cu(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status step_dq(const pa_dims* d, const void* q, const void* k, const void* v, const void* dout,
-                  const float* lse, const int32_t* seg, void* dq, void* ws, size_t ws_bytes, pa_stream_t stream) {
+                  const float* lse, const int32_t* seg, void* dq, void* ws, size_t ws_bytes, pa_stream_t stream,
+                  const pa_strides* strides = nullptr) {
   pa_status s = check_call(d, ws, ws_bytes, {q, k, v, dout, lse, dq}, seg);
   if (s != PA_OK) return s;
   pa::AttnParams p = make_params(d, seg, ws);
   p.lse_in = lse;
   p.dq = static_cast<__nv_bfloat16*>(dq);
-  return pa::launch_bwd_dq(p, d->D, q, k, v, dout, cu(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return pa::launch_bwd_dq(p, d->D, rows_of(d, strides), q, k, v, dout, cu(stream)) == cudaSuccess ? PA_OK
+                                                                                             : PA_ERR_CUDA;
 }
 
 pa_status step_dkv(const pa_dims* d, const void* q, const void* k, const void* v, const void* dout,
                    const float* lse, const int32_t* seg, void* dk, void* dv, void* ws, size_t ws_bytes,
-                   pa_stream_t stream) {
+                   pa_stream_t stream, const pa_strides* strides = nullptr) {
   pa_status s = check_call(d, ws, ws_bytes, {q, k, v, dout, lse, dk, dv}, seg);
   if (s != PA_OK) return s;
   pa::AttnParams p = make_params(d, seg, ws);
   p.lse_in = lse;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
-  return pa::launch_bwd_dkv(p, d->D, q, k, v, dout, cu(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return pa::launch_bwd_dkv(p, d->D, rows_of(d, strides), q, k, v, dout, cu(stream)) == cudaSuccess ? PA_OK
+                                                                                              : PA_ERR_CUDA;
 }
 
 pa_status fwd_impl(const pa_dims* d, const void* q, const void* k, const void* v, const int32_t* seg, void* out,
-                   float* lse, void* ws, size_t ws_bytes, pa_stream_t stream) {
+                   float* lse, void* ws, size_t ws_bytes, pa_stream_t stream, const pa_strides* strides = nullptr) {
   pa_status s = check_call(d, ws, ws_bytes, {q, k, v, out, lse}, seg);
   if (s != PA_OK) return s;
   if ((s = step_tile_table(d, seg, ws, ws_bytes, stream)) != PA_OK) return s;
-  return step_fwd(d, q, k, v, seg, out, lse, ws, ws_bytes, stream);
+  return step_fwd(d, q, k, v, seg, out, lse, ws, ws_bytes, stream, strides);
 }
 
 pa_status bwd_impl(const pa_dims* d, const void* q, const void* k, const void* v, const void* out,
                    const void* dout, const float* lse, const int32_t* seg, void* dq, void* dk, void* dv, void* ws,
-                   size_t ws_bytes, pa_stream_t stream) {
+                   size_t ws_bytes, pa_stream_t stream, const pa_strides* strides = nullptr) {
   pa_status s = check_call(d, ws, ws_bytes, {q, k, v, out, dout, lse, dq, dk, dv}, seg);
   if (s != PA_OK) return s;
   if ((s = step_tile_table(d, seg, ws, ws_bytes, stream)) != PA_OK) return s;
-  if ((s = step_delta(d, out, dout, lse, ws, ws_bytes, stream)) != PA_OK) return s;
-  if ((s = step_dq(d, q, k, v, dout, lse, seg, dq, ws, ws_bytes, stream)) != PA_OK) return s;
-  return step_dkv(d, q, k, v, dout, lse, seg, dk, dv, ws, ws_bytes, stream);
+  if ((s = step_delta(d, out, dout, lse, ws, ws_bytes, stream, strides)) != PA_OK) return s;
+  if ((s = step_dq(d, q, k, v, dout, lse, seg, dq, ws, ws_bytes, stream, strides)) != PA_OK) return s;
+  return step_dkv(d, q, k, v, dout, lse, seg, dk, dv, ws, ws_bytes, stream, strides);
 }
 
 // Single-pass backward: the fp32 dQ accumulator sits after the kernels'
@@ -237,7 +247,9 @@ pa_status bwd_fused_impl(const pa_dims* d, const void* q, const void* k, const v
   p.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + fused_acc_offset(d));
   p.dq_ld = d->D;
   const cudaStream_t st = cu(stream);
-  if (pa::launch_delta(p, d->D, st) != cudaSuccess || pa::launch_bwd_fused(p, d->D, q, k, v, dout, st) != cudaSuccess ||
+  const pa::RowStrides rs = rows_of(d, nullptr);
+  if (pa::launch_delta(p, d->D, rs, st) != cudaSuccess ||
+      pa::launch_bwd_fused(p, d->D, rs, q, k, v, dout, st) != cudaSuccess ||
       pa::launch_dq_round(p, d->D, st) != cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
@@ -253,10 +265,6 @@ pa_strides contiguous_strides(const pa_dims* d) {
   s.q_b = (int64_t)d->Hq * d->N * d->D;
   s.k_b = (int64_t)d->Hkv * d->N * d->D;
   return s;
-}
-
-bool same_strides(const pa_strides& a, const pa_strides& b) {
-  return a.q_b == b.q_b && a.q_h == b.q_h && a.q_n == b.q_n && a.k_b == b.k_b && a.k_h == b.k_h && a.k_n == b.k_n;
 }
 
 // Strides of at least D elements that keep every row 16-byte aligned.
@@ -364,8 +372,7 @@ pa_status fwd_any(const pa_dims* d, const pa_strides* s, int32_t io, const void*
   if ((why = io_ok(io)) != PA_OK) return why;
   const bool f32 = io == PA_IO_F32;
   if (s && (why = strides_ok(d, s, f32)) != PA_OK) return why;
-  if (!f32 && tiled(d) && (!s || same_strides(*s, contiguous_strides(d))))
-    return fwd_impl(d, q, k, v, seg, out, lse, ws, ws_bytes, stream);
+  if (!f32 && tiled(d)) return fwd_impl(d, q, k, v, seg, out, lse, ws, ws_bytes, stream, s);
   const pa_strides c = contiguous_strides(d);
   return fwd_staged(d, s ? s : &c, f32, q, k, v, seg, out, lse, ws, ws_bytes, stream);
 }
@@ -378,8 +385,7 @@ pa_status bwd_any(const pa_dims* d, const pa_strides* s, int32_t io, const void*
   if ((why = io_ok(io)) != PA_OK) return why;
   const bool f32 = io == PA_IO_F32;
   if (s && (why = strides_ok(d, s, f32)) != PA_OK) return why;
-  if (!f32 && tiled(d) && (!s || same_strides(*s, contiguous_strides(d))))
-    return bwd_impl(d, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream);
+  if (!f32 && tiled(d)) return bwd_impl(d, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream, s);
   const pa_strides c = contiguous_strides(d);
   return bwd_staged(d, s ? s : &c, f32, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream);
 }

@@ -63,7 +63,7 @@ struct DqMisc {
   alignas(16) int32_t segkv[3][128];
 };
 
-template <int D, int DM>
+template <int D, int DM, bool T4>
 __global__ void __launch_bounds__(352, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -123,16 +123,14 @@ __global__ void __launch_bounds__(352, 1)
     // ------------------------------------------------------------ producer
     // Lane 0 loads Q, dO and the K ring (with the key tiles' segment ids),
     // lane 1 the V ring: each ring refills as soon as its own stage is released.
-    const int krow0 = (b * p.Hkv + hk) * p.N;
     if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmDO);
       prefetch_tmap(&tmK);
-      const int qrow = (b * p.Hq + h) * p.N + tq * kTile;
       mbar_expect_tx(&m.q_full, 2 * L::TB);
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_2d(base + L::OFF_Q + c * L::CHUNK, &tmQ, &m.q_full, c * 64, qrow);
-        tma_load_2d(base + L::OFF_DO + c * L::CHUNK, &tmDO, &m.q_full, c * 64, qrow);
+        tma_load_rows(base + L::OFF_Q + c * L::CHUNK, &tmQ, &m.q_full, c * 64, tq * kTile, h, b, p.Hq, p.N, T4);
+        tma_load_rows(base + L::OFF_DO + c * L::CHUNK, &tmDO, &m.q_full, c * 64, tq * kTile, h, b, p.Hq, p.N, T4);
       }
       int jk = 0;
       int4 te, te_next;  // table entries of this and the next visited key tile
@@ -142,7 +140,8 @@ __global__ void __launch_bounds__(352, 1)
         if (!g.wait(&m.k_empty[sk], ((jk / NSK) & 1) ^ 1, 1)) break;
         mbar_expect_tx(&m.k_full[sk], L::TB + (p.seg ? 512 : 0));
         for (int c = 0; c < D / 64; ++c)
-          tma_load_2d(base + L::OFF_K + sk * L::TB + c * L::CHUNK, &tmK, &m.k_full[sk], c * 64, krow0 + tk * kTile);
+          tma_load_rows(base + L::OFF_K + sk * L::TB + c * L::CHUNK, &tmK, &m.k_full[sk], c * 64,
+                        tk * kTile, hk, b, p.Hkv, p.N, T4);
         if (p.seg) bulk_load(m.segkv[sk], p.seg + (size_t)b * p.N + tk * kTile, 512, &m.k_full[sk]);
       }
       // no copy may still be landing when the CTA exits
@@ -158,7 +157,8 @@ __global__ void __launch_bounds__(352, 1)
         if (!g.wait(&m.v_empty[sv], ((jv / NSV) & 1) ^ 1, 2)) break;
         mbar_expect_tx(&m.v_full[sv], L::TB);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_2d(base + L::OFF_V + sv * L::TB + c * L::CHUNK, &tmV, &m.v_full[sv], c * 64, krow0 + tk * kTile);
+          tma_load_rows(base + L::OFF_V + sv * L::TB + c * L::CHUNK, &tmV, &m.v_full[sv], c * 64,
+                        tk * kTile, hk, b, p.Hkv, p.N, T4);
       }
       for (int i = (jv > NSV ? jv - NSV : 0); i < jv; ++i) g.drain(&m.v_full[i % NSV], (i / NSV) & 1);
     }
@@ -341,8 +341,8 @@ __global__ void __launch_bounds__(352, 1)
       fence_async_smem();  // these writes are read by the TMA store
       mbar_arrive(&m.o_staged);
       if (warp == 3 && lane == 0 && g.wait(&m.o_staged, 0, 12)) {
-        const int qrow = (b * p.Hq + h) * p.N + tq * kTile;
-        for (int c = 0; c < D / 64; ++c) tma_store_2d(&tmDQ, so + c * L::CHUNK, c * 64, qrow);
+        for (int c = 0; c < D / 64; ++c) tma_store_rows(&tmDQ, so + c * L::CHUNK, c * 64, tq * kTile,
+                                                        h, b, p.Hq, p.N, T4);
         bulk_commit();
         bulk_wait_all();  // the store has read shared memory (and completed) before the CTA exits
       }
@@ -357,33 +357,45 @@ __global__ void __launch_bounds__(352, 1)
 }
 
 template <int D, int DM = D>
-cudaError_t launch_dq_d(const AttnParams& p, int Dio, const void* q, const void* k, const void* v, const void* dout,
-                        cudaStream_t st) {
+cudaError_t launch_dq_d(const AttnParams& p, int Dio, const RowStrides& rs, const void* q, const void* k, const void* v,
+                        const void* dout, cudaStream_t st) {
   using L = DqLayout<D>;
   CUtensorMap tq, tdo, tk, tv, tdq;
-  const uint64_t qrows = (uint64_t)p.B * p.Hq * p.N, krows = (uint64_t)p.B * p.Hkv * p.N;
-  if (!tmap_bf16_2d_sw128(&tq, q, Dio, qrows, 128) || !tmap_bf16_2d_sw128(&tdo, dout, Dio, qrows, 128) ||
-      !tmap_bf16_2d_sw128(&tk, k, Dio, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, Dio, krows, 128) ||
-      !tmap_bf16_2d_sw128(&tdq, p.dq, Dio, qrows, 128))
+  // contiguous tensors: 2-D maps over their rows (cheaper for TMA than the
+  // 4-D form, which strided tensors need)
+  AttnParams pp = p;
+  pp.tma4 = is_contiguous(rs, p.Hq, p.Hkv, p.N, Dio) ? 0 : 1;
+  const auto qmap = [&](CUtensorMap* m, const void* t) {
+    return pp.tma4 ? tmap_bf16_bhnd_sw128(m, t, Dio, p.N, p.Hq, p.B, rs.q_n, rs.q_h, rs.q_b)
+                   : tmap_bf16_2d_sw128(m, t, Dio, (uint64_t)p.B * p.Hq * p.N, 128);
+  };
+  const auto kmap = [&](CUtensorMap* m, const void* t) {
+    return pp.tma4 ? tmap_bf16_bhnd_sw128(m, t, Dio, p.N, p.Hkv, p.B, rs.k_n, rs.k_h, rs.k_b)
+                   : tmap_bf16_2d_sw128(m, t, Dio, (uint64_t)p.B * p.Hkv * p.N, 128);
+  };
+  if (!qmap(&tq, q) || !qmap(&tdo, dout) || !kmap(&tk, k) || !kmap(&tv, v) || !qmap(&tdq, p.dq))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(dq_kernel<D, DM>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+  // the tensor maps' form is fixed at compile time: the contiguous case runs
+  // exactly the 2-D code
+  const auto kfn = pp.tma4 ? dq_kernel<D, DM, true> : dq_kernel<D, DM, false>;
+  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.T * p.Hq * p.B);
-  dq_kernel<D, DM><<<grid, 352, L::SMEM, st>>>(tq, tdo, tk, tv, tdq, p);
+  kfn<<<grid, 352, L::SMEM, st>>>(tq, tdo, tk, tv, tdq, pp);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_dq(const AttnParams& p, int D, const void* q, const void* k, const void* v,
-                          const void* dout, cudaStream_t st) {
+cudaError_t launch_bwd_dq(const AttnParams& p, int D, const RowStrides& rs, const void* q, const void* k,
+                          const void* v, const void* dout, cudaStream_t st) {
   // head dim 96 runs the 128-wide tile layout: its tensor maps are 96
   // elements wide, so TMA fills columns 96..127 of every loaded tile with
   // zeros and drops them from every store; the MMAs contract over 96 (six
   // K-steps) and produce 96 columns (N = 96), so no work is spent on them.
-  if (D == 64) return launch_dq_d<64>(p, 64, q, k, v, dout, st);
-  if (D == 96) return launch_dq_d<128, 96>(p, 96, q, k, v, dout, st);
-  return launch_dq_d<128>(p, 128, q, k, v, dout, st);
+  if (D == 64) return launch_dq_d<64>(p, 64, rs, q, k, v, dout, st);
+  if (D == 96) return launch_dq_d<128, 96>(p, 96, rs, q, k, v, dout, st);
+  return launch_dq_d<128>(p, 128, rs, q, k, v, dout, st);
 }
 
 }  // namespace pa

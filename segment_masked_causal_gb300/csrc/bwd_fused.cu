@@ -71,7 +71,7 @@ struct FusedLayout {
   static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_A = 256, TM_B = 384, TMEM_COLS = 512;
 };
 
-template <int D, int DM>
+template <int D, int DM, bool T4>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     fused_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -139,11 +139,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      const int krow = (b * p.Hkv + hk) * p.N + tk * kTile;
       mbar_expect_tx(&m.kv_full, 2 * L::TB);
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_2d(base + L::OFF_K + c * L::CHUNK, &tmK, &m.kv_full, c * 64, krow);
-        tma_load_2d(base + L::OFF_V + c * L::CHUNK, &tmV, &m.kv_full, c * 64, krow);
+        tma_load_rows(base + L::OFF_K + c * L::CHUNK, &tmK, &m.kv_full, c * 64, tk * kTile, hk, b, p.Hkv, p.N, T4);
+        tma_load_rows(base + L::OFF_V + c * L::CHUNK, &tmV, &m.kv_full, c * 64, tk * kTile, hk, b, p.Hkv, p.N, T4);
       }
       int i = 0;
       bool ok = true;
@@ -156,7 +155,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           if (!g.wait(&m.q_empty[qs], ((i / kFQStages) & 1) ^ 1, 41)) { ok = false; break; }
           mbar_expect_tx(&m.q_full[qs], L::TB + 512);
           for (int c = 0; c < D / 64; ++c)
-            tma_load_2d(base + L::OFF_Q + qs * L::TB + c * L::CHUNK, &tmQ, &m.q_full[qs], c * 64, qrow);
+            tma_load_rows(base + L::OFF_Q + qs * L::TB + c * L::CHUNK, &tmQ, &m.q_full[qs], c * 64,
+                          tq * kTile, hq, b, p.Hq, p.N, T4);
           bulk_load(m.lse[qs], p.lse2 + qrow, 512, &m.q_full[qs]);
         }
       }
@@ -176,7 +176,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           if (!g.wait(&m.do_empty[ds], ((i / kFDoStages) & 1) ^ 1, 42)) { ok = false; break; }
           mbar_expect_tx(&m.do_full[ds], L::TB + 512);
           for (int c = 0; c < D / 64; ++c)
-            tma_load_2d(base + L::OFF_DO + ds * L::TB + c * L::CHUNK, &tmDO, &m.do_full[ds], c * 64, qrow);
+            tma_load_rows(base + L::OFF_DO + ds * L::TB + c * L::CHUNK, &tmDO, &m.do_full[ds], c * 64,
+                          tq * kTile, hq, b, p.Hq, p.N, T4);
           bulk_load(m.dl[ds], p.delta + qrow, 512, &m.do_full[ds]);
         }
       }
@@ -475,10 +476,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       fence_async_smem();
       mbar_arrive(&m.o_staged);
       if (warp == 3 && lane == 0 && g.wait(&m.o_staged, 0, 60)) {
-        const int krow = (b * p.Hkv + hk) * p.N + tk * kTile;
         for (int c = 0; c < D / 64; ++c) {
-          tma_store_2d(&tmDV, sv + c * L::CHUNK, c * 64, krow);
-          tma_store_2d(&tmDK, sk + c * L::CHUNK, c * 64, krow);
+          tma_store_rows(&tmDV, sv + c * L::CHUNK, c * 64, tk * kTile, hk, b, p.Hkv, p.N, T4);
+          tma_store_rows(&tmDK, sk + c * L::CHUNK, c * 64, tk * kTile, hk, b, p.Hkv, p.N, T4);
         }
         bulk_commit();
         bulk_wait_all();
@@ -494,19 +494,32 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 }
 
 template <int D, int DM = D>
-cudaError_t launch_fused_d(const AttnParams& p, int Dio, const void* q, const void* k, const void* v,
-                           const void* dout, cudaStream_t st) {
+cudaError_t launch_fused_d(const AttnParams& p, int Dio, const RowStrides& rs, const void* q, const void* k,
+                         const void* v, const void* dout, cudaStream_t st) {
   using L = FusedLayout<D>;
   CUtensorMap tq, tdo, tk, tv, tdk, tdv;
-  const uint64_t qrows = (uint64_t)p.B * p.Hq * p.N, krows = (uint64_t)p.B * p.Hkv * p.N;
-  if (!tmap_bf16_2d_sw128(&tq, q, Dio, qrows, 128) || !tmap_bf16_2d_sw128(&tdo, dout, Dio, qrows, 128) ||
-      !tmap_bf16_2d_sw128(&tk, k, Dio, krows, 128) || !tmap_bf16_2d_sw128(&tv, v, Dio, krows, 128) ||
-      !tmap_bf16_2d_sw128(&tdk, p.dk, Dio, krows, 128) || !tmap_bf16_2d_sw128(&tdv, p.dv, Dio, krows, 128))
+  // contiguous tensors: 2-D maps over their rows (cheaper for TMA than the
+  // 4-D form, which strided tensors need)
+  AttnParams pp = p;
+  pp.tma4 = is_contiguous(rs, p.Hq, p.Hkv, p.N, Dio) ? 0 : 1;
+  const auto qmap = [&](CUtensorMap* m, const void* t) {
+    return pp.tma4 ? tmap_bf16_bhnd_sw128(m, t, Dio, p.N, p.Hq, p.B, rs.q_n, rs.q_h, rs.q_b)
+                   : tmap_bf16_2d_sw128(m, t, Dio, (uint64_t)p.B * p.Hq * p.N, 128);
+  };
+  const auto kmap = [&](CUtensorMap* m, const void* t) {
+    return pp.tma4 ? tmap_bf16_bhnd_sw128(m, t, Dio, p.N, p.Hkv, p.B, rs.k_n, rs.k_h, rs.k_b)
+                   : tmap_bf16_2d_sw128(m, t, Dio, (uint64_t)p.B * p.Hkv * p.N, 128);
+  };
+  if (!qmap(&tq, q) || !qmap(&tdo, dout) || !kmap(&tk, k) || !kmap(&tv, v) || !kmap(&tdk, p.dk) ||
+      !kmap(&tdv, p.dv))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fused_bwd_kernel<D, DM>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+  // the tensor maps' form is fixed at compile time: the contiguous case runs
+  // exactly the 2-D code
+  const auto kfn = pp.tma4 ? fused_bwd_kernel<D, DM, true> : fused_bwd_kernel<D, DM, false>;
+  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.T * p.Hkv * p.B);
-  fused_bwd_kernel<D, DM><<<grid, kFusedThreads, L::SMEM, st>>>(tq, tdo, tk, tv, tdk, tdv, p);
+  kfn<<<grid, kFusedThreads, L::SMEM, st>>>(tq, tdo, tk, tv, tdk, tdv, pp);
   return cudaGetLastError();
 }
 
@@ -522,13 +535,13 @@ __global__ void __launch_bounds__(256) dq_round_kernel(const float4* __restrict_
 
 }  // namespace
 
-cudaError_t launch_bwd_fused(const AttnParams& p, int D, const void* q, const void* k, const void* v,
-                             const void* dout, cudaStream_t st) {
+cudaError_t launch_bwd_fused(const AttnParams& p, int D, const RowStrides& rs, const void* q, const void* k,
+                             const void* v, const void* dout, cudaStream_t st) {
   // head dim 96 runs the 128-wide tile layout with 96-wide MMAs, as the dK/dV
   // kernel does; the dQ reductions skip columns 96..127
-  if (D == 64) return launch_fused_d<64>(p, 64, q, k, v, dout, st);
-  if (D == 96) return launch_fused_d<128, 96>(p, 96, q, k, v, dout, st);
-  return launch_fused_d<128>(p, 128, q, k, v, dout, st);
+  if (D == 64) return launch_fused_d<64>(p, 64, rs, q, k, v, dout, st);
+  if (D == 96) return launch_fused_d<128, 96>(p, 96, rs, q, k, v, dout, st);
+  return launch_fused_d<128>(p, 128, rs, q, k, v, dout, st);
 }
 
 cudaError_t launch_dq_round(const AttnParams& p, int D, cudaStream_t st) {

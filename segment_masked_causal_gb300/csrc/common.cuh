@@ -51,6 +51,9 @@ struct AttnParams {
   // by the delta kernel when non-null
   float* dq_acc;
   int dq_ld;
+  // tensor maps of the (B, H, N, D) tensors: 2-D over B*H*N rows (contiguous
+  // tensors) or 4-D {D, N, H, B} with the caller's strides
+  int tma4;
 };
 
 __device__ __forceinline__ bool tiles_overlap(int4 a, int4 b) { return a.x <= b.y && b.x <= a.y; }

@@ -137,7 +137,7 @@ __device__ __forceinline__ void exp_store32(const uint32_t (&x)[32], uint64_t sc
 __device__ __forceinline__ bool needs_ids(const AttnParams& p, int4 te) { return p.seg && te.x != te.y; }
 __device__ __forceinline__ int seg_stage(int g, int n) { return g + 2 * (n & 1); }
 
-template <int D, int DM>
+template <int D, int DM, bool T4>
 __global__ void __launch_bounds__(352, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -204,13 +204,12 @@ __global__ void __launch_bounds__(352, 1)
     // Lane 0 loads Q, then per key tile its per-key segment ids where the
     // tile needs them (a ring of their own) and K (a 3-stage ring); lane 1
     // the V ring: each ring refills as soon as its own stage is released.
-    const int krow0 = (b * p.Hkv + hk) * p.N;
     if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
-      const int qrow = (b * p.Hq + h) * p.N + tq * kTile;
       mbar_expect_tx(&m.q_full, L::TB);
-      for (int c = 0; c < D / 64; ++c) tma_load_2d(base + L::OFF_Q + c * L::CHUNK, &tmQ, &m.q_full, c * 64, qrow);
+      for (int c = 0; c < D / 64; ++c) tma_load_rows(base + L::OFF_Q + c * L::CHUNK, &tmQ, &m.q_full, c * 64,
+                                                     tq * kTile, h, b, p.Hq, p.N, T4);
       int jk = 0;
       int ns[2] = {0, 0};  // segment-id copies issued for each softmax group's tiles
       int4 te, te_next;  // table entries of this and the next visited key tile
@@ -227,7 +226,8 @@ __global__ void __launch_bounds__(352, 1)
         if (!g.wait(&m.k_empty[sk], ((jk / NSK) & 1) ^ 1, 1)) break;
         mbar_expect_tx(&m.k_full[sk], L::TB);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_2d(base + L::OFF_K + sk * L::TB + c * L::CHUNK, &tmK, &m.k_full[sk], c * 64, krow0 + tk * kTile);
+          tma_load_rows(base + L::OFF_K + sk * L::TB + c * L::CHUNK, &tmK, &m.k_full[sk], c * 64,
+                        tk * kTile, hk, b, p.Hkv, p.N, T4);
       }
       // no copy may still be landing when the CTA exits
       g.drain(&m.q_full, 0);
@@ -244,7 +244,8 @@ __global__ void __launch_bounds__(352, 1)
         if (!g.wait(&m.v_empty[sv], ((jv / NSV) & 1) ^ 1, 2)) break;
         mbar_expect_tx(&m.v_full[sv], L::TB);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_2d(base + L::OFF_V + sv * L::TB + c * L::CHUNK, &tmV, &m.v_full[sv], c * 64, krow0 + tk * kTile);
+          tma_load_rows(base + L::OFF_V + sv * L::TB + c * L::CHUNK, &tmV, &m.v_full[sv], c * 64,
+                        tk * kTile, hk, b, p.Hkv, p.N, T4);
       }
       for (int i = (jv > NSV ? jv - NSV : 0); i < jv; ++i) g.drain(&m.v_full[i % NSV], (i / NSV) & 1);
     }
@@ -485,8 +486,8 @@ __global__ void __launch_bounds__(352, 1)
       fence_async_smem();  // these writes are read by the TMA store
       mbar_arrive(&m.o_staged);
       if (warp == 3 && lane == 0 && g.wait(&m.o_staged, 0, 15)) {
-        const int qrow = (b * p.Hq + h) * p.N + tq * kTile;
-        for (int c = 0; c < D / 64; ++c) tma_store_2d(&tmO, so + c * L::CHUNK, c * 64, qrow);
+        for (int c = 0; c < D / 64; ++c) tma_store_rows(&tmO, so + c * L::CHUNK, c * 64, tq * kTile,
+                                                        h, b, p.Hq, p.N, T4);
         bulk_commit();
         bulk_wait_all();  // the store has read shared memory (and completed) before the CTA exits
       }
@@ -502,31 +503,44 @@ __global__ void __launch_bounds__(352, 1)
 }
 
 template <int D, int DM = D>
-cudaError_t launch_fwd_d(const AttnParams& p, int Dio, const void* q, const void* k, const void* v, cudaStream_t st) {
+cudaError_t launch_fwd_d(const AttnParams& p, int Dio, const RowStrides& rs, const void* q, const void* k,
+                         const void* v, cudaStream_t st) {
   using L = FwdLayout<D>;
   CUtensorMap tq, tk, tv, to;
-  const uint64_t qrows = (uint64_t)p.B * p.Hq * p.N, krows = (uint64_t)p.B * p.Hkv * p.N;
-  if (!tmap_bf16_2d_sw128(&tq, q, Dio, qrows, 128) || !tmap_bf16_2d_sw128(&tk, k, Dio, krows, 128) ||
-      !tmap_bf16_2d_sw128(&tv, v, Dio, krows, 128) || !tmap_bf16_2d_sw128(&to, p.out, Dio, qrows, 128))
-    return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, DM>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+  // contiguous tensors: 2-D maps over their rows (cheaper for TMA than the
+  // 4-D form, which strided tensors need)
+  AttnParams pp = p;
+  pp.tma4 = is_contiguous(rs, p.Hq, p.Hkv, p.N, Dio) ? 0 : 1;
+  const auto qmap = [&](CUtensorMap* m, const void* t) {
+    return pp.tma4 ? tmap_bf16_bhnd_sw128(m, t, Dio, p.N, p.Hq, p.B, rs.q_n, rs.q_h, rs.q_b)
+                   : tmap_bf16_2d_sw128(m, t, Dio, (uint64_t)p.B * p.Hq * p.N, 128);
+  };
+  const auto kmap = [&](CUtensorMap* m, const void* t) {
+    return pp.tma4 ? tmap_bf16_bhnd_sw128(m, t, Dio, p.N, p.Hkv, p.B, rs.k_n, rs.k_h, rs.k_b)
+                   : tmap_bf16_2d_sw128(m, t, Dio, (uint64_t)p.B * p.Hkv * p.N, 128);
+  };
+  if (!qmap(&tq, q) || !kmap(&tk, k) || !kmap(&tv, v) || !qmap(&to, p.out)) return cudaErrorInvalidValue;
+  // the tensor maps' form is fixed at compile time: the contiguous case runs
+  // exactly the 2-D code
+  const auto kfn = pp.tma4 ? fwd_kernel<D, DM, true> : fwd_kernel<D, DM, false>;
+  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.T * p.Hq * p.B);
-  fwd_kernel<D, DM><<<grid, 352, L::SMEM, st>>>(tq, tk, tv, to, p);
+  kfn<<<grid, 352, L::SMEM, st>>>(tq, tk, tv, to, pp);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_fwd(const AttnParams& p, int D, const void* q, const void* k, const void* v,
+cudaError_t launch_fwd(const AttnParams& p, int D, const RowStrides& rs, const void* q, const void* k, const void* v,
                        cudaStream_t st) {
   // head dim 96 runs the 128-wide tile layout: its tensor maps are 96
   // elements wide, so TMA fills columns 96..127 of every loaded tile with
   // zeros and drops them from every store; the MMAs contract over 96 (six
   // K-steps) and produce 96 columns (N = 96), so no work is spent on them.
-  if (D == 64) return launch_fwd_d<64>(p, 64, q, k, v, st);
-  if (D == 96) return launch_fwd_d<128, 96>(p, 96, q, k, v, st);
-  return launch_fwd_d<128>(p, 128, q, k, v, st);
+  if (D == 64) return launch_fwd_d<64>(p, 64, rs, q, k, v, st);
+  if (D == 96) return launch_fwd_d<128, 96>(p, 96, rs, q, k, v, st);
+  return launch_fwd_d<128>(p, 128, rs, q, k, v, st);
 }
 
 }  // namespace pa

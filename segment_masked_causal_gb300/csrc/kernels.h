@@ -12,23 +12,38 @@ namespace pa {
 // the query itself fails). Cached per device.
 pa_status device_check();
 
+// Element strides of the (B, H, N, D) tensors the kernels read and write in
+// place (D contiguous): q, out, dout and dq use the q_* strides, k, v, dk and
+// dv the k_* strides.
+struct RowStrides {
+  int64_t q_n, q_h, q_b, k_n, k_h, k_b;
+};
+inline RowStrides contiguous_rows(int Hq, int Hkv, int N, int D) {
+  return RowStrides{D, (int64_t)N * D, (int64_t)Hq * N * D, D, (int64_t)N * D, (int64_t)Hkv * N * D};
+}
+inline bool is_contiguous(const RowStrides& s, int Hq, int Hkv, int N, int D) {
+  const RowStrides c = contiguous_rows(Hq, Hkv, N, D);
+  return s.q_n == c.q_n && s.q_h == c.q_h && s.q_b == c.q_b && s.k_n == c.k_n && s.k_h == c.k_h && s.k_b == c.k_b;
+}
+
 // Tile table (B, T) x {smin, smax, kv_lo, q_hi} and the two work lists; also
 // clears the status word.
 cudaError_t launch_tile_table(const AttnParams& p, int4* tiles, cudaStream_t st);
 // delta[b, h, i] = sum_c dO[b, h, i, c] * O[b, h, i, c] (fp32), and lse2 = lse * log2(e);
 // also zeroes the rows of p.dq_acc when it is non-null.
-cudaError_t launch_delta(const AttnParams& p, int D, cudaStream_t st);
+cudaError_t launch_delta(const AttnParams& p, int D, const RowStrides& rs, cudaStream_t st);
 // Self-test of the bounded waits: one warp waits on an mbarrier nothing arrives on.
 cudaError_t launch_wait_timeout_selftest(uint32_t* status, cudaStream_t st);
-cudaError_t launch_fwd(const AttnParams& p, int D, const void* q, const void* k, const void* v, cudaStream_t st);
-cudaError_t launch_bwd_dq(const AttnParams& p, int D, const void* q, const void* k, const void* v,
-                          const void* dout, cudaStream_t st);
-cudaError_t launch_bwd_dkv(const AttnParams& p, int D, const void* q, const void* k, const void* v,
-                           const void* dout, cudaStream_t st);
+cudaError_t launch_fwd(const AttnParams& p, int D, const RowStrides& rs, const void* q, const void* k, const void* v,
+                       cudaStream_t st);
+cudaError_t launch_bwd_dq(const AttnParams& p, int D, const RowStrides& rs, const void* q, const void* k,
+                          const void* v, const void* dout, cudaStream_t st);
+cudaError_t launch_bwd_dkv(const AttnParams& p, int D, const RowStrides& rs, const void* q, const void* k,
+                           const void* v, const void* dout, cudaStream_t st);
 // Single-pass backward: dK, dV and the fp32 dQ accumulator p.dq_acc (zeroed
 // beforehand), then p.dq = the accumulator rounded to bf16.
-cudaError_t launch_bwd_fused(const AttnParams& p, int D, const void* q, const void* k, const void* v,
-                             const void* dout, cudaStream_t st);
+cudaError_t launch_bwd_fused(const AttnParams& p, int D, const RowStrides& rs, const void* q, const void* k,
+                             const void* v, const void* dout, cudaStream_t st);
 cudaError_t launch_dq_round(const AttnParams& p, int D, cudaStream_t st);
 
 // A (B, H, N, D) bf16 or fp32 tensor with element strides sb, sh, sn (16-byte

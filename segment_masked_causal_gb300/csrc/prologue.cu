@@ -221,7 +221,8 @@ __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restr
                                                     const __nv_bfloat16* __restrict__ dout,
                                                     const float* __restrict__ lse, float* __restrict__ delta,
                                                     float* __restrict__ lse2, float* __restrict__ zero_acc,
-                                                    size_t rows) {
+                                                    size_t rows, bool contiguous, int N, int H, int64_t s_n,
+                                                    int64_t s_h, int64_t s_b) {
   // each of the row's LPR lanes takes every LPR-th 16-byte vector
   constexpr int VEC = D / 8;
   constexpr int LPR = delta_lanes(D);
@@ -231,11 +232,18 @@ __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restr
   const int sub = threadIdx.x % LPR;
   for (size_t t = gtid; t < rows * LPR; t += stride) {
     const size_t row = t / LPR;
+    // element offset of query row (b, h, n) of O and dO, row = (b * H + h) * N + n
+    // (rows < 2^31); contiguous tensors skip the divisions
+    size_t off = row * D;
+    if (!contiguous) {
+      const uint32_t r32 = (uint32_t)row, bh = r32 / (uint32_t)N, b = bh / (uint32_t)H;
+      off = (size_t)b * s_b + (size_t)(bh - b * (uint32_t)H) * s_h + (size_t)(r32 - bh * (uint32_t)N) * s_n;
+    }
     float acc = 0.f;
 #pragma unroll
     for (int v = sub; v < VEC; v += LPR) {
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + row * D) + v);
-      const uint4 c = __ldg(reinterpret_cast<const uint4*>(dout + row * D) + v);
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + off) + v);
+      const uint4 c = __ldg(reinterpret_cast<const uint4*>(dout + off) + v);
       acc = fmaf(bf16lo(a.x), bf16lo(c.x), acc);
       acc = fmaf(bf16hi(a.x), bf16hi(c.x), acc);
       acc = fmaf(bf16lo(a.y), bf16lo(c.y), acc);
@@ -309,7 +317,8 @@ cudaError_t launch_wait_timeout_selftest(uint32_t* status, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_delta(const AttnParams& p, int D, cudaStream_t st) {
+cudaError_t launch_delta(const AttnParams& p, int D, const RowStrides& rs, cudaStream_t st) {
+  const bool contig = rs.q_n == D && rs.q_h == (int64_t)p.N * D && rs.q_b == (int64_t)p.Hq * p.N * D;
   const size_t rows = (size_t)p.B * p.Hq * p.N;
   const size_t threads = rows * (size_t)delta_lanes(D);
   int dev = 0, sms = 148;
@@ -319,11 +328,14 @@ cudaError_t launch_delta(const AttnParams& p, int D, cudaStream_t st) {
   const size_t cap = (size_t)sms * 8;
   if (blocks > cap) blocks = cap;
   if (D == 128)
-    delta_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, p.dq_acc, rows);
+    delta_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, p.dq_acc, rows, contig,
+                                                     p.N, p.Hq, rs.q_n, rs.q_h, rs.q_b);
   else if (D == 96)
-    delta_kernel<96><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, p.dq_acc, rows);
+    delta_kernel<96><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, p.dq_acc, rows, contig,
+                                                     p.N, p.Hq, rs.q_n, rs.q_h, rs.q_b);
   else
-    delta_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, p.dq_acc, rows);
+    delta_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, p.dq_acc, rows, contig,
+                                                     p.N, p.Hq, rs.q_n, rs.q_h, rs.q_b);
   return cudaGetLastError();
 }
 

@@ -152,6 +152,39 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* s
                "r"(smem_u32(src)), "r"(c0), "r"(c1)
                : "memory");
 }
+// The same for a (B, H, N, D) tensor map (tmap_bf16_bhnd_sw128): the box of
+// 128 tokens from token n of head h of batch row b, columns c..c+63.
+__device__ __forceinline__ void tma_load_bhnd(void* dst, const CUtensorMap* m, uint64_t* bar, int32_t c, int32_t n,
+                                              int32_t h, int32_t b) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+      "[%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c), "r"(n), "r"(h), "r"(b)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_bhnd(const CUtensorMap* m, const void* src, int32_t c, int32_t n, int32_t h,
+                                               int32_t b) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(smem_u32(src)), "r"(c), "r"(n), "r"(h), "r"(b)
+               : "memory");
+}
+// Box of 128 tokens from token n of head h of batch row b (H heads of N
+// tokens), columns c..c+63, through either kind of map (AttnParams::tma4).
+__device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* m, uint64_t* bar, int32_t c, int32_t n,
+                                              int32_t h, int32_t b, int32_t H, int32_t N, int four) {
+  if (four)
+    tma_load_bhnd(dst, m, bar, c, n, h, b);
+  else
+    tma_load_2d(dst, m, bar, c, (b * H + h) * N + n);
+}
+__device__ __forceinline__ void tma_store_rows(const CUtensorMap* m, const void* src, int32_t c, int32_t n, int32_t h,
+                                               int32_t b, int32_t H, int32_t N, int four) {
+  if (four)
+    tma_store_bhnd(m, src, c, n, h, b);
+  else
+    tma_store_2d(m, src, c, (b * H + h) * N + n);
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk-async group of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }

@@ -58,4 +58,23 @@ inline bool tmap_bf16_2d_sw128(CUtensorMap* m, const void* base, uint64_t inner,
   return r == CUDA_SUCCESS;
 }
 
+// A (B, H, N, D) bf16 tensor whose element (b, h, n, c) sits at element
+// offset b*s_b + h*s_h + n*s_n + c (D contiguous; every stride * 2 a multiple
+// of 16), as a 4-D map {D, N, H, B}, read in boxes of 128 tokens x 64
+// elements (128 bytes) of one (b, h) with the 128-byte swizzle. Elements past
+// D read as zero and are dropped from stores.
+inline bool tmap_bf16_bhnd_sw128(CUtensorMap* m, const void* base, uint64_t D, uint64_t N, uint64_t H, uint64_t B,
+                                 int64_t s_n, int64_t s_h, int64_t s_b) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {D, N, H, B};
+  cuuint64_t strides[3] = {(cuuint64_t)s_n * 2, (cuuint64_t)s_h * 2, (cuuint64_t)s_b * 2};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace pa
