@@ -95,8 +95,9 @@ typedef enum {
 
 /*
  * Workspace size in bytes for `dims` (0 if dims are invalid), for the calls
- * on contiguous tensors. When N is not a multiple of 128 it includes room for
- * the staging copies described at pa_fwd_strided.
+ * on contiguous tensors. When N is not a multiple of 128 it also includes
+ * room for the staging copies described at pa_fwd_strided; the bf16 calls
+ * need only the size for N rounded up to 128, which this never undercuts.
  */
 size_t pa_workspace_bytes(const pa_dims* dims);
 
@@ -148,17 +149,19 @@ pa_status pa_bwd_causal(const pa_dims* dims, const void* q, const void* k, const
  * the bf16 call returns on the rounded inputs: fp32 is an I/O format here,
  * not a compute precision.
  *
- * How: with bf16 tensors and N % 128 == 0 the kernels read and write the
- * caller's tensors in place, whatever their strides (their TMA tensor maps
- * are 4-D, {D, N, H, B} with the given strides; workspace:
- * pa_workspace_bytes). Otherwise (fp32, or N % 128 != 0) the
- * call copies its inputs into (B, H, Np, D) buffers inside the workspace,
- * with Np = N rounded up to 128 and zero rows after N, runs the kernels there
- * and copies the results out (workspace: pa_workspace_bytes_strided). The
- * extra tokens lie after every real query, so causality hides them; their
- * zero dO keeps them out of dK and dV, and their outputs are dropped. The
- * copies are memory-bound kernels on the same stream; pa_fwd / pa_bwd and
- * the causal variants take the same path when N % 128 != 0.
+ * How: with bf16 tensors the kernels read and write the caller's tensors in
+ * place, whatever their strides and N: they work on Np = N rounded up to
+ * 128 tokens through 4-D TMA tensor maps {D, N, H, B} with the given strides,
+ * which read the tokens past N as zeros and never store them, and the
+ * segment ids are copied into the workspace with the row's last id repeated
+ * up to Np (workspace: pa_workspace_bytes for dims with N rounded up to
+ * 128). With fp32 tensors the call copies its inputs into bf16 (B, H, Np, D)
+ * buffers inside the workspace, runs the kernels there and copies the
+ * results out (workspace: pa_workspace_bytes_strided). Either way the extra
+ * tokens lie after every real query, so causality hides them; they get zero
+ * dO and delta and an infinite lse, so they add nothing to dK and dV, and
+ * their outputs are dropped. pa_fwd / pa_bwd and the causal variants take
+ * the same in-place path when N % 128 != 0.
  * Errors: as pa_fwd / pa_bwd, plus PA_ERR_NULL (strides), PA_ERR_SHAPE (a
  * stride < D), PA_ERR_ALIGN (a stride not a 16-byte multiple), PA_ERR_DTYPE.
  */

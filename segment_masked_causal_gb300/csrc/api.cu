@@ -27,7 +27,7 @@ inline bool tiled(const pa_dims* d) { return d->N % pa::kTile == 0; }
 // padded_n, then the staging copies used when the caller's tensors are not in
 // the kernels' layout (N not a multiple of 128, or strided tensors).
 struct WsLayout {
-  size_t status, tiles, work_q, work_k, delta, lse2, base;
+  size_t status, tiles, work_q, work_k, delta, lse2, pseg, base;
   size_t sq, sk, sv, so, sdo, sdq, sdk, sdv, slse, sseg, staged;
 };
 
@@ -57,7 +57,8 @@ WsLayout ws_layout(const pa_dims* d) {
   w.work_k = w.work_q + round_up((size_t)d->B * T * sizeof(int32_t));
   w.delta = w.work_k + round_up((size_t)d->B * T * sizeof(int32_t));
   w.lse2 = w.delta + round_up(qrows * sizeof(float));
-  w.base = w.lse2 + round_up(qrows * sizeof(float));
+  w.pseg = w.lse2 + round_up(qrows * sizeof(float));  // segment ids padded to whole tiles (ragged N)
+  w.base = w.pseg + round_up((size_t)d->B * Np * sizeof(int32_t));
   w.sq = w.base;
   w.so = w.sq + qb;
   w.sdo = w.so + qb;
@@ -99,9 +100,12 @@ pa_status pa::device_check() {
 
 namespace {
 
-pa::AttnParams make_params(const pa_dims* d, const int32_t* seg, void* ws) {
+// d holds the kernels' N (whole tiles); Nr > 0 is the caller's N when it is
+// not a whole number of tiles.
+pa::AttnParams make_params(const pa_dims* d, const int32_t* seg, void* ws, int Nr = 0) {
   pa::AttnParams p{};
   p.B = d->B; p.Hq = d->Hq; p.Hkv = d->Hkv; p.N = d->N; p.T = d->N / pa::kTile; p.G = d->Hq / d->Hkv;
+  p.Nr = Nr > 0 ? Nr : d->N;
   p.scale = d->scale > 0.f ? d->scale : 1.f / std::sqrt((float)d->D);
   p.scale_log2 = p.scale * 1.4426950408889634f;
   p.seg = seg;
@@ -150,6 +154,9 @@ pa::RowStrides rows_of(const pa_dims* d, const pa_strides* s) {
   if (!s) return pa::contiguous_rows(d->Hq, d->Hkv, d->N, d->D);
   return pa::RowStrides{s->q_n, s->q_h, s->q_b, s->k_n, s->k_h, s->k_b};
 }
+inline pa::RowStrides rows_or(const pa_dims* d, const pa::RowStrides* rs) {
+  return rs ? *rs : pa::contiguous_rows(d->Hq, d->Hkv, d->N, d->D);
+}
 
 pa_status step_tile_table(const pa_dims* d, const int32_t* seg, void* ws, size_t ws_bytes, pa_stream_t stream) {
   pa_status s = check_call(d, ws, ws_bytes, {}, seg);
@@ -159,68 +166,97 @@ pa_status step_tile_table(const pa_dims* d, const int32_t* seg, void* ws, size_t
 }
 
 pa_status step_fwd(const pa_dims* d, const void* q, const void* k, const void* v, const int32_t* seg, void* out,
-                   float* lse, void* ws, size_t ws_bytes, pa_stream_t stream, const pa_strides* strides = nullptr) {
+                   float* lse, void* ws, size_t ws_bytes, pa_stream_t stream, const pa::RowStrides* rs = nullptr,
+                   int Nr = 0) {
   pa_status s = check_call(d, ws, ws_bytes, {q, k, v, out, lse}, seg);
   if (s != PA_OK) return s;
-  pa::AttnParams p = make_params(d, seg, ws);
+  pa::AttnParams p = make_params(d, seg, ws, Nr);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
-  return pa::launch_fwd(p, d->D, rows_of(d, strides), q, k, v, cu(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return pa::launch_fwd(p, d->D, rows_or(d, rs), q, k, v, cu(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status step_delta(const pa_dims* d, const void* out, const void* dout, const float* lse, void* ws,
-                     size_t ws_bytes, pa_stream_t stream, const pa_strides* strides = nullptr) {
+                     size_t ws_bytes, pa_stream_t stream, const pa::RowStrides* rs = nullptr, int Nr = 0) {
   pa_status s = check_call(d, ws, ws_bytes, {out, dout, lse}, nullptr);
   if (s != PA_OK) return s;
-  pa::AttnParams p = make_params(d, nullptr, ws);
+  pa::AttnParams p = make_params(d, nullptr, ws, Nr);
   p.lse_in = lse;
   p.o = static_cast<const __nv_bfloat16*>(out);
   p.dout = static_cast<const __nv_bfloat16*>(dout);
-  return pa::launch_delta(p, d->D, rows_of(d, strides), cu(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return pa::launch_delta(p, d->D, rows_or(d, rs), cu(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status step_dq(const pa_dims* d, const void* q, const void* k, const void* v, const void* dout,
                   const float* lse, const int32_t* seg, void* dq, void* ws, size_t ws_bytes, pa_stream_t stream,
-                  const pa_strides* strides = nullptr) {
+                  const pa::RowStrides* rs = nullptr, int Nr = 0) {
   pa_status s = check_call(d, ws, ws_bytes, {q, k, v, dout, lse, dq}, seg);
   if (s != PA_OK) return s;
-  pa::AttnParams p = make_params(d, seg, ws);
+  pa::AttnParams p = make_params(d, seg, ws, Nr);
   p.lse_in = lse;
   p.dq = static_cast<__nv_bfloat16*>(dq);
-  return pa::launch_bwd_dq(p, d->D, rows_of(d, strides), q, k, v, dout, cu(stream)) == cudaSuccess ? PA_OK
+  return pa::launch_bwd_dq(p, d->D, rows_or(d, rs), q, k, v, dout, cu(stream)) == cudaSuccess ? PA_OK
                                                                                              : PA_ERR_CUDA;
 }
 
 pa_status step_dkv(const pa_dims* d, const void* q, const void* k, const void* v, const void* dout,
                    const float* lse, const int32_t* seg, void* dk, void* dv, void* ws, size_t ws_bytes,
-                   pa_stream_t stream, const pa_strides* strides = nullptr) {
+                   pa_stream_t stream, const pa::RowStrides* rs = nullptr, int Nr = 0) {
   pa_status s = check_call(d, ws, ws_bytes, {q, k, v, dout, lse, dk, dv}, seg);
   if (s != PA_OK) return s;
-  pa::AttnParams p = make_params(d, seg, ws);
+  pa::AttnParams p = make_params(d, seg, ws, Nr);
   p.lse_in = lse;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
-  return pa::launch_bwd_dkv(p, d->D, rows_of(d, strides), q, k, v, dout, cu(stream)) == cudaSuccess ? PA_OK
+  return pa::launch_bwd_dkv(p, d->D, rows_or(d, rs), q, k, v, dout, cu(stream)) == cudaSuccess ? PA_OK
                                                                                               : PA_ERR_CUDA;
 }
 
 pa_status fwd_impl(const pa_dims* d, const void* q, const void* k, const void* v, const int32_t* seg, void* out,
-                   float* lse, void* ws, size_t ws_bytes, pa_stream_t stream, const pa_strides* strides = nullptr) {
+                   float* lse, void* ws, size_t ws_bytes, pa_stream_t stream, const pa::RowStrides* rs = nullptr,
+                   int Nr = 0) {
   pa_status s = check_call(d, ws, ws_bytes, {q, k, v, out, lse}, seg);
   if (s != PA_OK) return s;
   if ((s = step_tile_table(d, seg, ws, ws_bytes, stream)) != PA_OK) return s;
-  return step_fwd(d, q, k, v, seg, out, lse, ws, ws_bytes, stream, strides);
+  return step_fwd(d, q, k, v, seg, out, lse, ws, ws_bytes, stream, rs, Nr);
 }
 
 pa_status bwd_impl(const pa_dims* d, const void* q, const void* k, const void* v, const void* out,
                    const void* dout, const float* lse, const int32_t* seg, void* dq, void* dk, void* dv, void* ws,
-                   size_t ws_bytes, pa_stream_t stream, const pa_strides* strides = nullptr) {
+                   size_t ws_bytes, pa_stream_t stream, const pa::RowStrides* rs = nullptr, int Nr = 0) {
   pa_status s = check_call(d, ws, ws_bytes, {q, k, v, out, dout, lse, dq, dk, dv}, seg);
   if (s != PA_OK) return s;
   if ((s = step_tile_table(d, seg, ws, ws_bytes, stream)) != PA_OK) return s;
-  if ((s = step_delta(d, out, dout, lse, ws, ws_bytes, stream, strides)) != PA_OK) return s;
-  if ((s = step_dq(d, q, k, v, dout, lse, seg, dq, ws, ws_bytes, stream, strides)) != PA_OK) return s;
-  return step_dkv(d, q, k, v, dout, lse, seg, dk, dv, ws, ws_bytes, stream, strides);
+  if ((s = step_delta(d, out, dout, lse, ws, ws_bytes, stream, rs, Nr)) != PA_OK) return s;
+  if ((s = step_dq(d, q, k, v, dout, lse, seg, dq, ws, ws_bytes, stream, rs, Nr)) != PA_OK) return s;
+  return step_dkv(d, q, k, v, dout, lse, seg, dk, dv, ws, ws_bytes, stream, rs, Nr);
+}
+
+// bf16 tensors whose N is not a whole number of tiles: the kernels run on
+// N rounded up to 128 (dp), reading the caller's tensors through 4-D maps
+// whose N extent is the real N (the tail reads as zeros and is never
+// stored), with the segment ids copied into the workspace padded by the
+// row's last id.
+struct Ragged {
+  pa_dims dp;
+  pa::RowStrides rs;
+  const int32_t* pseg;
+};
+pa_status ragged_prepare(const pa_dims* d, const pa_strides* s, const int32_t* seg, void* ws, size_t ws_bytes,
+                         std::initializer_list<const void*> required, pa_stream_t stream, Ragged* r) {
+  r->dp = *d;
+  r->dp.N = padded_n(d);
+  r->rs = rows_of(d, s);
+  pa_status st = check_call(&r->dp, ws, ws_bytes, required, seg);
+  if (st != PA_OK) return st;
+  r->pseg = nullptr;
+  if (seg) {
+    int32_t* pseg = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + ws_layout(&r->dp).pseg);
+    if (pa::launch_stage_words_in(pseg, seg, (uint64_t)d->B, d->N, r->dp.N, true, cu(stream)) != cudaSuccess)
+      return PA_ERR_CUDA;
+    r->pseg = pseg;
+  }
+  return PA_OK;
 }
 
 // Single-pass backward: the fp32 dQ accumulator sits after the kernels'
@@ -372,7 +408,16 @@ pa_status fwd_any(const pa_dims* d, const pa_strides* s, int32_t io, const void*
   if ((why = io_ok(io)) != PA_OK) return why;
   const bool f32 = io == PA_IO_F32;
   if (s && (why = strides_ok(d, s, f32)) != PA_OK) return why;
-  if (!f32 && tiled(d)) return fwd_impl(d, q, k, v, seg, out, lse, ws, ws_bytes, stream, s);
+  if (!f32 && tiled(d)) {
+    const pa::RowStrides rs = rows_of(d, s);
+    return fwd_impl(d, q, k, v, seg, out, lse, ws, ws_bytes, stream, &rs);
+  }
+  if (!f32) {
+    Ragged r;
+    pa_status st = ragged_prepare(d, s, seg, ws, ws_bytes, {q, k, v, out, lse}, stream, &r);
+    if (st != PA_OK) return st;
+    return fwd_impl(&r.dp, q, k, v, r.pseg, out, lse, ws, ws_bytes, stream, &r.rs, d->N);
+  }
   const pa_strides c = contiguous_strides(d);
   return fwd_staged(d, s ? s : &c, f32, q, k, v, seg, out, lse, ws, ws_bytes, stream);
 }
@@ -385,7 +430,16 @@ pa_status bwd_any(const pa_dims* d, const pa_strides* s, int32_t io, const void*
   if ((why = io_ok(io)) != PA_OK) return why;
   const bool f32 = io == PA_IO_F32;
   if (s && (why = strides_ok(d, s, f32)) != PA_OK) return why;
-  if (!f32 && tiled(d)) return bwd_impl(d, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream, s);
+  if (!f32 && tiled(d)) {
+    const pa::RowStrides rs = rows_of(d, s);
+    return bwd_impl(d, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream, &rs);
+  }
+  if (!f32) {
+    Ragged r;
+    pa_status st = ragged_prepare(d, s, seg, ws, ws_bytes, {q, k, v, out, dout, lse, dq, dk, dv}, stream, &r);
+    if (st != PA_OK) return st;
+    return bwd_impl(&r.dp, q, k, v, out, dout, lse, r.pseg, dq, dk, dv, ws, ws_bytes, stream, &r.rs, d->N);
+  }
   const pa_strides c = contiguous_strides(d);
   return bwd_staged(d, s ? s : &c, f32, q, k, v, out, dout, lse, seg, dq, dk, dv, ws, ws_bytes, stream);
 }

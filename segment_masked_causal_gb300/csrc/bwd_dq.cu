@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(352, 1)
     const int qidx = tq * kTile + r;
     const size_t row = (size_t)(b * p.Hq + h) * p.N + qidx;
     const int32_t segq = p.seg ? p.seg[(size_t)b * p.N + qidx] : 0;
-    const float lse2 = p.lse_in[row] * 1.4426950408889634f;
+    const float lse2 = p.lse2[row];  // lse * log2(e), from the delta step
     const float dlt = p.delta[row];
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
@@ -364,13 +364,13 @@ cudaError_t launch_dq_d(const AttnParams& p, int Dio, const RowStrides& rs, cons
   // contiguous tensors: 2-D maps over their rows (cheaper for TMA than the
   // 4-D form, which strided tensors need)
   AttnParams pp = p;
-  pp.tma4 = is_contiguous(rs, p.Hq, p.Hkv, p.N, Dio) ? 0 : 1;
+  pp.tma4 = (p.Nr == p.N && is_contiguous(rs, p.Hq, p.Hkv, p.N, Dio)) ? 0 : 1;
   const auto qmap = [&](CUtensorMap* m, const void* t) {
-    return pp.tma4 ? tmap_bf16_bhnd_sw128(m, t, Dio, p.N, p.Hq, p.B, rs.q_n, rs.q_h, rs.q_b)
+    return pp.tma4 ? tmap_bf16_bhnd_sw128(m, t, Dio, p.Nr, p.Hq, p.B, rs.q_n, rs.q_h, rs.q_b)
                    : tmap_bf16_2d_sw128(m, t, Dio, (uint64_t)p.B * p.Hq * p.N, 128);
   };
   const auto kmap = [&](CUtensorMap* m, const void* t) {
-    return pp.tma4 ? tmap_bf16_bhnd_sw128(m, t, Dio, p.N, p.Hkv, p.B, rs.k_n, rs.k_h, rs.k_b)
+    return pp.tma4 ? tmap_bf16_bhnd_sw128(m, t, Dio, p.Nr, p.Hkv, p.B, rs.k_n, rs.k_h, rs.k_b)
                    : tmap_bf16_2d_sw128(m, t, Dio, (uint64_t)p.B * p.Hkv * p.N, 128);
   };
   if (!qmap(&tq, q) || !qmap(&tdo, dout) || !kmap(&tk, k) || !kmap(&tv, v) || !qmap(&tdq, p.dq))

@@ -24,7 +24,10 @@ constexpr int kTile = 128;
 constexpr uint32_t kSelftestWaitSite = 99;
 
 struct AttnParams {
-  int B, Hq, Hkv, N, T, G;
+  // N: tokens per row as the kernels see them (whole tiles, T = N / 128);
+  // Nr <= N: the caller's tokens per row. Rows n >= Nr are a tail that TMA
+  // reads as zeros and never stores, with the row's last segment id.
+  int B, Hq, Hkv, N, T, G, Nr;
   float scale;       // softmax scale
   float scale_log2;  // scale * log2(e)
   const int32_t* seg;   // (B, N) or null (every token in one segment)

@@ -324,7 +324,8 @@ __global__ void __launch_bounds__(352, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int qidx = tq * kTile + r;
-    const size_t row = (size_t)(b * p.Hq + h) * p.N + qidx;
+    // this row's lse in the caller's (B, Hq, Nr) layout (tail rows have none)
+    const size_t lse_row = (size_t)(b * p.Hq + h) * p.Nr + qidx;
     const int32_t segq = p.seg ? p.seg[(size_t)b * p.N + qidx] : 0;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const uint32_t tO = tmem + lane_base + L::TM_O;
@@ -491,7 +492,7 @@ __global__ void __launch_bounds__(352, 1)
         bulk_commit();
         bulk_wait_all();  // the store has read shared memory (and completed) before the CTA exits
       }
-      if (grp == 0) p.lse[row] = m_fin * 0.6931471805599453f + logf(lt);
+      if (grp == 0 && qidx < p.Nr) p.lse[lse_row] = m_fin * 0.6931471805599453f + logf(lt);
     }
   }
   tc_fence_before();
@@ -510,13 +511,13 @@ cudaError_t launch_fwd_d(const AttnParams& p, int Dio, const RowStrides& rs, con
   // contiguous tensors: 2-D maps over their rows (cheaper for TMA than the
   // 4-D form, which strided tensors need)
   AttnParams pp = p;
-  pp.tma4 = is_contiguous(rs, p.Hq, p.Hkv, p.N, Dio) ? 0 : 1;
+  pp.tma4 = (p.Nr == p.N && is_contiguous(rs, p.Hq, p.Hkv, p.N, Dio)) ? 0 : 1;
   const auto qmap = [&](CUtensorMap* m, const void* t) {
-    return pp.tma4 ? tmap_bf16_bhnd_sw128(m, t, Dio, p.N, p.Hq, p.B, rs.q_n, rs.q_h, rs.q_b)
+    return pp.tma4 ? tmap_bf16_bhnd_sw128(m, t, Dio, p.Nr, p.Hq, p.B, rs.q_n, rs.q_h, rs.q_b)
                    : tmap_bf16_2d_sw128(m, t, Dio, (uint64_t)p.B * p.Hq * p.N, 128);
   };
   const auto kmap = [&](CUtensorMap* m, const void* t) {
-    return pp.tma4 ? tmap_bf16_bhnd_sw128(m, t, Dio, p.N, p.Hkv, p.B, rs.k_n, rs.k_h, rs.k_b)
+    return pp.tma4 ? tmap_bf16_bhnd_sw128(m, t, Dio, p.Nr, p.Hkv, p.B, rs.k_n, rs.k_h, rs.k_b)
                    : tmap_bf16_2d_sw128(m, t, Dio, (uint64_t)p.B * p.Hkv * p.N, 128);
   };
   if (!qmap(&tq, q) || !kmap(&tk, k) || !kmap(&tv, v) || !qmap(&to, p.out)) return cudaErrorInvalidValue;

@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restr
                                                     const __nv_bfloat16* __restrict__ dout,
                                                     const float* __restrict__ lse, float* __restrict__ delta,
                                                     float* __restrict__ lse2, float* __restrict__ zero_acc,
-                                                    size_t rows, bool contiguous, int N, int H, int64_t s_n,
+                                                    size_t rows, bool contiguous, int N, int Nr, int H, int64_t s_n,
                                                     int64_t s_h, int64_t s_b) {
   // each of the row's LPR lanes takes every LPR-th 16-byte vector
   constexpr int VEC = D / 8;
@@ -231,17 +231,24 @@ __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restr
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   const int sub = threadIdx.x % LPR;
   for (size_t t = gtid; t < rows * LPR; t += stride) {
+    // row = (b * H + h) * N + n of the kernels' rows; the caller's tensors
+    // hold n < Nr (rows < 2^31), and contiguous ones with Nr = N skip the
+    // divisions
     const size_t row = t / LPR;
-    // element offset of query row (b, h, n) of O and dO, row = (b * H + h) * N + n
-    // (rows < 2^31); contiguous tensors skip the divisions
-    size_t off = row * D;
+    size_t off = row * D, lrow = row;
+    bool tail = false;
     if (!contiguous) {
-      const uint32_t r32 = (uint32_t)row, bh = r32 / (uint32_t)N, b = bh / (uint32_t)H;
-      off = (size_t)b * s_b + (size_t)(bh - b * (uint32_t)H) * s_h + (size_t)(r32 - bh * (uint32_t)N) * s_n;
+      const uint32_t r32 = (uint32_t)row, bh = r32 / (uint32_t)N, b = bh / (uint32_t)H, n = r32 - bh * (uint32_t)N;
+      tail = n >= (uint32_t)Nr;
+      off = (size_t)b * s_b + (size_t)(bh - b * (uint32_t)H) * s_h + (size_t)n * s_n;
+      lrow = (size_t)bh * Nr + n;
     }
+    // a tail query row gets P = 0 (lse = +inf) and delta = 0, so it adds
+    // nothing; its lanes still take part in the shuffles below
     float acc = 0.f;
 #pragma unroll
     for (int v = sub; v < VEC; v += LPR) {
+      if (tail) break;
       const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + off) + v);
       const uint4 c = __ldg(reinterpret_cast<const uint4*>(dout + off) + v);
       acc = fmaf(bf16lo(a.x), bf16lo(c.x), acc);
@@ -259,10 +266,10 @@ __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restr
       }
     }
 #pragma unroll
-    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(~0u, acc, off);
+    for (int of = LPR / 2; of > 0; of >>= 1) acc += __shfl_xor_sync(~0u, acc, of);
     if (sub == 0) {
       delta[row] = acc;
-      lse2[row] = lse[row] * 1.4426950408889634f;  // for the dK/dV softmax, which works in base 2
+      lse2[row] = tail ? INFINITY : lse[lrow] * 1.4426950408889634f;  // the backward's softmax works in base 2
     }
   }
 }
@@ -318,7 +325,7 @@ cudaError_t launch_wait_timeout_selftest(uint32_t* status, cudaStream_t st) {
 }
 
 cudaError_t launch_delta(const AttnParams& p, int D, const RowStrides& rs, cudaStream_t st) {
-  const bool contig = rs.q_n == D && rs.q_h == (int64_t)p.N * D && rs.q_b == (int64_t)p.Hq * p.N * D;
+  const bool contig = p.Nr == p.N && rs.q_n == D && rs.q_h == (int64_t)p.N * D && rs.q_b == (int64_t)p.Hq * p.N * D;
   const size_t rows = (size_t)p.B * p.Hq * p.N;
   const size_t threads = rows * (size_t)delta_lanes(D);
   int dev = 0, sms = 148;
@@ -329,13 +336,13 @@ cudaError_t launch_delta(const AttnParams& p, int D, const RowStrides& rs, cudaS
   if (blocks > cap) blocks = cap;
   if (D == 128)
     delta_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, p.dq_acc, rows, contig,
-                                                     p.N, p.Hq, rs.q_n, rs.q_h, rs.q_b);
+                                                     p.N, p.Nr, p.Hq, rs.q_n, rs.q_h, rs.q_b);
   else if (D == 96)
     delta_kernel<96><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, p.dq_acc, rows, contig,
-                                                     p.N, p.Hq, rs.q_n, rs.q_h, rs.q_b);
+                                                     p.N, p.Nr, p.Hq, rs.q_n, rs.q_h, rs.q_b);
   else
     delta_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(p.o, p.dout, p.lse_in, p.delta, p.lse2, p.dq_acc, rows, contig,
-                                                     p.N, p.Hq, rs.q_n, rs.q_h, rs.q_b);
+                                                     p.N, p.Nr, p.Hq, rs.q_n, rs.q_h, rs.q_b);
   return cudaGetLastError();
 }
 

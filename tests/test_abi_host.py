@@ -103,7 +103,7 @@ def test_ragged_n_and_strided_workspace(L):
 
 def test_ragged_n_refusals(L):
     """The single-step calls need whole tiles; the full calls take any N and
-    then need the staged workspace."""
+    then need the workspace of N rounded up to whole tiles."""
     dims = d(N=200)
     assert L.pa_fwd_tiles(ctypes.byref(dims), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == 4
     assert L.pa_build_tile_table(ctypes.byref(dims), FAKE, FAKE, 1 << 40, None) == 4
@@ -111,8 +111,10 @@ def test_ragged_n_refusals(L):
     assert L.pa_bwd_dq(ctypes.byref(dims), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == 4
     assert L.pa_bwd_dkv(ctypes.byref(dims), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40,
                         None) == 4
+    # bf16 with ragged N runs on whole tiles (N rounded up to 256 here) in
+    # place: one byte below that workspace is refused before any launch
     base = L.pa_workspace_bytes(ctypes.byref(d(N=256)))
-    assert fwd(L, dims, ws_bytes=base) == 6
+    assert fwd(L, dims, ws_bytes=base - 1) == 6
     assert fwd(L, dims, q=None) == 1
 
 
