@@ -89,9 +89,10 @@ def strides(q_b, q_h, q_n, k_b, k_h, k_n):
 
 
 def test_ragged_n_and_strided_workspace(L):
-    """N not a multiple of 128 needs the staging copies: the workspace then
-    holds (B, H, Np, D) buffers for q, out, dout, dq (Hq heads) and k, v, dk,
-    dv (Hkv heads), plus lse and seg, with Np = N rounded up to 128."""
+    """For N not a multiple of 128 pa_workspace_bytes also counts the staging
+    copies that fp32 calls use: (B, H, Np, D) buffers for q, out, dout, dq
+    (Hq heads) and k, v, dk, dv (Hkv heads), plus lse and seg, with Np = N
+    rounded up to 128 (bf16 calls need less and never more)."""
     base = L.pa_workspace_bytes(ctypes.byref(d(N=256)))
     ragged = L.pa_workspace_bytes(ctypes.byref(d(N=200)))
     assert ragged == L.pa_workspace_bytes_strided(ctypes.byref(d(N=200)))

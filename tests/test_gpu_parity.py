@@ -44,7 +44,7 @@ SMALL = [
     # loads fill with zeros and the stores leave out
     ("ragged_gqa_d96", synth.custom(2, 4, 2, 512, 96, [[1, 130, 5, 120, 256], [512]], seed=29)),
     ("len1_runs_g3_d96", synth.custom(1, 3, 1, 384, 96, [[1] * 30 + [3] * 20 + [294]], seed=30)),
-    # N not a multiple of 128: staged through whole tiles inside the workspace
+    # N not a multiple of 128: whole tiles with a tail that TMA reads as zeros
     ("ragged_n200_d64", synth.custom(1, 2, 2, 200, 64, [[1, 100, 99]], seed=31)),
     ("ragged_n300_gqa_d128", synth.custom(2, 4, 2, 300, 128, [[150, 150], [1, 298, 1]], seed=32)),
     ("ragged_n129_d96", synth.custom(1, 3, 1, 129, 96, [[129]], seed=33)),

@@ -154,8 +154,8 @@ def test_one_segment_lists_are_the_causal_order(cuda_dev):
     np.testing.assert_array_equal(wk, [b * T + t for t in range(T) for b in range(B)])
 
 
-def test_ragged_n_staged_table(cuda_dev):
-    """N = 300 runs through the staging copies: the kernels see 3 tiles whose
+def test_ragged_n_padded_table(cuda_dev):
+    """N = 300 runs on whole tiles: the kernels see 3 tiles whose
     tail tokens repeat the row's last id, and the table describes that
     padded row."""
     w = synth.custom(2, 4, 2, 300, 128, [[150, 150], [1, 298, 1]], seed=32)

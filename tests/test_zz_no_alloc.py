@@ -45,7 +45,7 @@ RAGGED = synth.custom(2, 4, 2, 300, 128, [[150, 150], [1, 298, 1]], seed=32)
 @pytest.mark.parametrize("name,causal", [("packed_4x4096_short", False), ("causal_2k_gqa", True),
                                          ("ragged_n300", False)])
 def test_noalloc_matches_workspace_backward_twice(name, causal, cuda_dev):
-    """N = 300 goes through the staging copies, which fit in the scratch."""
+    """N = 300 runs on whole tiles with a zero tail; its workspace fits in the scratch."""
     w = RAGGED if name == "ragged_n300" else synth.workload(name)
     q, k, v, do, seg = _inputs(w, cuda_dev)
     seg_arg = None if causal else seg
@@ -85,7 +85,7 @@ def _noalloc(L, w, q, k, v, out, do, lse, seg):
 def test_noalloc_sequence_of_different_shapes(cuda_dev):
     """The shared array keeps whatever the previous call left in it: a large
     packed call, then a small causal one, then a ragged N that goes through
-    the staging copies, then the large packed call again must each match
+    whole tiles with a zero tail, then the large packed call again must each match
     pa_bwd with its own workspace."""
     L = pa.lib()
     runs = []
