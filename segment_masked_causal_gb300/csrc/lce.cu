@@ -6,11 +6,12 @@
 //
 // Forward:
 // Grid: (token tiles of 128) x (vocabulary splits). A CTA walks its split's
-// vocabulary tiles of 128 rows; for each, the tcgen05 tensor cores form the
-// 128 x 128 logit tile in TMEM from 64-wide K slices of H and W that TMA
-// streams through a 3-stage ring (two CTAs share an SM), and four epilogue warps (one thread per
-// token, reading its TMEM lane) fold the tile into a running maximum and sum
-// of exponentials and pick up the target logit when it falls in the tile.
+// vocabulary tiles of 256 rows; for each, the tcgen05 tensor cores form the
+// 128 x 256 logit tile in TMEM from 64-wide K slices of H and W that TMA
+// streams through a 4-stage ring (one CTA per SM), and four epilogue warps
+// (one thread per token, reading its TMEM lane) fold the tile into a running
+// maximum and sum of exponentials and pick up the target logit when it falls
+// in the tile.
 // Two TMEM accumulators let the next tile's products run while the epilogue
 // reads the previous one. Each CTA writes its split's (max, sum) per token
 // and, for tokens whose target lies in its split, the target logit; a merge
@@ -41,12 +42,18 @@
 namespace pa {
 namespace {
 
-constexpr int kLceStages = 3;  // 3 x 32 KB: two CTAs fit on an SM
-constexpr int kLceTile = 128;                  // tokens per CTA and vocabulary rows per tile
-constexpr uint32_t kLceSlice = 128 * 128;      // one 128 x 64 bf16 slice (128-byte rows), 16 KB
-constexpr uint32_t kLceStage = 2 * kLceSlice;  // H slice + W slice
+// The logit tiles are 128 tokens x 256 vocabulary rows, so every product is
+// an N = 256 MMA: those keep the tensor pipe at its full rate while the
+// epilogue warps' arithmetic shares the issuing warp's SM sub-partition,
+// where N = 128 products fall to about 84 of their 64 cycles.
+constexpr int kLceStages = 4;                  // 4 x 48 KB: one CTA per SM
+constexpr int kLceTile = 128;                  // tokens per CTA
+constexpr int kLceVTile = 256;                 // vocabulary rows per tile
+constexpr uint32_t kLceSlice = 128 * 128;      // one 128 x 64 bf16 slice of H (128-byte rows), 16 KB
+constexpr uint32_t kLceSliceW = 256 * 128;     // one 256 x 64 bf16 slice of W, 32 KB
+constexpr uint32_t kLceStage = kLceSlice + kLceSliceW;
 constexpr int kLceThreads = 256;
-constexpr uint32_t kLceTmemCols = 256;  // two 128-column fp32 accumulators
+constexpr uint32_t kLceTmemCols = 512;  // two 256-column fp32 accumulators
 
 struct LceMisc {
   uint64_t full[kLceStages], empty[kLceStages];
@@ -78,7 +85,7 @@ struct LceParams {
 // BWD = false: the forward's online log-sum-exp epilogue. BWD = true: the
 // backward's dz epilogue (grid.y splits the chunk's vocabulary tiles).
 template <bool BWD>
-__global__ void __launch_bounds__(kLceThreads, 2)
+__global__ void __launch_bounds__(kLceThreads, 1)
     lce_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW,
                const LceParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -88,7 +95,7 @@ __global__ void __launch_bounds__(kLceThreads, 2)
   const uint32_t sRing = smem_u32(ring);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tm = blockIdx.x;
-  const int VT = BWD ? p.vt_end : (p.V + kLceTile - 1) / kLceTile;  // end of the tiles this launch covers
+  const int VT = BWD ? p.vt_end : (p.V + kLceVTile - 1) / kLceVTile;  // end of the tiles this launch covers
   const int vt0 = (BWD ? p.vt_base : 0) + blockIdx.y * p.vt_per_split;
   const int vt1 = min(vt0 + p.vt_per_split, VT);
   const int nt = vt1 - vt0;  // >= 1 by construction of the grid
@@ -130,7 +137,7 @@ __global__ void __launch_bounds__(kLceThreads, 2)
           if (!g.wait(&m.empty[st], ((it / kLceStages) & 1) ^ 1, 40)) { ok = false; break; }
           mbar_expect_tx(&m.full[st], kLceStage);
           tma_load_2d(ring + st * kLceStage, &tmH, &m.full[st], kc * 64, tm * kLceTile);
-          tma_load_2d(ring + st * kLceStage + kLceSlice, &tmW, &m.full[st], kc * 64, (vt0 + j) * kLceTile);
+          tma_load_2d(ring + st * kLceStage + kLceSlice, &tmW, &m.full[st], kc * 64, (vt0 + j) * kLceVTile);
         }
       }
       // no copy may still be landing when the CTA exits
@@ -141,7 +148,7 @@ __global__ void __launch_bounds__(kLceThreads, 2)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const bool leader = lane == 0;
-    constexpr uint32_t idZ = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idZ = idesc_bf16_f32(128, 256, false, false);
     bool ok = true;
     int it = 0;
     for (int j = 0; ok && j < nt; ++j) {
@@ -158,7 +165,7 @@ __global__ void __launch_bounds__(kLceThreads, 2)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           if (leader)
-            umma_bf16(tmem + buf * 128, sdesc_add(hd, kk * 32), sdesc_add(wd, kk * 32), idZ,
+            umma_bf16(tmem + buf * 256, sdesc_add(hd, kk * 32), sdesc_add(wd, kk * 32), idZ,
                       (kc > 0 || kk > 0) ? 1u : 0u);
         if (leader) umma_commit(&m.empty[st]);
         __syncwarp();
@@ -194,12 +201,12 @@ __global__ void __launch_bounds__(kLceThreads, 2)
       ok = __all_sync(~0u, ok);
       if (!ok) break;
       tc_fence_after();
-      const int v0 = (vt0 + j) * kLceTile;
-      const int c0v = v0 - p.vt_base * kLceTile;  // column of v0 in the chunk
+      const int v0 = (vt0 + j) * kLceVTile;
+      const int c0v = v0 - p.vt_base * kLceVTile;  // column of v0 in the chunk
 #pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+      for (int c0 = 0; c0 < kLceVTile; c0 += 32) {
         uint32_t a[32];
-        tmem_ld32(tmem + lane_base + buf * 128 + c0, a);
+        tmem_ld32(tmem + lane_base + buf * 256 + c0, a);
         const int vc = v0 + c0;
         uint32_t w[16];
 #pragma unroll
@@ -250,11 +257,11 @@ __global__ void __launch_bounds__(kLceThreads, 2)
       ok = __all_sync(~0u, ok);
       if (!ok) break;
       tc_fence_after();
-      const int v0 = (vt0 + j) * kLceTile;
+      const int v0 = (vt0 + j) * kLceVTile;
 #pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+      for (int c0 = 0; c0 < kLceVTile; c0 += 32) {
         uint32_t a[32];
-        tmem_ld32(tmem + lane_base + buf * 128 + c0, a);
+        tmem_ld32(tmem + lane_base + buf * 256 + c0, a);
         const int vc = v0 + c0;
         float cmax = -INFINITY;
 #pragma unroll
@@ -311,7 +318,7 @@ __global__ void __launch_bounds__(256) lce_merge_kernel(const LceParams p, int s
   const int t = p.targets[i];
   float z = 0.f, n = 0.f;
   if (t >= 0 && t < p.V) {
-    z = p.part_t[(size_t)(t / kLceTile / p.vt_per_split) * p.N + i];
+    z = p.part_t[(size_t)(t / kLceVTile / p.vt_per_split) * p.N + i];
     n = l - z;
   }
   lse[i] = l;
@@ -320,19 +327,23 @@ __global__ void __launch_bounds__(256) lce_merge_kernel(const LceParams p, int s
 }
 
 // ------------------------------------------------------------------ GEMM
-// C (M x N) from A (M x K, K contiguous) and B (K x N, N contiguous): one
-// 128 x 128 output tile per CTA, K in steps of 64 through a 3-stage TMA ring
-// (A as one 128-row x 64 box, B as two 64-row x 64 boxes, all 128-byte
-// swizzled; elements past M, N or K read as zero), tcgen05 products into one
-// 128-column fp32 TMEM accumulator. Two CTAs fit on an SM, so one's epilogue
-// runs beside the other's products. The epilogue (one thread per output row)
-// stores bf16, or starts / adds to / finishes an fp32 accumulator in global
-// memory; each output tile belongs to one CTA, so no two threads touch the
-// same element.
-constexpr int kGemmStages = 3;
+// C (M x N) from A (M x K, K contiguous) and B (K x N, N contiguous) in
+// 128 x 256 output tiles (N = 256 products, which keep their full rate beside
+// the epilogue warps' arithmetic). One CTA per SM walks tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ... (N tiles fastest, so the CTAs that share an A
+// row block run together and keep it in L2), K in steps of 64 through a
+// 4-stage TMA ring (A as one 128-row x 64 box, B as four 64-row x 64 boxes,
+// all 128-byte swizzled; elements past M, N or K read as zero), tcgen05
+// products into two 256-column fp32 TMEM accumulators used by alternate
+// tiles, so a tile's epilogue runs beside the next tile's products. The
+// epilogue (one thread per output row) stores bf16, or starts / adds to /
+// finishes an fp32 accumulator in global memory; each output tile belongs to
+// one CTA, so no two threads touch the same element.
+constexpr int kGemmStages = 4;
+constexpr int kGemmN = 256;                               // output columns per tile
 constexpr uint32_t kGemmA = 128 * 128;                    // 128 rows x 64 K, 16 KB
 constexpr uint32_t kGemmBHalf = 64 * 128;                 // 64 K rows x 64 N columns, 8 KB
-constexpr uint32_t kGemmStage = kGemmA + 2 * kGemmBHalf;  // 32 KB
+constexpr uint32_t kGemmStage = kGemmA + 4 * kGemmBHalf;  // 48 KB
 constexpr int kGemmThreads = 192;
 constexpr uint32_t kGemmSmem = 1024 /* misc */ + 1024 /* alignment */ + kGemmStages * kGemmStage;
 
@@ -341,7 +352,8 @@ enum GemmMode : int { kStoreBf16 = 0, kAccInit = 1, kAccAdd = 2, kAccFinal = 3 }
 struct GemmParams {
   int M, N, K;         // N a multiple of 64
   int mode;            // GemmMode
-  int n_fastest;       // grid.x walks the N tiles (else the M tiles)
+  int n_tiles;         // N tiles per row block; tile t is (t / n_tiles, t % n_tiles)
+  int tiles;           // M tiles x N tiles
   __nv_bfloat16* c;    // bf16 result (kStoreBf16: the product; kAccFinal: accumulator + product)
   int ldc;
   float* acc;          // fp32 accumulator (kAccInit: set; kAccAdd: add; kAccFinal: read)
@@ -351,12 +363,13 @@ struct GemmParams {
 
 struct GemmMisc {
   uint64_t full[kGemmStages], empty[kGemmStages];
-  uint64_t acc_full, fin;
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t fin;
   uint32_t tmem_base;
   int abort_flag;
 };
 
-__global__ void __launch_bounds__(kGemmThreads, 2)
+__global__ void __launch_bounds__(kGemmThreads, 1)
     lce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -365,12 +378,10 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                                              ~uintptr_t(1023));
   const uint32_t sRing = smem_u32(ring);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // N tiles run fastest: the CTAs that share an A row block run together and
-  // keep it in L2 (with M tiles fastest, a launch read A about five times);
-  // past 65535 M tiles (grid.y's limit) the launch puts M in grid.x instead
-  const int m0 = (p.n_fastest ? blockIdx.y : blockIdx.x) * 128;
-  const int n0 = (p.n_fastest ? blockIdx.x : blockIdx.y) * 128;
   const int KB = (p.K + 63) / 64;
+  // this CTA's tiles: t = blockIdx.x + j * gridDim.x for j < nt (>= 1: the
+  // grid is never larger than the tile count)
+  const int nt = (p.tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
   const Guard g{&m.abort_flag, p.status};
 
   if (threadIdx.x == 0) {
@@ -379,12 +390,15 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
       mbar_init(&m.full[s], 1);
       mbar_init(&m.empty[s], 1);
     }
-    mbar_init(&m.acc_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&m.acc_full[b], 1);
+      mbar_init(&m.acc_empty[b], 128);
+    }
     mbar_init(&m.fin, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&m.tmem_base, 128);
+    tmem_alloc(&m.tmem_base, 2 * kGemmN);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -396,57 +410,75 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     if (lane == 0) {
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
-      int kb = 0;
-      for (; kb < KB; ++kb) {
-        const int st = kb % kGemmStages;
-        if (!g.wait(&m.empty[st], ((kb / kGemmStages) & 1) ^ 1, 45)) break;
-        uint8_t* sa = ring + st * kGemmStage;
-        mbar_expect_tx(&m.full[st], kGemmStage);
-        tma_load_2d(sa, &tmA, &m.full[st], kb * 64, m0);
-        tma_load_2d(sa + kGemmA, &tmB, &m.full[st], n0, kb * 64);
-        tma_load_2d(sa + kGemmA + kGemmBHalf, &tmB, &m.full[st], n0 + 64, kb * 64);
+      int it = 0;
+      bool ok = true;
+      for (int j = 0; ok && j < nt; ++j) {
+        const int t = (int)blockIdx.x + j * (int)gridDim.x;
+        const int m0 = (t / p.n_tiles) * 128, n0 = (t % p.n_tiles) * kGemmN;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int st = it % kGemmStages;
+          if (!g.wait(&m.empty[st], ((it / kGemmStages) & 1) ^ 1, 45)) { ok = false; break; }
+          uint8_t* sa = ring + st * kGemmStage;
+          mbar_expect_tx(&m.full[st], kGemmStage);
+          tma_load_2d(sa, &tmA, &m.full[st], kb * 64, m0);
+          for (int c = 0; c < kGemmN / 64; ++c)
+            tma_load_2d(sa + kGemmA + c * kGemmBHalf, &tmB, &m.full[st], n0 + 64 * c, kb * 64);
+        }
       }
       // no copy may still be landing when the CTA exits
-      for (int i = (kb > kGemmStages ? kb - kGemmStages : 0); i < kb; ++i)
+      for (int i = (it > kGemmStages ? it - kGemmStages : 0); i < it; ++i)
         g.drain(&m.full[i % kGemmStages], (i / kGemmStages) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
     const bool leader = lane == 0;
-    constexpr uint32_t idC = idesc_bf16_f32(128, 128, false, true);
+    constexpr uint32_t idC = idesc_bf16_f32(128, kGemmN, false, true);
     bool ok = true;
-    for (int kb = 0; kb < KB; ++kb) {
-      const int st = kb % kGemmStages;
-      if (!g.wait_warp(&m.full[st], (kb / kGemmStages) & 1, 46)) { ok = false; break; }
+    int it = 0;
+    for (int j = 0; ok && j < nt; ++j) {
+      const int buf = j & 1;
+      // accumulator buf is free once the epilogue has read tile j - 2 from it
+      if (j >= 2 && !g.wait_warp(&m.acc_empty[buf], ((j - 2) >> 1) & 1, 48)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t sa = sRing + st * kGemmStage;
-      const uint64_t ad = sdesc_sw128(sa, 16, 1024);
-      const uint64_t bd = sdesc_sw128(sa + kGemmA, kGemmBHalf, 1024);
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int st = it % kGemmStages;
+        if (!g.wait_warp(&m.full[st], (it / kGemmStages) & 1, 46)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sa = sRing + st * kGemmStage;
+        const uint64_t ad = sdesc_sw128(sa, 16, 1024);
+        const uint64_t bd = sdesc_sw128(sa + kGemmA, kGemmBHalf, 1024);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        if (leader)
-          umma_bf16(tmem, sdesc_add(ad, kk * 32), sdesc_add(bd, kk * 2048), idC, (kb > 0 || kk > 0) ? 1u : 0u);
-      if (leader) umma_commit(&m.empty[st]);
+        for (int kk = 0; kk < 4; ++kk)
+          if (leader)
+            umma_bf16(tmem + buf * kGemmN, sdesc_add(ad, kk * 32), sdesc_add(bd, kk * 2048), idC,
+                      (kb > 0 || kk > 0) ? 1u : 0u);
+        if (leader) umma_commit(&m.empty[st]);
+        __syncwarp();
+      }
+      if (ok && leader) umma_commit(&m.acc_full[buf]);
       __syncwarp();
     }
     if (leader) {
-      if (ok) umma_commit(&m.acc_full);
-      umma_commit(&m.fin);
+      umma_commit(&m.fin);  // every MMA issued has completed once this arrives
       g.drain(&m.fin, 0);
     }
     __syncwarp();
   } else {
     // warps 2..5: TMEM lane quarter warp % 4, one thread per output row
     const int quarter = warp & 3;
-    const int row = m0 + quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const bool ok = __all_sync(~0u, g.wait(&m.acc_full, 0, 47));
-    if (ok) {
+    for (int j = 0; j < nt; ++j) {
+      const int buf = j & 1;
+      const bool ok = __all_sync(~0u, g.wait(&m.acc_full[buf], (j >> 1) & 1, 47));
+      if (!ok) break;
       tc_fence_after();
+      const int t = (int)blockIdx.x + j * (int)gridDim.x;
+      const int m0 = (t / p.n_tiles) * 128, n0 = (t % p.n_tiles) * kGemmN;
+      const int row = m0 + quarter * 32 + lane;
 #pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+      for (int c0 = 0; c0 < kGemmN; c0 += 32) {
         uint32_t a[32];
-        tmem_ld32(tmem + lane_base + c0, a);
+        tmem_ld32(tmem + lane_base + buf * kGemmN + c0, a);
         const int col = n0 + c0;
         if (row >= p.M || col >= p.N) continue;  // N is a multiple of 64: 32 columns are all in or all out
         if (p.mode == kAccInit || p.mode == kAccAdd || p.mode == kAccFinal) {
@@ -482,13 +514,15 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                                pack_bf16x2(__uint_as_float(a[8 * q + 6]), __uint_as_float(a[8 * q + 7])));
         }
       }
+      tc_fence_before();
+      mbar_arrive(&m.acc_empty[buf]);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 2 * kGemmN);
   }
 }
 
@@ -500,9 +534,15 @@ cudaError_t launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, const Gemm
     attr = true;
   }
   GemmParams q = gp;
-  const unsigned mt = (unsigned)((gp.M + 127) / 128), nt = (unsigned)((gp.N + 127) / 128);
-  q.n_fastest = mt <= 65535;
-  const dim3 grid = q.n_fastest ? dim3(nt, mt) : dim3(mt, nt);
+  const long long mt = (gp.M + 127) / 128, ntl = (gp.N + kGemmN - 1) / kGemmN;
+  if (mt * ntl > (1ll << 30)) return cudaErrorInvalidValue;
+  q.n_tiles = (int)ntl;
+  q.tiles = (int)(mt * ntl);
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = q.tiles < sms ? q.tiles : sms;
+  if (grid < 1) return cudaSuccess;
   lce_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, st>>>(tA, tB, q);
   return cudaGetLastError();
 }
@@ -515,7 +555,7 @@ cudaError_t launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, const Gemm
 // one tile) are counted. At most kLceMaxSplits splits (the workspace's partial
 // sums are sized for that).
 LceSplit lce_split(int N, int V, int slots) {
-  const int TT = (N + kLceTile - 1) / kLceTile, VT = (V + kLceTile - 1) / kLceTile;
+  const int TT = (N + kLceTile - 1) / kLceTile, VT = (V + kLceVTile - 1) / kLceVTile;
   if (slots < 1) slots = 1;
   LceSplit best{1, VT};
   long long best_cost = -1;
@@ -532,14 +572,13 @@ LceSplit lce_split(int N, int V, int slots) {
 }
 
 int lce_slots() {
-  // the kernel is built for two resident CTAs per SM: 3 x 32 KB stages (about
-  // 100 KB of shared memory) and at most 128 registers a thread
-  static_assert(kLceSmem + 1024 <= 232448 / 2 + 1024, "two CTAs must fit an SM's shared memory");
+  // one resident CTA per SM: 4 x 48 KB stages and all 512 TMEM columns
+  static_assert(kLceSmem <= 232448, "shared memory");
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
       sms <= 0)
     sms = 148;
-  return 2 * sms;
+  return sms;
 }
 
 cudaError_t launch_lce_fwd(int N, int V, int D, const void* hidden, const void* head, const int32_t* targets,
@@ -547,7 +586,7 @@ cudaError_t launch_lce_fwd(int N, int V, int D, const void* hidden, const void* 
                            cudaStream_t st) {
   const LceSplit sp = lce_split(N, V, lce_slots());
   CUtensorMap tH, tW;
-  if (!tmap_bf16_2d_sw128(&tH, hidden, D, N, kLceTile) || !tmap_bf16_2d_sw128(&tW, head, D, V, kLceTile))
+  if (!tmap_bf16_2d_sw128(&tH, hidden, D, N, kLceTile) || !tmap_bf16_2d_sw128(&tW, head, D, V, kLceVTile))
     return cudaErrorInvalidValue;
   LceParams p{};
   p.N = N;
@@ -574,11 +613,12 @@ namespace pa {
 
 int lce_bwd_chunk(int N, int V) {
   // dz and dz^T of one chunk together take 4 N Vc bytes: at most 512 MiB
-  long long vc = ((1ll << 27) / (N > 0 ? N : 1)) / kLceTile * kLceTile;
-  const long long vmax = (long long)(V + kLceTile - 1) / kLceTile * kLceTile;
+  // (chunks are whole vocabulary tiles)
+  long long vc = ((1ll << 27) / (N > 0 ? N : 1)) / kLceVTile * kLceVTile;
+  const long long vmax = (long long)(V + kLceVTile - 1) / kLceVTile * kLceVTile;
   if (vc > 8192) vc = 8192;
   if (vc > vmax) vc = vmax;
-  if (vc < kLceTile) vc = kLceTile;
+  if (vc < kLceVTile) vc = kLceVTile;
   return (int)vc;
 }
 
@@ -604,7 +644,7 @@ cudaError_t launch_lce_bwd(int N, int V, int D, const void* hidden, const void* 
   __nv_bfloat16* dzt = reinterpret_cast<__nv_bfloat16*>(w + L.dzt);
   float* acc = reinterpret_cast<float*>(w + L.acc);
   CUtensorMap tH, tW, tHb;
-  if (!tmap_bf16_2d_sw128(&tH, hidden, D, N, kLceTile) || !tmap_bf16_2d_sw128(&tW, head, D, V, kLceTile) ||
+  if (!tmap_bf16_2d_sw128(&tH, hidden, D, N, kLceTile) || !tmap_bf16_2d_sw128(&tW, head, D, V, kLceVTile) ||
       !tmap_bf16_2d_sw128(&tHb, hidden, D, N, 64))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(lce_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLceSmem);
@@ -620,8 +660,8 @@ cudaError_t launch_lce_bwd(int N, int V, int D, const void* hidden, const void* 
     p.vt_per_split = sp.per;
     p.targets = targets;
     p.status = status;
-    p.vt_base = cv0 / kLceTile;
-    p.vt_end = (cv0 + kc + kLceTile - 1) / kLceTile;
+    p.vt_base = cv0 / kLceVTile;
+    p.vt_end = (cv0 + kc + kLceVTile - 1) / kLceVTile;
     p.lse = lse;
     p.g = g;
     p.dz = dz;
