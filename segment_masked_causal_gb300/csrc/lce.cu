@@ -82,8 +82,11 @@ struct LceParams {
   int ld_dzt;
 };
 
-// BWD = false: the forward's online log-sum-exp epilogue. BWD = true: the
-// backward's dz epilogue (grid.y splits the chunk's vocabulary tiles).
+// BWD = false: the forward's online log-sum-exp epilogue; the CTA walks the
+// vocabulary tiles of split blockIdx.y for token tile blockIdx.x. BWD =
+// true: the backward's dz epilogue, which keeps nothing from tile to tile,
+// so one CTA per SM takes the chunk's (token tile, vocabulary tile) pairs
+// blockIdx.x, blockIdx.x + gridDim.x, ..., vocabulary tile fastest.
 template <bool BWD>
 __global__ void __launch_bounds__(kLceThreads, 1)
     lce_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW,
@@ -94,11 +97,21 @@ __global__ void __launch_bounds__(kLceThreads, 1)
                                              ~uintptr_t(1023));
   const uint32_t sRing = smem_u32(ring);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tm = blockIdx.x;
-  const int VT = BWD ? p.vt_end : (p.V + kLceVTile - 1) / kLceVTile;  // end of the tiles this launch covers
-  const int vt0 = (BWD ? p.vt_base : 0) + blockIdx.y * p.vt_per_split;
-  const int vt1 = min(vt0 + p.vt_per_split, VT);
-  const int nt = vt1 - vt0;  // >= 1 by construction of the grid
+  const int VTc = BWD ? p.vt_end - p.vt_base : 0;  // the backward chunk's vocabulary tiles
+  int vt0 = 0, nt;                                  // nt >= 1 by construction of the grid
+  if (BWD) {
+    const int pairs = ((p.N + kLceTile - 1) / kLceTile) * VTc;
+    nt = (pairs - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  } else {
+    const int VT = (p.V + kLceVTile - 1) / kLceVTile;
+    vt0 = blockIdx.y * p.vt_per_split;
+    nt = min(vt0 + p.vt_per_split, VT) - vt0;
+  }
+  // token tile and vocabulary tile of this CTA's tile j
+  const auto tile_tm = [&](int j) { return BWD ? (int)(blockIdx.x + j * gridDim.x) / VTc : (int)blockIdx.x; };
+  const auto tile_vt = [&](int j) {
+    return BWD ? p.vt_base + (int)(blockIdx.x + j * gridDim.x) % VTc : vt0 + j;
+  };
   const int KS = p.D / 64;   // K slices per tile
   const Guard g{&m.abort_flag, p.status};
 
@@ -136,8 +149,8 @@ __global__ void __launch_bounds__(kLceThreads, 1)
           const int st = it % kLceStages;
           if (!g.wait(&m.empty[st], ((it / kLceStages) & 1) ^ 1, 40)) { ok = false; break; }
           mbar_expect_tx(&m.full[st], kLceStage);
-          tma_load_2d(ring + st * kLceStage, &tmH, &m.full[st], kc * 64, tm * kLceTile);
-          tma_load_2d(ring + st * kLceStage + kLceSlice, &tmW, &m.full[st], kc * 64, (vt0 + j) * kLceVTile);
+          tma_load_2d(ring + st * kLceStage, &tmH, &m.full[st], kc * 64, tile_tm(j) * kLceTile);
+          tma_load_2d(ring + st * kLceStage + kLceSlice, &tmW, &m.full[st], kc * 64, tile_vt(j) * kLceVTile);
         }
       }
       // no copy may still be landing when the CTA exits
@@ -187,21 +200,21 @@ __global__ void __launch_bounds__(kLceThreads, 1)
     // warp write 32 consecutive tokens of one vocabulary row.
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
-    const int token = tm * kLceTile + r;
-    const bool live = token < p.N;
-    const int t = live ? p.targets[token] : -1;
-    const bool use = live && t >= 0 && t < p.V;
-    const float gl = use ? p.g[token] : 0.f;
-    const float l2 = use ? p.lse[token] * 1.4426950408889634f : 0.f;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       const int buf = j & 1;
+      const int token = tile_tm(j) * kLceTile + r;
+      const bool live = token < p.N;
+      const int t = live ? p.targets[token] : -1;
+      const bool use = live && t >= 0 && t < p.V;
+      const float gl = use ? p.g[token] : 0.f;
+      const float l2 = use ? p.lse[token] * 1.4426950408889634f : 0.f;
       ok = g.wait(&m.acc_full[buf], (j >> 1) & 1, 44);
       ok = __all_sync(~0u, ok);
       if (!ok) break;
       tc_fence_after();
-      const int v0 = (vt0 + j) * kLceVTile;
+      const int v0 = tile_vt(j) * kLceVTile;
       const int c0v = v0 - p.vt_base * kLceVTile;  // column of v0 in the chunk
 #pragma unroll 1
       for (int c0 = 0; c0 < kLceVTile; c0 += 32) {
@@ -245,7 +258,7 @@ __global__ void __launch_bounds__(kLceThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
-    const int token = tm * kLceTile + r;
+    const int token = (int)blockIdx.x * kLceTile + r;
     const int t = token < p.N ? p.targets[token] : -1;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     float m_run = -INFINITY, s_run = 0.f, tgt = 0.f;
@@ -257,7 +270,7 @@ __global__ void __launch_bounds__(kLceThreads, 1)
       ok = __all_sync(~0u, ok);
       if (!ok) break;
       tc_fence_after();
-      const int v0 = (vt0 + j) * kLceVTile;
+      const int v0 = tile_vt(j) * kLceVTile;
 #pragma unroll 1
       for (int c0 = 0; c0 < kLceVTile; c0 += 32) {
         uint32_t a[32];
@@ -651,13 +664,13 @@ cudaError_t launch_lce_bwd(int N, int V, int D, const void* hidden, const void* 
   if (e != cudaSuccess) return e;
   for (int c = 0; c < L.chunks; ++c) {
     const int cv0 = c * L.vc, kc = (V - cv0 < L.vc) ? V - cv0 : L.vc;  // the chunk's vocabulary rows
-    // dz (and dz^T) of the chunk
-    const LceSplit sp = lce_split(N, kc, lce_slots());
+    // dz (and dz^T) of the chunk: one CTA per SM over its (token tile,
+    // vocabulary tile) pairs
     LceParams p{};
     p.N = N;
     p.V = V;
     p.D = D;
-    p.vt_per_split = sp.per;
+    p.vt_per_split = 0;
     p.targets = targets;
     p.status = status;
     p.vt_base = cv0 / kLceVTile;
@@ -668,7 +681,8 @@ cudaError_t launch_lce_bwd(int N, int V, int D, const void* hidden, const void* 
     p.ld_dz = L.vc;
     p.dzt = dhead ? dzt : nullptr;
     p.ld_dzt = L.ld_dzt;
-    lce_kernel<true><<<dim3((N + kLceTile - 1) / kLceTile, sp.splits), kLceThreads, kLceSmem, st>>>(tH, tW, p);
+    const int pairs = ((N + kLceTile - 1) / kLceTile) * (p.vt_end - p.vt_base);
+    lce_kernel<true><<<pairs < lce_slots() ? pairs : lce_slots(), kLceThreads, kLceSmem, st>>>(tH, tW, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // dW rows of the chunk = dz^T H (tokens are the contraction)
     if (dhead) {
