@@ -282,6 +282,22 @@ uint32_t pa_device_status(const void* ws, pa_stream_t stream);
 pa_status pa_selftest_wait_timeout(void* ws, size_t ws_bytes, pa_stream_t stream);
 
 /*
+ * Self-test of the forward's FMA-pipe exponential (the softmax's
+ * exp(s - m) taken as 2^t with t = (s - m) log2 e; mlx-train-perf 0.5.1
+ * README, "Packed attention"): y[i] = 2^x[i] for n fp32 values, computed on
+ * `stream` by the device routine the forward kernel can use for part of
+ * its keys (Cody-Waite range reduction and a fitted cubic, no MUFU; the
+ * build option PA_FWD_FMA_EX2_PAIRS sets how many, none by default).
+ * x and y are device pointers to n floats each (4-byte aligned; the caller
+ * owns both). Relative error about 1e-4 for results >= 2^-126; inputs <= -127
+ * (and -inf) give +0.0; inputs must be below 128. A lane mismatch inside
+ * the routine is reported as a NaN in y.
+ * Errors: PA_ERR_SHAPE (n < 0), PA_ERR_NULL, PA_ERR_ALIGN, PA_ERR_ARCH,
+ * PA_ERR_CUDA. n == 0 returns PA_OK without a device call.
+ */
+pa_status pa_selftest_exp2_fma(const float* x, float* y, int64_t n, pa_stream_t stream);
+
+/*
  * Host packer (mlx-train-perf changelog, "Added": the packed batch iterator
  * fills fixed rows with (tokens, offset) sequences after a seeded per-epoch
  * shuffle, by first-fit, and emits per-token segment buffers; the packed loss

@@ -31,7 +31,7 @@ STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_NULL", 2: "PA_ERR_HEAD_DIM", 3: "PA_ERR_G
 PA_IO_BF16, PA_IO_F32 = 0, 1
 EXPORTS = ["pa_workspace_bytes", "pa_fwd", "pa_bwd", "pa_fwd_causal", "pa_bwd_causal", "pa_build_tile_table",
            "pa_fwd_tiles", "pa_bwd_delta", "pa_bwd_dq", "pa_bwd_dkv", "pa_bwd_noalloc", "pa_device_status",
-           "pa_selftest_wait_timeout", "pa_pack_first_fit", "pa_workspace_bytes_strided", "pa_fwd_strided",
+           "pa_selftest_wait_timeout", "pa_selftest_exp2_fma", "pa_pack_first_fit", "pa_workspace_bytes_strided", "pa_fwd_strided",
            "pa_bwd_strided", "pa_lce_workspace_bytes", "pa_lce_fwd", "pa_lce_bwd_workspace_bytes", "pa_lce_bwd",
            "pa_bwd_fused_workspace_bytes", "pa_bwd_fused", "pa_status_string"]
 
@@ -92,6 +92,8 @@ def lib():
             L.pa_bwd_noalloc.restype = ctypes.c_int
             L.pa_selftest_wait_timeout.argtypes = [P, S, P]
             L.pa_selftest_wait_timeout.restype = ctypes.c_int
+            L.pa_selftest_exp2_fma.argtypes = [P, P, ctypes.c_int64, P]
+            L.pa_selftest_exp2_fma.restype = ctypes.c_int
             L.pa_device_status.argtypes = [P, P]
             L.pa_device_status.restype = ctypes.c_uint32
             ST = ctypes.POINTER(pa_strides)
@@ -361,6 +363,16 @@ def pa_selftest_wait_timeout(ws, stream=None):
     """Launch the bounded-wait self-test into the workspace status word (see
     include/pa.h); read the result with pa_device_status."""
     _check(lib().pa_selftest_wait_timeout(_ptr(ws, None, "ws"), ws.numel(), _stream(stream)))
+
+
+def pa_selftest_exp2_fma(x, y, stream=None):
+    """y = 2^x through the FMA-pipe exponential (see include/pa.h);
+    x and y are fp32 CUDA tensors of the same number of elements."""
+    import torch
+    if x.numel() != y.numel():
+        raise ValueError("x and y differ in size")
+    _check(lib().pa_selftest_exp2_fma(_ptr(x, torch.float32, "x"), _ptr(y, torch.float32, "y"), x.numel(),
+                                      _stream(stream)))
 
 
 def pa_device_status(ws, stream=None) -> int:

@@ -611,6 +611,17 @@ pa_status pa_selftest_wait_timeout(void* ws, size_t ws_bytes, pa_stream_t stream
   return PA_OK;
 }
 
+pa_status pa_selftest_exp2_fma(const float* x, float* y, int64_t n, pa_stream_t stream) {
+  if (n < 0) return PA_ERR_SHAPE;
+  if (n == 0) return PA_OK;
+  if (!x || !y) return PA_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 3u) return PA_ERR_ALIGN;
+  pa_status why = device_ok();
+  if (why != PA_OK) return why;
+  return pa::launch_exp2_fma_selftest(x, y, n, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                                                     : PA_ERR_CUDA;
+}
+
 uint32_t pa_device_status(const void* ws, pa_stream_t stream) {
   if (!ws) return 0xFFFFFFFFu;
   uint32_t h = 0;

@@ -106,10 +106,23 @@ __device__ __forceinline__ float max32(const uint32_t (&x)[32]) {
   return fmax3(a, b, fmaxf(__uint_as_float(x[30]), __uint_as_float(x[31])));
 }
 
+// Pairs of keys, of each 16, whose 2^t the FMA pipe computes (ex2_fma2)
+// instead of the MUFU. The polynomial costs about five issue slots a key
+// instead of one, and on GB300 the softmax warps are bound by issue, not by
+// the MUFU: with 2, 4 or 6 pairs of 16 the 8k forward took 0.490, 0.588 and
+// 0.509 ms against 0.450 ms with none (0.5% relative change in O), so the
+// default is none and the option stays for other parts.
+#ifndef PA_FWD_FMA_EX2_PAIRS
+#define PA_FWD_FMA_EX2_PAIRS 0
+#endif
+constexpr int kFmaPairs = PA_FWD_FMA_EX2_PAIRS;
+static_assert(kFmaPairs >= 0 && kFmaPairs <= 16, "pairs of 16");
+
 // P for 32 keys: 2^(s sl2 - moff) packed to bf16 pairs into 16 TMEM columns
 // (not waited); adds the exact weights to ls and, with ROUNDED, the
 // bf16-rounded ones to lr. The scaling and the sums run two keys per
-// instruction (packed FP32).
+// instruction (packed FP32). kFmaPairs of the 16 pairs, spread evenly, take
+// their exponentials on the FMA pipe.
 template <bool ROUNDED>
 __device__ __forceinline__ void exp_store32(const uint32_t (&x)[32], uint64_t sc, uint64_t off, uint32_t taddr,
                                             uint64_t& ls, uint64_t& lr) {
@@ -117,8 +130,18 @@ __device__ __forceinline__ void exp_store32(const uint32_t (&x)[32], uint64_t sc
   uint32_t pk[16];
 #pragma unroll
   for (int e = 0; e < 32; e += 2) {
-    const float2 t = f2_split(fma2(f2(__uint_as_float(x[e]), __uint_as_float(x[e + 1])), sc, off));
-    const float e0 = ex2(t.x), e1 = ex2(t.y);
+    const uint64_t t2 = fma2(f2(__uint_as_float(x[e]), __uint_as_float(x[e + 1])), sc, off);
+    const int i = e >> 1;
+    float e0, e1;
+    if ((i * kFmaPairs) / 16 != ((i + 1) * kFmaPairs) / 16) {
+      const float2 y2 = f2_split(ex2_fma2(t2));
+      e0 = y2.x;
+      e1 = y2.y;
+    } else {
+      const float2 t = f2_split(t2);
+      e0 = ex2(t.x);
+      e1 = ex2(t.y);
+    }
     const uint32_t y = pack_bf16x2(e0, e1);
     s2[(e >> 1) & 1] = add2(s2[(e >> 1) & 1], f2(e0, e1));
     if (ROUNDED)

@@ -34,6 +34,7 @@ cudaError_t launch_tile_table(const AttnParams& p, int4* tiles, cudaStream_t st)
 cudaError_t launch_delta(const AttnParams& p, int D, const RowStrides& rs, cudaStream_t st);
 // Self-test of the bounded waits: one warp waits on an mbarrier nothing arrives on.
 cudaError_t launch_wait_timeout_selftest(uint32_t* status, cudaStream_t st);
+cudaError_t launch_exp2_fma_selftest(const float* x, float* y, int64_t n, cudaStream_t st);
 cudaError_t launch_fwd(const AttnParams& p, int D, const RowStrides& rs, const void* q, const void* k, const void* v,
                        cudaStream_t st);
 cudaError_t launch_bwd_dq(const AttnParams& p, int D, const RowStrides& rs, const void* q, const void* k,

@@ -324,6 +324,22 @@ cudaError_t launch_wait_timeout_selftest(uint32_t* status, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// y[i] = 2^x[i] through the FMA-pipe exponential (ex2_fma2), each
+// input in both lanes of the packed pair; lane 1 must agree with lane 0.
+__global__ void exp2_fma_selftest_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const float2 r = f2_split(ex2_fma2(f2(x[i], x[i])));
+    y[i] = (__float_as_uint(r.x) == __float_as_uint(r.y)) ? r.x : __uint_as_float(0x7FC00001u);
+  }
+}
+
+cudaError_t launch_exp2_fma_selftest(const float* x, float* y, int64_t n, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const int64_t blocks = (n + 255) / 256;
+  exp2_fma_selftest_kernel<<<(unsigned)(blocks < 1024 ? blocks : 1024), 256, 0, st>>>(x, y, n);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_delta(const AttnParams& p, int D, const RowStrides& rs, cudaStream_t st) {
   const bool contig = p.Nr == p.N && rs.q_n == D && rs.q_h == (int64_t)p.N * D && rs.q_b == (int64_t)p.Hq * p.N * D;
   const size_t rows = (size_t)p.B * p.Hq * p.N;

@@ -517,4 +517,31 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// 2^t for two packed fp32 lanes on the FMA pipe, leaving the MUFU to the
+// other lanes of a softmax. Cody and Waite's range reduction for base 2:
+// adding 1.5 * 2^23 rounds t to the integer n, which then sits in the low
+// bits of u; f = t - n lies in [-1/2, 1/2] and is exact. 2^f is the cubic
+// 1 + c1 f + c2 f^2 + c3 f^3 whose coefficients minimise the largest
+// relative error over [-1/2, 1/2] (a linear program over a 4097-point grid,
+// fit_exp2_poly.py beside this file); 2^n enters as n << 23 added to the
+// cubic's bits (the high bits of u shift out). Relative error about
+// 1.0e-4 for results of 2^-126 and above. Inputs are clamped to -127, where
+// f = 0, the cubic is exactly 1 and the sum of the bits wraps to +0.0, so
+// -inf gives +0.0; results below 2^-126 are tiny non-negative values.
+// Inputs must stay below 128 (the callers pass t <= 8).
+__device__ __forceinline__ uint64_t ex2_fma2(uint64_t t2) {
+  constexpr float kC1 = 0x1.62f5f6p-1f, kC2 = 0x1.f00c56p-3f, kC3 = 0x1.c2a36p-5f;
+  const float2 t = f2_split(t2);
+  const uint64_t tc = f2(fmaxf(t.x, -127.f), fmaxf(t.y, -127.f));
+  const uint64_t magic = f2(12582912.f, 12582912.f);
+  const uint64_t u = add2(tc, magic);
+  const uint64_t f = add2(tc, fma2(u, f2(-1.f, -1.f), magic));  // t + (-n)
+  uint64_t q = fma2(f2(kC3, kC3), f, f2(kC2, kC2));
+  q = fma2(q, f, f2(kC1, kC1));
+  q = fma2(q, f, f2(1.f, 1.f));
+  const float2 qq = f2_split(q), uu = f2_split(u);
+  return f2(__uint_as_float(__float_as_uint(qq.x) + (__float_as_uint(uu.x) << 23)),
+            __uint_as_float(__float_as_uint(qq.y) + (__float_as_uint(uu.y) << 23)));
+}
+
 }  // namespace pa

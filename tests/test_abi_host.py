@@ -23,7 +23,7 @@ def L():
 def declared_functions():
     src = open(os.path.join(ROOT, "include", "pa.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_every_declared_symbol_is_exported(L):
@@ -158,6 +158,12 @@ def test_selftest_refusals(L):
     assert L.pa_selftest_wait_timeout(None, 1 << 20, None) == 1
     assert L.pa_selftest_wait_timeout(FAKE + 4, 1 << 20, None) == 5
     assert L.pa_selftest_wait_timeout(FAKE, 3, None) == 6
+    # the FMA-pipe exponential's self-test: shape, null and alignment first
+    assert L.pa_selftest_exp2_fma(FAKE, FAKE, -1, None) == 4
+    assert L.pa_selftest_exp2_fma(FAKE, FAKE, 0, None) == 0  # nothing to do, no device call
+    assert L.pa_selftest_exp2_fma(None, FAKE, 8, None) == 1
+    assert L.pa_selftest_exp2_fma(FAKE, None, 8, None) == 1
+    assert L.pa_selftest_exp2_fma(FAKE + 2, FAKE, 8, None) == 5
 
 
 def test_valid_call_without_a_gpu_is_refused_not_run(L):
@@ -167,6 +173,7 @@ def test_valid_call_without_a_gpu_is_refused_not_run(L):
     assert fwd(L, d()) in (7, 8)  # no device: arch / CUDA error, nothing launched
     assert fwd(L, d(N=200)) in (7, 8)  # ragged N passes the host checks, then the same
     assert L.pa_selftest_wait_timeout(FAKE, 1 << 20, None) in (7, 8)
+    assert L.pa_selftest_exp2_fma(FAKE, FAKE, 8, None) in (7, 8)
 
 
 def test_status_strings(L):
