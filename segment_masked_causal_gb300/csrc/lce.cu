@@ -363,8 +363,9 @@ __global__ void __launch_bounds__(256) lce_merge_kernel(const LceParams p, int s
 // C (M x N) from A (M x K, K contiguous) and B (K x N, N contiguous) in
 // 128 x 256 output tiles (N = 256 products, which keep their full rate beside
 // the epilogue warps' arithmetic). One CTA per SM walks tiles blockIdx.x,
-// blockIdx.x + gridDim.x, ... (N tiles fastest, so the CTAs that share an A
-// row block run together and keep it in L2), K in steps of 64 through a
+// blockIdx.x + gridDim.x, ... in groups of kGemmGroup row blocks (M tiles
+// fastest inside a group, so a group's A panels stay in L2 while it walks
+// every N tile), K in steps of 64 through a
 // 4-stage TMA ring (A as one 128-row x 64 box, B as four 64-row x 64 boxes,
 // all 128-byte swizzled; elements past M, N or K read as zero), tcgen05
 // products into two 256-column fp32 TMEM accumulators used by alternate
@@ -380,12 +381,25 @@ constexpr uint32_t kGemmStage = kGemmA + 4 * kGemmBHalf;  // 48 KB
 constexpr int kGemmThreads = 192;
 constexpr uint32_t kGemmSmem = 1024 /* misc */ + 1024 /* alignment */ + kGemmStages * kGemmStage;
 
+// Row blocks per group of the tile order. Measured on the N = 8192,
+// V = 151,936, D = 4096 backward (38 launches a call), in one run: 20.95,
+// 21.01, 20.62 and 20.99 ms with 1 (N tiles fastest), 8, 16 and 32, and
+// 21.17 ms with 16 on another box, as with 1 there: the order makes no
+// difference beyond the spread between runs. With N tiles fastest a launch
+// of 8192 x 4096 x 8192 read 0.60 GB from DRAM against 0.19 GB of operands
+// and kept the tensor pipe 78% busy.
+#ifndef PA_LCE_GEMM_GROUP
+#define PA_LCE_GEMM_GROUP 16
+#endif
+constexpr int kGemmGroup = PA_LCE_GEMM_GROUP;
+
 enum GemmMode : int { kStoreBf16 = 0, kAccInit = 1, kAccAdd = 2, kAccFinal = 3 };
 
 struct GemmParams {
   int M, N, K;         // N a multiple of 64
   int mode;            // GemmMode
-  int n_tiles;         // N tiles per row block; tile t is (t / n_tiles, t % n_tiles)
+  int m_tiles;         // row blocks of 128
+  int n_tiles;         // N tiles of kGemmN per row block
   int tiles;           // M tiles x N tiles
   __nv_bfloat16* c;    // bf16 result (kStoreBf16: the product; kAccFinal: accumulator + product)
   int ldc;
@@ -415,6 +429,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // this CTA's tiles: t = blockIdx.x + j * gridDim.x for j < nt (>= 1: the
   // grid is never larger than the tile count)
   const int nt = (p.tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  // first row and column of tile t: group gi holds row blocks g0 .. g0 + gs - 1
+  const auto tile_origin = [&](int t) -> int2 {
+    const int gi = t / (kGemmGroup * p.n_tiles), r = t - gi * kGemmGroup * p.n_tiles;
+    const int g0 = gi * kGemmGroup, gs = min(kGemmGroup, p.m_tiles - g0);
+    return make_int2((g0 + r % gs) * 128, (r / gs) * kGemmN);
+  };
   const Guard g{&m.abort_flag, p.status};
 
   if (threadIdx.x == 0) {
@@ -446,8 +466,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int it = 0;
       bool ok = true;
       for (int j = 0; ok && j < nt; ++j) {
-        const int t = (int)blockIdx.x + j * (int)gridDim.x;
-        const int m0 = (t / p.n_tiles) * 128, n0 = (t % p.n_tiles) * kGemmN;
+        const int2 o = tile_origin((int)blockIdx.x + j * (int)gridDim.x);
+        const int m0 = o.x, n0 = o.y;
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int st = it % kGemmStages;
           if (!g.wait(&m.empty[st], ((it / kGemmStages) & 1) ^ 1, 45)) { ok = false; break; }
@@ -505,8 +525,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const bool ok = __all_sync(~0u, g.wait(&m.acc_full[buf], (j >> 1) & 1, 47));
       if (!ok) break;
       tc_fence_after();
-      const int t = (int)blockIdx.x + j * (int)gridDim.x;
-      const int m0 = (t / p.n_tiles) * 128, n0 = (t % p.n_tiles) * kGemmN;
+      const int2 o = tile_origin((int)blockIdx.x + j * (int)gridDim.x);
+      const int m0 = o.x, n0 = o.y;
       const int row = m0 + quarter * 32 + lane;
 #pragma unroll 1
       for (int c0 = 0; c0 < kGemmN; c0 += 32) {
@@ -569,6 +589,7 @@ cudaError_t launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, const Gemm
   GemmParams q = gp;
   const long long mt = (gp.M + 127) / 128, ntl = (gp.N + kGemmN - 1) / kGemmN;
   if (mt * ntl > (1ll << 30)) return cudaErrorInvalidValue;
+  q.m_tiles = (int)mt;
   q.n_tiles = (int)ntl;
   q.tiles = (int)(mt * ntl);
   int dev = 0, sms = 148;
