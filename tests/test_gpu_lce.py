@@ -82,10 +82,13 @@ def test_lce_forward_is_deterministic(cuda_dev):
 # ------------------------------------------------------------------ backward
 # dH and dW of L = sum_i g_i nll_i against the oracle's fp64 backward, on the
 # forward's shapes plus one whose vocabulary spans three chunks (the fp32 dH
-# accumulator starts, adds and finishes). dz is rounded to bf16 and the
+# accumulator starts, adds and finishes) and one of 36 token tiles, whose
+# last group is partial in both the dz kernel's pair order (groups of 32
+# token tiles) and the GEMM's tile order (groups of 16 row blocks). dz is
+# rounded to bf16 and the
 # results are stored in bf16, so the bar is the attention gradients': relative
 # L2 <= 2e-2 over each tensor, and no row off by more than 10% of its norm.
-BWD_CASES = CASES + [("three_chunks", 384, 17000, 128)]
+BWD_CASES = CASES + [("three_chunks", 384, 17000, 128), ("partial_groups", 4500, 3000, 128)]
 GRAD_RELL2, ROW_REL = 2e-2, 0.1
 
 
