@@ -339,6 +339,32 @@ class Runner:
         return ms, h2d, d2h
 
 
+def host_link_gbs(dev, nbytes: int = 256 << 20, reps: int = 3):
+    """Pinned-memory copy rates of this machine, host to device and back (GB/s,
+    each direction alone), so that the e2e figure can be read against the
+    link it rides on. None if the measurement fails."""
+    import torch
+    try:
+        h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        d.copy_(h)
+        h.copy_(d)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        rates = {}
+        for name, dst, src in (("h2d", d, h), ("d2h", h, d)):
+            e0.record()
+            for _ in range(reps):
+                dst.copy_(src, non_blocking=True)
+            e1.record()
+            torch.cuda.synchronize()
+            rates[name] = round(nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+        del h, d
+        return rates
+    except Exception:
+        return None
+
+
 def cpu_baseline(w: synth.Workload, seconds: float = 12.0, max_heads: int = 8):
     """The oracle, as it stands, on a bounded sample: complete fwd+bwd of one
     query head against its kv head (the per-head share of dK/dV), repeated over
@@ -411,6 +437,7 @@ def run_ours(args):
 
     e2e_ms, h2d, d2h = r.e2e(args.steps, args.warmup)
     e2e_ms = reduce_max(e2e_ms, dev)
+    link = host_link_gbs(dev)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
@@ -429,7 +456,8 @@ def run_ours(args):
         "gpu_launches": 6 * args.steps,
         "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                "overlap": "input and output copies on their own streams, two device buffer sets"},
+                "overlap": "input and output copies on their own streams, two device buffer sets",
+                "host_link_gbs": link},
         "clocks": clocks,
     }
     if not args.no_extras and w.name == "8k_one_segment":
